@@ -1,0 +1,304 @@
+"""Pins for the CPU oracle: hand-worked blocks, bit-pattern invariants, exact
+rational brute force, and special cases where the int8 path reduces to the plain
+matmul.  CPU only."""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import gguf_synth as syn
+from oracle import gguf_oracle as O
+from tests import golden_blocks as gb
+
+
+# ---------------------------------------------------------------- hand-worked blocks
+
+@pytest.mark.parametrize("builder,decoder", [
+    (gb.q4_k, O.dequant_q4_k), (gb.q5_k, O.dequant_q5_k), (gb.q6_k, O.dequant_q6_k)])
+def test_hand_worked_kquant_blocks(builder, decoder):
+    blk, expected = builder()
+    w = decoder(blk[None, :])[0]
+    for e, v in expected.items():
+        assert w[e] == v, (e, w[e], v)
+
+
+def test_hand_worked_q8_0_blocks():
+    for blk, expected in gb.q8_0():
+        w = O.dequant_q8_0(blk[None, :])[0]
+        for e, v in expected.items():
+            assert w[e] == v, (e, w[e], v)
+
+
+def test_decode_6bit_fields_all_distinct_bits():
+    # each of the 16 six-bit fields set alone to 63 must light exactly one field
+    for i in range(16):
+        s = np.zeros((1, 12), np.uint8)
+        j, is_min = i % 8, i >= 8
+        if j < 4:
+            s[0, j + 4 * is_min] = 63
+        else:
+            s[0, j + 4] = 0xF0 if is_min else 0x0F
+            s[0, j - 4 + 4 * is_min] = 0xC0
+        vals = [int(O.decode_6bit(s, k)[0]) for k in range(16)]
+        assert vals[i] == 63 and sum(vals) == 63, (i, vals)
+
+
+# ---------------------------------------------------------------- invariants
+
+def _blocks_of(qtype, fill):
+    return np.full((3, syn.BLOCK_BYTES[qtype]), fill, np.uint8)
+
+
+def _set_f16(blk, off, val):
+    blk[:, off:off + 2] = np.array([val], np.float16).view(np.uint8)
+
+
+@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+def test_all_zero_blocks_decode_to_zero(qtype):
+    w = O._DECODERS[qtype](_blocks_of(qtype, 0))
+    assert np.all(w == 0)
+
+
+@pytest.mark.parametrize("qtype,value", [(O.Q4_K, 882.0), (O.Q5_K, 1890.0), (O.Q6_K, -31.0),
+                                         (O.Q8_0, -1.0)])
+def test_all_max_bit_patterns(qtype, value):
+    # all quant/scale bytes 0xFF, d = dmin = 1: sc = m = 63 and q at its maximum
+    blk = _blocks_of(qtype, 0xFF)
+    if qtype == O.Q8_0:
+        _set_f16(blk, 0, 1.0)
+    elif qtype == O.Q6_K:
+        _set_f16(blk, 208, 1.0)
+    else:
+        _set_f16(blk, 0, 1.0)
+        _set_f16(blk, 2, 1.0)
+    w = O._DECODERS[qtype](blk)
+    assert np.all(w == value)
+
+
+def test_q6k_zero_quants_give_minus_32_d_sc():
+    g = syn.rng(5)
+    blk = syn.weight_blocks(g, O.Q6_K, 4, 256).reshape(4, 210)
+    blk[:, 0:192] = 0
+    w = O.dequant_q6_k(blk)
+    d = O.f16_field(blk[:, 208:210])
+    sc = blk[:, 192:208].view(np.int8).astype(np.float64)
+    for e in range(256):
+        assert np.array_equal(w[:, e], -32 * d * sc[:, e // 16])
+
+
+@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+def test_scaling_d_by_power_of_two_scales_w(qtype):
+    g = syn.rng(7)
+    w = syn.weight_blocks(g, qtype, 2, 256)
+    blk = w.reshape(-1, syn.BLOCK_BYTES[qtype]).copy()
+    base = O._DECODERS[qtype](blk)
+    offs = {O.Q8_0: [0], O.Q4_K: [0, 2], O.Q5_K: [0, 2], O.Q6_K: [208]}[qtype]
+    for off in offs:
+        d = blk[:, off:off + 2].copy().view(np.float16)[:, 0]
+        blk[:, off:off + 2] = (d * np.float16(4)).astype(np.float16).view(np.uint8).reshape(-1, 2)
+    assert np.array_equal(O._DECODERS[qtype](blk), 4 * base)
+
+
+def test_synthetic_blocks_follow_the_recipe():
+    g = syn.rng(11)
+    w6 = syn.weight_blocks(g, O.Q6_K, 16, 1024).reshape(-1, 210)
+    sc = w6[:, 192:208].view(np.int8)
+    assert sc.min() >= -32 and sc.max() <= 31
+    w8 = syn.weight_blocks(g, O.Q8_0, 16, 1024).reshape(-1, 34)
+    q = w8[:, 2:].view(np.int8)
+    assert q.min() >= -127 and q.max() <= 127
+    d = O.f16_field(w8[:, 0:2])
+    assert np.all(d >= 0) and np.all(np.isfinite(d))
+
+
+# ---------------------------------------------------------------- matmul vs exact rationals
+
+@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+def test_matmul_exact_vs_fraction_brute_force(qtype):
+    g = syn.rng(100 + qtype)
+    N, K, M = 3, 256, 2
+    w = syn.weight_blocks(g, qtype, N, K)
+    x = syn.normal(g, (M, K), "f32").astype(np.float64)
+    r = syn.normal(g, (M, N), "f32").astype(np.float64)
+    w64 = O.dequant(w, qtype, N, K)
+    ref = O.matmul_exact(x, w64, r)
+    for m in range(M):
+        for n in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                acc += Fraction(float(x[m, k])) * Fraction(float(w64[n, k]))
+            acc += Fraction(float(r[m, n]))
+            assert abs(ref[m, n] - float(acc)) <= 1e-12 * max(1.0, abs(float(acc)))
+
+
+def test_dequant_row_major_block_order():
+    # a row of 2 blocks: decoding row-wise must equal decoding each block alone
+    g = syn.rng(3)
+    w = syn.weight_blocks(g, O.Q4_K, 2, 512)
+    w64 = O.dequant(w, O.Q4_K, 2, 512)
+    for n in range(2):
+        for kb in range(2):
+            blk = w[n, kb * 144:(kb + 1) * 144][None, :]
+            assert np.array_equal(w64[n, kb * 256:(kb + 1) * 256], O.dequant_q4_k(blk)[0])
+
+
+# ---------------------------------------------------------------- activation quantizer
+
+def test_act_quant_constant_blocks_hit_127():
+    x = np.zeros((2, 64), np.float32)
+    x[0, :32] = 0.3
+    x[0, 32:] = -7.25
+    x[1, :32] = 1e-20
+    qa, d_a, s = O.quantize_act_q8(x)
+    assert np.all(qa[0, :32] == 127) and np.all(qa[0, 32:] == -127)
+    assert np.all(qa[1, :32] == 127)
+    assert d_a[0, 0] == np.float32(0.3) / np.float32(127)
+    assert s[0, 0] == 127 * 32 and s[0, 1] == -127 * 32
+
+
+def test_act_quant_zero_block():
+    qa, d_a, s = O.quantize_act_q8(np.zeros((1, 32), np.float32))
+    assert np.all(qa == 0) and d_a[0, 0] == 0 and s[0, 0] == 0
+
+
+def test_act_quant_exact_multiples_roundtrip():
+    g = syn.rng(21)
+    n = g.integers(-127, 128, size=(3, 96))
+    n[:, ::32] = 127                                   # amax = 127 * 2**-3 in every block
+    x = (n * 2.0 ** -3).astype(np.float32)
+    qa, d_a, s = O.quantize_act_q8(x)
+    assert np.all(d_a == np.float32(2.0 ** -3))
+    assert np.array_equal(qa.astype(np.int64), n)
+    assert np.array_equal(s, n.reshape(3, 3, 32).sum(axis=2))
+
+
+def test_act_quant_rounds_half_away_from_zero():
+    x = np.zeros((1, 32), np.float32)
+    x[0, 0] = 127.0                                    # d_a = 1, id = 1
+    x[0, 1], x[0, 2], x[0, 3], x[0, 4] = 2.5, -2.5, 0.5, -0.5
+    qa, d_a, _ = O.quantize_act_q8(x)
+    assert d_a[0, 0] == 1.0
+    assert list(qa[0, 1:5]) == [3, -3, 1, -1]
+
+
+# ---------------------------------------------------------------- int8 path reduces to the plain matmul
+
+@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+def test_int8_path_equals_exact_when_activations_are_on_the_grid(qtype):
+    # x = d_a * integers with amax = 127 * d_a in every block: quantization is
+    # lossless, so the int8-path result must equal the exact matmul
+    g = syn.rng(40 + qtype)
+    N, K, M = 5, 512, 3
+    w = syn.weight_blocks(g, qtype, N, K)
+    n = g.integers(-127, 128, size=(M, K))
+    n[:, ::32] = -127
+    scale = 2.0 ** g.integers(-6, 2, size=(M, K // 32, 1))
+    x = (n.reshape(M, K // 32, 32) * scale).reshape(M, K).astype(np.float32)
+    r = syn.normal(g, (M, N), "f32")
+    y8 = O.gemv_int8_path(w, qtype, N, K, x, r)
+    ref = O.matmul_exact(x, O.dequant(w, qtype, N, K), r)
+    assert np.max(np.abs(y8 - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+def test_int8_path_close_to_exact_on_normal_data(qtype):
+    # the activation rounding error is the only gap: RMS ~ amax/(127*sqrt(12)) per value
+    g = syn.rng(60 + qtype)
+    N, K, M = 16, 1024, 2
+    w = syn.weight_blocks(g, qtype, N, K)
+    x = syn.normal(g, (M, K), "f32")
+    y8 = O.gemv_int8_path(w, qtype, N, K, x)
+    ref = O.matmul_exact(x, O.dequant(w, qtype, N, K))
+    assert np.max(np.abs(y8 - ref)) <= 3e-2 * np.max(np.abs(ref))
+    assert np.max(np.abs(y8 - ref)) > 0
+
+
+@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+def test_integer_terms_rebuild_the_decoded_weights(qtype):
+    g = syn.rng(80 + qtype)
+    N, K = 3, 512
+    w = syn.weight_blocks(g, qtype, N, K)
+    q_w, sub, scale, minv = O.weight_int_terms(w, qtype, N, K)
+    rebuilt = np.repeat(scale, sub, axis=1) * q_w - np.repeat(minv, sub, axis=1)
+    assert np.array_equal(rebuilt, O.dequant(w, qtype, N, K))
+
+
+def test_int8_dots_brute_force_tiny():
+    g = syn.rng(90)
+    q_w = g.integers(-32, 32, size=(2, 64))
+    qa = g.integers(-127, 128, size=(3, 64)).astype(np.int8)
+    D = O.int8_dots(q_w, 16, qa)
+    for m in range(3):
+        for n in range(2):
+            for j in range(4):
+                assert D[m, n, j] == sum(int(q_w[n, k]) * int(qa[m, k]) for k in range(16 * j, 16 * j + 16))
+
+
+# ---------------------------------------------------------------- Q6_K planes
+
+def test_q6k_planes_roundtrip_and_offsets():
+    g = syn.rng(13)
+    N, K = 6, 768
+    w = syn.weight_blocks(g, O.Q6_K, N, K)
+    nblk = N * K // 256
+    p = O.q6k_to_planes(w)
+    assert p.size == w.size == 210 * nblk                     # same size
+    assert O.q6k_planes_offsets(nblk) == (0, 128 * nblk, 192 * nblk, 208 * nblk, 210 * nblk)
+    back = O.q6k_from_planes(p, nblk)
+    assert np.array_equal(back.reshape(N, -1), w)             # same contents
+    blk = w.reshape(nblk, 210)
+    for b in (0, 1, nblk - 1):                                 # field by field
+        assert np.array_equal(p[128 * b:128 * b + 128], blk[b, 0:128])
+        assert np.array_equal(p[128 * nblk + 64 * b:128 * nblk + 64 * b + 64], blk[b, 128:192])
+        assert np.array_equal(p[192 * nblk + 16 * b:192 * nblk + 16 * b + 16], blk[b, 192:208])
+        assert np.array_equal(p[208 * nblk + 2 * b:208 * nblk + 2 * b + 2], blk[b, 208:210])
+    assert np.array_equal(O.dequant_q6k_planes(p, N, K), O.dequant(w, O.Q6_K, N, K))
+
+
+# ---------------------------------------------------------------- decode-once padded buffer
+
+def test_rounding_helpers_ties_to_even():
+    one = 1.0
+    assert O.round_f64_to_bf16_bits(np.array([one + 2 ** -8]))[0] == 0x3F80
+    assert O.round_f64_to_bf16_bits(np.array([one + 3 * 2 ** -8]))[0] == 0x3F82
+    assert O.round_f64_to_bf16_bits(np.array([one + 2 ** -8 + 2 ** -30]))[0] == 0x3F81
+    assert O.round_f64_to_bf16_bits(np.array([-2.0, 0.0]))[0] == 0xC000
+    assert O.round_f64_to_f16_bits(np.array([one + 2 ** -11]))[0] == 0x3C00
+    assert O.round_f64_to_f16_bits(np.array([one + 3 * 2 ** -11]))[0] == 0x3C02
+
+
+@pytest.mark.parametrize("odt", ["f16", "bf16"])
+def test_padding_changes_only_the_stride(odt):
+    g = syn.rng(17)
+    N, K = 4, 512
+    w = syn.weight_blocks(g, O.Q8_0, N, K)
+    packed = O.dequant_padded_bits(w, O.Q8_0, N, K, K, odt)
+    padded = O.dequant_padded_bits(w, O.Q8_0, N, K, K + 64, odt)
+    assert np.array_equal(padded[:, :K], packed)
+    assert np.all(padded[:, K:] == 0)
+
+
+# ---------------------------------------------------------------- MoE
+
+def test_moe_with_one_expert_equals_dense():
+    g = syn.rng(19)
+    E, N, K, T, top_k = 3, 8, 256, 4, 2
+    wE = syn.weight_blocks(g, O.Q4_K, E * N, K)
+    x = syn.normal(g, (T, K), "f32")
+    ids = np.zeros((T, top_k), np.int32)
+    ids[:, 0], ids[:, 1] = 2, 1
+    y = O.moe_mm_id_exact(wE, O.Q4_K, E, N, K, x, ids)
+    rb = wE.shape[1]
+    for slot, e in ((0, 2), (1, 1)):
+        dense = O.matmul_exact(x, O.dequant(wE[e * N:(e + 1) * N].reshape(N, rb), O.Q4_K, N, K))
+        assert np.max(np.abs(y[:, slot] - dense)) <= 1e-12 * np.max(np.abs(dense))
+
+
+def test_moe_routing_counts():
+    g = syn.rng(23)
+    ids = syn.zipf_ids(g, 64, 128, 8)
+    assert all(len(set(r)) == 8 for r in ids.tolist())
+    counts, offsets = O.moe_routing(ids, 128)
+    assert counts.sum() == 64 * 8 and offsets[0] == 0
+    assert np.array_equal(offsets[1:], np.cumsum(counts)[:-1])
+    assert counts[0] >= counts[64]                     # Zipf: low ranks hit more often
