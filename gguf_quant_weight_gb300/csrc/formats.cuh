@@ -1,0 +1,82 @@
+// Per-element GGUF block decoders (device).  Block structs follow the GGUF
+// on-disk layout (GGUF Support Proposal for mobius, section 7 "Quantization
+// Format Deep Dive" and the 1.2 type table; OpenVINO PR #39119 "Transformation"
+// for the Q6_K fields):
+//   Q8_0  {d f16, qs[32] i8}                                 w = d*q
+//   Q4_K  {d, dmin f16, scales[12], qs[128]}                 w = d*sc_j*q - dmin*m_j
+//   Q5_K  {d, dmin f16, scales[12], qh[32], qs[128]}         w = d*sc_j*q5 - dmin*m_j
+//   Q6_K  {ql[128], qh[64], scales[16] i8, d f16}            w = d*scales[e/16]*(q6 - 32)
+// The min is subtracted exactly, never folded into a rounded integer zero
+// point (OpenVINO PR #38696, "Details").
+#pragma once
+#include "common.cuh"
+
+namespace gg {
+
+__host__ __device__ constexpr int block_values(int qt) { return qt == GGUF_Q8_0 ? 32 : 256; }
+__host__ __device__ constexpr int block_bytes(int qt) {
+    return qt == GGUF_Q8_0 ? 34 : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176 : 210;
+}
+
+__device__ __forceinline__ float ld_f16_bytes(const uint8_t* p) {
+    return f16_bits_to_float((uint32_t)p[0] | ((uint32_t)p[1] << 8));
+}
+
+// Sub-block scale (i < 8) or min (i >= 8) from the 12 packed bytes.
+__device__ __forceinline__ int kquant_6bit(const uint8_t* s, int i) {
+    const int j = i & 7, mn = i >> 3;
+    if (j < 4) return s[j + 4 * mn] & 63;
+    const int low = mn ? (s[j + 4] >> 4) : (s[j + 4] & 15);
+    return low | ((s[j - 4 + 4 * mn] >> 6) << 4);
+}
+
+// 4-bit code of element e of a Q4_K/Q5_K super-block (qs = its 128 bytes).
+__device__ __forceinline__ int kquant_nibble(const uint8_t* qs, int e) {
+    const int p = e >> 6, r = e & 63;
+    const int byte = qs[32 * p + (r & 31)];
+    return r < 32 ? (byte & 15) : (byte >> 4);
+}
+
+// Q6_K code (0..63) of element e from its ql/qh fields.
+__device__ __forceinline__ int q6k_code(const uint8_t* ql, const uint8_t* qh, int e) {
+    const int h = e >> 7, r = e & 127, g = r >> 5, l = r & 31;
+    const int b = ql[64 * h + 32 * (g & 1) + l];
+    const int lo = g < 2 ? (b & 15) : (b >> 4);
+    const int hi = (qh[32 * h + l] >> (2 * g)) & 3;
+    return lo | (hi << 4);
+}
+
+// Weight value of element e of one block, as f32 (the products are exact in
+// f32; a K-quant's "- dmin*m" is the one rounding step).
+template <int QT>
+__device__ __forceinline__ float decode_elem(const uint8_t* blk, int e) {
+    if (QT == GGUF_Q8_0) {
+        return ld_f16_bytes(blk) * (float)static_cast<int8_t>(blk[2 + e]);
+    } else if (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
+        const float d = ld_f16_bytes(blk), dmin = ld_f16_bytes(blk + 2);
+        const uint8_t* s = blk + 4;
+        const int j = e >> 5;
+        int q;
+        if (QT == GGUF_Q4_K) {
+            q = kquant_nibble(blk + 16, e);
+        } else {
+            q = kquant_nibble(blk + 48, e) + 16 * ((blk[16 + (e & 31)] >> j) & 1);
+        }
+        return (d * (float)kquant_6bit(s, j)) * (float)q - dmin * (float)kquant_6bit(s, j + 8);
+    } else {
+        const float d = ld_f16_bytes(blk + 208);
+        const int8_t sc = static_cast<int8_t>(blk[192 + (e >> 4)]);
+        return (d * (float)sc) * (float)(q6k_code(blk, blk + 128, e) - 32);
+    }
+}
+
+// Q6_K element e of block b straight from the planes (nblk blocks in total).
+__device__ __forceinline__ float decode_q6k_planes_elem(const uint8_t* planes, int64_t nblk, int64_t b, int e) {
+    const uint8_t* ql = planes + 128 * b;
+    const uint8_t* qh = planes + 128 * nblk + 64 * b;
+    const int8_t sc = static_cast<int8_t>(planes[192 * nblk + 16 * b + (e >> 4)]);
+    const float d = ld_f16_bytes(planes + 208 * nblk + 2 * b);
+    return (d * (float)sc) * (float)(q6k_code(ql, qh, e) - 32);
+}
+
+}  // namespace gg

@@ -1,0 +1,233 @@
+// Tensor-core GEMMs on tcgen05 (sm_103a).
+//
+// Swap-AB form: the weight is UMMA operand A (M = 128 weight rows per CTA,
+// K-major) and the activations are operand B (N = BN token rows, K-major), so a
+// tile is 128 output features x BN tokens accumulated in f32 in TMEM (128 lanes
+// x BN columns).  Both operands sit in shared memory in the 128-byte-swizzled
+// K-major layout (8-row x 128-byte atoms), K advancing 64 values per stage.
+//
+// Warp roles in one CTA:
+//   warp 0        TMA producer (one elected lane)
+//   warp 1        TMEM allocation and MMA issue (one elected lane)
+//   warps 2..     A-operand producers when the weight is decoded in the kernel
+//                 (gemm_fused.cu), then the epilogue: TMEM -> registers,
+//                 + residual, round, store.
+// Every wait is a bounded mbarrier poll; a timeout is recorded in the status
+// word and the kernel still releases its TMEM before returning.
+//
+// This file holds the dense kernel used on a decoded weight buffer (ROCm
+// llama.cpp PR #37 "one-time K-padded f16 dequantization for prefill GEMMs",
+// "How it works": decode once into a K-padded buffer, then a plain GEMM with
+// the padded leading dimension) and the activation conversion pass.
+#include "tc_gemm.cuh"
+
+namespace gg {
+
+// ------------------------------------------------------------------ activation conversion
+
+namespace {
+
+__global__ void convert_act_kernel(const void* __restrict__ x, int xdt, int64_t total, uint16_t* __restrict__ out,
+                                   int odt_bf16) {
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < total;
+         i += (int64_t)gridDim.x * blockDim.x * 8) {
+        float v[8];
+        if (i + 8 <= total && xdt != GGUF_DT_F32) {
+            const uint4 t = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + i);
+            const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t lo = w4[j] & 0xFFFFu, hi = w4[j] >> 16;
+                if (xdt == GGUF_DT_BF16) { v[2 * j] = __uint_as_float(lo << 16); v[2 * j + 1] = __uint_as_float(hi << 16); }
+                else { v[2 * j] = f16_bits_to_float(lo); v[2 * j + 1] = f16_bits_to_float(hi); }
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = i + j < total ? load_act(x, xdt, i + j) : 0.f;
+        }
+        uint16_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            o[j] = odt_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v[j])) : __half_as_ushort(__float2half_rn(v[j]));
+        if (i + 8 <= total) {
+            *reinterpret_cast<uint4*>(out + i) = make_uint4(o[0] | (uint32_t)o[1] << 16, o[2] | (uint32_t)o[3] << 16,
+                                                            o[4] | (uint32_t)o[5] << 16, o[6] | (uint32_t)o[7] << 16);
+        } else {
+            for (int j = 0; j < 8 && i + j < total; ++j) out[i + j] = o[j];
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t convert_activations(const void* x, int xdt, int64_t M, int64_t K, void* out, int odt, int num_sms,
+                                cudaStream_t s) {
+    const int64_t total = M * K;
+    const int64_t blocks = std::min<int64_t>(ceil_div(total, 8 * 256), (int64_t)num_sms * 8);
+    convert_act_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(
+        x, xdt, total, static_cast<uint16_t*>(out), odt == GGUF_DT_BF16 ? 1 : 0);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t inner,
+                 uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return GGUF_ERR_CUDA;
+    (void)elem_bytes;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GGUF_OK : GGUF_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------------------------ dense kernel
+
+namespace {
+
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+    dense_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const TcEpilogue ep, int nk, int ab_bf16, int* status) {
+    using C = TcCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = align_up_1024(smem_raw);
+    uint8_t* sA = base;
+    uint8_t* sB = base + C::S * C::A_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::S * C::B_BYTES);
+    uint64_t* empty = full + C::S;
+    uint64_t* tfull = empty + C::S;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(tfull + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * 128, t0 = blockIdx.y * BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+        mbar_init(tfull, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % C::S;
+            const uint32_t ph = (uint32_t)((kb / C::S) & 1);
+            if (!mbar_wait(&empty[s], ph ^ 1, status)) break;
+            mbar_arrive_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
+            tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * 64, n0, &full[s]);
+            tma_load_2d(sB + s * C::B_BYTES, &tmB, kb * 64, t0, &full[s]);
+        }
+    } else if (warp == 1 && lane == 0) {
+        const uint32_t idesc = idesc_f16(128, BN, ab_bf16);
+        for (int kb = 0; kb < nk; ++kb) {
+            const int s = kb % C::S;
+            const uint32_t ph = (uint32_t)((kb / C::S) & 1);
+            if (!mbar_wait(&full[s], ph, status)) break;
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + s * C::A_BYTES), b0 = smem_u32(sB + s * C::B_BYTES);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                umma_f16(tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k), idesc, (kb | k) != 0);
+            umma_commit(&empty[s]);
+        }
+        umma_commit(tfull);
+    } else if (warp >= 2) {
+        if (mbar_wait(tfull, 0, status)) {
+            tc_fence_after();
+            tc_epilogue<BN>(ep, tmem, warp & 3, lane, n0, t0);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int BN>
+cudaError_t launch_dense(const CUtensorMap& a, const CUtensorMap& b, const TcEpilogue& ep, int nk, int ab_bf16,
+                         int* status, cudaStream_t s) {
+    using C = TcCfg<BN>;
+    auto k = dense_tc_kernel<BN>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)ceil_div(ep.N, 128), (unsigned)ceil_div(ep.M, BN));
+    k<<<grid, 192, C::SMEM, s>>>(a, b, ep, nk, ab_bf16, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int pick_bn(int64_t N, int64_t M, int num_sms) {
+    int best = 256;
+    double best_cost = 1e30;
+    for (int bn : {256, 128, 64, 32}) {
+        const int64_t tiles = ceil_div(N, 128) * ceil_div(M, bn);
+        const double cost = (double)ceil_div(tiles, num_sms) * (bn + 64);
+        if (cost < best_cost - 1e-9) { best_cost = cost; best = bn; }
+    }
+    return best;
+}
+
+size_t dense_workspace_bytes(int64_t N, int64_t K, int64_t M) {
+    (void)N;
+    return (size_t)(ceil_div(M * K * 2, 256) * 256);
+}
+
+int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
+                   const void* residual, void* y, int ydt, void* workspace, int num_sms, int* status,
+                   cudaStream_t stream) {
+    if (N > (int64_t)INT32_MAX || M > (int64_t)INT32_MAX) return GGUF_ERR_UNSUPPORTED;
+    const void* xb = x;
+    if (xdt != wdt) {
+        if (convert_activations(x, xdt, M, K, workspace, wdt, num_sms, stream) != cudaSuccess) return GGUF_ERR_CUDA;
+        xb = workspace;
+    }
+    const CUtensorMapDataType dt = wdt == GGUF_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int bn = pick_bn(N, M, num_sms);
+    CUtensorMap ta, tb;
+    int st = make_tmap_2d(&ta, wdense, dt, 2, (uint64_t)K, (uint64_t)N, (uint64_t)ld * 2, 64, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != GGUF_OK) return st;
+    st = make_tmap_2d(&tb, xb, dt, 2, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, (uint32_t)bn,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != GGUF_OK) return st;
+    TcEpilogue ep{residual, y, ydt, N, M};
+    const int nk = (int)(K / 64), bf = wdt == GGUF_DT_BF16 ? 1 : 0;
+    cudaError_t e;
+    switch (bn) {
+        case 256: e = launch_dense<256>(ta, tb, ep, nk, bf, status, stream); break;
+        case 128: e = launch_dense<128>(ta, tb, ep, nk, bf, status, stream); break;
+        case 64: e = launch_dense<64>(ta, tb, ep, nk, bf, status, stream); break;
+        default: e = launch_dense<32>(ta, tb, ep, nk, bf, status, stream); break;
+    }
+    return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
+}
+
+}  // namespace gg

@@ -1,0 +1,21 @@
+// Host entry points of the tensor-core GEMMs (fused decode-in-smem, and dense
+// on a decoded buffer).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace gg {
+
+size_t gemm_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t M);
+size_t dense_workspace_bytes(int64_t N, int64_t K, int64_t M);
+
+int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
+                   const void* residual, void* y, int ydt, void* workspace, int num_sms, int* status,
+                   cudaStream_t stream);
+
+int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
+                   const void* residual, void* y, int ydt, void* workspace, int num_sms, int* status,
+                   cudaStream_t stream);
+
+}  // namespace gg

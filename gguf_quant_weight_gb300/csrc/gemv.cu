@@ -1,0 +1,813 @@
+// Decode GEMV on GGUF blocks: Y[m, n] = sum_k X[m, k] W[n, k] (+ residual).
+//
+// OpenVINO PR #39119 "FullyConnectedGGUF", "Implementation", GEMV row: the
+// activations are quantized per 32 values to int8 (Q8-style, one f32 scale per
+// block) and every weight sub-block is dotted in integers straight against its
+// GGUF bytes; the float scales are applied once per sub-block.
+//
+// GB300 shape of it (two 256-thread CTAs per SM, rows of W dealt to warps):
+//  * at entry every warp requests the bytes of all its weight rows (up to a
+//    ring of R row slots in shared memory) with 16-byte coalesced async copies,
+//    so the whole matrix is in flight from the first microsecond; then the CTA
+//    tells the next kernel on the stream it may launch (programmatic dependent
+//    launch), so the next call's weight stream starts while this one finishes;
+//  * prologue, after waiting for the producer of X: the CTA quantizes the M
+//    activation rows into shared memory (codes, per-32 scale d_a, code sums);
+//  * a lane owns one "unit" of a row: half a 256-value super-block (or one
+//    Q8_0 block); a warp covers a whole row (or several rows when K is small);
+//    a lane's K slice never changes from row to row, so its activation codes
+//    and scales are loaded into registers once (M = 1, 2) or read from
+//    bank-conflict-free shared memory (larger M);
+//  * dp4a on 4 weights x 4 codes, integer sub-block scaling, one int->float per
+//    activation block, a (segmented) warp-shuffle reduction, and the residual
+//    Add fused into the store.
+#include "common.cuh"
+#include "gemv.cuh"
+#include <type_traits>
+
+namespace gg {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// Activation codes of row m live at qa + m*qa_row_stride(K), element k at byte
+// k + 16*(k/128): a lane reads the 16-byte pieces of one 128-value unit, and
+// the 16-byte pad after every 128 codes puts the 8 lanes of each quarter-warp
+// phase on different 4-bank groups (conflict-free 16-byte loads).
+__host__ __device__ constexpr int64_t qa_row_stride(int64_t K) { return K + 16 * ceil_div(K, 128); }
+__device__ __forceinline__ uint32_t qa_pos(uint32_t k) { return k + ((k >> 7) << 4); }
+
+// Per 32-value activation block and row: {d_a (f32), d_a * s (f32), s_lo, s_hi}
+// with s = sum of the 32 codes and s_lo / s_hi the sums of its two halves.
+struct Shared {
+    uint32_t qa;     // shared address of the codes
+    uint32_t ds;     // shared address of the per-block entries (16 bytes each)
+    uint32_t stage;  // shared address of the per-warp staging buffers
+    uint32_t qa_row; // bytes per code row
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+__device__ __forceinline__ float i2f(int v) { return (float)v; }
+
+// Nearest integer, halves away from zero, for |y| <= 127: truncate, then add
+// one unit when the (exact) remainder is at least one half.
+__device__ __forceinline__ int round_half_away(float y) {
+    const float a = fabsf(y);
+    const float t = truncf(a);
+    const int q = (int)t + (a - t >= 0.5f ? 1 : 0);
+    return y < 0.f ? -q : q;
+}
+
+__device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
+    return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
+}
+
+// ------------------------------------------------------------------ activation quantizer (prologue)
+// Per 32 values: amax, d_a = amax/127 (IEEE f32 divide), id = 1/d_a (0 for an
+// all-zero block), q = round-half-away(clamp(x*id, -127, 127)), s = sum q.
+template <int NT>
+__device__ void quantize_activations(const GemvParams& p, const Shared& sh) {
+    const int nb = (int)(p.K / 32);
+    const int total = p.M * nb;
+    for (int blk = threadIdx.x; blk < total; blk += NT) {
+        const int m = blk / nb, b = blk % nb;
+        const int64_t base = (int64_t)m * p.K + (int64_t)b * 32;
+        float v[32];
+        if (p.xdt == GGUF_DT_F32) {
+            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + base);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 t = src[i];
+                v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
+            }
+        } else {
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + base);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 t = src[i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t wv = comp(t, j), lo = wv & 0xFFFFu, hi = wv >> 16;
+                    if (p.xdt == GGUF_DT_BF16) {
+                        v[8 * i + 2 * j] = __uint_as_float(lo << 16);
+                        v[8 * i + 2 * j + 1] = __uint_as_float(hi << 16);
+                    } else {
+                        v[8 * i + 2 * j] = f16_bits_to_float(lo);
+                        v[8 * i + 2 * j + 1] = f16_bits_to_float(hi);
+                    }
+                }
+            }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const float d = amax / 127.0f;
+        const float id = d != 0.f ? 1.0f / d : 0.f;
+        int s_lo = 0, s_hi = 0;
+        uint32_t word[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            uint32_t wv = 0;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                float y = v[w * 4 + t] * id;
+                y = fminf(fmaxf(y, -127.f), 127.f);
+                const int q = round_half_away(y);
+                if (w < 4) s_lo += q; else s_hi += q;
+                wv |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * t);
+            }
+            word[w] = wv;
+        }
+        const uint32_t dst = sh.qa + (uint32_t)m * sh.qa_row + qa_pos(b * 32);
+        sts128(dst, make_uint4(word[0], word[1], word[2], word[3]));
+        sts128(dst + 16, make_uint4(word[4], word[5], word[6], word[7]));
+        sts128(sh.ds + 16u * (uint32_t)(m * nb + b),
+               make_uint4(__float_as_uint(d), __float_as_uint(d * (float)(s_lo + s_hi)), (uint32_t)s_lo,
+                          (uint32_t)s_hi));
+    }
+}
+
+// ------------------------------------------------------------------ per-lane activation slice
+// The codes (NQ/4 16-byte pieces) and block entries (NE) a lane needs for one
+// 128-value unit (NQ = 8, NE = 4) or one 32-value Q8_0 block (NQ = 2, NE = 1),
+// held in registers (REG) or read from shared memory on demand.
+template <int MT, bool REG, int NQ, int NE>
+struct ActSlice {
+    uint4 q[REG ? MT : 1][NQ];
+    uint4 e[REG ? MT : 1][NE];
+    uint32_t qa_base, ds_base, qa_row, ds_row;
+
+    __device__ __forceinline__ void init(const Shared& sh, int k0, int nb) {
+        qa_row = sh.qa_row;
+        ds_row = 16u * (uint32_t)nb;
+        qa_base = sh.qa + qa_pos((uint32_t)k0);
+        ds_base = sh.ds + 16u * (uint32_t)(k0 / 32);
+        if (REG) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) q[REG ? m : 0][i] = lds128(qa_base + m * qa_row + 16 * i);
+#pragma unroll
+                for (int b = 0; b < NE; ++b) e[REG ? m : 0][b] = lds128(ds_base + m * ds_row + 16 * b);
+            }
+        }
+    }
+    // 16 codes: elements 16i .. 16i+15 of the unit, row m
+    __device__ __forceinline__ uint4 codes(int m, int i) const {
+        if (REG) return q[REG ? m : 0][i];
+        return lds128(qa_base + m * qa_row + 16 * i);
+    }
+    __device__ __forceinline__ uint4 entry(int m, int b) const {
+        if (REG) return e[REG ? m : 0][b];
+        return lds128(ds_base + m * ds_row + 16 * b);
+    }
+};
+
+__device__ __forceinline__ void dump_D(const GemvParams& p, int m, int64_t n, int j, int sub, int v) {
+    p.dbg_D[((int64_t)m * p.N + n) * (p.K / sub) + j] = v;
+}
+
+// ------------------------------------------------------------------ Q4_K / Q5_K unit
+// Fragment: the 16-byte header (d, dmin, 12 scale bytes), qh (Q5_K) and the 64
+// qs bytes of half h.
+template <int QT>
+struct FragQ45 {
+    uint4 hdr;
+    uint4 qh[2];
+    uint4 qs[4];
+    // blk: shared address of the (16-byte aligned) block
+    __device__ __forceinline__ void load(uint32_t blk, int h) {
+        hdr = lds128(blk);
+        if (QT == GGUF_Q5_K) { qh[0] = lds128(blk + 16); qh[1] = lds128(blk + 32); }
+        const uint32_t q = blk + (QT == GGUF_Q5_K ? 48 : 16) + 64 * h;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qs[i] = lds128(q + 16 * i);
+    }
+};
+
+template <int QT, int MT, class A, bool DUMP>
+__device__ __forceinline__ void unit_q45k(const GemvParams& p, const FragQ45<QT>& f, const A& a, int kb, int h,
+                                          float acc[MT], int64_t n) {
+    const float d = f16_bits_to_float(f.hdr.x), dmin = f16_bits_to_float(f.hdr.x >> 16);
+    // 6-bit scales (scw) and mins (mnw) of the sub-blocks 4h..4h+3, one per byte
+    const uint32_t s0 = f.hdr.y, s1 = f.hdr.z, s2 = f.hdr.w;
+    const uint32_t scw = h ? ((s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u)) : (s0 & 0x3F3F3F3Fu);
+    const uint32_t mnw = h ? (((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u)) : (s1 & 0x3F3F3F3Fu);
+    float accd[MT], accm[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) accd[m] = accm[m] = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+        const int jj = 4 * h + 2 * pp;                 // sub-blocks jj (low nibbles) and jj+1 (high)
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t q = comp(f.qs[2 * pp + (i >> 2)], i);
+            lo[i] = q & 0x0F0F0F0Fu;
+            hi[i] = (q >> 4) & 0x0F0F0F0Fu;
+            if (QT == GGUF_Q5_K) {
+                // bit jj (resp. jj+1) of every qh byte rotated to bit 4 of that byte
+                const uint32_t hb = comp(f.qh[i >> 2], i);
+                lo[i] |= __funnelshift_l(hb, hb, (uint32_t)(4 - jj) & 31u) & 0x10101010u;
+                hi[i] |= __funnelshift_l(hb, hb, (uint32_t)(3 - jj) & 31u) & 0x10101010u;
+            }
+        }
+        const int sc0 = (scw >> (16 * pp)) & 0xFF, sc1 = (scw >> (16 * pp + 8)) & 0xFF;
+        const float mn0 = i2f((mnw >> (16 * pp)) & 0xFF), mn1 = i2f((mnw >> (16 * pp + 8)) & 0xFF);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < p.M) {
+                const uint4 l0 = a.codes(m, 4 * pp), l1 = a.codes(m, 4 * pp + 1);
+                const uint4 h0 = a.codes(m, 4 * pp + 2), h1 = a.codes(m, 4 * pp + 3);
+                int D0a = 0, D0b = 0, D1a = 0, D1b = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    D0a = dp4a(lo[i], comp(l0, i), D0a);
+                    D0b = dp4a(lo[4 + i], comp(l1, i), D0b);
+                    D1a = dp4a(hi[i], comp(h0, i), D1a);
+                    D1b = dp4a(hi[4 + i], comp(h1, i), D1b);
+                }
+                const int D0 = D0a + D0b, D1 = D1a + D1b;
+                const uint4 e0 = a.entry(m, 2 * pp), e1 = a.entry(m, 2 * pp + 1);
+                accd[m] += __uint_as_float(e0.x) * i2f(sc0 * D0) + __uint_as_float(e1.x) * i2f(sc1 * D1);
+                accm[m] += mn0 * __uint_as_float(e0.y) + mn1 * __uint_as_float(e1.y);
+                if (DUMP && p.dbg_D) {
+                    dump_D(p, m, n, kb * 8 + jj, 32, D0);
+                    dump_D(p, m, n, kb * 8 + jj + 1, 32, D1);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] += d * accd[m] - dmin * accm[m];
+}
+
+// ------------------------------------------------------------------ Q6_K unit
+struct FragQ6 {
+    uint4 ql[4];   // 64 bytes of ql for half h
+    uint4 qh[2];   // 32 bytes of qh for half h
+    uint2 sc;      // 8 scales for half h
+    uint32_t d;    // f16 bits
+};
+
+template <int MT, class A, bool DUMP>
+__device__ __forceinline__ void unit_q6k(const GemvParams& p, const FragQ6& f, const A& a, int kb, int h,
+                                         float acc[MT], int64_t n) {
+    const float d = f16_bits_to_float(f.d);
+    int sc[8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        sc[t] = (int)(int8_t)((f.sc.x >> (8 * t)) & 0xFF);
+        sc[4 + t] = (int)(int8_t)((f.sc.y >> (8 * t)) & 0xFF);
+    }
+    int S[MT][4];   // per activation block b (0..3 of the unit): sum of sc_t * D_t over its two sub-blocks
+#pragma unroll
+    for (int m = 0; m < MT; ++m) S[m][0] = S[m][1] = S[m][2] = S[m][3] = 0;
+#pragma unroll
+    for (int gp = 0; gp < 2; ++gp) {
+        // gp = 0: groups g = 0 (low nibbles) and g = 2 (high nibbles) of ql[0..31]
+        // gp = 1: groups g = 1 and g = 3 of ql[32..63]
+        uint32_t qlo[8], qhi[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t X = comp(f.ql[2 * gp + (i >> 2)], i), H = comp(f.qh[i >> 2], i);
+            qlo[i] = (X & 0x0F0F0F0Fu) | ((H << (4 - 2 * gp)) & 0x30303030u);
+            qhi[i] = ((X >> 4) & 0x0F0F0F0Fu) | ((H >> (2 * gp)) & 0x30303030u);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < p.M) {
+                const uint4 l0 = a.codes(m, 2 * gp), l1 = a.codes(m, 2 * gp + 1);
+                const uint4 h0 = a.codes(m, 4 + 2 * gp), h1 = a.codes(m, 5 + 2 * gp);
+                int Dl0 = 0, Dl1 = 0, Dh0 = 0, Dh1 = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    Dl0 = dp4a(qlo[i], comp(l0, i), Dl0);
+                    Dl1 = dp4a(qlo[4 + i], comp(l1, i), Dl1);
+                    Dh0 = dp4a(qhi[i], comp(h0, i), Dh0);
+                    Dh1 = dp4a(qhi[4 + i], comp(h1, i), Dh1);
+                }
+                const uint4 el = a.entry(m, gp), eh = a.entry(m, 2 + gp);
+                // dots of (q6 - 32): subtract 32 * (sum of the 16 activation codes)
+                Dl0 -= 32 * (int)el.z; Dl1 -= 32 * (int)el.w;
+                Dh0 -= 32 * (int)eh.z; Dh1 -= 32 * (int)eh.w;
+                S[m][gp] += sc[2 * gp] * Dl0 + sc[2 * gp + 1] * Dl1;
+                S[m][2 + gp] += sc[4 + 2 * gp] * Dh0 + sc[5 + 2 * gp] * Dh1;
+                if (DUMP && p.dbg_D) {
+                    dump_D(p, m, n, kb * 16 + 8 * h + 2 * gp, 16, Dl0);
+                    dump_D(p, m, n, kb * 16 + 8 * h + 2 * gp + 1, 16, Dl1);
+                    dump_D(p, m, n, kb * 16 + 8 * h + 4 + 2 * gp, 16, Dh0);
+                    dump_D(p, m, n, kb * 16 + 8 * h + 5 + 2 * gp, 16, Dh1);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (m < p.M) {
+            float u = 0.f;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) u += __uint_as_float(a.entry(m, b).x) * i2f(S[m][b]);
+            acc[m] += d * u;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ Q8_0 unit (from shared memory)
+template <int MT, class A, bool DUMP>
+__device__ __forceinline__ void unit_q8_0(const GemvParams& p, uint32_t blk, const A& a, int b, float acc[MT],
+                                          int64_t n) {
+    const float d = f16_bits_to_float(lds16(blk));
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = lds16(blk + 2 + 4 * i) | (lds16(blk + 4 + 4 * i) << 16);
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (m < p.M) {
+            const uint4 c0 = a.codes(m, 0), c1 = a.codes(m, 1);
+            int Da = 0, Db = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                Da = dp4a(q[i], comp(c0, i), Da);
+                Db = dp4a(q[4 + i], comp(c1, i), Db);
+            }
+            const int D = Da + Db;
+            acc[m] += d * (__uint_as_float(a.entry(m, 0).x) * i2f(D));
+            if (DUMP && p.dbg_D) dump_D(p, m, n, b, 32, D);
+        }
+    }
+}
+
+// Q6_K fragment of half h from a 2-byte-aligned raw block in shared memory.
+__device__ __forceinline__ void frag_q6_from_smem(FragQ6& f, uint32_t blk, int h) {
+    auto w32 = [&](uint32_t a) { return lds16(a) | (lds16(a + 2) << 16); };
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t q = blk + 64 * h + 16 * i;
+        f.ql[i] = make_uint4(w32(q), w32(q + 4), w32(q + 8), w32(q + 12));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t q = blk + 128 + 32 * h + 16 * i;
+        f.qh[i] = make_uint4(w32(q), w32(q + 4), w32(q + 8), w32(q + 12));
+    }
+    f.sc = make_uint2(w32(blk + 192 + 8 * h), w32(blk + 196 + 8 * h));
+    f.d = lds16(blk + 208);
+}
+
+// Q6_K fragment of half h from the plane pieces staged in shared memory.
+__device__ __forceinline__ void frag_q6_from_planes(FragQ6& f, uint32_t ql, uint32_t qh, uint32_t sc, uint32_t d,
+                                                    int h) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f.ql[i] = lds128(ql + 64 * h + 16 * i);
+    f.qh[0] = lds128(qh + 32 * h);
+    f.qh[1] = lds128(qh + 32 * h + 16);
+    f.sc = make_uint2(lds32(sc + 8 * h), lds32(sc + 8 * h + 4));
+    f.d = lds16(d);
+}
+
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Stages global bytes [lo, hi) of the weight buffer (total bytes) in shared
+// memory at dst, starting from the 16-byte boundary at or below lo: byte x
+// lands at dst + (x - (lo & ~15)).  The 16-byte-granular body goes as one 1-D
+// bulk (TMA) copy that completes its bytes on `bar`; the few bytes past the
+// last whole 16-byte piece of the buffer are stored by this thread.  Returns
+// the bulk byte count (the caller adds it to the barrier's expected bytes
+// before issuing).  Called by one lane.
+struct BulkPiece {
+    uint32_t dst;
+    const uint8_t* src;
+    uint32_t bytes;
+};
+__device__ __forceinline__ BulkPiece stage_range(uint32_t dst, const uint8_t* w, int64_t lo, int64_t hi,
+                                                 int64_t total) {
+    const int64_t a0 = lo & ~int64_t(15);
+    const int64_t e = min((hi + 15) & ~int64_t(15), total & ~int64_t(15));
+    for (int64_t x = max(e, a0); x < min(hi, total); ++x)
+        asm volatile("st.shared.u8 [%0], %1;" ::"r"(dst + (uint32_t)(x - a0)), "h"((unsigned short)w[x]));
+    return BulkPiece{dst, w + a0, e > a0 ? (uint32_t)(e - a0) : 0u};
+}
+
+// ------------------------------------------------------------------ the kernel
+// Row groups: a warp pass covers P rows (P = 32 / U when a row has U < 32
+// units, else 1); groups are dealt to warps round-robin.  Each warp stages its
+// groups through a ring of R slots of p.stage_bytes in shared memory.
+template <int QT, int MT, int LAYOUT, bool REG, bool DUMP>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
+    constexpr int NT = kThreads, NW = NT / 32;
+    constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
+    constexpr int NQ = QT == GGUF_Q8_0 ? 2 : 8, NE = QT == GGUF_Q8_0 ? 1 : 4;
+    constexpr int UV = QT == GGUF_Q8_0 ? 32 : 128;   // values per unit
+    constexpr int bb = QT == GGUF_Q8_0 ? 34 : QT == GGUF_Q4_K ? 144 : QT == GGUF_Q5_K ? 176 : 210;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nb = (int)(p.K / 32);
+    Shared sh;
+    sh.qa_row = (uint32_t)qa_row_stride(p.K);
+    sh.qa = smem_u32(smem_raw);
+    sh.ds = sh.qa + (uint32_t)p.M * sh.qa_row;
+    sh.stage = sh.ds + 16u * (uint32_t)(p.M * nb);
+
+    const int64_t row0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int64_t row_end = min(p.N, row0 + p.rows_per_cta);
+    const int U = (int)(p.K / UV);                  // units per row
+    const int seg = U < 32 ? U : 32;
+    const int P = U < 32 ? 32 / U : 1;              // rows per warp pass
+    const int64_t KB = p.K / 256, nblk = p.N * KB, total = p.N * p.rb;
+    const int u0 = U < 32 ? lane % U : lane;        // this lane's first unit
+    const int sub_row = U < 32 ? lane / U : 0;
+    const bool lane_on = U >= 32 || lane < P * U;
+    const int groups = row0 < row_end ? (int)ceil_div(row_end - row0, P) : 0;
+    const int R = p.stages;
+    const uint32_t ring = sh.stage + (uint32_t)(warp * R) * (uint32_t)p.stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + (sh.stage - sh.qa) + (size_t)NW * R * p.stage_bytes) +
+                     warp * R;
+    const int64_t pb = (int64_t)P * KB;             // blocks per group (planes)
+    if (lane == 0) {
+        for (int i = 0; i < R; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    // slot layout: raw bytes of the group's rows; or the four plane pieces
+    // QL | QH | SC | D of its pb blocks (D from its 16-byte boundary)
+    auto issue = [&](int g, int slot) {
+        if (lane != 0) return;
+        const int64_t r_begin = row0 + (int64_t)g * P;
+        const int64_t rows = min((int64_t)P, row_end - r_begin);
+        const uint32_t dst = ring + (uint32_t)slot * (uint32_t)p.stage_bytes;
+        BulkPiece pc[4];
+        int np = 0;
+        if (PLANES) {
+            const int64_t b0 = r_begin * KB, cb = rows * KB;
+            pc[np++] = stage_range(dst, p.w, 128 * b0, 128 * (b0 + cb), total);
+            pc[np++] = stage_range(dst + (uint32_t)(128 * pb), p.w, 128 * nblk + 64 * b0, 128 * nblk + 64 * (b0 + cb), total);
+            pc[np++] = stage_range(dst + (uint32_t)(192 * pb), p.w, 192 * nblk + 16 * b0, 192 * nblk + 16 * (b0 + cb), total);
+            pc[np++] = stage_range(dst + (uint32_t)(208 * pb), p.w, 208 * nblk + 2 * b0, 208 * nblk + 2 * (b0 + cb), total);
+        } else {
+            pc[np++] = stage_range(dst, p.w, r_begin * p.rb, (r_begin + rows) * p.rb, total);
+        }
+        uint32_t tx = 0;
+        for (int i = 0; i < np; ++i) tx += pc[i].bytes;
+        // the slot was last read through the generic proxy: order those reads
+        // before the bulk copy's writes
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[slot], tx);
+        for (int i = 0; i < np; ++i)
+            if (pc[i].bytes) bulk_g2s_u32(pc[i].dst, pc[i].src, pc[i].bytes, &bars[slot]);
+    };
+
+    // 1. request the first R groups of this warp
+    for (int i = 0; i < R && warp + i * NW < groups; ++i) issue(warp + i * NW, i);
+    pdl_launch_dependents();
+
+    // 2. activation prologue, once the producer of X has finished
+    pdl_wait();
+    quantize_activations<NT>(p, sh);
+    __syncthreads();
+    if (DUMP && blockIdx.x == 0) {
+        for (int64_t i = tid; i < (int64_t)p.M * p.K; i += NT) {
+            const uint32_t a = sh.qa + (uint32_t)(i / p.K) * sh.qa_row + qa_pos((uint32_t)(i % p.K));
+            if (p.dbg_qa) p.dbg_qa[i] = (int8_t)(lds32(a & ~3u) >> (8 * (a & 3)));
+        }
+        for (int i = tid; i < p.M * nb; i += NT) {
+            const uint4 e = lds128(sh.ds + 16u * i);
+            if (p.dbg_da) p.dbg_da[i] = __uint_as_float(e.x);
+            if (p.dbg_s) p.dbg_s[i] = (int32_t)(e.z + e.w);
+        }
+    }
+    ActSlice<MT, REG, NQ, NE> act;   // this lane's slice (its only unit when U <= 32)
+    act.init(sh, UV * u0, nb);
+    const bool single_unit = U <= 32;
+
+    // 3. rows
+    const int seg_end = (lane / seg) * seg + seg;   // one segment of lanes per row
+    const bool head = lane_on && (lane % seg) == 0;
+    const uint32_t rb32 = (uint32_t)p.rb;
+    int slot = 0;
+    uint32_t phase = 0;   // bit i: parity of the next completion of slot i
+    for (int g = warp; g < groups; g += NW) {
+        const int ok = mbar_wait(&bars[slot], (phase >> slot) & 1u, p.status) ? 1 : 0;
+        phase ^= 1u << slot;
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const uint32_t sbase = ring + (uint32_t)slot * (uint32_t)p.stage_bytes;
+        const int64_t r_begin = row0 + (int64_t)g * P;
+        const int64_t n = r_begin + sub_row;
+        const bool valid = lane_on && n < row_end;
+        float acc[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        if (valid) {
+            const uint32_t rowp = sbase + (uint32_t)((uint64_t)r_begin * p.rb & 15) + (uint32_t)sub_row * rb32;
+            for (int u = u0; u < U; u += (U < 32 ? U : 32)) {
+                const int kb = u >> 1, h = u & 1;
+                ActSlice<MT, false, NQ, NE> as;
+                if (!single_unit) as.init(sh, UV * u, nb);
+                if constexpr (QT == GGUF_Q8_0) {
+                    if (single_unit) unit_q8_0<MT, decltype(act), DUMP>(p, rowp + 34u * u, act, u, acc, n);
+                    else unit_q8_0<MT, decltype(as), DUMP>(p, rowp + 34u * u, as, u, acc, n);
+                } else if constexpr (QT == GGUF_Q6_K) {
+                    FragQ6 f;
+                    if constexpr (PLANES) {
+                        const uint32_t bi = (uint32_t)(sub_row * KB + kb);
+                        const uint32_t dq = sbase + (uint32_t)(208 * pb) + (uint32_t)(((r_begin * KB) * 2) & 15);
+                        frag_q6_from_planes(f, sbase + 128u * bi, sbase + (uint32_t)(128 * pb) + 64u * bi,
+                                            sbase + (uint32_t)(192 * pb) + 16u * bi, dq + 2u * bi, h);
+                    } else {
+                        frag_q6_from_smem(f, rowp + 210u * kb, h);
+                    }
+                    if (single_unit) unit_q6k<MT, decltype(act), DUMP>(p, f, act, kb, h, acc, n);
+                    else unit_q6k<MT, decltype(as), DUMP>(p, f, as, kb, h, acc, n);
+                } else {
+                    FragQ45<QT> f;
+                    f.load(rowp + (uint32_t)(bb * kb), h);
+                    if (single_unit) unit_q45k<QT, MT, decltype(act), DUMP>(p, f, act, kb, h, acc, n);
+                    else unit_q45k<QT, MT, decltype(as), DUMP>(p, f, as, kb, h, acc, n);
+                }
+            }
+        }
+        // refill this slot with the group R passes ahead, once every lane is done with it
+        __syncwarp();
+        if (g + R * NW < groups) issue(g + R * NW, slot);
+        if (++slot == R) slot = 0;
+        if (seg == 32) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+            }
+        } else {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float t = __shfl_down_sync(0xffffffffu, acc[m], o);
+                    if (lane + o < seg_end) acc[m] += t;
+                }
+            }
+        }
+        if (head && valid) {
+            for (int m = 0; m < p.M && m < MT; ++m) {
+                float v = acc[m];
+                if (p.residual) v += load_act(p.residual, p.ydt, (int64_t)m * p.N + n);
+                store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ direct-load kernel
+// For the layouts whose unit fields are 16-byte aligned (Q4_K, Q5_K blocks and
+// the Q6_K planes): each lane fetches exactly its unit's bytes with 128-bit
+// loads straight into registers, one (row, unit) item ahead of the one it
+// computes; the first item is requested before waiting on the producer of X.
+__device__ __forceinline__ uint4 ldg128(const uint8_t* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint2 ldg64(const uint8_t* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ uint32_t ldg16(const uint8_t* p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+template <int QT>
+__device__ __forceinline__ void load_global(FragQ45<QT>& f, const uint8_t* blk, int h) {
+    f.hdr = ldg128(blk);
+    if (QT == GGUF_Q5_K) { f.qh[0] = ldg128(blk + 16); f.qh[1] = ldg128(blk + 32); }
+    const uint8_t* q = blk + (QT == GGUF_Q5_K ? 48 : 16) + 64 * h;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f.qs[i] = ldg128(q + 16 * i);
+}
+
+__device__ __forceinline__ void load_global_planes(FragQ6& f, const uint8_t* w, int64_t nblk, int64_t b, int h) {
+    const uint8_t* ql = w + 128 * b + 64 * h;
+    const uint8_t* qh = w + 128 * nblk + 64 * b + 32 * h;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f.ql[i] = ldg128(ql + 16 * i);
+    f.qh[0] = ldg128(qh);
+    f.qh[1] = ldg128(qh + 16);
+    f.sc = ldg64(w + 192 * nblk + 16 * b + 8 * h);
+    f.d = ldg16(w + 208 * nblk + 2 * b);
+}
+
+constexpr int kDirectThreads = 512;   // one CTA of 16 warps per SM
+
+template <int QT, int MT, bool DUMP>
+__global__ void __launch_bounds__(kDirectThreads, 1) gemv_direct_kernel(const GemvParams p) {
+    constexpr int NT = kDirectThreads, NW = NT / 32;
+    constexpr int bb = QT == GGUF_Q4_K ? 144 : QT == GGUF_Q5_K ? 176 : 210;
+    using Frag = typename std::conditional<QT == GGUF_Q6_K, FragQ6, FragQ45<QT == GGUF_Q6_K ? GGUF_Q4_K : QT>>::type;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nb = (int)(p.K / 32);
+    Shared sh;
+    sh.qa_row = (uint32_t)qa_row_stride(p.K);
+    sh.qa = smem_u32(smem_raw);
+    sh.ds = sh.qa + (uint32_t)p.M * sh.qa_row;
+    sh.stage = 0;
+
+    const int64_t row0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int64_t row_end = min(p.N, row0 + p.rows_per_cta);
+    const int U = (int)(p.K / 128);                 // units per row
+    const int seg = U < 32 ? U : 32;
+    const int P = U < 32 ? 32 / U : 1;              // rows per warp pass
+    const int ustep = U < 32 ? U : 32;
+    const int64_t KB = p.K / 256, nblk = p.N * KB;
+    const int u0 = U < 32 ? lane % U : lane;
+    const int sub_row = U < 32 ? lane / U : 0;
+    const bool lane_on = U >= 32 || lane < P * U;
+    const int groups = row0 < row_end ? (int)ceil_div(row_end - row0, P) : 0;
+
+    Frag cur, nxt;
+    auto fetch = [&](Frag& f, int g, int u) {
+        const int64_t n = row0 + (int64_t)g * P + sub_row;
+        if (!lane_on || n >= row_end) return;
+        const int kb = u >> 1, h = u & 1;
+        if constexpr (QT == GGUF_Q6_K) load_global_planes(f, p.w, nblk, n * KB + kb, h);
+        else load_global<QT>(f, p.w + n * p.rb + (int64_t)kb * bb, h);
+    };
+    int g = warp, u = u0;
+    if (g < groups) fetch(cur, g, u);
+    pdl_launch_dependents();
+
+    pdl_wait();
+    quantize_activations<NT>(p, sh);
+    __syncthreads();
+    if (DUMP && blockIdx.x == 0) {
+        for (int64_t i = tid; i < (int64_t)p.M * p.K; i += NT) {
+            const uint32_t a = sh.qa + (uint32_t)(i / p.K) * sh.qa_row + qa_pos((uint32_t)(i % p.K));
+            if (p.dbg_qa) p.dbg_qa[i] = (int8_t)(lds32(a & ~3u) >> (8 * (a & 3)));
+        }
+        for (int i = tid; i < p.M * nb; i += NT) {
+            const uint4 e = lds128(sh.ds + 16u * i);
+            if (p.dbg_da) p.dbg_da[i] = __uint_as_float(e.x);
+            if (p.dbg_s) p.dbg_s[i] = (int32_t)(e.z + e.w);
+        }
+    }
+    const bool single_unit = U <= 32;
+    ActSlice<MT, false, 8, 4> fixed;
+    fixed.init(sh, 128 * u0, nb);
+    const int seg_end = (lane / seg) * seg + seg;
+    const bool head = lane_on && (lane % seg) == 0;
+
+    float acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    while (g < groups) {
+        int gn = g, un = u + ustep;
+        if (un >= U) { un = u0; gn = g + NW; }
+        if (gn < groups) fetch(nxt, gn, un);
+        const int64_t n = row0 + (int64_t)g * P + sub_row;
+        const bool valid = lane_on && n < row_end;
+        if (valid) {
+            ActSlice<MT, false, 8, 4> moving;
+            if (!single_unit) moving.init(sh, 128 * u, nb);
+            const ActSlice<MT, false, 8, 4>& a = single_unit ? fixed : moving;
+            const int kb = u >> 1, h = u & 1;
+            if constexpr (QT == GGUF_Q6_K) unit_q6k<MT, ActSlice<MT, false, 8, 4>, DUMP>(p, cur, a, kb, h, acc, n);
+            else unit_q45k<QT, MT, ActSlice<MT, false, 8, 4>, DUMP>(p, cur, a, kb, h, acc, n);
+        }
+        if (gn != g) {
+            if (seg == 32) {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+                }
+            } else {
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float t = __shfl_down_sync(0xffffffffu, acc[m], o);
+                        if (lane + o < seg_end) acc[m] += t;
+                    }
+                }
+            }
+            if (head && valid) {
+                for (int m = 0; m < p.M && m < MT; ++m) {
+                    float v = acc[m];
+                    if (p.residual) v += load_act(p.residual, p.ydt, (int64_t)m * p.N + n);
+                    store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+        }
+        cur = nxt;
+        g = gn;
+        u = un;
+    }
+}
+
+template <int QT, int MT, int LAYOUT, bool DUMP>
+cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
+    const int U = (int)(p.K / (QT == GGUF_Q8_0 ? 32 : 128));
+    auto k = gemv_kernel<QT, MT, LAYOUT, false, DUMP>;
+    if constexpr (MT == 1) {
+        if (U <= 32) k = gemv_kernel<QT, MT, LAYOUT, true, DUMP>;
+    }
+    if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K || (QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES)) {
+        if (p.direct) k = gemv_direct_kernel<QT, MT, DUMP>;
+    }
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(p.direct ? kDirectThreads : kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+template <int QT, int LAYOUT, bool DUMP>
+cudaError_t launch_mt(const GemvParams& p, int grid, size_t smem, cudaStream_t s) {
+    if (p.M <= 1) return launch_one<QT, 1, LAYOUT, DUMP>(p, grid, smem, s);
+    if (p.M <= 2) return launch_one<QT, 2, LAYOUT, DUMP>(p, grid, smem, s);
+    if (p.M <= 4) return launch_one<QT, 4, LAYOUT, DUMP>(p, grid, smem, s);
+    return launch_one<QT, 8, LAYOUT, DUMP>(p, grid, smem, s);
+}
+
+template <bool DUMP>
+cudaError_t launch_dispatch(const GemvParams& p, int grid, size_t smem, cudaStream_t s) {
+    switch (p.qtype) {
+        case GGUF_Q8_0: return launch_mt<GGUF_Q8_0, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
+        case GGUF_Q4_K: return launch_mt<GGUF_Q4_K, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
+        case GGUF_Q5_K: return launch_mt<GGUF_Q5_K, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
+        case GGUF_Q6_K:
+            return p.layout == GGUF_LAYOUT_Q6K_PLANES
+                       ? launch_mt<GGUF_Q6_K, GGUF_LAYOUT_Q6K_PLANES, DUMP>(p, grid, smem, s)
+                       : launch_mt<GGUF_Q6_K, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem) {
+    const int bv = p.qtype == GGUF_Q8_0 ? 32 : 256;
+    const int bb = p.qtype == GGUF_Q8_0 ? 34 : p.qtype == GGUF_Q4_K ? 144 : p.qtype == GGUF_Q5_K ? 176 : 210;
+    p.rb = p.K / bv * bb;
+    const int64_t nb32 = p.K / 32;
+    const int64_t act = p.M * qa_row_stride(p.K) + p.M * nb32 * 16;
+    const int U = (int)(p.K / (p.qtype == GGUF_Q8_0 ? 32 : 128));
+    const int64_t P = U < 32 ? 32 / U : 1;
+    const int NW = kThreads / 32;
+    // a slot holds one row group plus 16-byte alignment slack (the D plane
+    // piece of the planes layout gets its own slack)
+    p.stage_bytes = ceil_div(P * p.rb + 48, 16) * 16;
+    // one CTA per SM; it keeps to half of the shared memory so that a CTA of
+    // the next call on the stream (programmatic dependent launch) fits beside it
+    const int64_t rpc = ceil_div(p.N, (int64_t)num_sms);
+    const int64_t groups_per_warp = ceil_div(ceil_div(rpc, P), NW);
+    const int64_t half = std::min<int64_t>(max_smem, 232448 / 2 - 1024);
+    int64_t R = std::min<int64_t>({groups_per_warp, 8, (half - act) / (NW * p.stage_bytes)});
+    if (R < 1) R = std::min<int64_t>({groups_per_warp, 8, (max_smem - act) / (NW * p.stage_bytes)});
+    if (R < 1) return GGUF_ERR_UNSUPPORTED;
+    p.stages = (int)R;
+    p.direct = (p.qtype == GGUF_Q4_K || p.qtype == GGUF_Q5_K ||
+                (p.qtype == GGUF_Q6_K && p.layout == GGUF_LAYOUT_Q6K_PLANES)) ? 1 : 0;
+    p.rows_per_cta = rpc;
+    p.chunk_rows = 0;
+    *grid = (int)ceil_div(p.N, rpc);
+    *smem = p.direct ? (size_t)act : (size_t)(act + NW * R * p.stage_bytes + NW * R * 8);
+    return GGUF_OK;
+}
+
+cudaError_t gemv_launch(const GemvParams& p, int grid, size_t smem, bool dump, cudaStream_t stream) {
+    return dump ? launch_dispatch<true>(p, grid, smem, stream) : launch_dispatch<false>(p, grid, smem, stream);
+}
+
+}  // namespace gg

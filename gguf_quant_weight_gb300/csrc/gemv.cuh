@@ -1,0 +1,39 @@
+// Host-visible parameters of the decode GEMV kernel.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <algorithm>
+
+namespace gg {
+
+struct GemvParams {
+    const uint8_t* w;
+    int qtype, layout;
+    int64_t N, K;
+    const void* x;
+    int xdt, M;
+    const void* residual;
+    void* y;
+    int ydt;
+    int* status;
+    int pdl;               // launch with programmatic stream serialization
+    int direct;            // unit fields 16-byte aligned: load straight into registers
+    // plan (filled by gemv_plan)
+    int64_t rb;            // bytes per weight row (raw layout)
+    int64_t rows_per_cta;  // rows owned by one CTA
+    int chunk_rows;        // rows per staged chunk
+    int stages;            // chunk buffers in shared memory
+    int64_t stage_bytes;
+    // test-only dumps (nullptr in production)
+    int8_t* dbg_qa;
+    float* dbg_da;
+    int32_t* dbg_s;
+    int32_t* dbg_D;
+};
+
+// Fills the plan fields; returns GGUF_OK or GGUF_ERR_UNSUPPORTED when the
+// activations and one chunk do not fit in max_smem bytes of shared memory.
+int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem);
+cudaError_t gemv_launch(const GemvParams& p, int grid, size_t smem, bool dump, cudaStream_t stream);
+
+}  // namespace gg

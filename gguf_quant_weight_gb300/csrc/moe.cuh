@@ -1,0 +1,15 @@
+// Host entry points of the MoE expert GEMM (mul_mm_id).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stddef.h>
+
+namespace gg {
+
+size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k);
+
+int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
+            int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
+            int num_sms, int* status, cudaStream_t stream);
+
+}  // namespace gg

@@ -1,0 +1,183 @@
+/*
+ * gguf_mm.h -- C ABI of libgguf_mm.so: matrix multiplication run directly on
+ * GGUF block-quantized weights on one NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is DEVICE memory owned by the caller, unless the
+ *    argument says otherwise.  The library never frees, retains or caches a
+ *    caller pointer past the call.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and the call returns without a host synchronisation.  A returned
+ *    GGUF_OK means the work was validated and launched; device-side failures
+ *    (a bounded wait that expired) are reported later by gguf_mm_check_errors().
+ *  - Matrices are row-major and contiguous.  X is [M, K], Y is [M, N]; the
+ *    optional residual has Y's dtype and shape and may alias Y.
+ *  - A weight tensor W[N, K] stays in GGUF byte blocks: row n is the K/blk
+ *    blocks covering W[n, 0..K) back to back, i.e. a [N, K/blk*block_bytes] u8
+ *    array (OpenVINO PR #39119 "FullyConnectedGGUF", "Why a new primitive").
+ *  - Block structs (GGUF on-disk layout; GGUF Support Proposal for mobius,
+ *    sections 1.2 and 7): Q8_0 34 B / 32 values {d f16, qs[32] i8}, w = d*q;
+ *    Q4_K 144 B / 256 {d, dmin f16, scales[12], qs[128]}; Q5_K 176 B / 256
+ *    {d, dmin, scales[12], qh[32], qs[128]}; for both w = d*sc_j*q - dmin*m_j
+ *    (OpenVINO PR #38696 "Details"); Q6_K 210 B / 256 {ql[128], qh[64],
+ *    scales[16] i8, d f16}, w = d*scales[j]*(q6 - 32).
+ *  - Alignment: w, x, y, residual and workspace must be 16-byte aligned.
+ *  - All entry points are thread-safe with respect to the host; calls that
+ *    share a workspace must be ordered on one stream.
+ *
+ * Status codes: 0 = OK, negative = error (see gguf_status).  Argument errors
+ * are detected on the host before anything is launched.
+ */
+#ifndef GGUF_MM_H
+#define GGUF_MM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gguf_stream_t; /* same type as cudaStream_t */
+
+typedef enum { GGUF_Q8_0 = 8, GGUF_Q4_K = 12, GGUF_Q5_K = 13, GGUF_Q6_K = 14 } gguf_qtype;
+
+/* GGUF_LAYOUT_Q6K_PLANES: the Q6_K tensor regrouped once into
+ * QL[nblk][128] | QH[nblk][64] | SC[nblk][16] | D[nblk] (2 bytes each), same
+ * size and contents as the blocks (OpenVINO PR #39119, "Transformation"). */
+typedef enum { GGUF_LAYOUT_BLOCKS = 0, GGUF_LAYOUT_Q6K_PLANES = 1 } gguf_layout;
+
+typedef enum { GGUF_DT_F32 = 0, GGUF_DT_F16 = 1, GGUF_DT_BF16 = 2 } gguf_dtype;
+
+/* Execution path of gguf_mm_gemm (OpenVINO PR #39119, "Implementation": the
+ * path follows the activation row count; an internal option forces a path).
+ * AUTO: M < 8 or f32 activations -> GEMV, otherwise the fused tensor-core GEMM. */
+typedef enum { GGUF_PATH_AUTO = 0, GGUF_PATH_GEMV = 1, GGUF_PATH_FUSED = 2 } gguf_path;
+
+typedef enum {
+    GGUF_OK = 0,
+    GGUF_ERR_INVALID_ARG = -1,  /* null pointer, non-positive size, K not a multiple of the block */
+    GGUF_ERR_UNSUPPORTED = -2,  /* type / layout / dtype / size combination not implemented */
+    GGUF_ERR_MISALIGNED = -3,   /* a pointer is not 16-byte aligned */
+    GGUF_ERR_WORKSPACE = -4,    /* workspace missing or smaller than gguf_mm_workspace_size() */
+    GGUF_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed */
+    GGUF_ERR_TIMEOUT = -6,      /* a bounded device-side wait expired (reported by check_errors) */
+    GGUF_ERR_NO_DEVICE = -7     /* no sm_103 device current */
+} gguf_status;
+
+typedef enum { GGUF_OP_GEMV = 0, GGUF_OP_GEMM = 1, GGUF_OP_ID = 2, GGUF_OP_DENSE = 3 } gguf_op;
+
+/* Bytes of device workspace the given call needs (0 = none; pass NULL then).
+ * op GGUF_OP_GEMV/GEMM take (t, N, K, M); GGUF_OP_ID takes all arguments with M
+ * the token count T; GGUF_OP_DENSE takes (N, K, M).  Returns 0 for invalid input. */
+size_t gguf_mm_workspace_size(int op, int qtype, int64_t N, int64_t K, int64_t M,
+                              int64_t n_expert, int64_t top_k);
+
+/* Decode GEMV: Y[m, n] = sum_k X[m, k] * W[n, k] (+ residual[m, n]) for M <= 8.
+ * (OpenVINO PR #39119, "Implementation", GEMV row: activations are quantized per
+ * 32 values to int8 with one f32 scale per block -- d_a = amax/127, q =
+ * round(x/d_a) -- and every weight sub-block is dotted in integers against them.)
+ *   w        [N, K/blk*bb] u8 blocks, or Q6_K planes when layout = PLANES
+ *   qtype    GGUF_Q8_0 / Q4_K / Q5_K / Q6_K;  K % 256 == 0 (K % 32 for Q8_0)
+ *   x        [M, K] of xdt (F32, F16 or BF16), 1 <= M <= 8
+ *   residual [M, N] of ydt or NULL;  y [M, N] of ydt
+ *   workspace / ws_bytes: unused (may be NULL / 0)
+ * Errors: INVALID_ARG, UNSUPPORTED (M > 8, M*K too large for on-chip staging),
+ * MISALIGNED, CUDA.
+ * Weights are static inputs: the kernel is launched with programmatic
+ * dependent launch and starts fetching w while the kernel before it on the
+ * stream may still be running (x and residual are read, and y written, only
+ * after that kernel has finished).  So w must be complete before the preceding
+ * kernel on the stream starts; a weight written by a kernel right before this
+ * call needs a stream/event synchronization in between, or GGUF_MM_PDL=0 in the
+ * environment, which turns the early fetch off. */
+int gguf_mm_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K,
+                 const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
+                 void* workspace, size_t ws_bytes, gguf_stream_t stream);
+
+/* Prefill GEMM (or GEMV when the path says so), same arguments and semantics as
+ * gguf_mm_gemv plus `path` (gguf_path) and any M >= 1.  The fused path stages
+ * weight blocks in shared memory, decodes each 256-value block once to f16 and
+ * feeds it to tcgen05 tensor-core MMAs with TMEM accumulators; activations are
+ * converted to f16 into the workspace first (OpenVINO PR #39119,
+ * "Implementation", DPAS prefill row: decode each block once, reuse it across
+ * activation rows, overlap loading with decoding, tile grows with M).
+ * Workspace: gguf_mm_workspace_size(GGUF_OP_GEMM, ...) bytes. */
+int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K,
+                 const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
+                 void* workspace, size_t ws_bytes, int path, gguf_stream_t stream);
+
+/* MoE expert GEMM (llama.cpp PR #28301 "metal : skip the empty half of the
+ * mul_mm_id token tile", "Overview"): for every token t and slot k,
+ *   Y[t, k, :] = X[t, :] . W_{ids[t, k]}^T (+ residual[t, k, :]).
+ *   w_experts n_expert weight tensors [N, K/blk*bb] back to back (Q4_K/Q5_K/Q6_K/Q8_0 blocks)
+ *   x [T, K] of xdt (F16 or BF16); ids [T, top_k] int32 (device), each in [0, n_expert)
+ *   residual [T, top_k, N] of ydt or NULL;  y [T, top_k, N] of ydt (F32, F16, BF16)
+ * Rows are grouped by expert on the device; each (expert, 128-row weight tile,
+ * token tile) issues MMAs only for round_up(rows, 16) token columns, so the
+ * empty part of an underfilled token tile costs nothing.  Ids outside
+ * [0, n_expert) are skipped (their Y rows are left untouched).
+ * Workspace: gguf_mm_workspace_size(GGUF_OP_ID, ...) bytes. */
+int gguf_mm_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K,
+               const void* x, int xdt, int64_t T, const int32_t* ids, int64_t top_k,
+               const void* residual, void* y, int ydt,
+               void* workspace, size_t ws_bytes, gguf_stream_t stream);
+
+/* Q6_K plane regrouping (OpenVINO PR #39119, "Transformation"): blocks ->
+ * QL[nblk][128] | QH[nblk][64] | SC[nblk][16] | D[nblk][2] (inverse = 0), or
+ * back (inverse = 1).  src and dst are 210*nblk bytes each and must not
+ * overlap; blocks are in row-major (n, kb) order.  Done once per weight. */
+int gguf_repack_q6k_planes(const void* src, void* dst, int64_t nblk, int inverse,
+                           gguf_stream_t stream);
+
+/* Decode-once to a K-padded buffer (ROCm llama.cpp PR #37 "one-time K-padded
+ * f16 dequantization for prefill GEMMs", "How it works"): out[n, k] = w[n, k]
+ * rounded to odt (F16 or BF16) for k < K and 0 for K <= k < ld.  ld >= K, ld % 8
+ * == 0; ld = K + 64 pads each row by one 128-byte line. */
+int gguf_dequant_padded(const void* w, int qtype, int layout, int64_t N, int64_t K,
+                        void* out, int odt, int64_t ld, gguf_stream_t stream);
+
+/* Dense tensor-core GEMM on a decoded weight: Y[m, n] = sum_k X[m, k] * Wd[n, k]
+ * (+ residual), Wd [N, ld] of wdt (F16 or BF16), X [M, K] of xdt (F16/BF16);
+ * activations are converted to wdt into the workspace first
+ * (gguf_mm_workspace_size(GGUF_OP_DENSE, 0, N, K, M, 0, 0) bytes).
+ * K % 64 == 0, ld % 8 == 0. */
+int gguf_dense_gemm(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K,
+                    const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
+                    void* workspace, size_t ws_bytes, gguf_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device status word of the
+ * current device: GGUF_OK, GGUF_ERR_TIMEOUT (a bounded wait in a kernel expired;
+ * that kernel's outputs are undefined), or GGUF_ERR_CUDA for a pending CUDA error. */
+int gguf_mm_check_errors(gguf_stream_t stream);
+
+/* Static string for a status code. */
+const char* gguf_mm_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int gguf_mm_version(void);
+
+/* Test hook: runs the GEMV kernel of gguf_mm_gemv in a build that also writes
+ * its integer intermediates, so they can be compared bit for bit with a CPU
+ * restatement: qa [M, K] i8, d_a [M, K/32] f32 and s [M, K/32] i32 from the
+ * activation quantizer (taken from the first CTA), and the integer sub-block
+ * dots D [M, N, K/sub] i32, sub = 16 for Q6_K and 32 otherwise.  Q6_K dots are
+ * of (q6 - 32), Q4_K/Q5_K of the unsigned quant, Q8_0 of the signed quant.
+ * Any debug pointer may be NULL.  Also writes y like gguf_mm_gemv. */
+int gguf_mm_debug_gemv_terms(const void* w, int qtype, int layout, int64_t N, int64_t K,
+                             const void* x, int xdt, int64_t M, void* y, int ydt,
+                             int8_t* qa, float* d_a, int32_t* s, int32_t* D,
+                             gguf_stream_t stream);
+
+/* Test hook for the bounded device waits: launches a kernel whose wait on an
+ * mbarrier that nothing completes gives up after about `spin_limit` polls and
+ * records GGUF_ERR_TIMEOUT in the device status word (read it with
+ * gguf_mm_check_errors).  No GPU fault is involved. */
+int gguf_mm_debug_timeout(int64_t spin_limit, gguf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GGUF_MM_H */

@@ -1,0 +1,64 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/gguf_mm.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gguf_quant_weight_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "gguf_mm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z_0-9]*\s*\*?\s*(gguf_[a-z0-9_]+)\s*\(", src,
+                                 flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gguf_quant_weight_gb300 import _build
+    _build.build()
+    return g.load_library()
+
+
+def test_header_lists_the_entry_points():
+    names = _declared()
+    for n in ("gguf_mm_gemv", "gguf_mm_gemm", "gguf_mm_id", "gguf_repack_q6k_planes", "gguf_dequant_padded",
+              "gguf_dense_gemm", "gguf_mm_check_errors", "gguf_mm_workspace_size"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert name in g.exported_symbols(), f"binding lacks {name}"
+
+
+def test_version_and_status_strings(lib):
+    assert g.gguf_mm_version() >= 100
+    assert g.status_string(0) == "ok"
+    assert "aligned" in g.status_string(g.GGUF_ERR_MISALIGNED)
+
+
+def test_argument_errors_need_no_gpu(lib):
+    # null pointers / bad sizes / bad types are rejected before any CUDA call
+    f = g.raw_status
+    assert f("gguf_mm_gemv", None, 12, 0, 4, 256, None, 2, 1, None, None, 2, None, 0, None) == g.GGUF_ERR_INVALID_ARG
+    assert f("gguf_mm_gemv", 16, 12, 0, 4, 100, 16, 2, 1, None, 16, 2, None, 0, None) == g.GGUF_ERR_INVALID_ARG
+    assert f("gguf_mm_gemv", 16, 99, 0, 4, 256, 16, 2, 1, None, 16, 2, None, 0, None) == g.GGUF_ERR_UNSUPPORTED
+    assert f("gguf_mm_gemv", 16, 12, 1, 4, 256, 16, 2, 1, None, 16, 2, None, 0, None) == g.GGUF_ERR_UNSUPPORTED
+    assert f("gguf_mm_gemv", 18, 12, 0, 4, 256, 16, 2, 1, None, 16, 2, None, 0, None) == g.GGUF_ERR_MISALIGNED
+    assert f("gguf_mm_gemm", 16, 12, 0, 4, 256, 16, 2, 8, None, 16, 2, None, 0, 9, None) == g.GGUF_ERR_INVALID_ARG
+    assert f("gguf_repack_q6k_planes", 16, 16, 4, 0, None) == g.GGUF_ERR_INVALID_ARG
+    assert f("gguf_dequant_padded", 16, 8, 0, 4, 64, 16, 2, 60, None) == g.GGUF_ERR_INVALID_ARG
+    assert f("gguf_dense_gemm", 16, 1, 256, 4, 200, 16, 1, 8, None, 16, 2, None, 0, None) == g.GGUF_ERR_INVALID_ARG
+    assert f("gguf_mm_id", 16, 12, 0, 4, 256, 16, 2, 8, None, 8, None, 16, 2, None, 0, None) == g.GGUF_ERR_INVALID_ARG
+
+
+def test_workspace_sizes_are_consistent(lib):
+    assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 13, 4096, 4096, 1) == 0
+    assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 13, 4096, 4096, 0) == 0
