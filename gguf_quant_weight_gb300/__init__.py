@@ -42,6 +42,8 @@ _SIGS = {
     "gguf_dequant_padded": (_c_int, [_c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp]),
     "gguf_dense_gemm": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_vp,
                                  _c_int, _c_vp, _c_sz, _c_vp]),
+    "gguf_dense_gemm_noalloc": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp,
+                                         _c_vp, _c_int, _c_vp]),
     "gguf_mm_check_errors": (_c_int, [_c_vp]),
     "gguf_mm_status_string": (ctypes.c_char_p, [_c_int]),
     "gguf_mm_version": (_c_int, []),
@@ -146,6 +148,11 @@ def gguf_dequant_padded(w, qtype, layout, N, K, out, odt, ld, stream=None):
 def gguf_dense_gemm(wdense, wdt, ld, N, K, x, xdt, M, residual, y, ydt, workspace=None, ws_bytes=0, stream=None):
     return _check("gguf_dense_gemm", load_library().gguf_dense_gemm(
         _p(wdense), wdt, ld, N, K, _p(x), xdt, M, _p(residual), _p(y), ydt, _p(workspace), ws_bytes, _s(stream)))
+
+
+def gguf_dense_gemm_noalloc(wdense, wdt, ld, N, K, x, xdt, M, residual, y, ydt, stream=None):
+    return _check("gguf_dense_gemm_noalloc", load_library().gguf_dense_gemm_noalloc(
+        _p(wdense), wdt, ld, N, K, _p(x), xdt, M, _p(residual), _p(y), ydt, _s(stream)))
 
 
 def gguf_mm_check_errors(stream=None) -> int:

@@ -134,6 +134,15 @@ __global__ void timeout_probe_kernel(long long limit, int* status) {
 
 }  // namespace
 
+int gg::current_device_launch_facts(int* num_sms, int** status) {
+    DeviceFacts* f = nullptr;
+    const int st = facts(&f);
+    if (st != GGUF_OK) return st;
+    *num_sms = f->num_sms;
+    *status = f->status;
+    return GGUF_OK;
+}
+
 extern "C" {
 
 int gguf_mm_version(void) { return 100; }

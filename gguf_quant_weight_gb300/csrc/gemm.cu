@@ -19,6 +19,8 @@
 // llama.cpp PR #37 "one-time K-padded f16 dequantization for prefill GEMMs",
 // "How it works": decode once into a K-padded buffer, then a plain GEMM with
 // the padded leading dimension) and the activation conversion pass.
+#include <mutex>
+
 #include "tc_gemm.cuh"
 
 namespace gg {
@@ -231,3 +233,66 @@ int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K
 }
 
 }  // namespace gg
+
+namespace gg {
+
+// ------------------------------------------------------------------ allocation-free variant of the dense GEMM
+//
+// Some callers hand this library only their input and output buffers and may
+// not obtain device memory at all: code embedded in a host program that owns
+// every device allocation through its own fixed pool, or code running where a
+// cudaMalloc would implicitly synchronize the device and stall the other work
+// in flight.  For them gguf_dense_gemm_noalloc keeps its scratch (the
+// activations converted to the weight's 16-bit type) in the array below, which
+// is part of this library's device image: every GPU that loads the library
+// holds these 8 MiB until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) uint8_t g_dense_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_scratch_ptr[64];
+
+// In host code the array's name is only a host-side stand-in; the device
+// address is looked up once per device, with that device current.
+int noalloc_scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GGUF_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_scratch_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_dense_noalloc_scratch) != cudaSuccess || p == nullptr) return GGUF_ERR_CUDA;
+        g_noalloc_scratch_ptr[dev] = p;
+    }
+    *out = g_noalloc_scratch_ptr[dev];
+    return GGUF_OK;
+}
+
+}  // namespace
+
+}  // namespace gg
+
+extern "C" int gguf_dense_gemm_noalloc(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K, const void* x,
+                                       int xdt, int64_t M, const void* residual, void* y, int ydt,
+                                       gguf_stream_t stream) {
+    using namespace gg;
+    if (!wdense || !x || !y || N <= 0 || K <= 0 || M <= 0) return GGUF_ERR_INVALID_ARG;
+    if ((wdt != GGUF_DT_F16 && wdt != GGUF_DT_BF16) || (xdt != GGUF_DT_F16 && xdt != GGUF_DT_BF16) ||
+        (ydt != GGUF_DT_F32 && ydt != GGUF_DT_F16 && ydt != GGUF_DT_BF16))
+        return GGUF_ERR_UNSUPPORTED;
+    if (K % 64 != 0 || ld < K || ld % 8 != 0) return GGUF_ERR_INVALID_ARG;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!a16(wdense) || !a16(x) || !a16(y) || (residual && !a16(residual))) return GGUF_ERR_MISALIGNED;
+    // the converted activations must fit the built-in scratch: M * K * 2 bytes <= 8 MiB
+    if (M > (int64_t)(kNoAllocScratchBytes / 2) || dense_workspace_bytes(N, K, M) > kNoAllocScratchBytes)
+        return GGUF_ERR_WORKSPACE;
+    int num_sms = 0;
+    int* status = nullptr;
+    int st = current_device_launch_facts(&num_sms, &status);
+    if (st != GGUF_OK) return st;
+    void* scratch = nullptr;
+    if ((st = noalloc_scratch_address(&scratch)) != GGUF_OK) return st;
+    return dense_gemm_run(wdense, wdt, ld, N, K, x, xdt, M, residual, y, ydt, scratch, num_sms, status,
+                          (cudaStream_t)stream);
+}

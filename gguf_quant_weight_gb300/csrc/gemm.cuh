@@ -18,4 +18,8 @@ int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K
                    const void* residual, void* y, int ydt, void* workspace, int num_sms, int* status,
                    cudaStream_t stream);
 
+// Launch facts of the current device (SM count, device address of the status
+// word), as the C entry points use them.
+int current_device_launch_facts(int* num_sms, int** status);
+
 }  // namespace gg

@@ -147,6 +147,24 @@ int gguf_dense_gemm(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t 
                     const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
                     void* workspace, size_t ws_bytes, gguf_stream_t stream);
 
+/* Allocation-free form of gguf_dense_gemm, for callers that may not obtain
+ * device memory (their host program owns every allocation, or a cudaMalloc
+ * there would synchronize the device at the wrong moment): same arguments
+ * minus the workspace; the scratch this call needs (the activations converted
+ * to wdt, M*K*2 bytes) lives in an 8 MiB array built into the library, which
+ * every GPU that loads the library keeps until the process exits.  The pages
+ * have no counterpart of this entry point.
+ *   - M*K*2 > 8 MiB returns GGUF_ERR_WORKSPACE before anything is launched.
+ *   - The call allocates nothing.  Its first call on a device looks up the
+ *     array's device address (cudaGetSymbolAddress, with that device current);
+ *     make that first call before any stream capture.
+ *   - All calls share the one array and each overwrites, before reading, the
+ *     part it uses, so nothing in it needs to start at zero; calls that overlap
+ *     on the GPU (other streams, other host threads) race on it. */
+int gguf_dense_gemm_noalloc(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K,
+                            const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
+                            gguf_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device status word of the
  * current device: GGUF_OK, GGUF_ERR_TIMEOUT (a bounded wait in a kernel expired;
  * that kernel's outputs are undefined), or GGUF_ERR_CUDA for a pending CUDA error. */
