@@ -80,12 +80,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Longest legitimate wait: about one second of wall time.
+constexpr uint64_t kWaitNs = 1000000000ull;
+
 // Bounded wait for the phase with the given parity to complete.  Returns false
-// (and records a timeout) if it did not complete within kSpinLimit polls.
+// (and records a timeout) if it did not complete within `limit` polls or about
+// one second, whichever comes first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           long long limit = kSpinLimit) {
-    for (long long i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (long long i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255) == 255 && globaltimer_ns() - t0 > kWaitNs) break;
+    }
     report(status, GGUF_ERR_TIMEOUT);
     return false;
 }

@@ -1,6 +1,412 @@
+// Fused prefill GEMM on GGUF blocks: Y = X . W^T (+ residual) with the weight
+// decoded inside the kernel.
+//
+// OpenVINO PR #39119 "FullyConnectedGGUF", "Implementation", DPAS prefill row:
+// each 256-value weight block is decoded once into on-chip memory and reused
+// across all the activation rows of the tile; block loading overlaps decoding;
+// the tile grows with the row count.
+//
+// GB300 shape of it (one 128-weight-row x BN-token tile per CTA, swap-AB):
+//   warp 0     TMA producer: the tile's raw super-block bytes (one 256-value
+//              column of 128 rows per raw slot: Q4_K/Q5_K/Q8_0 blocks, raw
+//              Q6_K rows from their 16-byte boundary, or the four Q6_K
+//              planes), and the f16 activation tile of each 64-value k step
+//   warp 1     TMEM allocation and tcgen05.mma issue (128 x BN x 16 per MMA,
+//              f32 accumulators in TMEM), one commit per stage
+//   warps 2-9  decoders: each k step, 256 threads turn 128 rows x 64 values of
+//              raw bytes into f16 (w = d*sc*q - dmin*m in f32, one rounding)
+//              written straight into the 128-byte-swizzled K-major operand
+//              layout the MMA reads; then the epilogue (TMEM -> registers,
+//              + residual, store)
+// The MMA never waits on decode of the same stage it consumes: stages ring
+// through S slots, so decode of step i+1.. overlaps the MMAs of step i.
+#include <cstring>
+
 #include "tc_gemm.cuh"
+#include "formats.cuh"
+
 namespace gg {
+
+namespace {
+
+constexpr int kDecodeWarps = 8;
+constexpr int kFusedThreads = 64 + 32 * kDecodeWarps;   // 320
+
+__host__ __device__ constexpr int raw_pitch(int qt, int layout) {
+    // bytes per weight row in one raw slot (= the TMA box's inner extent)
+    return qt == GGUF_Q8_0 ? 272 : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176 : (layout ? 0 : 224);
+}
+// bytes of one raw slot (128 rows); the Q6_K planes slot is QL | QH | SC | D
+__host__ __device__ constexpr int raw_slot_bytes(int qt, int layout) {
+    return (qt == GGUF_Q6_K && layout) ? 128 * (128 + 64 + 16 + 16) : 128 * raw_pitch(qt, layout);
+}
+
+template <int BN>
+struct FusedCfg {
+    static constexpr int A_BYTES = 128 * 64 * 2;
+    static constexpr int B_BYTES = BN * 64 * 2;
+    static constexpr int S = BN >= 256 ? 3 : 4;        // operand stages
+    static constexpr int RS = 2;                        // raw slots
+    static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+};
+
+struct FusedParams {
+    int64_t N, M;
+    int KB;              // super-blocks along K
+    const void* residual;
+    void* y;
+    int ydt;
+    int* status;
+};
+
+__device__ __forceinline__ uint4 lds128u(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32u(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16u(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_w2(uint32_t a) {   // 32-bit word at a 2-byte aligned address
+    return lds16u(a) | (lds16u(a + 2) << 16);
+}
+__device__ __forceinline__ void sts128u(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
+}
+__device__ __forceinline__ uint32_t byte_of(uint32_t w, int i) { return (w >> (8 * i)) & 0xFFu; }
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// 32 decoded values -> 4 x (8 f16) chunks.  q4 holds the 32 unsigned codes
+// (one byte each, element l in byte l%4 of word l/4); w = scale*code - offset.
+__device__ __forceinline__ void emit32(const uint32_t q4[8], float scale, float offset, uint4 out[4]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        uint32_t h[4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t w = q4[2 * c + t];
+            h[2 * t] = pack_h2(fmaf(scale, (float)byte_of(w, 0), -offset), fmaf(scale, (float)byte_of(w, 1), -offset));
+            h[2 * t + 1] = pack_h2(fmaf(scale, (float)byte_of(w, 2), -offset), fmaf(scale, (float)byte_of(w, 3), -offset));
+        }
+        out[c] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
+// Decode values 32*hf .. 32*hf+31 of k step q (values 64q .. 64q+63 of the
+// super-block) of one weight row whose raw bytes start at shared address `row`.
+template <int QT, int LAYOUT>
+__device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int q, int hf, int kb, uint4 out[4]) {
+    if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
+        const uint4 hdr = lds128u(row);
+        const float d = f16_bits_to_float(hdr.x), dmin = f16_bits_to_float(hdr.x >> 16);
+        const int j = 2 * q + hf;   // 32-wide sub-block
+        const uint32_t scw = j < 4 ? (hdr.y & 0x3F3F3F3Fu) : ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u));
+        const uint32_t mnw = j < 4 ? (hdr.z & 0x3F3F3F3Fu) : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
+        const float scale = d * (float)byte_of(scw, j & 3), offset = dmin * (float)byte_of(mnw, j & 3);
+        const uint32_t qs = row + (QT == GGUF_Q5_K ? 48 : 16) + 32 * q;
+        const uint4 a = lds128u(qs), b = lds128u(qs + 16);
+        uint32_t q4[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = word_of(i < 4 ? a : b, i & 3);
+            q4[i] = hf ? ((w >> 4) & 0x0F0F0F0Fu) : (w & 0x0F0F0F0Fu);
+        }
+        if constexpr (QT == GGUF_Q5_K) {
+            const uint4 h0 = lds128u(row + 16), h1 = lds128u(row + 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t hb = word_of(i < 4 ? h0 : h1, i & 3);
+                q4[i] |= ((hb >> j) & 0x01010101u) << 4;
+            }
+        }
+        emit32(q4, scale, offset, out);
+    } else if constexpr (QT == GGUF_Q8_0) {
+        const uint32_t blk = row + 34u * (uint32_t)(2 * q + hf);   // 2-byte aligned
+        const float d = f16_bits_to_float(lds16u(blk));
+        uint32_t qw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qw[i] = lds_w2(blk + 2 + 4 * i);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t h[4];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const uint32_t w = qw[2 * c + t];
+                h[2 * t] = pack_h2(d * (float)(int8_t)byte_of(w, 0), d * (float)(int8_t)byte_of(w, 1));
+                h[2 * t + 1] = pack_h2(d * (float)(int8_t)byte_of(w, 2), d * (float)(int8_t)byte_of(w, 3));
+            }
+            out[c] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+    } else {
+        // Q6_K: values 64q + 32hf + l = 128h + 32g + l with h = q/2, g = 2(q%2) + hf
+        const int h = q >> 1, g = 2 * (q & 1) + hf;
+        uint32_t ql, qh, sc, dq;
+        if constexpr (LAYOUT == GGUF_LAYOUT_Q6K_PLANES) {
+            ql = slot + 128u * r;
+            qh = slot + 128u * 128 + 64u * r;
+            sc = slot + 128u * 192 + 16u * r;
+            dq = slot + 128u * 208 + 16u * r + (uint32_t)((2 * kb) & 15);
+        } else {
+            const uint32_t blk = row;   // 2-byte aligned
+            ql = blk;
+            qh = blk + 128;
+            sc = blk + 192;
+            dq = blk + 208;
+        }
+        const float d = f16_bits_to_float(lds16u(dq));
+        uint32_t x8[8], h8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if constexpr (LAYOUT == GGUF_LAYOUT_Q6K_PLANES) {
+                x8[i] = lds32u(ql + 64 * h + 32 * (g & 1) + 4 * i);
+                h8[i] = lds32u(qh + 32 * h + 4 * i);
+            } else {
+                x8[i] = lds_w2(ql + 64 * h + 32 * (g & 1) + 4 * i);
+                h8[i] = lds_w2(qh + 32 * h + 4 * i);
+            }
+        }
+        uint32_t q4[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t lo = g < 2 ? (x8[i] & 0x0F0F0F0Fu) : ((x8[i] >> 4) & 0x0F0F0F0Fu);
+            q4[i] = lo | (((h8[i] >> (2 * g)) & 0x03030303u) << 4);
+        }
+        // two 16-value sub-blocks, each with its own signed scale: w = d*sc*(q6 - 32)
+        const int j0 = 8 * h + 2 * g;
+        const uint32_t scw = LAYOUT == GGUF_LAYOUT_Q6K_PLANES ? lds32u(sc + (j0 & ~3)) : lds_w2(sc + (j0 & ~3));
+        const float s0 = d * (float)(int8_t)byte_of(scw, j0 & 3), s1 = d * (float)(int8_t)byte_of(scw, (j0 & 3) + 1);
+        uint4 o0[4], o1[4];
+        emit32(q4, s0, 32.f * s0, o0);
+        emit32(q4, s1, 32.f * s1, o1);
+        out[0] = o0[0]; out[1] = o0[1]; out[2] = o1[2]; out[3] = o1[3];
+    }
+}
+
+template <int QT, int LAYOUT, int BN>
+__global__ void __launch_bounds__(kFusedThreads, 1)
+    fused_tc_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
+                    const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW3,
+                    const __grid_constant__ CUtensorMap tmB, const FusedParams fp) {
+    using C = FusedCfg<BN>;
+    constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
+    constexpr int RAW = raw_slot_bytes(QT, LAYOUT);
+    constexpr int PITCH = raw_pitch(QT, LAYOUT);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = align_up_1024(smem_raw);
+    uint8_t* sA = base;
+    uint8_t* sB = sA + C::S * C::A_BYTES;
+    uint8_t* sR = sB + C::S * C::B_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sR + C::RS * RAW);
+    uint64_t* empty = full + C::S;
+    uint64_t* rfull = empty + C::S;
+    uint64_t* rempty = rfull + C::RS;
+    uint64_t* tfull = rempty + C::RS;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(tfull + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n0 = (int64_t)blockIdx.x * 128, t0 = (int64_t)blockIdx.y * BN;
+    const int KB = fp.KB, nk = 4 * KB;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], 1 + kDecodeWarps); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < C::RS; ++s) { mbar_init(&rfull[s], 1); mbar_init(&rempty[s], kDecodeWarps); }
+        mbar_init(tfull, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            prefetch_tmap(&tmW0);
+            prefetch_tmap(&tmB);
+            int i = 0;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int rs = kb % C::RS;
+                if (!mbar_wait(&rempty[rs], ((kb / C::RS) & 1) ^ 1, fp.status)) break;
+                uint8_t* dst = sR + rs * RAW;
+                mbar_arrive_expect_tx(&rfull[rs], RAW);
+                if constexpr (PLANES) {
+                    tma_load_2d(dst, &tmW0, kb * 64, (int)n0, &rfull[rs]);                       // QL: 128 B per row
+                    tma_load_2d(dst + 128 * 128, &tmW1, kb * 32, (int)n0, &rfull[rs]);           // QH: 64 B
+                    tma_load_2d(dst + 128 * 192, &tmW2, kb * 8, (int)n0, &rfull[rs]);            // SC: 16 B
+                    tma_load_2d(dst + 128 * 208, &tmW3, ((2 * kb) & ~15) / 2, (int)n0, &rfull[rs]);  // D: 16 B
+                } else if constexpr (QT == GGUF_Q6_K) {
+                    tma_load_2d(dst, &tmW0, ((210 * kb) & ~15) / 2, (int)n0, &rfull[rs]);
+                } else {
+                    tma_load_2d(dst, &tmW0, kb * (PITCH / 2), (int)n0, &rfull[rs]);
+                }
+                bool ok = true;
+                for (int q = 0; q < 4; ++q, ++i) {
+                    const int s = i % C::S;
+                    if (!mbar_wait(&empty[s], ((i / C::S) & 1) ^ 1, fp.status)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&full[s], C::B_BYTES);
+                    tma_load_2d(sB + s * C::B_BYTES, &tmB, i * 64, (int)t0, &full[s]);
+                }
+                if (!ok) break;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16(128, BN, 0);
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % C::S;
+                if (!mbar_wait(&full[s], (i / C::S) & 1, fp.status)) break;
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + s * C::A_BYTES), b0 = smem_u32(sB + s * C::B_BYTES);
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    umma_f16(tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k), idesc, (i | k) != 0);
+                umma_commit(&empty[s]);
+            }
+            umma_commit(tfull);
+        }
+    } else {
+        // decoders: thread dt handles row r = dt % 128 and half hf = dt / 128 of each k step
+        const int dt = threadIdx.x - 64, r = dt & 127, hf = dt >> 7;
+        const uint32_t rsw = (uint32_t)(r & 7);
+        const uint32_t a_row = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+        int i = 0;
+        bool ok = true;
+        for (int kb = 0; kb < KB && ok; ++kb) {
+            const int rs = kb % C::RS;
+            ok = mbar_wait(&rfull[rs], (kb / C::RS) & 1, fp.status);
+            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            const uint32_t slot = smem_u32(sR + rs * RAW);
+            uint32_t row = slot + (uint32_t)(r * PITCH);
+            if constexpr (QT == GGUF_Q6_K && !PLANES) row += (uint32_t)((210 * kb) & 15);
+            for (int q = 0; q < 4; ++q, ++i) {
+                const int s = i % C::S;
+                ok = mbar_wait(&empty[s], ((i / C::S) & 1) ^ 1, fp.status);
+                if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+                uint4 out[4];
+                decode32<QT, LAYOUT>(row, slot, r, q, hf, kb, out);
+                const uint32_t a = smem_u32(sA + s * C::A_BYTES) + a_row;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sts128u(a + (((uint32_t)(4 * hf + c) ^ rsw) << 4), out[c]);
+                fence_proxy_async_smem();     // generic-proxy writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full[s]);
+            }
+            __syncwarp();
+            if (ok && lane == 0) mbar_arrive(&rempty[rs]);
+        }
+        // epilogue: decoder warp w reads TMEM lane quarter (w % 4), columns half (w - 2) / 4
+        if (mbar_wait(tfull, 0, fp.status)) {
+            tc_fence_after();
+            TcEpilogue ep{fp.residual, fp.y, fp.ydt, fp.N, fp.M};
+            const int qd = warp & 3, half = (warp - 2) >> 2;
+            const int64_t n = n0 + 32 * qd + lane;
+#pragma unroll 1
+            for (int c = half * (BN / 32); c < (half + 1) * (BN / 32); ++c) {
+                uint32_t v[16];
+                tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + 16 * c, v);
+                tmem_ld_wait();
+                if (n < ep.N) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int64_t m = t0 + 16 * c + j;
+                        if (m < ep.M) {
+                            float o = __uint_as_float(v[j]);
+                            if (ep.residual) o += load_act(ep.residual, ep.ydt, m * ep.N + n);
+                            store_out(ep.y, ep.ydt, m * ep.N + n, o);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template <int QT, int LAYOUT, int BN>
+cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const FusedParams& fp, cudaStream_t s) {
+    using C = FusedCfg<BN>;
+    const int smem = C::S * (C::A_BYTES + C::B_BYTES) + C::RS * raw_slot_bytes(QT, LAYOUT) + 1024 + 256;
+    auto k = fused_tc_kernel<QT, LAYOUT, BN>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)ceil_div(fp.N, 128), (unsigned)ceil_div(fp.M, BN));
+    k<<<grid, kFusedThreads, smem, s>>>(w[0], w[1], w[2], w[3], b, fp);
+    return cudaGetLastError();
+}
+
+template <int QT, int LAYOUT>
+cudaError_t launch_bn(int bn, const CUtensorMap* w, const CUtensorMap& b, const FusedParams& fp, cudaStream_t s) {
+    switch (bn) {
+        case 256: return launch_fused<QT, LAYOUT, 256>(w, b, fp, s);
+        case 128: return launch_fused<QT, LAYOUT, 128>(w, b, fp, s);
+        case 64: return launch_fused<QT, LAYOUT, 64>(w, b, fp, s);
+        default: return launch_fused<QT, LAYOUT, 32>(w, b, fp, s);
+    }
+}
+
+}  // namespace
+
 size_t gemm_workspace_bytes(int, int64_t, int64_t K, int64_t M) { return (size_t)(ceil_div(M * K * 2, 256) * 256); }
-int gemm_fused_run(const void*, int, int, int64_t, int64_t, const void*, int, int64_t, const void*, void*, int, void*,
-                   int, int*, cudaStream_t) { return GGUF_ERR_UNSUPPORTED; }
+
+int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
+                   const void* residual, void* y, int ydt, void* workspace, int num_sms, int* status,
+                   cudaStream_t stream) {
+    if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
+    const int64_t KB = K / 256;
+    if (qtype == GGUF_Q6_K && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;   // 16-byte row strides for TMA
+    if (N > INT32_MAX || M > INT32_MAX || KB > (1 << 20)) return GGUF_ERR_UNSUPPORTED;
+    if (convert_activations(x, xdt, M, K, workspace, GGUF_DT_F16, num_sms, stream) != cudaSuccess) return GGUF_ERR_CUDA;
+
+    const int bb = block_bytes(qtype) * (qtype == GGUF_Q8_0 ? 8 : 1);   // bytes of one 256-value column
+    const int64_t rb = KB * bb;
+    CUtensorMap tw[4];
+    std::memset(tw, 0, sizeof(tw));
+    int st;
+    const CUtensorMapDataType u16 = CU_TENSOR_MAP_DATA_TYPE_UINT16;
+    const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (qtype == GGUF_Q6_K && layout == GGUF_LAYOUT_Q6K_PLANES) {
+        const int64_t nblk = N * KB;
+        const uint8_t* p = static_cast<const uint8_t*>(w);
+        if ((st = make_tmap_2d(&tw[0], p, u16, 2, 64 * KB, N, 128 * KB, 64, 128, none)) != GGUF_OK) return st;
+        if ((st = make_tmap_2d(&tw[1], p + 128 * nblk, u16, 2, 32 * KB, N, 64 * KB, 32, 128, none)) != GGUF_OK) return st;
+        if ((st = make_tmap_2d(&tw[2], p + 192 * nblk, u16, 2, 8 * KB, N, 16 * KB, 8, 128, none)) != GGUF_OK) return st;
+        if ((st = make_tmap_2d(&tw[3], p + 208 * nblk, u16, 2, KB, N, 2 * KB, 8, 128, none)) != GGUF_OK) return st;
+    } else {
+        const uint32_t box = (uint32_t)raw_pitch(qtype, 0) / 2;
+        if ((st = make_tmap_2d(&tw[0], w, u16, 2, (uint64_t)rb / 2, N, rb, box, 128, none)) != GGUF_OK) return st;
+        tw[1] = tw[2] = tw[3] = tw[0];
+    }
+    const int bn = pick_bn(N, M, num_sms);
+    CUtensorMap tb;
+    if ((st = make_tmap_2d(&tb, workspace, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)K, (uint64_t)M,
+                           (uint64_t)K * 2, 64, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B)) != GGUF_OK)
+        return st;
+    FusedParams fp{N, M, (int)KB, residual, y, ydt, status};
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (qtype) {
+        case GGUF_Q8_0: e = launch_bn<GGUF_Q8_0, 0>(bn, tw, tb, fp, stream); break;
+        case GGUF_Q4_K: e = launch_bn<GGUF_Q4_K, 0>(bn, tw, tb, fp, stream); break;
+        case GGUF_Q5_K: e = launch_bn<GGUF_Q5_K, 0>(bn, tw, tb, fp, stream); break;
+        case GGUF_Q6_K:
+            e = layout == GGUF_LAYOUT_Q6K_PLANES ? launch_bn<GGUF_Q6_K, 1>(bn, tw, tb, fp, stream)
+                                                 : launch_bn<GGUF_Q6_K, 0>(bn, tw, tb, fp, stream);
+            break;
+    }
+    return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
+}
+
 }  // namespace gg
