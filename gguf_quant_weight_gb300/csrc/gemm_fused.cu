@@ -14,7 +14,8 @@
 //   warp 1     TMEM allocation and tcgen05.mma issue (128 x BN x 16 per MMA,
 //              f32 accumulators in TMEM), one commit per stage
 //   warps 2-9  decoders: each k step, 256 threads turn 128 rows x 64 values of
-//              raw bytes into f16 (w = d*sc*q - dmin*m in f32, one rounding)
+//              raw bytes into f16 (packed f16 math: w = fl16(d*sc)*q - fl16(dmin*m)
+//              in one fused multiply-add per value pair)
 //              written straight into the 128-byte-swizzled K-major operand
 //              layout the MMA reads; then the epilogue (TMEM -> registers,
 //              + residual, store)
@@ -41,13 +42,18 @@ __host__ __device__ constexpr int raw_slot_bytes(int qt, int layout) {
     return (qt == GGUF_Q6_K && layout) ? 128 * (128 + 64 + 16 + 16) : 128 * raw_pitch(qt, layout);
 }
 
-template <int BN>
+template <int BN, int RAW>
 struct FusedCfg {
     static constexpr int A_BYTES = 128 * 64 * 2;
     static constexpr int B_BYTES = BN * 64 * 2;
     static constexpr int S = BN >= 256 ? 3 : 4;        // operand stages
-    static constexpr int RS = 2;                        // raw slots
+    // raw slots: whatever shared memory the operand stages leave (each covers
+    // four k steps, so a deep raw ring is what hides the HBM latency)
+    static constexpr int RS_FIT = (232448 - 2048 - S * (A_BYTES + B_BYTES)) / RAW;
+    static constexpr int RS = RS_FIT > 6 ? 6 : RS_FIT;
     static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
+    static constexpr int SMEM = S * (A_BYTES + B_BYTES) + RS * RAW + 1024 + 256;
+    static_assert(RS >= 2, "raw ring needs two slots");
 };
 
 struct FusedParams {
@@ -57,6 +63,11 @@ struct FusedParams {
     void* y;
     int ydt;
     int* status;
+    // grouped (MoE) mode: one CTA row per (expert, token tile) work item
+    const int4* tiles;   // {expert, first row inside the expert's group, rows, 0}
+    const int* ntiles;   // number of work items
+    const int* offsets;  // [n_expert + 1] start of each expert's group in the gathered activations
+    const int* rows;     // entry (token * top_k + slot) of every gathered row
 };
 
 __device__ __forceinline__ uint4 lds128u(uint32_t a) {
@@ -89,17 +100,31 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// 32 decoded values -> 4 x (8 f16) chunks.  q4 holds the 32 unsigned codes
-// (one byte each, element l in byte l%4 of word l/4); w = scale*code - offset.
-__device__ __forceinline__ void emit32(const uint32_t q4[8], float scale, float offset, uint4 out[4]) {
+// ---- packed f16 decode
+// A code byte b (0..255) becomes the f16 value 1024 + b by placing it under the
+// exponent byte 0x64 (one byte permute makes two such values); subtracting
+// 1024 (plus any bias) is exact, and one fused multiply-add applies the
+// block's scale and min:  w = fl16(scale) * q - fl16(offset), rounded once.
+__device__ __forceinline__ __half2 h2_bits(uint32_t v) { return *reinterpret_cast<const __half2*>(&v); }
+__device__ __forceinline__ uint32_t bits_h2(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+
+// codes of bytes 0,1 (lo) and 2,3 (hi) of w as f16 (1024 + b)
+__device__ __forceinline__ __half2 magic_lo(uint32_t w) { return h2_bits(__byte_perm(w, 0x64646464u, 0x4140)); }
+__device__ __forceinline__ __half2 magic_hi(uint32_t w) { return h2_bits(__byte_perm(w, 0x64646464u, 0x4342)); }
+
+// 8 words of 4 codes (32 values) -> 4 chunks of 8 f16:  w = scale * (code - bias) - offset
+// (scale2/offset2: per-16-value halves given separately for Q6_K's sub-blocks)
+__device__ __forceinline__ void emit32_h(const uint32_t q4[8], __half2 bias, __half2 sc_a, __half2 off_a,
+                                         __half2 sc_b, __half2 off_b, uint4 out[4]) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
+        const __half2 sc = c < 2 ? sc_a : sc_b, off = c < 2 ? off_a : off_b;
         uint32_t h[4];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             const uint32_t w = q4[2 * c + t];
-            h[2 * t] = pack_h2(fmaf(scale, (float)byte_of(w, 0), -offset), fmaf(scale, (float)byte_of(w, 1), -offset));
-            h[2 * t + 1] = pack_h2(fmaf(scale, (float)byte_of(w, 2), -offset), fmaf(scale, (float)byte_of(w, 3), -offset));
+            h[2 * t] = bits_h2(__hfma2(__hsub2(magic_lo(w), bias), sc, __hneg2(off)));
+            h[2 * t + 1] = bits_h2(__hfma2(__hsub2(magic_hi(w), bias), sc, __hneg2(off)));
         }
         out[c] = make_uint4(h[0], h[1], h[2], h[3]);
     }
@@ -109,13 +134,15 @@ __device__ __forceinline__ void emit32(const uint32_t q4[8], float scale, float 
 // super-block) of one weight row whose raw bytes start at shared address `row`.
 template <int QT, int LAYOUT>
 __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int q, int hf, int kb, uint4 out[4]) {
+    const __half2 zero2 = __float2half2_rn(0.f);
     if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
         const uint4 hdr = lds128u(row);
         const float d = f16_bits_to_float(hdr.x), dmin = f16_bits_to_float(hdr.x >> 16);
         const int j = 2 * q + hf;   // 32-wide sub-block
         const uint32_t scw = j < 4 ? (hdr.y & 0x3F3F3F3Fu) : ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u));
         const uint32_t mnw = j < 4 ? (hdr.z & 0x3F3F3F3Fu) : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
-        const float scale = d * (float)byte_of(scw, j & 3), offset = dmin * (float)byte_of(mnw, j & 3);
+        const __half2 sc = __float2half2_rn(d * (float)byte_of(scw, j & 3));
+        const __half2 off = __float2half2_rn(dmin * (float)byte_of(mnw, j & 3));
         const uint32_t qs = row + (QT == GGUF_Q5_K ? 48 : 16) + 32 * q;
         const uint4 a = lds128u(qs), b = lds128u(qs + 16);
         uint32_t q4[8];
@@ -132,24 +159,15 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
                 q4[i] |= ((hb >> j) & 0x01010101u) << 4;
             }
         }
-        emit32(q4, scale, offset, out);
+        emit32_h(q4, __float2half2_rn(1024.f), sc, off, sc, off, out);
     } else if constexpr (QT == GGUF_Q8_0) {
+        // signed codes: flipping the sign bit gives b = q + 128 in 0..255
         const uint32_t blk = row + 34u * (uint32_t)(2 * q + hf);   // 2-byte aligned
-        const float d = f16_bits_to_float(lds16u(blk));
-        uint32_t qw[8];
+        const __half2 d2 = h2_bits(lds16u(blk) * 0x10001u);
+        uint32_t q4[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) qw[i] = lds_w2(blk + 2 + 4 * i);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t h[4];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const uint32_t w = qw[2 * c + t];
-                h[2 * t] = pack_h2(d * (float)(int8_t)byte_of(w, 0), d * (float)(int8_t)byte_of(w, 1));
-                h[2 * t + 1] = pack_h2(d * (float)(int8_t)byte_of(w, 2), d * (float)(int8_t)byte_of(w, 3));
-            }
-            out[c] = make_uint4(h[0], h[1], h[2], h[3]);
-        }
+        for (int i = 0; i < 8; ++i) q4[i] = lds_w2(blk + 2 + 4 * i) ^ 0x80808080u;
+        emit32_h(q4, __float2half2_rn(1152.f), d2, zero2, d2, zero2, out);
     } else {
         // Q6_K: values 64q + 32hf + l = 128h + 32g + l with h = q/2, g = 2(q%2) + hf
         const int h = q >> 1, g = 2 * (q & 1) + hf;
@@ -168,12 +186,17 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
         }
         const float d = f16_bits_to_float(lds16u(dq));
         uint32_t x8[8], h8[8];
+        if constexpr (LAYOUT == GGUF_LAYOUT_Q6K_PLANES) {
+            const uint4 x0 = lds128u(ql + 64 * h + 32 * (g & 1)), x1 = lds128u(ql + 64 * h + 32 * (g & 1) + 16);
+            const uint4 y0 = lds128u(qh + 32 * h), y1 = lds128u(qh + 32 * h + 16);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if constexpr (LAYOUT == GGUF_LAYOUT_Q6K_PLANES) {
-                x8[i] = lds32u(ql + 64 * h + 32 * (g & 1) + 4 * i);
-                h8[i] = lds32u(qh + 32 * h + 4 * i);
-            } else {
+            for (int i = 0; i < 8; ++i) {
+                x8[i] = word_of(i < 4 ? x0 : x1, i & 3);
+                h8[i] = word_of(i < 4 ? y0 : y1, i & 3);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
                 x8[i] = lds_w2(ql + 64 * h + 32 * (g & 1) + 4 * i);
                 h8[i] = lds_w2(qh + 32 * h + 4 * i);
             }
@@ -184,25 +207,23 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
             const uint32_t lo = g < 2 ? (x8[i] & 0x0F0F0F0Fu) : ((x8[i] >> 4) & 0x0F0F0F0Fu);
             q4[i] = lo | (((h8[i] >> (2 * g)) & 0x03030303u) << 4);
         }
-        // two 16-value sub-blocks, each with its own signed scale: w = d*sc*(q6 - 32)
+        // two 16-value sub-blocks with signed scales: w = d*sc*(q6 - 32)
         const int j0 = 8 * h + 2 * g;
         const uint32_t scw = LAYOUT == GGUF_LAYOUT_Q6K_PLANES ? lds32u(sc + (j0 & ~3)) : lds_w2(sc + (j0 & ~3));
-        const float s0 = d * (float)(int8_t)byte_of(scw, j0 & 3), s1 = d * (float)(int8_t)byte_of(scw, (j0 & 3) + 1);
-        uint4 o0[4], o1[4];
-        emit32(q4, s0, 32.f * s0, o0);
-        emit32(q4, s1, 32.f * s1, o1);
-        out[0] = o0[0]; out[1] = o0[1]; out[2] = o1[2]; out[3] = o1[3];
+        const __half2 s0 = __float2half2_rn(d * (float)(int8_t)byte_of(scw, j0 & 3));
+        const __half2 s1 = __float2half2_rn(d * (float)(int8_t)byte_of(scw, (j0 & 3) + 1));
+        emit32_h(q4, __float2half2_rn(1056.f), s0, zero2, s1, zero2, out);
     }
 }
 
-template <int QT, int LAYOUT, int BN>
+template <int QT, int LAYOUT, int BN, bool MOE>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     fused_tc_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                     const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW3,
                     const __grid_constant__ CUtensorMap tmB, const FusedParams fp) {
-    using C = FusedCfg<BN>;
-    constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
     constexpr int RAW = raw_slot_bytes(QT, LAYOUT);
+    using C = FusedCfg<BN, RAW>;
+    constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
     constexpr int PITCH = raw_pitch(QT, LAYOUT);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align_up_1024(smem_raw);
@@ -216,8 +237,28 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     uint64_t* tfull = rempty + C::RS;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(tfull + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n0 = (int64_t)blockIdx.x * 128, t0 = (int64_t)blockIdx.y * BN;
+    const int64_t n0 = (int64_t)blockIdx.x * 128;   // first output feature of the tile
     const int KB = fp.KB, nk = 4 * KB;
+    // tile geometry: weight row coordinate, activation row coordinate, valid token columns
+    int64_t wrow0, brow0, t0 = 0;
+    int cols, expert = 0, gstart = 0;
+    if constexpr (MOE) {
+        if ((int)blockIdx.y >= *fp.ntiles) return;   // uniform exit before any shared state exists
+        const int4 tl = fp.tiles[blockIdx.y];
+        expert = tl.x;
+        gstart = fp.offsets[tl.x] + tl.y;
+        wrow0 = (int64_t)tl.x * fp.N + n0;
+        brow0 = gstart;
+        cols = tl.z;
+    } else {
+        t0 = (int64_t)blockIdx.y * BN;
+        wrow0 = n0;
+        brow0 = t0;
+        cols = (int)min((int64_t)BN, fp.M - t0);
+    }
+    // MMA width: the tile's valid token columns rounded up to 16, so an
+    // underfilled tile issues only the MMA columns it needs
+    const int n_mma = min(BN, (cols + 15) & ~15);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], 1 + kDecodeWarps); mbar_init(&empty[s], 1); }
@@ -242,28 +283,28 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 uint8_t* dst = sR + rs * RAW;
                 mbar_arrive_expect_tx(&rfull[rs], RAW);
                 if constexpr (PLANES) {
-                    tma_load_2d(dst, &tmW0, kb * 64, (int)n0, &rfull[rs]);                       // QL: 128 B per row
-                    tma_load_2d(dst + 128 * 128, &tmW1, kb * 32, (int)n0, &rfull[rs]);           // QH: 64 B
-                    tma_load_2d(dst + 128 * 192, &tmW2, kb * 8, (int)n0, &rfull[rs]);            // SC: 16 B
-                    tma_load_2d(dst + 128 * 208, &tmW3, ((2 * kb) & ~15) / 2, (int)n0, &rfull[rs]);  // D: 16 B
+                    tma_load_2d(dst, &tmW0, kb * 64, (int)wrow0, &rfull[rs]);                     // QL: 128 B per row
+                    tma_load_2d(dst + 128 * 128, &tmW1, kb * 32, (int)wrow0, &rfull[rs]);         // QH: 64 B
+                    tma_load_2d(dst + 128 * 192, &tmW2, kb * 8, (int)wrow0, &rfull[rs]);          // SC: 16 B
+                    tma_load_2d(dst + 128 * 208, &tmW3, ((2 * kb) & ~15) / 2, (int)wrow0, &rfull[rs]);  // D: 16 B
                 } else if constexpr (QT == GGUF_Q6_K) {
-                    tma_load_2d(dst, &tmW0, ((210 * kb) & ~15) / 2, (int)n0, &rfull[rs]);
+                    tma_load_2d(dst, &tmW0, ((210 * kb) & ~15) / 2, (int)wrow0, &rfull[rs]);
                 } else {
-                    tma_load_2d(dst, &tmW0, kb * (PITCH / 2), (int)n0, &rfull[rs]);
+                    tma_load_2d(dst, &tmW0, kb * (PITCH / 2), (int)wrow0, &rfull[rs]);
                 }
                 bool ok = true;
                 for (int q = 0; q < 4; ++q, ++i) {
                     const int s = i % C::S;
                     if (!mbar_wait(&empty[s], ((i / C::S) & 1) ^ 1, fp.status)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[s], C::B_BYTES);
-                    tma_load_2d(sB + s * C::B_BYTES, &tmB, i * 64, (int)t0, &full[s]);
+                    tma_load_2d(sB + s * C::B_BYTES, &tmB, i * 64, (int)brow0, &full[s]);
                 }
                 if (!ok) break;
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16(128, BN, 0);
+            const uint32_t idesc = idesc_f16(128, n_mma, 0);
             for (int i = 0; i < nk; ++i) {
                 const int s = i % C::S;
                 if (!mbar_wait(&full[s], (i / C::S) & 1, fp.status)) break;
@@ -309,41 +350,45 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         // epilogue: decoder warp w reads TMEM lane quarter (w % 4), columns half (w - 2) / 4
         if (mbar_wait(tfull, 0, fp.status)) {
             tc_fence_after();
-            TcEpilogue ep{fp.residual, fp.y, fp.ydt, fp.N, fp.M};
             const int qd = warp & 3, half = (warp - 2) >> 2;
             const int64_t n = n0 + 32 * qd + lane;
 #pragma unroll 1
             for (int c = half * (BN / 32); c < (half + 1) * (BN / 32); ++c) {
+                if (16 * c >= n_mma) break;   // columns past the MMA width hold nothing
                 uint32_t v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + 16 * c, v);
                 tmem_ld_wait();
-                if (n < ep.N) {
+                if (n < fp.N) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int64_t m = t0 + 16 * c + j;
-                        if (m < ep.M) {
+                        const int col = 16 * c + j;
+                        if (col < cols) {
+                            // output row: token m (dense) or the routed entry (grouped)
+                            const int64_t orow = MOE ? (int64_t)fp.rows[gstart + col] : t0 + col;
                             float o = __uint_as_float(v[j]);
-                            if (ep.residual) o += load_act(ep.residual, ep.ydt, m * ep.N + n);
-                            store_out(ep.y, ep.ydt, m * ep.N + n, o);
+                            if (fp.residual) o += load_act(fp.residual, fp.ydt, orow * fp.N + n);
+                            store_out(fp.y, fp.ydt, orow * fp.N + n, o);
                         }
                     }
                 }
             }
         }
+        (void)expert;
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template <int QT, int LAYOUT, int BN>
-cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const FusedParams& fp, cudaStream_t s) {
-    using C = FusedCfg<BN>;
-    const int smem = C::S * (C::A_BYTES + C::B_BYTES) + C::RS * raw_slot_bytes(QT, LAYOUT) + 1024 + 256;
-    auto k = fused_tc_kernel<QT, LAYOUT, BN>;
+template <int QT, int LAYOUT, int BN, bool MOE = false>
+cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const FusedParams& fp, cudaStream_t s,
+                         int grid_y = 0) {
+    using C = FusedCfg<BN, raw_slot_bytes(QT, LAYOUT)>;
+    const int smem = C::SMEM;
+    auto k = fused_tc_kernel<QT, LAYOUT, BN, MOE>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)ceil_div(fp.N, 128), (unsigned)ceil_div(fp.M, BN));
+    dim3 grid((unsigned)ceil_div(fp.N, 128), MOE ? (unsigned)grid_y : (unsigned)ceil_div(fp.M, BN));
     k<<<grid, kFusedThreads, smem, s>>>(w[0], w[1], w[2], w[3], b, fp);
     return cudaGetLastError();
 }
@@ -395,7 +440,7 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
     if ((st = make_tmap_2d(&tb, workspace, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)K, (uint64_t)M,
                            (uint64_t)K * 2, 64, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B)) != GGUF_OK)
         return st;
-    FusedParams fp{N, M, (int)KB, residual, y, ydt, status};
+    FusedParams fp{N, M, (int)KB, residual, y, ydt, status, nullptr, nullptr, nullptr, nullptr};
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {
         case GGUF_Q8_0: e = launch_bn<GGUF_Q8_0, 0>(bn, tw, tb, fp, stream); break;
@@ -405,6 +450,38 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
             e = layout == GGUF_LAYOUT_Q6K_PLANES ? launch_bn<GGUF_Q6_K, 1>(bn, tw, tb, fp, stream)
                                                  : launch_bn<GGUF_Q6_K, 0>(bn, tw, tb, fp, stream);
             break;
+    }
+    return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
+}
+
+int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* xg,
+                     int64_t rows_cap, const int4* tiles, const int* ntiles, const int* offsets, const int* rows,
+                     int64_t max_tiles, const void* residual, void* y, int ydt, int* status, cudaStream_t stream) {
+    const int64_t KB = K / 256;
+    if (qtype == GGUF_Q6_K && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;   // 16-byte row strides for TMA
+    if (max_tiles > 65535 || KB > (1 << 20)) return GGUF_ERR_UNSUPPORTED;
+    const int bb = block_bytes(qtype) * (qtype == GGUF_Q8_0 ? 8 : 1);
+    const int64_t rb = KB * bb;
+    CUtensorMap tw[4];
+    std::memset(tw, 0, sizeof(tw));
+    // every expert's [N, rb] block rows back to back: one [E*N, rb] tensor
+    const uint32_t box = (uint32_t)raw_pitch(qtype, 0) / 2;
+    int st = make_tmap_2d(&tw[0], w_experts, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, (uint64_t)rb / 2,
+                          (uint64_t)(n_expert * N), rb, box, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != GGUF_OK) return st;
+    tw[1] = tw[2] = tw[3] = tw[0];
+    CUtensorMap tb;
+    if ((st = make_tmap_2d(&tb, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)K, (uint64_t)rows_cap,
+                           (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != GGUF_OK)
+        return st;
+    FusedParams fp{N, rows_cap, (int)KB, residual, y, ydt, status, tiles, ntiles, offsets, rows};
+    const int gy = (int)max_tiles;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (qtype) {
+        case GGUF_Q8_0: e = launch_fused<GGUF_Q8_0, 0, 128, true>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q4_K: e = launch_fused<GGUF_Q4_K, 0, 128, true>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q5_K: e = launch_fused<GGUF_Q5_K, 0, 128, true>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q6_K: e = launch_fused<GGUF_Q6_K, 0, 128, true>(tw, tb, fp, stream, gy); break;
     }
     return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
 }

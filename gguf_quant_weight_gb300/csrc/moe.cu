@@ -1,7 +1,194 @@
+// MoE expert GEMM (mul_mm_id): Y[t, k, :] = X[t, :] . W_{ids[t,k]}^T (+ residual).
+//
+// llama.cpp PR #28301 "metal : skip the empty half of the mul_mm_id token
+// tile", "Overview" and "Additional information": every routed (token, slot)
+// row multiplies its expert's weight; experts receive few rows per ubatch
+// (rows per expert ~ ubatch * n_used / n_expert, skewed by routing), so most
+// token tiles are underfilled, and the padded rows should cost nothing.
+//
+// GB300 shape of it, three kernels on the caller's stream:
+//   1. route  (one CTA): per-expert row counts, a block-wide scan for each
+//      expert's group offset and first work item, the work list of
+//      (expert, token tile of up to 128 rows), and the grouped row list
+//      (entry = token * top_k + slot of each row, grouped by expert);
+//   2. gather: the activation row of every grouped entry, converted to f16,
+//      packed contiguously so each token tile is one TMA box;
+//   3. the fused tensor-core GEMM in grouped mode: one CTA per (128 weight
+//      rows, work item), the expert's GGUF blocks decoded in the kernel, and
+//      MMAs issued for round_up(rows, 16) token columns only.
+// Nothing waits on the host: the counts never leave the device, so the GEMM
+// grid is the upper bound on work items and surplus CTAs exit at once.
 #include "common.cuh"
+#include "formats.cuh"
+#include "gemm.cuh"
 #include "moe.cuh"
+
 namespace gg {
-size_t moe_workspace_bytes(int, int64_t, int64_t, int64_t, int64_t, int64_t) { return 16; }
-int moe_run(const void*, int, int64_t, int64_t, int64_t, const void*, int, int64_t, const int32_t*, int64_t,
-            const void*, void*, int, void*, int, int*, cudaStream_t) { return GGUF_ERR_UNSUPPORTED; }
+
+namespace {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kMoeTile = 128;   // token rows per work item (the GEMM's BN)
+
+struct MoeLayout {
+    int* offsets;   // [E + 1]
+    int* ntiles;    // [1]
+    int4* tiles;    // [max_tiles]
+    int* rows;      // [T * top_k]
+    uint16_t* xg;   // [T * top_k, K] f16
+    int64_t max_tiles;
+    size_t bytes;
+};
+
+MoeLayout moe_layout(void* base, int64_t E, int64_t K, int64_t T, int64_t top_k) {
+    const int64_t entries = T * top_k;
+    MoeLayout L{};
+    L.max_tiles = std::min(E, entries) + ceil_div(entries, kMoeTile);
+    auto r256 = [](int64_t b) { return ceil_div(b, 256) * 256; };
+    int64_t off = 0;
+    uint8_t* p = static_cast<uint8_t*>(base);
+    auto take = [&](int64_t bytes) { uint8_t* q = p ? p + off : nullptr; off += r256(bytes); return q; };
+    L.offsets = reinterpret_cast<int*>(take(4 * (E + 1)));
+    L.ntiles = reinterpret_cast<int*>(take(4));
+    L.tiles = reinterpret_cast<int4*>(take(16 * L.max_tiles));
+    L.rows = reinterpret_cast<int*>(take(4 * entries));
+    L.xg = reinterpret_cast<uint16_t*>(take(2 * entries * K));
+    L.bytes = (size_t)off;
+    return L;
+}
+
+// Exclusive block-wide prefix sums of two values (1024 threads).
+__device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int& ta, int& tb, int* wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int xa = __shfl_up_sync(0xffffffffu, ia, o), xb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) { ia += xa; ib += xb; }
+    }
+    if (lane == 31) { wsum[warp] = ia; wsum[32 + warp] = ib; }
+    __syncthreads();
+    if (warp == 0) {
+        int va = wsum[lane], vb = wsum[32 + lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int xa = __shfl_up_sync(0xffffffffu, va, o), xb = __shfl_up_sync(0xffffffffu, vb, o);
+            if (lane >= o) { va += xa; vb += xb; }
+        }
+        wsum[64 + lane] = va;   // inclusive scan of warp totals
+        wsum[96 + lane] = vb;
+    }
+    __syncthreads();
+    const int pa = warp ? wsum[64 + warp - 1] : 0, pb = warp ? wsum[96 + warp - 1] : 0;
+    ea = pa + ia - a;
+    eb = pb + ib - b;
+    ta = wsum[64 + 31];
+    tb = wsum[96 + 31];
+}
+
+__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const int32_t* __restrict__ ids, int total, int E,
+                                                                  int max_tiles, int* offsets, int* ntiles,
+                                                                  int4* tiles, int* rows) {
+    extern __shared__ int sm[];
+    int* cnt = sm;             // [E] rows per expert
+    int* cur = sm + E;         // [E] next free position of each group
+    int* wsum = sm + 2 * E;    // [128] scan scratch
+    const int tid = threadIdx.x;
+    for (int e = tid; e < E; e += kRouteThreads) cnt[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < total; i += kRouteThreads) {
+        const int e = ids[i];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+    }
+    __syncthreads();
+    // thread tid owns experts [tid*per, tid*per + per)
+    const int per = (E + kRouteThreads - 1) / kRouteThreads;
+    const int e0 = tid * per, e1 = min(E, e0 + per);
+    int my_rows = 0, my_tiles = 0;
+    for (int e = e0; e < e1; ++e) {
+        my_rows += cnt[e];
+        my_tiles += (cnt[e] + kMoeTile - 1) / kMoeTile;
+    }
+    int row_base, tile_base, all_rows, all_tiles;
+    block_scan2(my_rows, my_tiles, row_base, tile_base, all_rows, all_tiles, wsum);
+    for (int e = e0; e < e1; ++e) {
+        offsets[e] = row_base;
+        cur[e] = row_base;
+        for (int s = 0; s < cnt[e]; s += kMoeTile) {
+            if (tile_base < max_tiles) tiles[tile_base] = make_int4(e, s, min(kMoeTile, cnt[e] - s), 0);
+            ++tile_base;
+        }
+        row_base += cnt[e];
+    }
+    if (tid == 0) {
+        offsets[E] = all_rows;
+        *ntiles = min(all_tiles, max_tiles);
+    }
+    __syncthreads();
+    for (int i = tid; i < total; i += kRouteThreads) {
+        const int e = ids[i];
+        if (e >= 0 && e < E) rows[atomicAdd(&cur[e], 1)] = i;
+    }
+}
+
+// One warp per grouped row: x[token] -> f16, 8 values per lane step.
+__global__ void __launch_bounds__(256) moe_gather_kernel(const void* __restrict__ x, int xdt, int64_t K, int top_k,
+                                                         const int* __restrict__ row_count,
+                                                         const int* __restrict__ rows, int64_t cap,
+                                                         uint16_t* __restrict__ xg) {
+    const int lane = threadIdx.x & 31;
+    const int64_t p = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (p >= cap || p >= *row_count) return;
+    const int64_t t = rows[p] / top_k;
+    const uint16_t* src = static_cast<const uint16_t*>(x) + t * K;
+    uint16_t* dst = xg + p * K;
+    for (int64_t k = 8 * lane; k < K; k += 256) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + k);
+        if (xdt == GGUF_DT_F16) {
+            *reinterpret_cast<uint4*>(dst + k) = v;
+        } else {
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float a = __uint_as_float(w4[j] << 16), b = __uint_as_float(w4[j] & 0xFFFF0000u);
+                const __half2 h = __floats2half2_rn(a, b);
+                o[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+}
+
+}  // namespace
+
+size_t moe_workspace_bytes(int, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k) {
+    (void)N;
+    return moe_layout(nullptr, n_expert, K, T, top_k).bytes;
+}
+
+int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
+            int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
+            int num_sms, int* status, cudaStream_t stream) {
+    (void)num_sms;
+    if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
+    const int64_t entries = T * top_k;
+    if (entries > INT32_MAX / 2 || n_expert * N > INT32_MAX) return GGUF_ERR_UNSUPPORTED;
+    const MoeLayout L = moe_layout(workspace, n_expert, K, T, top_k);
+    const size_t route_smem = (size_t)(2 * n_expert + 128) * sizeof(int);
+    if (route_smem > 48 * 1024 &&
+        cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem) !=
+            cudaSuccess)
+        return GGUF_ERR_CUDA;
+    moe_route_kernel<<<1, kRouteThreads, route_smem, stream>>>(ids, (int)entries, (int)n_expert, (int)L.max_tiles,
+                                                              L.offsets, L.ntiles, L.tiles, L.rows);
+    if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;
+    moe_gather_kernel<<<(unsigned)ceil_div(entries, 8), 256, 0, stream>>>(x, xdt, K, (int)top_k,
+                                                                           L.offsets + n_expert, L.rows, entries,
+                                                                           L.xg);
+    if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;
+    return grouped_gemm_run(w_experts, qtype, n_expert, N, K, L.xg, entries, L.tiles, L.ntiles, L.offsets, L.rows,
+                            L.max_tiles, residual, y, ydt, status, stream);
+}
+
 }  // namespace gg

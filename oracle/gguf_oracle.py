@@ -379,7 +379,10 @@ def moe_mm_id_exact(w_experts, qtype: int, n_expert: int, N: int, K: int, x: np.
                     token_rows: np.ndarray | None = None) -> np.ndarray:
     """y[t, k, :] = x[t, :] . W_{ids[t, k]}^T (+ residual[t, k, :]), float64.
     x [T, K] (the same activation row for all of a token's slots); ids [T, top_k].
-    token_rows optionally restricts the evaluation to those tokens (NaN elsewhere)."""
+    An id outside [0, n_expert) selects no expert: that row stays NaN (reading:
+    the pages route every slot to a real expert; the library leaves such rows
+    unwritten).  token_rows optionally restricts the evaluation to those tokens
+    (NaN elsewhere)."""
     T, top_k = ids.shape
     rb = K // BLOCK_VALUES[qtype] * BLOCK_BYTES[qtype]
     wE = np.asarray(w_experts, dtype=np.uint8).reshape(n_expert, N, rb)
@@ -390,6 +393,8 @@ def moe_mm_id_exact(w_experts, qtype: int, n_expert: int, N: int, K: int, x: np.
     for t in rows:
         for k in range(top_k):
             e = int(ids[t, k])
+            if not 0 <= e < n_expert:
+                continue
             if e not in decoded:
                 decoded[e] = dequant(wE[e], qtype, N, K)
             y[t, k] = decoded[e] @ x64[t]

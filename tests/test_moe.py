@@ -1,0 +1,90 @@
+"""MoE expert GEMM (gguf_mm_id) against the exact oracle (llama.cpp PR #28301,
+"Overview": every routed (token, slot) row multiplies its expert's weight)."""
+import numpy as np
+import pytest
+import torch
+
+import gguf_quant_weight_gb300 as g
+import gguf_synth as syn
+from oracle import gguf_oracle as O
+from tests import gpu_util as U
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    U.require_gpu()
+
+
+def _run(qtype, E, N, K, T, top_k, ids, residual=False, ydt="bf16", seed=0, token_rows=None, sentinel=None):
+    rs = syn.rng(seed + E + N + K + T)
+    wE = syn.weight_blocks(rs, qtype, E * N, K)
+    x = syn.normal(rs, (T, K), "bf16")
+    r = syn.normal(rs, (T, top_k, N), ydt) if residual else None
+    y = torch.full((T, top_k, N), float("nan") if sentinel is None else sentinel, dtype=U.TORCH_DT[ydt],
+                   device="cuda")
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    g.gguf_mm_id(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids.astype(np.int32)),
+                 top_k, None if r is None else U.dev(r, ydt), y, U.DT[ydt], ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert g.gguf_mm_check_errors() == 0
+    ref = O.moe_mm_id_exact(wE, qtype, E, N, K, U.act_f64(x, "bf16"), ids,
+                            None if r is None else U.act_f64(r, ydt), token_rows=token_rows)
+    return U.host64(y), ref
+
+
+def _distinct_ids(rs, T, E, top_k):
+    return np.stack([rs.choice(E, size=top_k, replace=False) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,top_k", [(1, 1), (5, 2), (40, 4), (130, 2)])
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q5_K, syn.Q8_0])
+def test_moe_small_all_rows(qtype, T, top_k):
+    E, N, K = 8, 256, 512
+    ids = _distinct_ids(syn.rng(T + top_k), T, E, top_k)
+    got, ref = _run(qtype, E, N, K, T, top_k, ids)
+    U.check_close(got.reshape(T * top_k, N), ref.reshape(T * top_k, N), "bf16")
+
+
+def test_moe_q6k():
+    E, N, K, T, top_k = 4, 128, 2048, 24, 2
+    ids = _distinct_ids(syn.rng(9), T, E, top_k)
+    got, ref = _run(syn.Q6_K, E, N, K, T, top_k, ids)
+    U.check_close(got.reshape(-1, N), ref.reshape(-1, N), "bf16")
+
+
+def test_moe_one_expert_spans_several_tiles_with_residual():
+    # 300 rows on one expert: work items of 128, 128 and 44 rows
+    E, N, K, T, top_k = 4, 384, 256, 300, 1
+    ids = np.full((T, 1), 2, np.int32)
+    got, ref = _run(syn.Q4_K, E, N, K, T, top_k, ids, residual=True)
+    U.check_close(got.reshape(-1, N), ref.reshape(-1, N), "bf16")
+
+
+def test_moe_invalid_ids_leave_rows_untouched():
+    E, N, K, T, top_k = 8, 128, 256, 10, 2
+    ids = _distinct_ids(syn.rng(3), T, E, top_k)
+    ids[2, 1] = -1
+    ids[7, 0] = E
+    got, ref = _run(syn.Q4_K, E, N, K, T, top_k, ids, sentinel=1024.0)
+    valid = (ids >= 0) & (ids < E)
+    assert np.all(got[~valid] == 1024.0)
+    U.check_close(got[valid], ref[valid], "bf16")
+
+
+def test_moe_f32_output():
+    E, N, K, T, top_k = 8, 256, 512, 17, 3
+    ids = _distinct_ids(syn.rng(4), T, E, top_k)
+    got, ref = _run(syn.Q5_K, E, N, K, T, top_k, ids, ydt="f32")
+    U.check_close(got.reshape(-1, N), ref.reshape(-1, N), "f32", rel=2e-3)
+
+
+@pytest.mark.parametrize("T", [32, 64, 256, 512])
+def test_moe_config_128_experts_top8_768x2048(T):
+    E, N, K, top_k = 128, 768, 2048, 8
+    ids = syn.zipf_ids(syn.rng(1004 + T), T, E, top_k, 1.1)
+    tok = np.arange(0, T, max(1, T // 8))
+    got, ref = _run(syn.Q4_K, E, N, K, T, top_k, ids, seed=1004, token_rows=tok)
+    U.check_close(got[tok].reshape(-1, N), ref[tok].reshape(-1, N), "bf16")

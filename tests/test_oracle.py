@@ -302,3 +302,13 @@ def test_moe_routing_counts():
     assert counts.sum() == 64 * 8 and offsets[0] == 0
     assert np.array_equal(offsets[1:], np.cumsum(counts)[:-1])
     assert counts[0] >= counts[64]                     # Zipf: low ranks hit more often
+
+
+def test_moe_out_of_range_ids_select_no_expert():
+    g = syn.rng(29)
+    E, N, K = 2, 4, 256
+    wE = syn.weight_blocks(g, O.Q8_0, E * N, K)
+    x = syn.normal(g, (3, K), "f32")
+    ids = np.array([[0], [-1], [E]], np.int32)
+    y = O.moe_mm_id_exact(wE, O.Q8_0, E, N, K, x, ids)
+    assert np.all(np.isfinite(y[0])) and np.all(np.isnan(y[1])) and np.all(np.isnan(y[2]))
