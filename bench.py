@@ -190,6 +190,113 @@ def recorded_traffic():
     return d.get("dram_bytes_per_launch")
 
 
+def time_graph(fn, reps, stream, calls):
+    """Mean device time of one call: `calls` calls captured in a CUDA graph,
+    replayed `reps` times (after two untimed replays)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(2):
+            fn(i)
+        stream.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(calls):
+                fn(i)
+        gr.replay()
+        gr.replay()
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(stream)
+        e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3 / (reps * calls)
+
+
+def prefill_figures(dev, stream, tc_peak):
+    """Tensor-core figures for the prefill and MoE workloads (context for the
+    second half of the metric); weights rotate over copies larger than L2."""
+    import torch
+    import gguf_quant_weight_gb300 as g
+    import gguf_synth as syn
+    out = {}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    def copies_of(arr):
+        c = max(2, int(np.ceil(2.2 * l2 / arr.size)))
+        return torch.from_numpy(arr.reshape(-1)).to(dev).repeat(c).view(c, -1), c
+
+    rs = syn.rng(1002)
+    for qt, name, layout in ((14, "q6_k_planes", 1), (13, "q5_k", 0)):
+        N, K = 14336, 4096
+        w = syn.weight_blocks(rs, qt, N, K)
+        W, c = copies_of(w)
+        if layout:   # regroup every copy into the QL | QH | SC | D planes on the GPU
+            P = torch.empty_like(W)
+            for i in range(c):
+                g.gguf_repack_q6k_planes(W[i], P[i], N * K // 256, 0, stream=stream)
+            stream.synchronize()
+            W = P
+        for M in (512, 2048):
+            x = torch.from_numpy(syn.normal(rs, (M, K), "bf16")).to(dev).view(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qt, N, K, M)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], qt, layout, N, K, x, g.GGUF_DT_BF16, M, None, y,
+                                                    g.GGUF_DT_BF16, ws, wsb, g.GGUF_PATH_FUSED, stream=stream),
+                           5, stream, c)
+            tf = 2 * M * N * K / t / 1e12
+            out[f"{name}_14336x4096_m{M}_fused"] = {"us": t * 1e6, "tflops": tf, "tc_frac": tf / tc_peak}
+    # Q8_0 2048x8192: fused vs decode-once (K-padded f16) + dense GEMM
+    N, K = 2048, 8192
+    w = syn.weight_blocks(syn.rng(1003), 8, N, K)
+    W, c = copies_of(w)
+    ld = K + 64
+    wd = torch.empty((N, ld), dtype=torch.float16, device=dev)
+    g.gguf_dequant_padded(W[0], 8, 0, N, K, wd, g.GGUF_DT_F16, ld, stream=stream)
+    cd = max(2, int(np.ceil(2.2 * l2 / (wd.numel() * 2))))
+    WD = wd.unsqueeze(0).repeat(cd, 1, 1)
+    t_dec = time_graph(lambda i: g.gguf_dequant_padded(W[i % c], 8, 0, N, K, wd, g.GGUF_DT_F16, ld, stream=stream),
+                       5, stream, c)
+    out["q8_0_2048x8192_decode_once"] = {"us": t_dec * 1e6, "gbs": (w.size + N * ld * 2) / t_dec / 1e9}
+    for M in (128, 512, 4096):
+        x = torch.from_numpy(syn.normal(rs, (M, K), "bf16")).to(dev).view(torch.bfloat16)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 8, N, K, M)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], 8, 0, N, K, x, g.GGUF_DT_BF16, M, None, y, g.GGUF_DT_BF16,
+                                                ws, wsb, g.GGUF_PATH_FUSED, stream=stream), 5, stream, c)
+        t2 = time_graph(lambda i: g.gguf_dense_gemm(WD[i % cd], g.GGUF_DT_F16, ld, N, K, x, g.GGUF_DT_BF16, M, None,
+                                                    y, g.GGUF_DT_BF16, ws, wsb, stream=stream), 5, stream, cd)
+        fl = 2 * M * N * K
+        out[f"q8_0_2048x8192_m{M}_fused"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "tc_frac": fl / t / 1e12 / tc_peak}
+        out[f"q8_0_2048x8192_m{M}_dense_after_decode_once"] = {"us": t2 * 1e6, "tflops": fl / t2 / 1e12,
+                                                                 "tc_frac": fl / t2 / 1e12 / tc_peak}
+    # MoE: 128 experts top-8, Q4_K 768x2048; ids rotate over 8 Zipf(1.1) draws
+    E, N, K, top_k = 128, 768, 2048, 8
+    wE = syn.weight_blocks(syn.rng(1004), 12, E * N, K)
+    WE, c = copies_of(wE)
+    per_expert = N * (K // 256) * 144
+    for T in (32, 512):
+        id_sets = [syn.zipf_ids(syn.rng(2000 + T + j), T, E, top_k, 1.1) for j in range(8)]
+        IDS = [torch.from_numpy(a).to(dev) for a in id_sets]
+        touched = float(np.mean([len(np.unique(a)) for a in id_sets])) * per_expert
+        x = torch.from_numpy(syn.normal(rs, (T, K), "bf16")).to(dev).view(torch.bfloat16)
+        y = torch.empty((T, top_k, N), dtype=torch.bfloat16, device=dev)
+        wsb = g.gguf_mm_workspace_size(g.GGUF_OP_ID, 12, N, K, T, E, top_k)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        calls = 8 * c
+        t = time_graph(lambda i: g.gguf_mm_id(WE[i % c], 12, E, N, K, x, g.GGUF_DT_BF16, T, IDS[i % 8], top_k, None,
+                                              y, g.GGUF_DT_BF16, ws, wsb, stream=stream), 3, stream, calls)
+        fl = 2 * top_k * T * N * K
+        out[f"q4_k_moe_128x768x2048_top8_t{T}"] = {"us": t * 1e6, "tflops": fl / t / 1e12,
+                                                   "tc_frac": fl / t / 1e12 / tc_peak,
+                                                   "touched_gbs": touched / t / 1e9}
+    return out
+
+
 def run_gpu(args):
     import torch
     import gguf_quant_weight_gb300 as g
@@ -335,6 +442,9 @@ def run_gpu(args):
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
     }
     if rank == 0:
+        if not args.no_prefill:
+            line["prefill"] = prefill_figures(dev, stream, tc)
+            line["prefill"]["peak_tflops"] = tc
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
@@ -349,6 +459,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
