@@ -318,6 +318,8 @@ def run_gpu(args):
     xs = {m: torch.from_numpy(syn.normal(rs, (m, K), "bf16")).to(dev).view(torch.bfloat16) for m in MS}
     rsd = {m: torch.from_numpy(syn.normal(rs, (m, N), "bf16")).to(dev).view(torch.bfloat16) for m in MS}
     ys = {m: torch.empty((m, N), dtype=torch.bfloat16, device=dev) for m in MS}
+    wsz = {m: g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, QTYPE, N, K, m) for m in MS}
+    wss = {m: torch.empty(wsz[m], dtype=torch.uint8, device=dev) for m in MS}
     stream = torch.cuda.Stream(device=dev)
     # one graph replay walks every copy exactly once (3 calls per step), so a
     # copy is reused only after all the others: never an L2 hit
@@ -330,7 +332,7 @@ def run_gpu(args):
                 xs[m].copy_(xsrc[m], non_blocking=True)
                 rsd[m].copy_(rsrc[m], non_blocking=True)
             g.gguf_mm_gemv(W[state["c"] % copies], QTYPE, 0, N, K, xs[m], g.GGUF_DT_BF16, m, rsd[m], ys[m],
-                           g.GGUF_DT_BF16, stream=stream)
+                           g.GGUF_DT_BF16, wss[m], wsz[m], stream=stream)
             if ydst is not None:
                 ydst[m].copy_(ys[m], non_blocking=True)
             state["c"] += 1
@@ -423,8 +425,8 @@ def run_gpu(args):
     e2e = weight_bytes / esec / 1e9
     hbm, tc, tc_sus, peak_kind = peaks()
     algo = sum(W_BYTES + m * K * 2 + 2 * m * N * 2 for m in MS) / len(MS)   # weights + x + residual + y
-    launches = steps * len(MS)
-    achieved = algo * launches / (sec * ws / ws) / 1e9
+    calls = steps * len(MS)
+    achieved = algo * calls / sec / 1e9   # one call = the quantizer + GEMV pair, chained
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps, "warmup": args.warmup,
         "ms_per_step": sec / steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -437,8 +439,9 @@ def run_gpu(args):
         "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": recorded_traffic(), "peak_kind": peak_kind,
-                     "kernel": "gemv_direct_kernel", "algorithmic_bytes_per_launch": algo},
-        "gpu_launches": launches,
+                     "kernel": "gemv_direct_kernel (+ act_quant_kernel, overlapped by programmatic launch)",
+                     "algorithmic_bytes_per_launch": algo},
+        "gpu_launches": 2 * calls,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
     }
     if rank == 0:

@@ -2,6 +2,7 @@
 // device status word, and dispatch to the kernels.  Nothing here allocates
 // device memory: every buffer is the caller's, and the status word is a
 // module-scope __device__ variable.
+#include <algorithm>
 #include <mutex>
 #include <cstring>
 #include <cstdlib>
@@ -90,11 +91,13 @@ int check_common(const void* w, int qtype, int layout, int64_t N, int64_t K, con
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA; }
 
 int run_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
-             const void* residual, void* y, int ydt, cudaStream_t stream, int8_t* qa, float* da, int32_t* s,
-             int32_t* D, bool dump) {
+             const void* residual, void* y, int ydt, void* workspace, size_t ws_bytes, cudaStream_t stream,
+             int8_t* qa, float* da, int32_t* s, int32_t* D, bool dump) {
     int st = check_common(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt);
     if (st != GGUF_OK) return st;
     if (M > 8) return GGUF_ERR_UNSUPPORTED;
+    if (!workspace || ws_bytes < gemv_workspace_bytes(M, K)) return GGUF_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return GGUF_ERR_MISALIGNED;
     DeviceFacts* f = nullptr;
     if ((st = facts(&f)) != GGUF_OK) return st;
     GemvParams p{};
@@ -111,6 +114,7 @@ int run_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K, const v
     p.ydt = ydt;
     p.status = f->status;
     p.pdl = pdl_enabled() ? 1 : 0;
+    p.act_image = workspace;
     p.dbg_qa = qa;
     p.dbg_da = da;
     p.dbg_s = s;
@@ -165,8 +169,9 @@ size_t gguf_mm_workspace_size(int op, int qtype, int64_t N, int64_t K, int64_t M
                               int64_t top_k) {
     if (N <= 0 || K <= 0 || M <= 0) return 0;
     switch (op) {
-        case GGUF_OP_GEMV: return 0;
-        case GGUF_OP_GEMM: return gemm_workspace_bytes(qtype, N, K, M);
+        case GGUF_OP_GEMV: return M <= 8 ? gemv_workspace_bytes(M, K) : 0;
+        case GGUF_OP_GEMM:
+            return std::max(gemm_workspace_bytes(qtype, N, K, M), M <= 8 ? gemv_workspace_bytes(M, K) : size_t(0));
         case GGUF_OP_DENSE: return dense_workspace_bytes(N, K, M);
         case GGUF_OP_ID:
             if (n_expert <= 0 || top_k <= 0) return 0;
@@ -176,16 +181,24 @@ size_t gguf_mm_workspace_size(int op, int qtype, int64_t N, int64_t K, int64_t M
 }
 
 int gguf_mm_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
-                 const void* residual, void* y, int ydt, void* /*workspace*/, size_t /*ws_bytes*/,
+                 const void* residual, void* y, int ydt, void* workspace, size_t ws_bytes,
                  gguf_stream_t stream) {
-    return run_gemv(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, (cudaStream_t)stream, nullptr, nullptr,
-                    nullptr, nullptr, false);
+    return run_gemv(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace, ws_bytes, (cudaStream_t)stream,
+                    nullptr, nullptr, nullptr, nullptr, false);
 }
 
 int gguf_mm_debug_gemv_terms(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt,
                              int64_t M, void* y, int ydt, int8_t* qa, float* d_a, int32_t* s, int32_t* D,
                              gguf_stream_t stream) {
-    return run_gemv(w, qtype, layout, N, K, x, xdt, M, nullptr, y, ydt, (cudaStream_t)stream, qa, d_a, s, D, true);
+    // a debugging aid: it owns a stream-ordered workspace for the one call
+    if (M <= 0 || M > 8 || K <= 0) return GGUF_ERR_UNSUPPORTED;
+    const size_t ws = gemv_workspace_bytes(M, K);
+    void* buf = nullptr;
+    if (cudaMallocAsync(&buf, ws, (cudaStream_t)stream) != cudaSuccess) return GGUF_ERR_CUDA;
+    const int st = run_gemv(w, qtype, layout, N, K, x, xdt, M, nullptr, y, ydt, buf, ws, (cudaStream_t)stream, qa,
+                            d_a, s, D, true);
+    const cudaError_t e = cudaFreeAsync(buf, (cudaStream_t)stream);
+    return st != GGUF_OK ? st : cuda_status(e);
 }
 
 int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
@@ -196,8 +209,8 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K, con
     if (path != GGUF_PATH_AUTO && path != GGUF_PATH_GEMV && path != GGUF_PATH_FUSED) return GGUF_ERR_INVALID_ARG;
     if (path == GGUF_PATH_AUTO) path = (M < 8 || xdt == GGUF_DT_F32) ? GGUF_PATH_GEMV : GGUF_PATH_FUSED;
     if (path == GGUF_PATH_GEMV)
-        return run_gemv(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, (cudaStream_t)stream, nullptr,
-                        nullptr, nullptr, nullptr, false);
+        return run_gemv(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace, ws_bytes,
+                        (cudaStream_t)stream, nullptr, nullptr, nullptr, nullptr, false);
     if (xdt == GGUF_DT_F32) return GGUF_ERR_UNSUPPORTED;
     const size_t need = gemm_workspace_bytes(qtype, N, K, M);
     if (need && (!workspace || ws_bytes < need)) return GGUF_ERR_WORKSPACE;

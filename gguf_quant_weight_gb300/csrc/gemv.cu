@@ -67,6 +67,10 @@ __device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
 }
 __device__ __forceinline__ float i2f(int v) { return (float)v; }
 
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+
 // Nearest integer, halves away from zero, for |y| <= 127: truncate, then add
 // one unit when the (exact) remainder is at least one half.
 __device__ __forceinline__ int round_half_away(float y) {
@@ -83,66 +87,94 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
 // ------------------------------------------------------------------ activation quantizer (prologue)
 // Per 32 values: amax, d_a = amax/127 (IEEE f32 divide), id = 1/d_a (0 for an
 // all-zero block), q = round-half-away(clamp(x*id, -127, 127)), s = sum q.
-template <int NT>
-__device__ void quantize_activations(const GemvParams& p, const Shared& sh) {
+// The image it writes is the GEMV's shared-memory layout byte for byte:
+// [M][qa_row_stride(K)] codes, then [M][K/32] entries of 16 bytes.
+__global__ void __launch_bounds__(256) act_quant_kernel(const GemvParams p) {
+    pdl_launch_dependents();
+    pdl_wait();   // X may come from the kernel before this one on the stream
+    uint8_t* img = static_cast<uint8_t*>(p.act_image);
+    const int64_t qa_row = qa_row_stride(p.K);
+    uint8_t* ds = img + (int64_t)p.M * qa_row;
+    // four threads per 32-value block, eight values each; the block's amax and
+    // code sums are combined with shuffles inside each group of four lanes
     const int nb = (int)(p.K / 32);
-    const int total = p.M * nb;
-    for (int blk = threadIdx.x; blk < total; blk += NT) {
-        const int m = blk / nb, b = blk % nb;
-        const int64_t base = (int64_t)m * p.K + (int64_t)b * 32;
-        float v[32];
-        if (p.xdt == GGUF_DT_F32) {
-            const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + base);
+    const int quarters = 4 * p.M * nb;
+    const int idx = blockIdx.x * 256 + threadIdx.x;
+    const bool on = idx < quarters;
+    const int blk = on ? idx >> 2 : 0, qtr = idx & 3;
+    const int m = blk / nb, b = blk % nb;
+    const int64_t off = (int64_t)m * p.K + (int64_t)b * 32 + 8 * qtr;
+    float v[8];
+    if (!on) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 t = src[i];
-                v[4 * i] = t.x; v[4 * i + 1] = t.y; v[4 * i + 2] = t.z; v[4 * i + 3] = t.w;
-            }
-        } else {
-            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + base);
+        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    } else if (p.xdt == GGUF_DT_F32) {
+        const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + off);
+        const float4 a = src[0], c = src[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+    } else {
+        const uint4 t = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + off);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 t = src[i];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t wv = comp(t, j), lo = wv & 0xFFFFu, hi = wv >> 16;
-                    if (p.xdt == GGUF_DT_BF16) {
-                        v[8 * i + 2 * j] = __uint_as_float(lo << 16);
-                        v[8 * i + 2 * j + 1] = __uint_as_float(hi << 16);
-                    } else {
-                        v[8 * i + 2 * j] = f16_bits_to_float(lo);
-                        v[8 * i + 2 * j + 1] = f16_bits_to_float(hi);
-                    }
-                }
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t wv = comp(t, j), lo = wv & 0xFFFFu, hi = wv >> 16;
+            if (p.xdt == GGUF_DT_BF16) {
+                v[2 * j] = __uint_as_float(lo << 16);
+                v[2 * j + 1] = __uint_as_float(hi << 16);
+            } else {
+                v[2 * j] = f16_bits_to_float(lo);
+                v[2 * j + 1] = f16_bits_to_float(hi);
             }
         }
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const float d = amax / 127.0f;
-        const float id = d != 0.f ? 1.0f / d : 0.f;
-        int s_lo = 0, s_hi = 0;
-        uint32_t word[8];
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            uint32_t wv = 0;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                float y = v[w * 4 + t] * id;
-                y = fminf(fmaxf(y, -127.f), 127.f);
-                const int q = round_half_away(y);
-                if (w < 4) s_lo += q; else s_hi += q;
-                wv |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * t);
-            }
-            word[w] = wv;
-        }
-        const uint32_t dst = sh.qa + (uint32_t)m * sh.qa_row + qa_pos(b * 32);
-        sts128(dst, make_uint4(word[0], word[1], word[2], word[3]));
-        sts128(dst + 16, make_uint4(word[4], word[5], word[6], word[7]));
-        sts128(sh.ds + 16u * (uint32_t)(m * nb + b),
-               make_uint4(__float_as_uint(d), __float_as_uint(d * (float)(s_lo + s_hi)), (uint32_t)s_lo,
-                          (uint32_t)s_hi));
     }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float d = amax / 127.0f;
+    const float id = d != 0.f ? 1.0f / d : 0.f;
+    int s8 = 0;
+    uint32_t word[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float y = v[i] * id;
+        y = fminf(fmaxf(y, -127.f), 127.f);
+        const int q = round_half_away(y);
+        s8 += q;
+        word[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
+    }
+    const int s_pair = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);   // s_lo (quarters 0,1) or s_hi (2,3)
+    const int s_other = __shfl_xor_sync(0xffffffffu, s_pair, 2);
+    if (on) {
+        *reinterpret_cast<uint2*>(img + (int64_t)m * qa_row + qa_pos(b * 32) + 8 * qtr) = make_uint2(word[0], word[1]);
+        if (qtr == 0) {
+            const int s = s_pair + s_other;
+            *reinterpret_cast<uint4*>(ds + 16 * ((int64_t)m * nb + b)) =
+                make_uint4(__float_as_uint(d), __float_as_uint(d * (float)s), (uint32_t)s_pair, (uint32_t)s_other);
+        }
+    }
+}
+
+// Bytes of the activation image.
+__host__ __device__ constexpr int64_t act_image_bytes(int64_t M, int64_t K) {
+    return M * qa_row_stride(K) + M * (K / 32) * 16;
+}
+
+// Pulls the activation image into shared memory (one bulk copy) once the
+// quantizer has finished; every thread returns after it has landed (or after
+// the bounded wait gave up and reported GGUF_ERR_TIMEOUT).
+__device__ __forceinline__ bool load_act_image(const GemvParams& p, const Shared& sh, uint64_t* bar) {
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = (uint32_t)act_image_bytes(p.M, p.K);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s_u32(sh.qa, p.act_image, bytes, bar);
+    }
+    return mbar_wait(bar, 0, p.status);
 }
 
 // ------------------------------------------------------------------ per-lane activation slice
@@ -203,61 +235,80 @@ struct FragQ45 {
     }
 };
 
-template <int QT, int MT, class A, bool DUMP>
-__device__ __forceinline__ void unit_q45k(const GemvParams& p, const FragQ45<QT>& f, const A& a, int kb, int h,
-                                          float acc[MT], int64_t n) {
-    const float d = f16_bits_to_float(f.hdr.x), dmin = f16_bits_to_float(f.hdr.x >> 16);
-    // 6-bit scales (scw) and mins (mnw) of the sub-blocks 4h..4h+3, one per byte
-    const uint32_t s0 = f.hdr.y, s1 = f.hdr.z, s2 = f.hdr.w;
-    const uint32_t scw = h ? ((s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u)) : (s0 & 0x3F3F3F3Fu);
-    const uint32_t mnw = h ? (((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u)) : (s1 & 0x3F3F3F3Fu);
-    float accd[MT], accm[MT];
+// R rows of the same unit at once: every activation-code load is shared by the
+// R rows' dot products.  f[r], acc[r], n[r], on[r]: fragment, accumulators,
+// output row and validity of row r.
+template <int QT, int MT, int R, class A, bool DUMP>
+__device__ __forceinline__ void unit_q45k(const GemvParams& p, const FragQ45<QT>* const* f, const A& a, int kb,
+                                          int h, float (*acc)[MT], const int64_t* n, const bool* on) {
+    float d[R], dmin[R];
+    uint32_t scw[R], mnw[R];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) accd[m] = accm[m] = 0.f;
+    for (int r = 0; r < R; ++r) {
+        d[r] = f16_bits_to_float(f[r]->hdr.x);
+        dmin[r] = f16_bits_to_float(f[r]->hdr.x >> 16);
+        // 6-bit scales (scw) and mins (mnw) of the sub-blocks 4h..4h+3, one per byte
+        const uint32_t s0 = f[r]->hdr.y, s1 = f[r]->hdr.z, s2 = f[r]->hdr.w;
+        scw[r] = h ? ((s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u)) : (s0 & 0x3F3F3F3Fu);
+        mnw[r] = h ? (((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u)) : (s1 & 0x3F3F3F3Fu);
+    }
+    float accd[R][MT], accm[R][MT];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) accd[r][m] = accm[r][m] = 0.f;
 #pragma unroll
     for (int pp = 0; pp < 2; ++pp) {
         const int jj = 4 * h + 2 * pp;                 // sub-blocks jj (low nibbles) and jj+1 (high)
-        uint32_t lo[8], hi[8];
+        uint32_t lo[R][8], hi[R][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t q = comp(f.qs[2 * pp + (i >> 2)], i);
-            lo[i] = q & 0x0F0F0F0Fu;
-            hi[i] = (q >> 4) & 0x0F0F0F0Fu;
-            if (QT == GGUF_Q5_K) {
-                // bit jj (resp. jj+1) of every qh byte rotated to bit 4 of that byte
-                const uint32_t hb = comp(f.qh[i >> 2], i);
-                lo[i] |= __funnelshift_l(hb, hb, (uint32_t)(4 - jj) & 31u) & 0x10101010u;
-                hi[i] |= __funnelshift_l(hb, hb, (uint32_t)(3 - jj) & 31u) & 0x10101010u;
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t q = comp(f[r]->qs[2 * pp + (i >> 2)], i);
+                lo[r][i] = q & 0x0F0F0F0Fu;
+                hi[r][i] = (q >> 4) & 0x0F0F0F0Fu;
+                if (QT == GGUF_Q5_K) {
+                    // bit jj (resp. jj+1) of every qh byte rotated to bit 4 of that byte
+                    const uint32_t hb = comp(f[r]->qh[i >> 2], i);
+                    lo[r][i] |= __funnelshift_l(hb, hb, (uint32_t)(4 - jj) & 31u) & 0x10101010u;
+                    hi[r][i] |= __funnelshift_l(hb, hb, (uint32_t)(3 - jj) & 31u) & 0x10101010u;
+                }
             }
         }
-        const int sc0 = (scw >> (16 * pp)) & 0xFF, sc1 = (scw >> (16 * pp + 8)) & 0xFF;
-        const float mn0 = i2f((mnw >> (16 * pp)) & 0xFF), mn1 = i2f((mnw >> (16 * pp + 8)) & 0xFF);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m < p.M) {
                 const uint4 l0 = a.codes(m, 4 * pp), l1 = a.codes(m, 4 * pp + 1);
                 const uint4 h0 = a.codes(m, 4 * pp + 2), h1 = a.codes(m, 4 * pp + 3);
-                int D0a = 0, D0b = 0, D1a = 0, D1b = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    D0a = dp4a(lo[i], comp(l0, i), D0a);
-                    D0b = dp4a(lo[4 + i], comp(l1, i), D0b);
-                    D1a = dp4a(hi[i], comp(h0, i), D1a);
-                    D1b = dp4a(hi[4 + i], comp(h1, i), D1b);
-                }
-                const int D0 = D0a + D0b, D1 = D1a + D1b;
                 const uint4 e0 = a.entry(m, 2 * pp), e1 = a.entry(m, 2 * pp + 1);
-                accd[m] += __uint_as_float(e0.x) * i2f(sc0 * D0) + __uint_as_float(e1.x) * i2f(sc1 * D1);
-                accm[m] += mn0 * __uint_as_float(e0.y) + mn1 * __uint_as_float(e1.y);
-                if (DUMP && p.dbg_D) {
-                    dump_D(p, m, n, kb * 8 + jj, 32, D0);
-                    dump_D(p, m, n, kb * 8 + jj + 1, 32, D1);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    int D0a = 0, D0b = 0, D1a = 0, D1b = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        D0a = dp4a(lo[r][i], comp(l0, i), D0a);
+                        D0b = dp4a(lo[r][4 + i], comp(l1, i), D0b);
+                        D1a = dp4a(hi[r][i], comp(h0, i), D1a);
+                        D1b = dp4a(hi[r][4 + i], comp(h1, i), D1b);
+                    }
+                    const int D0 = D0a + D0b, D1 = D1a + D1b;
+                    const int sc0 = (scw[r] >> (16 * pp)) & 0xFF, sc1 = (scw[r] >> (16 * pp + 8)) & 0xFF;
+                    const float mn0 = i2f((mnw[r] >> (16 * pp)) & 0xFF), mn1 = i2f((mnw[r] >> (16 * pp + 8)) & 0xFF);
+                    accd[r][m] += __uint_as_float(e0.x) * i2f(sc0 * D0) + __uint_as_float(e1.x) * i2f(sc1 * D1);
+                    accm[r][m] += mn0 * __uint_as_float(e0.y) + mn1 * __uint_as_float(e1.y);
+                    if (DUMP && p.dbg_D && on[r]) {
+                        dump_D(p, m, n[r], kb * 8 + jj, 32, D0);
+                        dump_D(p, m, n[r], kb * 8 + jj + 1, 32, D1);
+                    }
                 }
             }
         }
     }
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m] += d * accd[m] - dmin * accm[m];
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[r][m] += d[r] * accd[r][m] - dmin[r] * accm[r][m];
 }
 
 // ------------------------------------------------------------------ Q6_K unit
@@ -268,54 +319,66 @@ struct FragQ6 {
     uint32_t d;    // f16 bits
 };
 
-template <int MT, class A, bool DUMP>
-__device__ __forceinline__ void unit_q6k(const GemvParams& p, const FragQ6& f, const A& a, int kb, int h,
-                                         float acc[MT], int64_t n) {
-    const float d = f16_bits_to_float(f.d);
-    int sc[8];
+template <int MT, int R, class A, bool DUMP>
+__device__ __forceinline__ void unit_q6k(const GemvParams& p, const FragQ6* const* f, const A& a, int kb, int h,
+                                         float (*acc)[MT], const int64_t* n, const bool* on) {
+    float d[R];
+    int sc[R][8];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        sc[t] = (int)(int8_t)((f.sc.x >> (8 * t)) & 0xFF);
-        sc[4 + t] = (int)(int8_t)((f.sc.y >> (8 * t)) & 0xFF);
+    for (int r = 0; r < R; ++r) {
+        d[r] = f16_bits_to_float(f[r]->d);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            sc[r][t] = (int)(int8_t)((f[r]->sc.x >> (8 * t)) & 0xFF);
+            sc[r][4 + t] = (int)(int8_t)((f[r]->sc.y >> (8 * t)) & 0xFF);
+        }
     }
-    int S[MT][4];   // per activation block b (0..3 of the unit): sum of sc_t * D_t over its two sub-blocks
+    int S[R][MT][4];   // per activation block b (0..3 of the unit): sum of sc_t * D_t over its two sub-blocks
 #pragma unroll
-    for (int m = 0; m < MT; ++m) S[m][0] = S[m][1] = S[m][2] = S[m][3] = 0;
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) S[r][m][0] = S[r][m][1] = S[r][m][2] = S[r][m][3] = 0;
 #pragma unroll
     for (int gp = 0; gp < 2; ++gp) {
         // gp = 0: groups g = 0 (low nibbles) and g = 2 (high nibbles) of ql[0..31]
         // gp = 1: groups g = 1 and g = 3 of ql[32..63]
-        uint32_t qlo[8], qhi[8];
+        uint32_t qlo[R][8], qhi[R][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t X = comp(f.ql[2 * gp + (i >> 2)], i), H = comp(f.qh[i >> 2], i);
-            qlo[i] = (X & 0x0F0F0F0Fu) | ((H << (4 - 2 * gp)) & 0x30303030u);
-            qhi[i] = ((X >> 4) & 0x0F0F0F0Fu) | ((H >> (2 * gp)) & 0x30303030u);
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t X = comp(f[r]->ql[2 * gp + (i >> 2)], i), H = comp(f[r]->qh[i >> 2], i);
+                qlo[r][i] = (X & 0x0F0F0F0Fu) | ((H << (4 - 2 * gp)) & 0x30303030u);
+                qhi[r][i] = ((X >> 4) & 0x0F0F0F0Fu) | ((H >> (2 * gp)) & 0x30303030u);
+            }
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             if (m < p.M) {
                 const uint4 l0 = a.codes(m, 2 * gp), l1 = a.codes(m, 2 * gp + 1);
                 const uint4 h0 = a.codes(m, 4 + 2 * gp), h1 = a.codes(m, 5 + 2 * gp);
-                int Dl0 = 0, Dl1 = 0, Dh0 = 0, Dh1 = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    Dl0 = dp4a(qlo[i], comp(l0, i), Dl0);
-                    Dl1 = dp4a(qlo[4 + i], comp(l1, i), Dl1);
-                    Dh0 = dp4a(qhi[i], comp(h0, i), Dh0);
-                    Dh1 = dp4a(qhi[4 + i], comp(h1, i), Dh1);
-                }
                 const uint4 el = a.entry(m, gp), eh = a.entry(m, 2 + gp);
-                // dots of (q6 - 32): subtract 32 * (sum of the 16 activation codes)
-                Dl0 -= 32 * (int)el.z; Dl1 -= 32 * (int)el.w;
-                Dh0 -= 32 * (int)eh.z; Dh1 -= 32 * (int)eh.w;
-                S[m][gp] += sc[2 * gp] * Dl0 + sc[2 * gp + 1] * Dl1;
-                S[m][2 + gp] += sc[4 + 2 * gp] * Dh0 + sc[5 + 2 * gp] * Dh1;
-                if (DUMP && p.dbg_D) {
-                    dump_D(p, m, n, kb * 16 + 8 * h + 2 * gp, 16, Dl0);
-                    dump_D(p, m, n, kb * 16 + 8 * h + 2 * gp + 1, 16, Dl1);
-                    dump_D(p, m, n, kb * 16 + 8 * h + 4 + 2 * gp, 16, Dh0);
-                    dump_D(p, m, n, kb * 16 + 8 * h + 5 + 2 * gp, 16, Dh1);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    int Dl0 = 0, Dl1 = 0, Dh0 = 0, Dh1 = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        Dl0 = dp4a(qlo[r][i], comp(l0, i), Dl0);
+                        Dl1 = dp4a(qlo[r][4 + i], comp(l1, i), Dl1);
+                        Dh0 = dp4a(qhi[r][i], comp(h0, i), Dh0);
+                        Dh1 = dp4a(qhi[r][4 + i], comp(h1, i), Dh1);
+                    }
+                    // dots of (q6 - 32): subtract 32 * (sum of the 16 activation codes)
+                    Dl0 -= 32 * (int)el.z; Dl1 -= 32 * (int)el.w;
+                    Dh0 -= 32 * (int)eh.z; Dh1 -= 32 * (int)eh.w;
+                    S[r][m][gp] += sc[r][2 * gp] * Dl0 + sc[r][2 * gp + 1] * Dl1;
+                    S[r][m][2 + gp] += sc[r][4 + 2 * gp] * Dh0 + sc[r][5 + 2 * gp] * Dh1;
+                    if (DUMP && p.dbg_D && on[r]) {
+                        dump_D(p, m, n[r], kb * 16 + 8 * h + 2 * gp, 16, Dl0);
+                        dump_D(p, m, n[r], kb * 16 + 8 * h + 2 * gp + 1, 16, Dl1);
+                        dump_D(p, m, n[r], kb * 16 + 8 * h + 4 + 2 * gp, 16, Dh0);
+                        dump_D(p, m, n[r], kb * 16 + 8 * h + 5 + 2 * gp, 16, Dh1);
+                    }
                 }
             }
         }
@@ -323,10 +386,16 @@ __device__ __forceinline__ void unit_q6k(const GemvParams& p, const FragQ6& f, c
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
         if (m < p.M) {
-            float u = 0.f;
+            float da[4];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) u += __uint_as_float(a.entry(m, b).x) * i2f(S[m][b]);
-            acc[m] += d * u;
+            for (int b = 0; b < 4; ++b) da[b] = __uint_as_float(a.entry(m, b).x);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float u = 0.f;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) u += da[b] * i2f(S[r][m][b]);
+                acc[r][m] += d[r] * u;
+            }
         }
     }
 }
@@ -384,8 +453,6 @@ __device__ __forceinline__ void frag_q6_from_planes(FragQ6& f, uint32_t ql, uint
     f.d = lds16(d);
 }
 
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Stages global bytes [lo, hi) of the weight buffer (total bytes) in shared
 // memory at dst, starting from the 16-byte boundary at or below lo: byte x
@@ -483,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
 
     // 2. activation prologue, once the producer of X has finished
     pdl_wait();
-    quantize_activations<NT>(p, sh);
+    load_act_image(p, sh, bars + (NW - warp) * R);   // the barrier after the ring's
     __syncthreads();
     if (DUMP && blockIdx.x == 0) {
         for (int64_t i = tid; i < (int64_t)p.M * p.K; i += NT) {
@@ -536,13 +603,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
                     } else {
                         frag_q6_from_smem(f, rowp + 210u * kb, h);
                     }
-                    if (single_unit) unit_q6k<MT, decltype(act), DUMP>(p, f, act, kb, h, acc, n);
-                    else unit_q6k<MT, decltype(as), DUMP>(p, f, as, kb, h, acc, n);
+                    const FragQ6* fp1[1] = {&f};
+                    const int64_t n1[1] = {n};
+                    const bool on1[1] = {true};
+                    if (single_unit) unit_q6k<MT, 1, decltype(act), DUMP>(p, fp1, act, kb, h, &acc, n1, on1);
+                    else unit_q6k<MT, 1, decltype(as), DUMP>(p, fp1, as, kb, h, &acc, n1, on1);
                 } else {
                     FragQ45<QT> f;
                     f.load(rowp + (uint32_t)(bb * kb), h);
-                    if (single_unit) unit_q45k<QT, MT, decltype(act), DUMP>(p, f, act, kb, h, acc, n);
-                    else unit_q45k<QT, MT, decltype(as), DUMP>(p, f, as, kb, h, acc, n);
+                    const FragQ45<QT>* fp1[1] = {&f};
+                    const int64_t n1[1] = {n};
+                    const bool on1[1] = {true};
+                    if (single_unit) unit_q45k<QT, MT, 1, decltype(act), DUMP>(p, fp1, act, kb, h, &acc, n1, on1);
+                    else unit_q45k<QT, MT, 1, decltype(as), DUMP>(p, fp1, as, kb, h, &acc, n1, on1);
                 }
             }
         }
@@ -617,11 +690,12 @@ __device__ __forceinline__ void load_global_planes(FragQ6& f, const uint8_t* w, 
     f.d = ldg16(w + 208 * nblk + 2 * b);
 }
 
-constexpr int kDirectThreads = 512;   // one CTA of 16 warps per SM
+// One CTA per SM: 16 warps for M = 1, fewer as the per-lane state grows with M.
+__host__ __device__ constexpr int direct_threads(int mt) { return mt == 1 ? 512 : mt == 2 ? 384 : 256; }
 
 template <int QT, int MT, bool DUMP>
-__global__ void __launch_bounds__(kDirectThreads, 1) gemv_direct_kernel(const GemvParams p) {
-    constexpr int NT = kDirectThreads, NW = NT / 32;
+__global__ void __launch_bounds__(direct_threads(MT), 1) gemv_direct_kernel(const GemvParams p) {
+    constexpr int NT = direct_threads(MT), NW = NT / 32;
     constexpr int bb = QT == GGUF_Q4_K ? 144 : QT == GGUF_Q5_K ? 176 : 210;
     using Frag = typename std::conditional<QT == GGUF_Q6_K, FragQ6, FragQ45<QT == GGUF_Q6_K ? GGUF_Q4_K : QT>>::type;
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -645,7 +719,7 @@ __global__ void __launch_bounds__(kDirectThreads, 1) gemv_direct_kernel(const Ge
     const bool lane_on = U >= 32 || lane < P * U;
     const int groups = row0 < row_end ? (int)ceil_div(row_end - row0, P) : 0;
 
-    Frag cur, nxt;
+    Frag f0, f1;   // two-slot ring: the item being computed and the next one
     auto fetch = [&](Frag& f, int g, int u) {
         const int64_t n = row0 + (int64_t)g * P + sub_row;
         if (!lane_on || n >= row_end) return;
@@ -653,12 +727,23 @@ __global__ void __launch_bounds__(kDirectThreads, 1) gemv_direct_kernel(const Ge
         if constexpr (QT == GGUF_Q6_K) load_global_planes(f, p.w, nblk, n * KB + kb, h);
         else load_global<QT>(f, p.w + n * p.rb + (int64_t)kb * bb, h);
     };
+    // items (row group g, unit u) of this lane in order
+    auto advance = [&](int g, int u, int& gn, int& un) {
+        un = u + ustep;
+        gn = g;
+        if (un >= U) { un = u0; gn = g + NW; }
+    };
     int g = warp, u = u0;
-    if (g < groups) fetch(cur, g, u);
+    {
+        int g1, u1;
+        advance(g, u, g1, u1);
+        if (g < groups) fetch(f0, g, u);
+        if (g1 < groups) fetch(f1, g1, u1);
+    }
     pdl_launch_dependents();
 
     pdl_wait();
-    quantize_activations<NT>(p, sh);
+    load_act_image(p, sh, reinterpret_cast<uint64_t*>(smem_raw + (sh.ds - sh.qa) + 16 * p.M * nb));
     __syncthreads();
     if (DUMP && blockIdx.x == 0) {
         for (int64_t i = tid; i < (int64_t)p.M * p.K; i += NT) {
@@ -677,53 +762,94 @@ __global__ void __launch_bounds__(kDirectThreads, 1) gemv_direct_kernel(const Ge
     const int seg_end = (lane / seg) * seg + seg;
     const bool head = lane_on && (lane % seg) == 0;
 
+    using Act = ActSlice<MT, false, 8, 4>;
+    // reduction of one row's lane partials and the fused residual store
+    auto finish_row = [&](float (&acc)[MT], int64_t n, bool valid) {
+        if (seg == 32) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
+            }
+        } else {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float t = __shfl_down_sync(0xffffffffu, acc[m], o);
+                    if (lane + o < seg_end) acc[m] += t;
+                }
+            }
+        }
+        if (head && valid) {
+            for (int m = 0; m < p.M && m < MT; ++m) {
+                float v = acc[m];
+                if (p.residual) v += load_act(p.residual, p.ydt, (int64_t)m * p.N + n);
+                store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
+            }
+        }
+    };
+
+    if (single_unit) {
+        // each lane has one unit per row: take the warp's rows two at a time, so
+        // that every activation-code load serves both rows
+        const int kb = u0 >> 1, h = u0 & 1;
+        for (; g < groups; g += 2 * NW) {
+            const int64_t n0r = row0 + (int64_t)g * P + sub_row, n1r = n0r + (int64_t)NW * P;
+            const bool v0 = lane_on && n0r < row_end;
+            const bool v1 = lane_on && g + NW < groups && n1r < row_end;
+            float acc[2][MT];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int m = 0; m < MT; ++m) acc[r][m] = 0.f;
+            const Frag* fr[2] = {&f0, &f1};
+            const int64_t nn[2] = {n0r, n1r};
+            const bool on[2] = {v0, v1};
+            if constexpr (QT == GGUF_Q6_K) unit_q6k<MT, 2, Act, DUMP>(p, fr, fixed, kb, h, acc, nn, on);
+            else unit_q45k<QT, MT, 2, Act, DUMP>(p, fr, fixed, kb, h, acc, nn, on);
+            if (g + 2 * NW < groups) fetch(f0, g + 2 * NW, u0);
+            if (g + 3 * NW < groups) fetch(f1, g + 3 * NW, u0);
+            finish_row(acc[0], n0r, v0);
+            finish_row(acc[1], n1r, v1);
+        }
+        return;
+    }
+
+    // long rows (several units per lane): one item at a time, the ring refilled
+    // with the item two ahead
     float acc[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-    while (g < groups) {
-        int gn = g, un = u + ustep;
-        if (un >= U) { un = u0; gn = g + NW; }
-        if (gn < groups) fetch(nxt, gn, un);
+    auto step = [&](Frag& f) -> bool {
+        if (g >= groups) return false;
+        int gn, un, g2, u2;
+        advance(g, u, gn, un);
+        advance(gn, un, g2, u2);
         const int64_t n = row0 + (int64_t)g * P + sub_row;
         const bool valid = lane_on && n < row_end;
         if (valid) {
-            ActSlice<MT, false, 8, 4> moving;
-            if (!single_unit) moving.init(sh, 128 * u, nb);
-            const ActSlice<MT, false, 8, 4>& a = single_unit ? fixed : moving;
+            Act moving;
+            moving.init(sh, 128 * u, nb);
             const int kb = u >> 1, h = u & 1;
-            if constexpr (QT == GGUF_Q6_K) unit_q6k<MT, ActSlice<MT, false, 8, 4>, DUMP>(p, cur, a, kb, h, acc, n);
-            else unit_q45k<QT, MT, ActSlice<MT, false, 8, 4>, DUMP>(p, cur, a, kb, h, acc, n);
+            const Frag* fr[1] = {&f};
+            const int64_t nn[1] = {n};
+            const bool on[1] = {true};
+            float(*a1)[MT] = reinterpret_cast<float(*)[MT]>(&acc);
+            if constexpr (QT == GGUF_Q6_K) unit_q6k<MT, 1, Act, DUMP>(p, fr, moving, kb, h, a1, nn, on);
+            else unit_q45k<QT, MT, 1, Act, DUMP>(p, fr, moving, kb, h, a1, nn, on);
         }
+        if (g2 < groups) fetch(f, g2, u2);
         if (gn != g) {
-            if (seg == 32) {
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) acc[m] += __shfl_xor_sync(0xffffffffu, acc[m], o);
-                }
-            } else {
-#pragma unroll
-                for (int m = 0; m < MT; ++m) {
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        const float t = __shfl_down_sync(0xffffffffu, acc[m], o);
-                        if (lane + o < seg_end) acc[m] += t;
-                    }
-                }
-            }
-            if (head && valid) {
-                for (int m = 0; m < p.M && m < MT; ++m) {
-                    float v = acc[m];
-                    if (p.residual) v += load_act(p.residual, p.ydt, (int64_t)m * p.N + n);
-                    store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
-                }
-            }
+            finish_row(acc, n, valid);
 #pragma unroll
             for (int m = 0; m < MT; ++m) acc[m] = 0.f;
         }
-        cur = nxt;
         g = gn;
         u = un;
+        return true;
+    };
+    while (step(f0) && step(f1)) {
     }
 }
 
@@ -741,7 +867,7 @@ cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t 
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(p.direct ? kDirectThreads : kThreads);
+    cfg.blockDim = dim3(p.direct ? direct_threads(MT) : kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -780,8 +906,7 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
     const int bv = p.qtype == GGUF_Q8_0 ? 32 : 256;
     const int bb = p.qtype == GGUF_Q8_0 ? 34 : p.qtype == GGUF_Q4_K ? 144 : p.qtype == GGUF_Q5_K ? 176 : 210;
     p.rb = p.K / bv * bb;
-    const int64_t nb32 = p.K / 32;
-    const int64_t act = p.M * qa_row_stride(p.K) + p.M * nb32 * 16;
+    const int64_t act = act_image_bytes(p.M, p.K);
     const int U = (int)(p.K / (p.qtype == GGUF_Q8_0 ? 32 : 128));
     const int64_t P = U < 32 ? 32 / U : 1;
     const int NW = kThreads / 32;
@@ -802,12 +927,29 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
     p.rows_per_cta = rpc;
     p.chunk_rows = 0;
     *grid = (int)ceil_div(p.N, rpc);
-    *smem = p.direct ? (size_t)act : (size_t)(act + NW * R * p.stage_bytes + NW * R * 8);
+    // + the image barrier (8 bytes, after the per-warp ring barriers)
+    *smem = p.direct ? (size_t)(act + 8) : (size_t)(act + NW * R * p.stage_bytes + NW * R * 8 + 8);
     return GGUF_OK;
 }
 
 cudaError_t gemv_launch(const GemvParams& p, int grid, size_t smem, bool dump, cudaStream_t stream) {
+    // 1. per-32 activation quantizer -> image in the workspace
+    const int quarters = 4 * p.M * (int)(p.K / 32);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ceil_div(quarters, 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, act_quant_kernel, p);
+    if (e != cudaSuccess) return e;
+    // 2. the GEMV
     return dump ? launch_dispatch<true>(p, grid, smem, stream) : launch_dispatch<false>(p, grid, smem, stream);
 }
+
+size_t gemv_workspace_bytes(int64_t M, int64_t K) { return (size_t)(ceil_div(act_image_bytes(M, K), 256) * 256); }
 
 }  // namespace gg

@@ -17,6 +17,7 @@ struct GemvParams {
     int ydt;
     int* status;
     int pdl;               // launch with programmatic stream serialization
+    void* act_image;       // workspace: the quantized activations (codes + per-block entries)
     int direct;            // unit fields 16-byte aligned: load straight into registers
     // plan (filled by gemv_plan)
     int64_t rb;            // bytes per weight row (raw layout)
@@ -34,6 +35,8 @@ struct GemvParams {
 // Fills the plan fields; returns GGUF_OK or GGUF_ERR_UNSUPPORTED when the
 // activations and one chunk do not fit in max_smem bytes of shared memory.
 int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem);
+// Workspace bytes of a GEMV call (the quantized activation image).
+size_t gemv_workspace_bytes(int64_t M, int64_t K);
 cudaError_t gemv_launch(const GemvParams& p, int grid, size_t smem, bool dump, cudaStream_t stream);
 
 }  // namespace gg

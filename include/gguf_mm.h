@@ -69,7 +69,8 @@ typedef enum {
 typedef enum { GGUF_OP_GEMV = 0, GGUF_OP_GEMM = 1, GGUF_OP_ID = 2, GGUF_OP_DENSE = 3 } gguf_op;
 
 /* Bytes of device workspace the given call needs (0 = none; pass NULL then).
- * op GGUF_OP_GEMV/GEMM take (t, N, K, M); GGUF_OP_ID takes all arguments with M
+ * op GGUF_OP_GEMV/GEMM take (t, N, K, M) -- the GEMM figure also covers the
+ * GEMV path that GGUF_PATH_AUTO/GEMV may take for M <= 8; GGUF_OP_ID takes all arguments with M
  * the token count T; GGUF_OP_DENSE takes (N, K, M).  Returns 0 for invalid input. */
 size_t gguf_mm_workspace_size(int op, int qtype, int64_t N, int64_t K, int64_t M,
                               int64_t n_expert, int64_t top_k);
@@ -82,16 +83,22 @@ size_t gguf_mm_workspace_size(int op, int qtype, int64_t N, int64_t K, int64_t M
  *   qtype    GGUF_Q8_0 / Q4_K / Q5_K / Q6_K;  K % 256 == 0 (K % 32 for Q8_0)
  *   x        [M, K] of xdt (F32, F16 or BF16), 1 <= M <= 8
  *   residual [M, N] of ydt or NULL;  y [M, N] of ydt
- *   workspace / ws_bytes: unused (may be NULL / 0)
+ *   workspace  device buffer of at least gguf_mm_workspace_size(GGUF_OP_GEMV,
+ *              qtype, N, K, M, 0, 0) bytes, caller-owned, 16-byte aligned.  A
+ *              first kernel writes the quantized activations there (codes, then
+ *              per-32 {d_a, d_a*s, s_lo, s_hi}); the GEMV kernel copies that
+ *              image into every CTA's shared memory.  Its contents are
+ *              meaningless between calls.
  * Errors: INVALID_ARG, UNSUPPORTED (M > 8, M*K too large for on-chip staging),
- * MISALIGNED, CUDA.
+ * WORKSPACE (missing or too small), MISALIGNED, CUDA.
  * Weights are static inputs: the kernel is launched with programmatic
  * dependent launch and starts fetching w while the kernel before it on the
  * stream may still be running (x and residual are read, and y written, only
  * after that kernel has finished).  So w must be complete before the preceding
  * kernel on the stream starts; a weight written by a kernel right before this
  * call needs a stream/event synchronization in between, or GGUF_MM_PDL=0 in the
- * environment, which turns the early fetch off. */
+ * environment, which turns the early fetch off.  The workspace is written only
+ * after the preceding kernel has finished. */
 int gguf_mm_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K,
                  const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
                  void* workspace, size_t ws_bytes, gguf_stream_t stream);
@@ -182,7 +189,8 @@ int gguf_mm_version(void);
  * activation quantizer (taken from the first CTA), and the integer sub-block
  * dots D [M, N, K/sub] i32, sub = 16 for Q6_K and 32 otherwise.  Q6_K dots are
  * of (q6 - 32), Q4_K/Q5_K of the unsigned quant, Q8_0 of the signed quant.
- * Any debug pointer may be NULL.  Also writes y like gguf_mm_gemv. */
+ * Any debug pointer may be NULL.  Also writes y like gguf_mm_gemv.  It takes
+ * no workspace: it allocates one stream-ordered for the call (cudaMallocAsync). */
 int gguf_mm_debug_gemv_terms(const void* w, int qtype, int layout, int64_t N, int64_t K,
                              const void* x, int xdt, int64_t M, void* y, int ydt,
                              int8_t* qa, float* d_a, int32_t* s, int32_t* D,

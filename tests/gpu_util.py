@@ -68,3 +68,10 @@ def check_close(got: np.ndarray, ref: np.ndarray, out_dtype: str, rel: float | N
 def require_gpu():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     g.load_library()
+
+
+def gemv_workspace(M: int, K: int):
+    """A device workspace for gguf_mm_gemv of M rows of K values: (tensor, bytes)."""
+    import gguf_quant_weight_gb300 as g
+    n = g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 0, 1, K, M)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device="cuda"), n

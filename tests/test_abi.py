@@ -52,6 +52,9 @@ def test_argument_errors_need_no_gpu(lib):
     assert f("gguf_mm_gemv", 16, 99, 0, 4, 256, 16, 2, 1, None, 16, 2, None, 0, None) == g.GGUF_ERR_UNSUPPORTED
     assert f("gguf_mm_gemv", 16, 12, 1, 4, 256, 16, 2, 1, None, 16, 2, None, 0, None) == g.GGUF_ERR_UNSUPPORTED
     assert f("gguf_mm_gemv", 18, 12, 0, 4, 256, 16, 2, 1, None, 16, 2, None, 0, None) == g.GGUF_ERR_MISALIGNED
+    assert f("gguf_mm_gemv", 16, 12, 0, 4, 256, 16, 2, 1, None, 16, 2, None, 0, None) == g.GGUF_ERR_WORKSPACE
+    assert f("gguf_mm_gemv", 16, 12, 0, 4, 256, 16, 2, 1, None, 16, 2, 16, 64, None) == g.GGUF_ERR_WORKSPACE
+    assert f("gguf_mm_gemv", 16, 12, 0, 4, 256, 16, 2, 1, None, 16, 2, 24, 1024, None) == g.GGUF_ERR_MISALIGNED
     assert f("gguf_mm_gemm", 16, 12, 0, 4, 256, 16, 2, 8, None, 16, 2, None, 0, 9, None) == g.GGUF_ERR_INVALID_ARG
     assert f("gguf_repack_q6k_planes", 16, 16, 4, 0, None) == g.GGUF_ERR_INVALID_ARG
     assert f("gguf_dequant_padded", 16, 8, 0, 4, 64, 16, 2, 60, None) == g.GGUF_ERR_INVALID_ARG
@@ -60,5 +63,11 @@ def test_argument_errors_need_no_gpu(lib):
 
 
 def test_workspace_sizes_are_consistent(lib):
-    assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 13, 4096, 4096, 1) == 0
+    # GEMV: the quantized activation image, M rows of K codes with 16 pad bytes
+    # after every 128, then 16 bytes per 32-value block and row, 256-rounded
+    for M, K in ((1, 4096), (3, 768), (8, 14336), (2, 32)):
+        img = M * (K + 16 * -(-K // 128)) + M * (K // 32) * 16
+        assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 13, 4096, K, M) == -(-img // 256) * 256
+        assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 13, 4096, K, M) >= -(-img // 256) * 256
+    assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 13, 4096, 4096, 9) == 0
     assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 13, 4096, 4096, 0) == 0

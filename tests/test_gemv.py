@@ -17,8 +17,9 @@ QTYPES = [syn.Q8_0, syn.Q4_K, syn.Q5_K, syn.Q6_K]
 
 def _run_gemv(w_dev, qtype, layout, N, K, x, xdt, M, r, ydt):
     y = torch.empty((M, N), dtype=U.TORCH_DT[ydt], device="cuda")
+    ws, ws_bytes = U.gemv_workspace(M, K)
     g.gguf_mm_gemv(w_dev, qtype, layout, N, K, U.dev(x, xdt), U.DT[xdt], M,
-                   None if r is None else U.dev(r, ydt), y, U.DT[ydt])
+                   None if r is None else U.dev(r, ydt), y, U.DT[ydt], ws, ws_bytes)
     torch.cuda.synchronize()
     return y
 
@@ -78,7 +79,9 @@ def test_gemv_residual_may_alias_output():
     x = syn.normal(rs, (M, K), "bf16")
     r = syn.normal(rs, (M, N), "bf16")
     y = U.dev(r, "bf16").clone()
-    g.gguf_mm_gemv(U.dev(w), syn.Q5_K, 0, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, y, y, g.GGUF_DT_BF16)
+    ws, ws_bytes = U.gemv_workspace(M, K)
+    g.gguf_mm_gemv(U.dev(w), syn.Q5_K, 0, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, y, y, g.GGUF_DT_BF16,
+                   ws, ws_bytes)
     torch.cuda.synchronize()
     ref = O.gemv_int8_path(w, syn.Q5_K, N, K, U.act_f32(x, "bf16"), U.act_f64(r, "bf16"))
     U.check_close(U.host64(y), ref, "bf16")
