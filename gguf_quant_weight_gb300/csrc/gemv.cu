@@ -70,44 +70,40 @@ __device__ __forceinline__ float i2f(int v) { return (float)v; }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+__device__ __forceinline__ float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
 
-// Nearest integer, halves away from zero, for |y| <= 127: truncate, then add
-// one unit when the (exact) remainder is at least one half.
+// Nearest integer, halves away from zero, for |y| <= 127.5: y + copysign(0.5, y)
+// rounded toward zero, then truncated.  Rounding the sum toward zero never
+// carries it across an integer (integers are representable), so the result is
+// floor(|y| + 0.5) with y's sign.
 __device__ __forceinline__ int round_half_away(float y) {
-    const float a = fabsf(y);
-    const float t = truncf(a);
-    const int q = (int)t + (a - t >= 0.5f ? 1 : 0);
-    return y < 0.f ? -q : q;
+    return __float2int_rz(__fadd_rz(y, copysignf(0.5f, y)));
 }
 
 __device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
     return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
 }
 
-// ------------------------------------------------------------------ activation quantizer (prologue)
+// ------------------------------------------------------------------ activation quantizer
 // Per 32 values: amax, d_a = amax/127 (IEEE f32 divide), id = 1/d_a (0 for an
 // all-zero block), q = round-half-away(clamp(x*id, -127, 127)), s = sum q.
 // The image it writes is the GEMV's shared-memory layout byte for byte:
-// [M][qa_row_stride(K)] codes, then [M][K/32] entries of 16 bytes.
-__global__ void __launch_bounds__(256) act_quant_kernel(const GemvParams p) {
-    pdl_launch_dependents();
-    pdl_wait();   // X may come from the kernel before this one on the stream
-    uint8_t* img = static_cast<uint8_t*>(p.act_image);
-    const int64_t qa_row = qa_row_stride(p.K);
-    uint8_t* ds = img + (int64_t)p.M * qa_row;
-    // four threads per 32-value block, eight values each; the block's amax and
-    // code sums are combined with shuffles inside each group of four lanes
-    const int nb = (int)(p.K / 32);
-    const int quarters = 4 * p.M * nb;
-    const int idx = blockIdx.x * 256 + threadIdx.x;
-    const bool on = idx < quarters;
-    const int blk = on ? idx >> 2 : 0, qtr = idx & 3;
-    const int m = blk / nb, b = blk % nb;
-    const int64_t off = (int64_t)m * p.K + (int64_t)b * 32 + 8 * qtr;
-    float v[8];
-    if (!on) {
+// [M][qa_row_stride(K)] codes, then [M][K/32] entries of 16 bytes
+// {d_a, d_a*s, s_lo, s_hi}.
+//
+// Four threads per 32-value block (8 values each, lanes 4j..4j+3 of a warp);
+// the block's amax and code sums are combined with shuffles inside the group,
+// so every lane of the warp must take part (on = false for padding lanes).
+
+// The 8 activation values at element offset `off` of X, as f32.
+__device__ __forceinline__ void load_quarter(const GemvParams& p, bool on, int64_t off, float (&v)[8]) {
+    if (!on) {   // padding lane: any finite non-zero block (nothing is stored)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.f;
+        for (int i = 0; i < 8; ++i) v[i] = 1.f;
     } else if (p.xdt == GGUF_DT_F32) {
         const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x) + off);
         const float4 a = src[0], c = src[1];
@@ -116,43 +112,113 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const GemvParams p) {
         const uint4 t = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x) + off);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const uint32_t wv = comp(t, j), lo = wv & 0xFFFFu, hi = wv >> 16;
+            const uint32_t wv = comp(t, j);
             if (p.xdt == GGUF_DT_BF16) {
-                v[2 * j] = __uint_as_float(lo << 16);
-                v[2 * j + 1] = __uint_as_float(hi << 16);
+                v[2 * j] = __uint_as_float(wv << 16);
+                v[2 * j + 1] = __uint_as_float(wv & 0xFFFF0000u);
             } else {
-                v[2 * j] = f16_bits_to_float(lo);
-                v[2 * j + 1] = f16_bits_to_float(hi);
+                v[2 * j] = f16_bits_to_float(wv & 0xFFFFu);
+                v[2 * j + 1] = f16_bits_to_float(wv >> 16);
             }
         }
     }
+}
+
+// Quantizes one quarter; writes its 8 codes at `codes` and (quarter 0) the
+// block's entry at `entry` (generic pointers: global workspace or shared).
+__device__ __forceinline__ void quant_values(const float (&v)[8], bool on, int qtr, uint8_t* codes, uint8_t* entry) {
+    // amax propagates NaN (a NaN anywhere in the block makes d_a NaN)
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    for (int i = 0; i < 8; ++i) amax = max_nan(amax, fabsf(v[i]));
+    amax = max_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max_nan(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const float d = amax / 127.0f;
     const float id = d != 0.f ? 1.0f / d : 0.f;
-    int s8 = 0;
-    uint32_t word[2] = {0u, 0u};
+    // clamp, then round (NaN clamps to -127); no branch, so the quarters of a
+    // round interleave
+    int q[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        float y = v[i] * id;
-        y = fminf(fmaxf(y, -127.f), 127.f);
-        const int q = round_half_away(y);
-        s8 += q;
-        word[i >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i & 3));
+    for (int i = 0; i < 8; ++i) q[i] = round_half_away(fminf(fmaxf(v[i] * id, -127.f), 127.f));
+    uint32_t word[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        // cvt.pack.sat.s8.s32.b32 d, a, b, c: d = (c << 16) | (a << 8) | b
+        // (a, b saturated to s8), so the inner pair becomes the upper bytes
+        uint32_t hi;
+        asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi) : "r"(q[4 * j + 3]), "r"(q[4 * j + 2]));
+        asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(word[j]) : "r"(q[4 * j + 1]), "r"(q[4 * j]), "r"(hi));
     }
+    const int s8 = dp4a(word[0], 0x01010101u, dp4a(word[1], 0x01010101u, 0));
     const int s_pair = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);   // s_lo (quarters 0,1) or s_hi (2,3)
     const int s_other = __shfl_xor_sync(0xffffffffu, s_pair, 2);
     if (on) {
-        *reinterpret_cast<uint2*>(img + (int64_t)m * qa_row + qa_pos(b * 32) + 8 * qtr) = make_uint2(word[0], word[1]);
+        *reinterpret_cast<uint2*>(codes) = make_uint2(word[0], word[1]);
         if (qtr == 0) {
             const int s = s_pair + s_other;
-            *reinterpret_cast<uint4*>(ds + 16 * ((int64_t)m * nb + b)) =
+            *reinterpret_cast<uint4*>(entry) =
                 make_uint4(__float_as_uint(d), __float_as_uint(d * (float)s), (uint32_t)s_pair, (uint32_t)s_other);
         }
     }
+}
+
+// Quarter qtr of block b of row m, into an image over all of K at img.
+__device__ __forceinline__ void quant_quarter(const GemvParams& p, bool on, int m, int b, int qtr, uint8_t* img) {
+    const int64_t qa_row = qa_row_stride(p.K);
+    const int nb = (int)(p.K / 32);
+    float v[8];
+    load_quarter(p, on, (int64_t)m * p.K + (int64_t)b * 32 + 8 * qtr, v);
+    quant_values(v, on, qtr, img + (int64_t)m * qa_row + qa_pos(b * 32) + 8 * qtr,
+                 img + (int64_t)p.M * qa_row + 16 * ((int64_t)m * nb + b));
+}
+
+// Threads [0, nthreads) of a block quantize the K slice [k0, k0 + klen) of all
+// M rows into an image of that slice at img (codes [M][qa_row_stride(klen)],
+// then [M][klen/32] entries).  Each thread takes UNR quarters per round and
+// issues all their loads before quantizing any; a warp stops once its first
+// quarter of a round is past the end (the group shuffles stay warp-uniform).
+template <int UNR>
+__device__ __forceinline__ void quantize_slice(const GemvParams& p, int64_t k0, int klen, uint8_t* img, int t0,
+                                               int nthreads) {
+    const int nb = klen / 32;
+    const int per_row = 4 * nb;
+    const int quarters = p.M * per_row;
+    const uint32_t qa_row = (uint32_t)qa_row_stride(klen);
+    const int qtr = t0 & 3;
+    for (int base = 0; base < quarters; base += UNR * nthreads) {
+        if (base + (t0 & ~31) >= quarters) break;
+        float v[UNR][8];
+        int m[UNR], b[UNR];
+        bool on[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int idx = base + u * nthreads + t0;
+            on[u] = idx < quarters;
+            const int i = on[u] ? idx : 0;
+            m[u] = i / per_row;
+            b[u] = (i - m[u] * per_row) >> 2;
+            load_quarter(p, on[u], (int64_t)m[u] * p.K + k0 + 32 * b[u] + 8 * qtr, v[u]);
+        }
+        // straight-line over the UNR quarters (padding quarters compute on
+        // zeros and store nothing), so their dependency chains interleave
+#pragma unroll
+        for (int u = 0; u < UNR; ++u)
+            quant_values(v[u], on[u], qtr, img + m[u] * qa_row + qa_pos(32 * b[u]) + 8 * qtr,
+                         img + (uint32_t)p.M * qa_row + 16u * (uint32_t)(m[u] * nb + b[u]));
+    }
+}
+
+// The stand-alone quantizer for the kernels that take the image from the
+// workspace: one thread per quarter block.
+__global__ void __launch_bounds__(256) act_quant_kernel(const GemvParams p) {
+    pdl_launch_dependents();
+    pdl_wait();   // X may come from the kernel before this one on the stream
+    const int nb = (int)(p.K / 32);
+    const int quarters = 4 * p.M * nb;
+    const int idx = blockIdx.x * 256 + threadIdx.x;
+    const bool on = idx < quarters;
+    const int blk = on ? idx >> 2 : 0;
+    quant_quarter(p, on, blk / nb, blk % nb, idx & 3, static_cast<uint8_t*>(p.act_image));
 }
 
 // Bytes of the activation image.
@@ -743,7 +809,20 @@ __global__ void __launch_bounds__(direct_threads(MT), 1) gemv_direct_kernel(cons
     pdl_launch_dependents();
 
     pdl_wait();
+    // the CTA's residual values: one round trip for all of them, under the
+    // image copy (shared memory after the image barrier)
+    float* res = reinterpret_cast<float*>(smem_raw + (sh.ds - sh.qa) + 16 * p.M * nb + 16);
+    const int nrows = row0 < row_end ? (int)(row_end - row0) : 0;
+    float res0 = 0.f;
+    if (p.residual && tid < p.M * nrows)
+        res0 = load_act(p.residual, p.ydt, (int64_t)(tid / nrows) * p.N + row0 + tid % nrows);
     load_act_image(p, sh, reinterpret_cast<uint64_t*>(smem_raw + (sh.ds - sh.qa) + 16 * p.M * nb));
+    if (p.residual) {
+        if (tid < p.M * nrows) res[(tid / nrows) * p.rows_per_cta + tid % nrows] = res0;
+        for (int i = tid + NT; i < p.M * nrows; i += NT)
+            res[(i / nrows) * p.rows_per_cta + i % nrows] =
+                load_act(p.residual, p.ydt, (int64_t)(i / nrows) * p.N + row0 + i % nrows);
+    }
     __syncthreads();
     if (DUMP && blockIdx.x == 0) {
         for (int64_t i = tid; i < (int64_t)p.M * p.K; i += NT) {
@@ -784,7 +863,7 @@ __global__ void __launch_bounds__(direct_threads(MT), 1) gemv_direct_kernel(cons
         if (head && valid) {
             for (int m = 0; m < p.M && m < MT; ++m) {
                 float v = acc[m];
-                if (p.residual) v += load_act(p.residual, p.ydt, (int64_t)m * p.N + n);
+                if (p.residual) v += res[m * p.rows_per_cta + (n - row0)];
                 store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
             }
         }
@@ -853,6 +932,230 @@ __global__ void __launch_bounds__(direct_threads(MT), 1) gemv_direct_kernel(cons
     }
 }
 
+// ------------------------------------------------------------------ tile kernel
+// Q4_K / Q5_K blocks, for shapes where a CTA's share of W and its activation
+// image fit in half of an SM's shared memory.  Two CTAs then share an SM: the
+// CTA of the next call on the stream (programmatic dependent launch) becomes
+// resident while this call computes, and its first act is to request all of
+// its weight bytes with bulk copies -- so the next call's weight stream runs
+// under this call's compute and a chain of calls is bound by HBM rather than
+// by per-call latency.
+//
+// Split K: the S CTAs of a thread-block cluster take the S K slices of the same
+// rows.  After its dependency wait each CTA quantizes only its slice of X (no
+// second kernel, no second wait in the chain, and the quantizer work is not
+// repeated by every CTA); the slices' partial row sums meet in distributed
+// shared memory, each CTA adding up an equal share of the rows in slice order.
+// One mbarrier per group of P rows (the rows a warp pass covers); warps take
+// groups round-robin; a lane's unit is the same for every row, so at M = 1 its
+// activation codes stay in registers.
+// warps per CTA: 16 at M = 1 (more rows in flight; registers allow it), else 8
+__host__ __device__ constexpr int tile_warps(int mt) { return mt == 1 ? 16 : 8; }
+
+// Shared-memory layout of the tile kernel (byte offsets).
+struct TileLayout {
+    int64_t img, part, res, bars, total;
+};
+__host__ __device__ inline TileLayout tile_layout(int64_t M, int64_t klen, int64_t rows_per_cta, int64_t slice_bytes,
+                                                  int S) {
+    const int64_t U = klen / 128;
+    const int64_t P = U < 32 ? 32 / U : 1;
+    TileLayout L;
+    L.img = ceil_div(rows_per_cta * slice_bytes, 128) * 128;
+    L.part = L.img + ceil_div(act_image_bytes(M, klen), 16) * 16;
+    L.res = L.part + (S > 1 ? ceil_div(4 * M * rows_per_cta, 16) * 16 : 0);
+    L.bars = L.res + ceil_div(4 * M * rows_per_cta, 16) * 16;
+    L.total = L.bars + 8 * ceil_div(rows_per_cta, P);
+    return L;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+    return v;
+}
+
+template <int QT, int MT, bool DUMP>
+__global__ void __launch_bounds__(tile_warps(MT) * 32, 2) gemv_tile_kernel(const GemvParams p) {
+    constexpr int NW = tile_warps(MT), NT = NW * 32;
+    constexpr int bb = QT == GGUF_Q4_K ? 144 : 176;
+    constexpr bool AREG = false;     // activation codes read from shared memory
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int S = p.ksplit;
+    const int s = (int)(blockIdx.x % S);          // the CTA's rank in its cluster of S
+    const int64_t row0 = (int64_t)(blockIdx.x / S) * p.rows_per_cta;
+    const int rows = (int)min(p.rows_per_cta, p.N - row0);
+    const int klen = (int)(p.K / S);              // values in this CTA's K slice
+    const int kb0 = s * (klen / 256);             // its first super-block
+    const int nbs = klen / 32;                    // activation blocks in the slice
+    const int U = klen / 128;                     // units per row slice
+    const int P = U < 32 ? 32 / U : 1;            // rows per warp pass
+    const int ngroups = (rows + P - 1) / P;
+    const uint32_t sb = (uint32_t)(klen / 256) * bb;   // bytes of one row slice
+    const TileLayout L = tile_layout(p.M, klen, p.rows_per_cta, sb, S);
+    const uint32_t tile = smem_u32(smem_raw);
+    uint8_t* img = smem_raw + L.img;
+    float* part = reinterpret_cast<float*>(smem_raw + L.part);
+    float* res = reinterpret_cast<float*>(smem_raw + L.res);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bars);
+    Shared sh;
+    sh.qa_row = (uint32_t)qa_row_stride(klen);
+    sh.qa = smem_u32(img);
+    sh.ds = sh.qa + (uint32_t)p.M * sh.qa_row;
+    sh.stage = tile;
+
+    // 1. every row slice requested at once, before the dependency wait (the
+    // lanes of warp 0 share the issuing; one barrier per group of P rows)
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int gi = 0; gi < ngroups; ++gi) mbar_init(&bars[gi], 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        for (int gi = lane; gi < ngroups; gi += 32) {
+            const int r = gi * P, nr = min(P, rows - r);
+            mbar_arrive_expect_tx(&bars[gi], (uint32_t)nr * sb);
+            for (int j = 0; j < nr; ++j)
+                bulk_g2s_u32(tile + (uint32_t)(r + j) * sb, p.w + (row0 + r + j) * p.rb + (int64_t)kb0 * bb, sb,
+                             &bars[gi]);
+        }
+    }
+    pdl_launch_dependents();
+
+    // 2. the producer of X has finished: the tile's residual values are read
+    // now (one round trip for all of them, under the quantizer) and this K
+    // slice is quantized
+    pdl_wait();
+    const bool res_now = p.residual && S == 1;
+    float res0 = 0.f;   // this thread's first residual value, held until after the quantizer
+    if (res_now && tid < p.M * rows) {
+        const int m = tid / rows, r = tid - m * rows;
+        res0 = load_act(p.residual, p.ydt, (int64_t)m * p.N + row0 + r);
+    }
+    {
+        const int rounds = (4 * p.M * (klen / 32) + NT - 1) / NT;   // quarters per thread
+        if (rounds >= 4) quantize_slice<4>(p, (int64_t)s * klen, klen, img, tid, NT);
+        else if (rounds >= 2) quantize_slice<2>(p, (int64_t)s * klen, klen, img, tid, NT);
+        else quantize_slice<1>(p, (int64_t)s * klen, klen, img, tid, NT);
+    }
+    if (res_now) {
+        if (tid < p.M * rows) res[(tid / rows) * p.rows_per_cta + tid % rows] = res0;
+        for (int i = tid + NT; i < p.M * rows; i += NT) {
+            const int m = i / rows, r = i - m * rows;
+            res[m * p.rows_per_cta + r] = load_act(p.residual, p.ydt, (int64_t)m * p.N + row0 + r);
+        }
+    }
+    __syncthreads();   // the image, and the barrier initialisation, are visible
+    if (DUMP && row0 == 0) {
+        for (int i = tid; i < p.M * klen; i += NT) {
+            const int m = i / klen, k = i % klen;
+            const uint32_t a = sh.qa + (uint32_t)m * sh.qa_row + qa_pos((uint32_t)k);
+            if (p.dbg_qa) p.dbg_qa[(int64_t)m * p.K + (int64_t)s * klen + k] = (int8_t)(lds32(a & ~3u) >> (8 * (a & 3)));
+        }
+        for (int i = tid; i < p.M * nbs; i += NT) {
+            const int m = i / nbs, b = i % nbs;
+            const uint4 e = lds128(sh.ds + 16u * i);
+            const int64_t o = (int64_t)m * (p.K / 32) + (int64_t)s * nbs + b;
+            if (p.dbg_da) p.dbg_da[o] = __uint_as_float(e.x);
+            if (p.dbg_s) p.dbg_s[o] = (int32_t)(e.z + e.w);
+        }
+    }
+
+    // 3. rows: lane -> (row of the pass, unit); a segmented shuffle reduction
+    using Act = ActSlice<MT, AREG, 8, 4>;
+    const int seg = U < 32 ? U : 32;
+    const int sub_row = U < 32 ? lane / U : 0;
+    const int u0 = U < 32 ? lane % U : lane;
+    const bool lane_on = U >= 32 || lane < P * U;
+    const int seg_end = (lane / seg) * seg + seg;
+    const bool head = lane_on && (lane % seg) == 0;
+    Act fixed;
+    if (U <= 32) fixed.init(sh, 128 * u0, nbs);
+    for (int gi = warp; gi < ngroups; gi += NW) {
+        mbar_wait(&bars[gi], 0, p.status);
+        const int r = gi * P + sub_row;
+        const bool valid = lane_on && r < rows;
+        const int64_t n = row0 + r;
+        float acc[1][MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[0][m] = 0.f;
+        if (valid) {
+            const int64_t nn[1] = {n};
+            const bool on[1] = {true};
+            if (U <= 32) {
+                FragQ45<QT> f;
+                f.load(tile + (uint32_t)r * sb + (uint32_t)(u0 >> 1) * bb, u0 & 1);
+                const FragQ45<QT>* fr[1] = {&f};
+                unit_q45k<QT, MT, 1, Act, DUMP>(p, fr, fixed, kb0 + (u0 >> 1), u0 & 1, acc, nn, on);
+            } else {
+                for (int u = u0; u < U; u += 32) {
+                    FragQ45<QT> f;
+                    f.load(tile + (uint32_t)r * sb + (uint32_t)(u >> 1) * bb, u & 1);
+                    ActSlice<MT, false, 8, 4> a;
+                    a.init(sh, 128 * u, nbs);
+                    const FragQ45<QT>* fr[1] = {&f};
+                    unit_q45k<QT, MT, 1, ActSlice<MT, false, 8, 4>, DUMP>(p, fr, a, kb0 + (u >> 1), u & 1, acc, nn,
+                                                                        on);
+                }
+            }
+        }
+        if (seg == 32) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc[0][m] += __shfl_xor_sync(0xffffffffu, acc[0][m], o);
+            }
+        } else {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float t = __shfl_down_sync(0xffffffffu, acc[0][m], o);
+                    if (lane + o < seg_end) acc[0][m] += t;
+                }
+            }
+        }
+        if (head && valid) {
+            for (int m = 0; m < p.M && m < MT; ++m) {
+                if (S > 1) {
+                    part[m * p.rows_per_cta + r] = acc[0][m];
+                } else {
+                    float v = acc[0][m];
+                    if (p.residual) v += res[m * p.rows_per_cta + r];
+                    store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
+                }
+            }
+        }
+    }
+
+    // 4. split K: the slices' partials meet in distributed shared memory; CTA s
+    // finishes rows [s*share, (s+1)*share) of the group, adding slices in order
+    if (S > 1) {
+        cluster_sync_all();
+        const int share = (rows + S - 1) / S;
+        const int rbeg = min(rows, s * share), cnt = min(rows, rbeg + share) - rbeg;
+        for (int i = tid; i < cnt * p.M; i += NT) {
+            const int m = i / cnt, r = rbeg + i % cnt;
+            const uint32_t la = smem_u32(part + m * p.rows_per_cta + r);
+            float v = 0.f;
+            for (int q = 0; q < S; ++q) v += ld_dsmem_f32(dsmem_map(la, (uint32_t)q));
+            const int64_t n = row0 + r;
+            if (p.residual) v += load_act(p.residual, p.ydt, (int64_t)m * p.N + n);
+            store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
+        }
+        cluster_sync_all();   // every CTA's partials stay in place until all are read
+    }
+}
+
 template <int QT, int MT, int LAYOUT, bool DUMP>
 cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
     const int U = (int)(p.K / (QT == GGUF_Q8_0 ? 32 : 128));
@@ -860,21 +1163,35 @@ cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t 
     if constexpr (MT == 1) {
         if (U <= 32) k = gemv_kernel<QT, MT, LAYOUT, true, DUMP>;
     }
+    int threads = p.direct ? direct_threads(MT) : kThreads;
     if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K || (QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES)) {
         if (p.direct) k = gemv_direct_kernel<QT, MT, DUMP>;
+    }
+    if constexpr ((QT == GGUF_Q4_K || QT == GGUF_Q5_K) && LAYOUT == GGUF_LAYOUT_BLOCKS) {
+        if (p.tile) {
+            k = gemv_tile_kernel<QT, MT, DUMP>;
+            threads = tile_warps(MT) * 32;
+        }
     }
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(p.direct ? direct_threads(MT) : kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.tile && p.ksplit > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)p.ksplit;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, k, p);
 }
 
@@ -915,9 +1232,37 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
     p.stage_bytes = ceil_div(P * p.rb + 48, 16) * 16;
     // one CTA per SM; it keeps to half of the shared memory so that a CTA of
     // the next call on the stream (programmatic dependent launch) fits beside it
+    const int64_t half = std::min<int64_t>(max_smem, 232448 / 2 - 1024);
+    // the tile kernel when a CTA's share of W and its image fit beside a second
+    // CTA: K split over a cluster of ksplit CTAs (2 keeps every SM in use; the
+    // quantizer work per CTA halves) unless one activation row is all there is
+    p.tile = 0;
+    p.ksplit = 1;
+    if ((p.qtype == GGUF_Q4_K || p.qtype == GGUF_Q5_K) && p.layout == GGUF_LAYOUT_BLOCKS) {
+        const int64_t KB = p.K / 256;
+        for (int S : {1}) {
+            if (S == 2 && (p.M < 2 || KB % 2 != 0 || num_sms % 2 != 0)) continue;
+            // the quantizer is repeated by every CTA: worth it for one row,
+            // beaten by the stand-alone quantizer kernel from two rows on
+            if (p.M > 1) continue;
+            const int64_t klen = p.K / S, sb = (klen / 256) * bb;
+            const int64_t G = num_sms / S;
+            const int64_t rpc_t = ceil_div(p.N, G);
+            const TileLayout L = tile_layout(p.M, klen, rpc_t, sb, S);
+            if (L.total <= half) {
+                p.tile = 1;
+                p.ksplit = S;
+                p.direct = 0;
+                p.rows_per_cta = rpc_t;
+                p.stage_bytes = L.img;
+                *grid = (int)(ceil_div(p.N, rpc_t) * S);
+                *smem = (size_t)L.total;
+                return GGUF_OK;
+            }
+        }
+    }
     const int64_t rpc = ceil_div(p.N, (int64_t)num_sms);
     const int64_t groups_per_warp = ceil_div(ceil_div(rpc, P), NW);
-    const int64_t half = std::min<int64_t>(max_smem, 232448 / 2 - 1024);
     int64_t R = std::min<int64_t>({groups_per_warp, 8, (half - act) / (NW * p.stage_bytes)});
     if (R < 1) R = std::min<int64_t>({groups_per_warp, 8, (max_smem - act) / (NW * p.stage_bytes)});
     if (R < 1) return GGUF_ERR_UNSUPPORTED;
@@ -928,11 +1273,14 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
     p.chunk_rows = 0;
     *grid = (int)ceil_div(p.N, rpc);
     // + the image barrier (8 bytes, after the per-warp ring barriers)
-    *smem = p.direct ? (size_t)(act + 8) : (size_t)(act + NW * R * p.stage_bytes + NW * R * 8 + 8);
+    // direct: image, its barrier (16 bytes with padding), the residual values
+    *smem = p.direct ? (size_t)(act + 16 + 4 * p.M * rpc)
+                     : (size_t)(act + NW * R * p.stage_bytes + NW * R * 8 + 8);
     return GGUF_OK;
 }
 
 cudaError_t gemv_launch(const GemvParams& p, int grid, size_t smem, bool dump, cudaStream_t stream) {
+    if (p.tile) return dump ? launch_dispatch<true>(p, grid, smem, stream) : launch_dispatch<false>(p, grid, smem, stream);
     // 1. per-32 activation quantizer -> image in the workspace
     const int quarters = 4 * p.M * (int)(p.K / 32);
     cudaLaunchConfig_t cfg = {};

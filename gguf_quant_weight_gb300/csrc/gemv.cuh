@@ -19,6 +19,8 @@ struct GemvParams {
     int pdl;               // launch with programmatic stream serialization
     void* act_image;       // workspace: the quantized activations (codes + per-block entries)
     int direct;            // unit fields 16-byte aligned: load straight into registers
+    int tile;              // the CTA's rows staged whole in shared memory, two CTAs per SM
+    int ksplit;            // tile kernel: K slices per row group (a cluster of that many CTAs)
     // plan (filled by gemv_plan)
     int64_t rb;            // bytes per weight row (raw layout)
     int64_t rows_per_cta;  // rows owned by one CTA

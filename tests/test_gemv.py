@@ -170,3 +170,40 @@ def test_gemv_config_q5k_4096x4096_residual(M):
 
 def test_gemv_status_ok_after_runs():
     assert g.gguf_mm_check_errors() == 0
+
+
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q6_K])
+def test_gemv_activation_quantizer_non_finite_and_extreme_blocks(qtype):
+    # the same rule as the oracle on every input: ties away from zero over a
+    # whole range of halves, a NaN block (NaN scale, every code -127), an inf
+    # block (scale inf, codes 0 except -127 at the inf), a block whose 1/d_a
+    # overflows (every code 127), one just above that limit, and huge values.
+    # Q4_K runs the quantizer inside the GEMV kernel, raw Q6_K the stand-alone one.
+    N, K, M = 8, 512, 2
+    rs = syn.rng(11)
+    w = syn.weight_blocks(rs, qtype, N, K)
+    x = np.zeros((M, K), np.float32)
+    x[0, 0] = 127.0
+    x[0, 1:32] = np.arange(-15, 16) + 0.5
+    x[0, 32:64] = np.linspace(-3, 3, 32)
+    x[0, 37] = np.nan
+    x[0, 64:96] = 1.0
+    x[0, 72] = np.inf
+    x[0, 96:128] = 1e-39
+    x[0, 128:160] = 4e-37 * rs.standard_normal(32)
+    x[0, 160:192] = 3.0e38 * np.sign(rs.standard_normal(32))
+    x[0, 192:224] = -np.inf
+    x[1] = rs.standard_normal(K).astype(np.float32)
+    x[1, 256:288] = np.float32(127.0) * (np.arange(32) % 2) - 0.5 * (np.arange(32) % 3)
+    qa = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+    da = torch.zeros((M, K // 32), dtype=torch.float32, device="cuda")
+    s = torch.zeros((M, K // 32), dtype=torch.int32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    g.gguf_mm_debug_gemv_terms(U.dev(w), qtype, 0, N, K, U.dev(x), g.GGUF_DT_F32, M, y, g.GGUF_DT_F32,
+                               qa, da, s, None)
+    torch.cuda.synchronize()
+    with np.errstate(all="ignore"):
+        rqa, rda, rs_ = O.quantize_act_q8(x)
+    assert np.array_equal(qa.cpu().numpy(), rqa)
+    assert np.array_equal(da.cpu().numpy(), rda, equal_nan=True)
+    assert np.array_equal(s.cpu().numpy(), rs_)
