@@ -7,18 +7,21 @@
 // the tile grows with the row count.
 //
 // GB300 shape of it (one 128-weight-row x BN-token tile per CTA, swap-AB):
-//   warp 0     TMA producer: the tile's raw super-block bytes (one 256-value
-//              column of 128 rows per raw slot: Q4_K/Q5_K/Q8_0 blocks, raw
-//              Q6_K rows from their 16-byte boundary, or the four Q6_K
-//              planes), and the f16 activation tile of each 64-value k step
+//   warp 0     TMA producer of the raw weights: the tile's super-block bytes
+//              (one 256-value column of 128 rows per raw slot: Q4_K/Q5_K/Q8_0
+//              blocks, raw Q6_K rows from their 16-byte boundary, or the four
+//              Q6_K planes), up to RS super-blocks ahead -- its own warp, so the
+//              weight stream never waits on the MMA's operand stages
 //   warp 1     TMEM allocation and tcgen05.mma issue (128 x BN x 16 per MMA,
 //              f32 accumulators in TMEM), one commit per stage
-//   warps 2-9  decoders: each k step, 256 threads turn 128 rows x 64 values of
-//              raw bytes into f16 (packed f16 math: w = fl16(d*sc)*q - fl16(dmin*m)
-//              in one fused multiply-add per value pair)
-//              written straight into the 128-byte-swizzled K-major operand
-//              layout the MMA reads; then the epilogue (TMEM -> registers,
-//              + residual, store)
+//   warp 2     TMA producer of the f16 activation tile of each 64-value k step
+//   warps 3..  decoders (16 warps for Q4_K/Q5_K/Q6_K planes, 8 otherwise):
+//              each k step they turn 128 rows x 64 values of raw bytes into f16
+//              (packed f16 math: w = fl16(d*sc)*q - fl16(dmin*m) in one fused
+//              multiply-add per value pair; the scales of a super-block are
+//              computed once, at its first k step), written straight into the
+//              128-byte-swizzled K-major operand layout the MMA reads; then the
+//              epilogue (TMEM -> registers, + residual, store)
 // The MMA never waits on decode of the same stage it consumes: stages ring
 // through S slots, so decode of step i+1.. overlaps the MMAs of step i.
 #include <cstring>
@@ -30,8 +33,15 @@ namespace gg {
 
 namespace {
 
-constexpr int kDecodeWarps = 8;
-constexpr int kFusedThreads = 64 + 32 * kDecodeWarps;   // 320
+// decoder warps: 16 (each thread a quarter of a 64-value k step) for the
+// layouts decoded from a per-super-block state, else 8 (each thread a half)
+__host__ __device__ constexpr bool state_decoder(int qt, int layout) {
+    return qt == GGUF_Q4_K || qt == GGUF_Q5_K || (qt == GGUF_Q6_K && layout == GGUF_LAYOUT_Q6K_PLANES);
+}
+__host__ __device__ constexpr int decode_warps(int qt, int layout) { return state_decoder(qt, layout) ? 16 : 8; }
+// warp 0: raw-weight TMA producer; warp 1: TMEM + MMA issue; warp 2: activation
+// TMA producer; warps 3..: decoders (and the epilogue)
+__host__ __device__ constexpr int fused_threads(int qt, int layout) { return 96 + 32 * decode_warps(qt, layout); }
 
 __host__ __device__ constexpr int raw_pitch(int qt, int layout) {
     // bytes per weight row in one raw slot (= the TMA box's inner extent)
@@ -44,16 +54,25 @@ __host__ __device__ constexpr int raw_slot_bytes(int qt, int layout) {
 
 template <int BN, int RAW>
 struct FusedCfg {
-    static constexpr int A_BYTES = 128 * 64 * 2;
+    // The decoded weight tile (the MMA's A operand, 128 rows x 64 f16 per k
+    // step) lives in tensor memory: decoders write it with tcgen05.st and the
+    // MMA reads it from there, so shared memory carries only the activation
+    // tiles (B) and the raw blocks.  One ring of S stages covers both operands
+    // of a k step (one "full" barrier: the decoder warps plus the activation
+    // TMA; one "empty" barrier: one commit), which keeps the single MMA-issuing
+    // thread's work per step small -- that thread, not the tensor core, is
+    // what limits the step rate at these tile shapes.
+    static constexpr int A_COLS = 32;                 // TMEM columns per decoded stage
+    static constexpr int A_COL0 = 256;                // first decoded-stage column (after the accumulator)
     static constexpr int B_BYTES = BN * 64 * 2;
-    static constexpr int S = BN >= 256 ? 3 : 4;        // operand stages
-    // raw slots: whatever shared memory the operand stages leave (each covers
-    // four k steps, so a deep raw ring is what hides the HBM latency)
-    static constexpr int RS_FIT = (232448 - 2048 - S * (A_BYTES + B_BYTES)) / RAW;
+    static constexpr int S = BN >= 256 ? 4 : 6;       // stages
+    // raw slots: what the activation stages leave (each covers four k steps)
+    static constexpr int RS_FIT = (232448 - 2048 - S * B_BYTES) / RAW;
     static constexpr int RS = RS_FIT > 6 ? 6 : RS_FIT;
-    static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
-    static constexpr int SMEM = S * (A_BYTES + B_BYTES) + RS * RAW + 1024 + 256;
+    static constexpr int TMEM_COLS = 512;             // accumulator [0, BN) + decoded stages
+    static constexpr int SMEM = S * B_BYTES + RS * RAW + 1024 + 256;
     static_assert(RS >= 2, "raw ring needs two slots");
+    static_assert(A_COL0 + S * A_COLS <= TMEM_COLS && BN <= A_COL0, "TMEM columns");
 };
 
 struct FusedParams {
@@ -125,6 +144,173 @@ __device__ __forceinline__ void emit32_h(const uint32_t q4[8], __half2 bias, __h
             const uint32_t w = q4[2 * c + t];
             h[2 * t] = bits_h2(__hfma2(__hsub2(magic_lo(w), bias), sc, __hneg2(off)));
             h[2 * t + 1] = bits_h2(__hfma2(__hsub2(magic_hi(w), bias), sc, __hneg2(off)));
+        }
+        out[c] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
+// ---- per-super-block decoder state
+// A decoder thread owns one weight row r and one half hf of every 64-value k
+// step, i.e. the 32-value sub-blocks j = 2q + hf (q = 0..3) of each super-block
+// (Q4_K/Q5_K) or the 16-value sub-blocks 8(q/2) + 2g, +1 with g = 2(q%2) + hf
+// (Q6_K).  Everything that depends only on the super-block -- the f16 scale
+// and min of those sub-blocks, Q5_K's high-bit bytes -- is read and computed
+// once per super-block, leaving four lean k steps.
+template <int QT, int LAYOUT>
+struct KbState {
+    __half2 sc[4], noff[4];   // per k step (Q6_K: first / second 16-value half)
+    uint32_t qh[8];           // Q5_K: the 32 high-bit bytes
+    // hh >= 0: a quarter-step decoder (16 warps) -- only its own 16 qh bytes
+    // are kept (in qh[0..3]) and, for Q6_K, only its 16-value sub-block's scale
+    // (in sc[q]); hh < 0: a half-step decoder
+    __device__ __forceinline__ void prepare(uint32_t row, uint32_t slot, int r, int hf, int kb, int hh = -1) {
+        if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
+            const uint4 hdr = lds128u(row);
+            const float d = f16_bits_to_float(hdr.x), dmin = f16_bits_to_float(hdr.x >> 16);
+            // 6-bit scale/min of sub-blocks 0..3 (low bytes) and 4..7 (packed)
+            const uint32_t sc_lo = hdr.y & 0x3F3F3F3Fu, mn_lo = hdr.z & 0x3F3F3F3Fu;
+            const uint32_t sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+            const uint32_t mn_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = 2 * q + hf;   // runtime only through hf
+                const uint32_t scw = q < 2 ? sc_lo : sc_hi, mnw = q < 2 ? mn_lo : mn_hi;
+                const int bi = (2 * q + hf) & 3;
+                (void)j;
+                sc[q] = __float2half2_rn(d * (float)byte_of(scw, bi));
+                noff[q] = __hneg2(__float2half2_rn(dmin * (float)byte_of(mnw, bi)));
+            }
+            if constexpr (QT == GGUF_Q5_K) {
+                if (hh >= 0) {
+                    const uint4 h0 = lds128u(row + 16 + 16 * hh);
+                    qh[0] = h0.x; qh[1] = h0.y; qh[2] = h0.z; qh[3] = h0.w;
+                } else {
+                    const uint4 h0 = lds128u(row + 16), h1 = lds128u(row + 32);
+                    qh[0] = h0.x; qh[1] = h0.y; qh[2] = h0.z; qh[3] = h0.w;
+                    qh[4] = h1.x; qh[5] = h1.y; qh[6] = h1.z; qh[7] = h1.w;
+                }
+            }
+        } else if constexpr (QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES) {
+            const uint32_t sc_addr = slot + 128u * 192 + 16u * r;
+            const uint32_t dq = slot + 128u * 208 + 16u * r + (uint32_t)((2 * kb) & 15);
+            const float d = f16_bits_to_float(lds16u(dq));
+            const uint4 scv = lds128u(sc_addr);   // the 16 signed scales
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int h = q >> 1;
+                const int j0 = 8 * h + 4 * (q & 1) + 2 * hf;   // 8h + 2g
+                const uint32_t w = word_of(scv, j0 >> 2);
+                const int b = j0 & 3;
+                if (hh >= 0) {
+                    sc[q] = __float2half2_rn(d * (float)(int8_t)byte_of(w, b + hh));
+                } else {
+                    sc[q] = __float2half2_rn(d * (float)(int8_t)byte_of(w, b));
+                    noff[q] = __float2half2_rn(d * (float)(int8_t)byte_of(w, b + 1));   // second half's scale
+                }
+            }
+        }
+    }
+};
+
+// k step q of a super-block from a prepared state (Q4_K, Q5_K, Q6_K planes)
+template <int QT, int LAYOUT>
+__device__ __forceinline__ void decode_step(const KbState<QT, LAYOUT>& st, uint32_t row, uint32_t slot, int r, int q,
+                                            int hf, uint4 out[4]) {
+    uint32_t q4[8];
+    if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
+        const uint32_t qs = row + (QT == GGUF_Q5_K ? 48 : 16) + 32 * q;
+        const uint4 a = lds128u(qs), b = lds128u(qs + 16);
+        const uint32_t sh = 4u * (uint32_t)hf;
+        const uint32_t rot = (uint32_t)(4 - (2 * q + hf)) & 31u;   // bit j of a byte -> bit 4
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = word_of(i < 4 ? a : b, i & 3);
+            uint32_t v = (w >> sh) & 0x0F0F0F0Fu;
+            if constexpr (QT == GGUF_Q5_K) v |= __funnelshift_l(st.qh[i], st.qh[i], rot) & 0x10101010u;
+            q4[i] = v;
+        }
+        const __half2 bias = __float2half2_rn(1024.f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t h[4];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const uint32_t w = q4[2 * c + t];
+                h[2 * t] = bits_h2(__hfma2(__hsub2(magic_lo(w), bias), st.sc[q], st.noff[q]));
+                h[2 * t + 1] = bits_h2(__hfma2(__hsub2(magic_hi(w), bias), st.sc[q], st.noff[q]));
+            }
+            out[c] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+    } else {
+        // Q6_K planes: values 64q + 32hf + l = 128h + 32g + l, h = q/2, g = 2(q%2) + hf
+        const int h = q >> 1, g = 2 * (q & 1) + hf;
+        const uint32_t ql = slot + 128u * r + 64u * h + 32u * (uint32_t)(g & 1);
+        const uint32_t qhp = slot + 128u * 128 + 64u * r + 32u * h;
+        const uint4 x0 = lds128u(ql), x1 = lds128u(ql + 16);
+        const uint4 y0 = lds128u(qhp), y1 = lds128u(qhp + 16);
+        const uint32_t lsh = g < 2 ? 0u : 4u, hsh = 2u * (uint32_t)g;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t x = word_of(i < 4 ? x0 : x1, i & 3), y = word_of(i < 4 ? y0 : y1, i & 3);
+            q4[i] = ((x >> lsh) & 0x0F0F0F0Fu) | (((y >> hsh) << 4) & 0x30303030u);
+        }
+        // two 16-value sub-blocks with signed scales: w = d*sc*(q6 - 32)
+        const __half2 bias = __float2half2_rn(1056.f), zero2 = __float2half2_rn(0.f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const __half2 scv = c < 2 ? st.sc[q] : st.noff[q];
+            uint32_t hh[4];
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+                const uint32_t w = q4[2 * c + t];
+                hh[2 * t] = bits_h2(__hfma2(__hsub2(magic_lo(w), bias), scv, zero2));
+                hh[2 * t + 1] = bits_h2(__hfma2(__hsub2(magic_hi(w), bias), scv, zero2));
+            }
+            out[c] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+        }
+    }
+}
+
+// The same for a quarter of the k step: values 32hf + 16hh .. +15 (one 16-byte
+// piece of the code bytes; Q6_K: exactly one 16-value sub-block).
+template <int QT, int LAYOUT>
+__device__ __forceinline__ void decode_quarter(const KbState<QT, LAYOUT>& st, uint32_t row, uint32_t slot, int r,
+                                               int q, int hf, int hh, uint4 out[2]) {
+    uint32_t q4[4];
+    __half2 scv, noffv, bias;
+    if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
+        const uint4 a = lds128u(row + (QT == GGUF_Q5_K ? 48 : 16) + 32 * q + 16 * hh);
+        const uint32_t sh = 4u * (uint32_t)hf;
+        const uint32_t rot = (uint32_t)(4 - (2 * q + hf)) & 31u;   // bit j of a byte -> bit 4
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t v = (word_of(a, i) >> sh) & 0x0F0F0F0Fu;
+            if constexpr (QT == GGUF_Q5_K) v |= __funnelshift_l(st.qh[i], st.qh[i], rot) & 0x10101010u;
+            q4[i] = v;
+        }
+        scv = st.sc[q];
+        noffv = st.noff[q];
+        bias = __float2half2_rn(1024.f);
+    } else {
+        const int h = q >> 1, g = 2 * (q & 1) + hf;
+        const uint4 x = lds128u(slot + 128u * r + 64u * h + 32u * (uint32_t)(g & 1) + 16u * hh);
+        const uint4 y = lds128u(slot + 128u * 128 + 64u * r + 32u * h + 16u * hh);
+        const uint32_t lsh = g < 2 ? 0u : 4u, hsh = 2u * (uint32_t)g;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            q4[i] = ((word_of(x, i) >> lsh) & 0x0F0F0F0Fu) | (((word_of(y, i) >> hsh) << 4) & 0x30303030u);
+        scv = st.sc[q];   // this quarter's 16-value sub-block scale
+        noffv = __float2half2_rn(0.f);
+        bias = __float2half2_rn(1056.f);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        uint32_t h[4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint32_t w = q4[2 * c + t];
+            h[2 * t] = bits_h2(__hfma2(__hsub2(magic_lo(w), bias), scv, noffv));
+            h[2 * t + 1] = bits_h2(__hfma2(__hsub2(magic_hi(w), bias), scv, noffv));
         }
         out[c] = make_uint4(h[0], h[1], h[2], h[3]);
     }
@@ -217,7 +403,7 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
 }
 
 template <int QT, int LAYOUT, int BN, bool MOE>
-__global__ void __launch_bounds__(kFusedThreads, 1)
+__global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
     fused_tc_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                     const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW3,
                     const __grid_constant__ CUtensorMap tmB, const FusedParams fp) {
@@ -225,13 +411,13 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     using C = FusedCfg<BN, RAW>;
     constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
     constexpr int PITCH = raw_pitch(QT, LAYOUT);
+    constexpr int DW = decode_warps(QT, LAYOUT);   // decoder warps
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align_up_1024(smem_raw);
-    uint8_t* sA = base;
-    uint8_t* sB = sA + C::S * C::A_BYTES;
+    uint8_t* sB = base;
     uint8_t* sR = sB + C::S * C::B_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sR + C::RS * RAW);
-    uint64_t* empty = full + C::S;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sR + C::RS * RAW);    // decoded tile + activation tile ready
+    uint64_t* empty = full + C::S;                                      // stage consumed (one MMA commit)
     uint64_t* rfull = empty + C::S;
     uint64_t* rempty = rfull + C::RS;
     uint64_t* tfull = rempty + C::RS;
@@ -261,8 +447,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int n_mma = min(BN, (cols + 15) & ~15);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], 1 + kDecodeWarps); mbar_init(&empty[s], 1); }
-        for (int s = 0; s < C::RS; ++s) { mbar_init(&rfull[s], 1); mbar_init(&rempty[s], kDecodeWarps); }
+        for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], DW + 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < C::RS; ++s) { mbar_init(&rfull[s], 1); mbar_init(&rempty[s], DW); }
         mbar_init(tfull, 1);
         fence_mbar_init();
     }
@@ -273,10 +459,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const uint32_t tmem = *tslot;
 
     if (warp == 0) {
+        // raw super-blocks, as far ahead as the raw ring allows
         if (lane == 0) {
             prefetch_tmap(&tmW0);
-            prefetch_tmap(&tmB);
-            int i = 0;
             for (int kb = 0; kb < KB; ++kb) {
                 const int rs = kb % C::RS;
                 if (!mbar_wait(&rempty[rs], ((kb / C::RS) & 1) ^ 1, fp.status)) break;
@@ -292,36 +477,44 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                 } else {
                     tma_load_2d(dst, &tmW0, kb * (PITCH / 2), (int)wrow0, &rfull[rs]);
                 }
-                bool ok = true;
-                for (int q = 0; q < 4; ++q, ++i) {
-                    const int s = i % C::S;
-                    if (!mbar_wait(&empty[s], ((i / C::S) & 1) ^ 1, fp.status)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&full[s], C::B_BYTES);
-                    tma_load_2d(sB + s * C::B_BYTES, &tmB, i * 64, (int)brow0, &full[s]);
-                }
-                if (!ok) break;
+            }
+        }
+    } else if (warp == 2) {
+        // the activation tile of every 64-value k step, one operand stage ahead
+        if (lane == 0) {
+            prefetch_tmap(&tmB);
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % C::S;
+                if (!mbar_wait(&empty[s], ((i / C::S) & 1) ^ 1, fp.status)) break;
+                mbar_arrive_expect_tx(&full[s], C::B_BYTES);
+                tma_load_2d(sB + s * C::B_BYTES, &tmB, i * 64, (int)brow0, &full[s]);
             }
         }
     } else if (warp == 1) {
         if (lane == 0) {
             const uint32_t idesc = idesc_f16(128, n_mma, 0);
+            // B descriptor of stage s, k slice k: the start-address field is
+            // linear in the address (+B_BYTES/16 per stage, +2 per 16 values)
+            const uint64_t bdesc0 = sw128_desc(smem_u32(sB));
             for (int i = 0; i < nk; ++i) {
                 const int s = i % C::S;
                 if (!mbar_wait(&full[s], (i / C::S) & 1, fp.status)) break;
                 tc_fence_after();
-                const uint32_t a0 = smem_u32(sA + s * C::A_BYTES), b0 = smem_u32(sB + s * C::B_BYTES);
+                const uint32_t a0 = tmem + (uint32_t)(C::A_COL0 + s * C::A_COLS);
+                const uint64_t b0 = bdesc0 + (uint64_t)(s * (C::B_BYTES >> 4));
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    umma_f16(tmem, sw128_desc(a0 + 32 * k), sw128_desc(b0 + 32 * k), idesc, (i | k) != 0);
+                for (int k = 0; k < 4; ++k) umma_f16_ts(tmem, a0 + 8 * k, b0 + 2 * k, idesc, (i | k) != 0);
                 umma_commit(&empty[s]);
             }
             umma_commit(tfull);
         }
     } else {
-        // decoders: thread dt handles row r = dt % 128 and half hf = dt / 128 of each k step
-        const int dt = threadIdx.x - 64, r = dt & 127, hf = dt >> 7;
-        const uint32_t rsw = (uint32_t)(r & 7);
-        const uint32_t a_row = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
+        // decoders: warp w handles the 32 rows of TMEM lane quarter w % 4 (row
+        // r = 32 * (w % 4) + lane) and part (w - 3) / 4 of every k step: a half
+        // hf (8 warps) or a quarter (hf, hh) (16 warps) of its 64 values
+        const int part = (warp - 3) >> 2, r = 32 * (warp & 3) + lane;
+        const int hf = DW == 16 ? part >> 1 : part, hh = DW == 16 ? part & 1 : 0;
+        const uint32_t t_lane = (uint32_t)(32 * (warp & 3)) << 16;
         int i = 0;
         bool ok = true;
         for (int kb = 0; kb < KB && ok; ++kb) {
@@ -331,29 +524,48 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const uint32_t slot = smem_u32(sR + rs * RAW);
             uint32_t row = slot + (uint32_t)(r * PITCH);
             if constexpr (QT == GGUF_Q6_K && !PLANES) row += (uint32_t)((210 * kb) & 15);
+            constexpr bool STATE = QT == GGUF_Q4_K || QT == GGUF_Q5_K || PLANES;
+            KbState<QT, LAYOUT> st;
+            if constexpr (STATE) st.prepare(row, slot, r, hf, kb, DW == 16 ? hh : -1);
+#pragma unroll
             for (int q = 0; q < 4; ++q, ++i) {
                 const int s = i % C::S;
                 ok = mbar_wait(&empty[s], ((i / C::S) & 1) ^ 1, fp.status);
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                uint4 out[4];
-                decode32<QT, LAYOUT>(row, slot, r, q, hf, kb, out);
-                const uint32_t a = smem_u32(sA + s * C::A_BYTES) + a_row;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) sts128u(a + (((uint32_t)(4 * hf + c) ^ rsw) << 4), out[c]);
-                fence_proxy_async_smem();     // generic-proxy writes -> visible to the tensor core
+                tc_fence_after();   // the MMAs that read this stage have completed
+                const uint32_t ta = tmem + t_lane + (uint32_t)(C::A_COL0 + s * C::A_COLS);
+                if constexpr (DW == 16) {
+                    uint4 out[2];
+                    decode_quarter<QT, LAYOUT>(st, row, slot, r, q, hf, hh, out);
+                    const uint32_t v[8] = {out[0].x, out[0].y, out[0].z, out[0].w,
+                                           out[1].x, out[1].y, out[1].z, out[1].w};
+                    tmem_st8(ta + (uint32_t)(16 * hf + 8 * hh), v);   // values 32hf + 16hh .. +15
+                } else {
+                    uint4 out[4];
+                    if constexpr (STATE) decode_step<QT, LAYOUT>(st, row, slot, r, q, hf, out);
+                    else decode32<QT, LAYOUT>(row, slot, r, q, hf, kb, out);
+                    const uint32_t v[16] = {out[0].x, out[0].y, out[0].z, out[0].w, out[1].x, out[1].y,
+                                            out[1].z, out[1].w, out[2].x, out[2].y, out[2].z, out[2].w,
+                                            out[3].x, out[3].y, out[3].z, out[3].w};
+                    tmem_st16(ta + (uint32_t)(16 * hf), v);                // values 32hf .. +31
+                }
+                tmem_st_wait();
+                tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&full[s]);
             }
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(&rempty[rs]);
         }
-        // epilogue: decoder warp w reads TMEM lane quarter (w % 4), columns half (w - 2) / 4
+        // epilogue: decoder warp w reads TMEM lane quarter (w % 4) and column
+        // group (w - 3) / 4 of DW / 4 groups of 16-column chunks
         if (mbar_wait(tfull, 0, fp.status)) {
             tc_fence_after();
-            const int qd = warp & 3, half = (warp - 2) >> 2;
+            constexpr int G = DW / 4, CH = BN / 16;
+            const int qd = warp & 3, grp = (warp - 3) >> 2;
             const int64_t n = n0 + 32 * qd + lane;
 #pragma unroll 1
-            for (int c = half * (BN / 32); c < (half + 1) * (BN / 32); ++c) {
+            for (int c = grp * CH / G; c < (grp + 1) * CH / G; ++c) {
                 if (16 * c >= n_mma) break;   // columns past the MMA width hold nothing
                 uint32_t v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + 16 * c, v);
@@ -389,7 +601,7 @@ cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const Fused
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)ceil_div(fp.N, 128), MOE ? (unsigned)grid_y : (unsigned)ceil_div(fp.M, BN));
-    k<<<grid, kFusedThreads, smem, s>>>(w[0], w[1], w[2], w[3], b, fp);
+    k<<<grid, fused_threads(QT, LAYOUT), smem, s>>>(w[0], w[1], w[2], w[3], b, fp);
     return cudaGetLastError();
 }
 
