@@ -24,6 +24,7 @@
 //              epilogue (TMEM -> registers, + residual, store)
 // The MMA never waits on decode of the same stage it consumes: stages ring
 // through S slots, so decode of step i+1.. overlaps the MMAs of step i.
+#include <algorithm>
 #include <cstring>
 
 #include "tc_gemm.cuh"
@@ -212,67 +213,9 @@ struct KbState {
     }
 };
 
-// k step q of a super-block from a prepared state (Q4_K, Q5_K, Q6_K planes)
-template <int QT, int LAYOUT>
-__device__ __forceinline__ void decode_step(const KbState<QT, LAYOUT>& st, uint32_t row, uint32_t slot, int r, int q,
-                                            int hf, uint4 out[4]) {
-    uint32_t q4[8];
-    if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
-        const uint32_t qs = row + (QT == GGUF_Q5_K ? 48 : 16) + 32 * q;
-        const uint4 a = lds128u(qs), b = lds128u(qs + 16);
-        const uint32_t sh = 4u * (uint32_t)hf;
-        const uint32_t rot = (uint32_t)(4 - (2 * q + hf)) & 31u;   // bit j of a byte -> bit 4
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t w = word_of(i < 4 ? a : b, i & 3);
-            uint32_t v = (w >> sh) & 0x0F0F0F0Fu;
-            if constexpr (QT == GGUF_Q5_K) v |= __funnelshift_l(st.qh[i], st.qh[i], rot) & 0x10101010u;
-            q4[i] = v;
-        }
-        const __half2 bias = __float2half2_rn(1024.f);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t h[4];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const uint32_t w = q4[2 * c + t];
-                h[2 * t] = bits_h2(__hfma2(__hsub2(magic_lo(w), bias), st.sc[q], st.noff[q]));
-                h[2 * t + 1] = bits_h2(__hfma2(__hsub2(magic_hi(w), bias), st.sc[q], st.noff[q]));
-            }
-            out[c] = make_uint4(h[0], h[1], h[2], h[3]);
-        }
-    } else {
-        // Q6_K planes: values 64q + 32hf + l = 128h + 32g + l, h = q/2, g = 2(q%2) + hf
-        const int h = q >> 1, g = 2 * (q & 1) + hf;
-        const uint32_t ql = slot + 128u * r + 64u * h + 32u * (uint32_t)(g & 1);
-        const uint32_t qhp = slot + 128u * 128 + 64u * r + 32u * h;
-        const uint4 x0 = lds128u(ql), x1 = lds128u(ql + 16);
-        const uint4 y0 = lds128u(qhp), y1 = lds128u(qhp + 16);
-        const uint32_t lsh = g < 2 ? 0u : 4u, hsh = 2u * (uint32_t)g;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t x = word_of(i < 4 ? x0 : x1, i & 3), y = word_of(i < 4 ? y0 : y1, i & 3);
-            q4[i] = ((x >> lsh) & 0x0F0F0F0Fu) | (((y >> hsh) << 4) & 0x30303030u);
-        }
-        // two 16-value sub-blocks with signed scales: w = d*sc*(q6 - 32)
-        const __half2 bias = __float2half2_rn(1056.f), zero2 = __float2half2_rn(0.f);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const __half2 scv = c < 2 ? st.sc[q] : st.noff[q];
-            uint32_t hh[4];
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const uint32_t w = q4[2 * c + t];
-                hh[2 * t] = bits_h2(__hfma2(__hsub2(magic_lo(w), bias), scv, zero2));
-                hh[2 * t + 1] = bits_h2(__hfma2(__hsub2(magic_hi(w), bias), scv, zero2));
-            }
-            out[c] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-        }
-    }
-}
-
-// The same for a quarter of the k step: values 32hf + 16hh .. +15 (one 16-byte
-// piece of the code bytes; Q6_K: exactly one 16-value sub-block).
+// A quarter of k step q of a super-block from a prepared state (Q4_K, Q5_K,
+// Q6_K planes): values 32hf + 16hh .. +15 of the step (one 16-byte piece of the
+// code bytes; Q6_K: exactly one 16-value sub-block).
 template <int QT, int LAYOUT>
 __device__ __forceinline__ void decode_quarter(const KbState<QT, LAYOUT>& st, uint32_t row, uint32_t slot, int r,
                                                int q, int hf, int hh, uint4 out[2]) {
@@ -293,8 +236,12 @@ __device__ __forceinline__ void decode_quarter(const KbState<QT, LAYOUT>& st, ui
         bias = __float2half2_rn(1024.f);
     } else {
         const int h = q >> 1, g = 2 * (q & 1) + hf;
-        const uint4 x = lds128u(slot + 128u * r + 64u * h + 32u * (uint32_t)(g & 1) + 16u * hh);
-        const uint4 y = lds128u(slot + 128u * 128 + 64u * r + 32u * h + 16u * hh);
+        // QL rows: 128-byte swizzle (16-byte chunk c of row r at c ^ (r % 8));
+        // QH rows: 64-byte swizzle (chunk c of row r at c ^ ((r / 2) % 4))
+        const uint32_t xc = (uint32_t)(4 * h + 2 * (g & 1) + hh) ^ (uint32_t)(r & 7);
+        const uint32_t yc = (uint32_t)(2 * h + hh) ^ (uint32_t)((r >> 1) & 3);
+        const uint4 x = lds128u(slot + 128u * r + (xc << 4));
+        const uint4 y = lds128u(slot + 128u * 128 + 64u * r + (yc << 4));
         const uint32_t lsh = g < 2 ? 0u : 4u, hsh = 2u * (uint32_t)g;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -320,33 +267,11 @@ __device__ __forceinline__ void decode_quarter(const KbState<QT, LAYOUT>& st, ui
 // super-block) of one weight row whose raw bytes start at shared address `row`.
 template <int QT, int LAYOUT>
 __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int q, int hf, int kb, uint4 out[4]) {
+    static_assert(QT == GGUF_Q8_0 || (QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_BLOCKS),
+                  "the other layouts decode from a per-super-block state");
+    (void)slot; (void)r; (void)kb;
     const __half2 zero2 = __float2half2_rn(0.f);
-    if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
-        const uint4 hdr = lds128u(row);
-        const float d = f16_bits_to_float(hdr.x), dmin = f16_bits_to_float(hdr.x >> 16);
-        const int j = 2 * q + hf;   // 32-wide sub-block
-        const uint32_t scw = j < 4 ? (hdr.y & 0x3F3F3F3Fu) : ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u));
-        const uint32_t mnw = j < 4 ? (hdr.z & 0x3F3F3F3Fu) : (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u));
-        const __half2 sc = __float2half2_rn(d * (float)byte_of(scw, j & 3));
-        const __half2 off = __float2half2_rn(dmin * (float)byte_of(mnw, j & 3));
-        const uint32_t qs = row + (QT == GGUF_Q5_K ? 48 : 16) + 32 * q;
-        const uint4 a = lds128u(qs), b = lds128u(qs + 16);
-        uint32_t q4[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t w = word_of(i < 4 ? a : b, i & 3);
-            q4[i] = hf ? ((w >> 4) & 0x0F0F0F0Fu) : (w & 0x0F0F0F0Fu);
-        }
-        if constexpr (QT == GGUF_Q5_K) {
-            const uint4 h0 = lds128u(row + 16), h1 = lds128u(row + 32);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t hb = word_of(i < 4 ? h0 : h1, i & 3);
-                q4[i] |= ((hb >> j) & 0x01010101u) << 4;
-            }
-        }
-        emit32_h(q4, __float2half2_rn(1024.f), sc, off, sc, off, out);
-    } else if constexpr (QT == GGUF_Q8_0) {
+    if constexpr (QT == GGUF_Q8_0) {
         // signed codes: flipping the sign bit gives b = q + 128 in 0..255
         const uint32_t blk = row + 34u * (uint32_t)(2 * q + hf);   // 2-byte aligned
         const __half2 d2 = h2_bits(lds16u(blk) * 0x10001u);
@@ -355,47 +280,20 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
         for (int i = 0; i < 8; ++i) q4[i] = lds_w2(blk + 2 + 4 * i) ^ 0x80808080u;
         emit32_h(q4, __float2half2_rn(1152.f), d2, zero2, d2, zero2, out);
     } else {
-        // Q6_K: values 64q + 32hf + l = 128h + 32g + l with h = q/2, g = 2(q%2) + hf
+        // raw Q6_K: values 64q + 32hf + l = 128h + 32g + l with h = q/2, g = 2(q%2) + hf
         const int h = q >> 1, g = 2 * (q & 1) + hf;
-        uint32_t ql, qh, sc, dq;
-        if constexpr (LAYOUT == GGUF_LAYOUT_Q6K_PLANES) {
-            ql = slot + 128u * r;
-            qh = slot + 128u * 128 + 64u * r;
-            sc = slot + 128u * 192 + 16u * r;
-            dq = slot + 128u * 208 + 16u * r + (uint32_t)((2 * kb) & 15);
-        } else {
-            const uint32_t blk = row;   // 2-byte aligned
-            ql = blk;
-            qh = blk + 128;
-            sc = blk + 192;
-            dq = blk + 208;
-        }
+        const uint32_t ql = row, qh = row + 128, sc = row + 192, dq = row + 208;   // 2-byte aligned
         const float d = f16_bits_to_float(lds16u(dq));
-        uint32_t x8[8], h8[8];
-        if constexpr (LAYOUT == GGUF_LAYOUT_Q6K_PLANES) {
-            const uint4 x0 = lds128u(ql + 64 * h + 32 * (g & 1)), x1 = lds128u(ql + 64 * h + 32 * (g & 1) + 16);
-            const uint4 y0 = lds128u(qh + 32 * h), y1 = lds128u(qh + 32 * h + 16);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                x8[i] = word_of(i < 4 ? x0 : x1, i & 3);
-                h8[i] = word_of(i < 4 ? y0 : y1, i & 3);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                x8[i] = lds_w2(ql + 64 * h + 32 * (g & 1) + 4 * i);
-                h8[i] = lds_w2(qh + 32 * h + 4 * i);
-            }
-        }
         uint32_t q4[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const uint32_t lo = g < 2 ? (x8[i] & 0x0F0F0F0Fu) : ((x8[i] >> 4) & 0x0F0F0F0Fu);
-            q4[i] = lo | (((h8[i] >> (2 * g)) & 0x03030303u) << 4);
+            const uint32_t x = lds_w2(ql + 64 * h + 32 * (g & 1) + 4 * i), y = lds_w2(qh + 32 * h + 4 * i);
+            const uint32_t lo = g < 2 ? (x & 0x0F0F0F0Fu) : ((x >> 4) & 0x0F0F0F0Fu);
+            q4[i] = lo | (((y >> (2 * g)) & 0x03030303u) << 4);
         }
         // two 16-value sub-blocks with signed scales: w = d*sc*(q6 - 32)
         const int j0 = 8 * h + 2 * g;
-        const uint32_t scw = LAYOUT == GGUF_LAYOUT_Q6K_PLANES ? lds32u(sc + (j0 & ~3)) : lds_w2(sc + (j0 & ~3));
+        const uint32_t scw = lds_w2(sc + (j0 & ~3));
         const __half2 s0 = __float2half2_rn(d * (float)(int8_t)byte_of(scw, j0 & 3));
         const __half2 s1 = __float2half2_rn(d * (float)(int8_t)byte_of(scw, (j0 & 3) + 1));
         emit32_h(q4, __float2half2_rn(1056.f), s0, zero2, s1, zero2, out);
@@ -542,8 +440,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
                     tmem_st8(ta + (uint32_t)(16 * hf + 8 * hh), v);   // values 32hf + 16hh .. +15
                 } else {
                     uint4 out[4];
-                    if constexpr (STATE) decode_step<QT, LAYOUT>(st, row, slot, r, q, hf, out);
-                    else decode32<QT, LAYOUT>(row, slot, r, q, hf, kb, out);
+                    decode32<QT, LAYOUT>(row, slot, r, q, hf, kb, out);
                     const uint32_t v[16] = {out[0].x, out[0].y, out[0].z, out[0].w, out[1].x, out[1].y,
                                             out[1].z, out[1].w, out[2].x, out[2].y, out[2].z, out[2].w,
                                             out[3].x, out[3].y, out[3].z, out[3].w};
@@ -592,6 +489,21 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+// Token-tile width: the fewest rounds of CTAs over the SMs; ties keep the
+// smaller tile (fewer zero-filled activation rows staged).  A tile's time is nearly flat in BN (the k-step rate is set by the
+// MMA-issuing thread and the decoders, not by the MMA width): measured about
+// 28 us at BN = 128 and 31 us at BN = 256 for K = 4096, i.e. cost ~ bn + 1150.
+int pick_bn_fused(int64_t N, int64_t M, int num_sms) {
+    int best = 32;
+    double best_cost = 1e30;
+    for (int bn : {32, 64, 128, 256}) {   // ties keep the smaller tile
+        const int64_t tiles = ceil_div(N, 128) * ceil_div(M, bn);
+        const double cost = (double)ceil_div(tiles, num_sms) * (std::min<int64_t>(bn, M) + 1150);
+        if (cost < best_cost - 1e-9) { best_cost = cost; best = bn; }
+    }
+    return best;
+}
+
 template <int QT, int LAYOUT, int BN, bool MOE = false>
 cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const FusedParams& fp, cudaStream_t s,
                          int grid_y = 0) {
@@ -638,8 +550,14 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
     if (qtype == GGUF_Q6_K && layout == GGUF_LAYOUT_Q6K_PLANES) {
         const int64_t nblk = N * KB;
         const uint8_t* p = static_cast<const uint8_t*>(w);
-        if ((st = make_tmap_2d(&tw[0], p, u16, 2, 64 * KB, N, 128 * KB, 64, 128, none)) != GGUF_OK) return st;
-        if ((st = make_tmap_2d(&tw[1], p + 128 * nblk, u16, 2, 32 * KB, N, 64 * KB, 32, 128, none)) != GGUF_OK) return st;
+        // QL (128 B per row) and QH (64 B) land swizzled, so that the decoders'
+        // 16-byte reads of 32 consecutive rows spread over all banks
+        if ((st = make_tmap_2d(&tw[0], p, u16, 2, 64 * KB, N, 128 * KB, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            GGUF_OK)
+            return st;
+        if ((st = make_tmap_2d(&tw[1], p + 128 * nblk, u16, 2, 32 * KB, N, 64 * KB, 32, 128,
+                               CU_TENSOR_MAP_SWIZZLE_64B)) != GGUF_OK)
+            return st;
         if ((st = make_tmap_2d(&tw[2], p + 192 * nblk, u16, 2, 8 * KB, N, 16 * KB, 8, 128, none)) != GGUF_OK) return st;
         if ((st = make_tmap_2d(&tw[3], p + 208 * nblk, u16, 2, KB, N, 2 * KB, 8, 128, none)) != GGUF_OK) return st;
     } else {
@@ -647,7 +565,7 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
         if ((st = make_tmap_2d(&tw[0], w, u16, 2, (uint64_t)rb / 2, N, rb, box, 128, none)) != GGUF_OK) return st;
         tw[1] = tw[2] = tw[3] = tw[0];
     }
-    const int bn = pick_bn(N, M, num_sms);
+    const int bn = pick_bn_fused(N, M, num_sms);
     CUtensorMap tb;
     if ((st = make_tmap_2d(&tb, workspace, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)K, (uint64_t)M,
                            (uint64_t)K * 2, 64, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B)) != GGUF_OK)
