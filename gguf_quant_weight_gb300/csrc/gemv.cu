@@ -949,8 +949,11 @@ __global__ void __launch_bounds__(direct_threads(MT), 1) gemv_direct_kernel(cons
 // One mbarrier per group of P rows (the rows a warp pass covers); warps take
 // groups round-robin; a lane's unit is the same for every row, so at M = 1 its
 // activation codes stay in registers.
-// warps per CTA: 16 at M = 1 (more rows in flight; registers allow it), else 8
+// warps per CTA -- 16 at M = 1 (more rows in flight; the registers allow it),
+// else 8 -- and row groups per warp iteration (one: measured faster at M = 1
+// than 8 warps taking two rows at a time)
 __host__ __device__ constexpr int tile_warps(int mt) { return mt == 1 ? 16 : 8; }
+__host__ __device__ constexpr int tile_rows(int mt) { return 1; }
 
 // Shared-memory layout of the tile kernel (byte offsets).
 struct TileLayout {
@@ -987,6 +990,7 @@ template <int QT, int MT, bool DUMP>
 __global__ void __launch_bounds__(tile_warps(MT) * 32, 2) gemv_tile_kernel(const GemvParams p) {
     constexpr int NW = tile_warps(MT), NT = NW * 32;
     constexpr int bb = QT == GGUF_Q4_K ? 144 : 176;
+    constexpr int TR = tile_rows(MT);
     constexpr bool AREG = false;     // activation codes read from shared memory
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1080,58 +1084,77 @@ __global__ void __launch_bounds__(tile_warps(MT) * 32, 2) gemv_tile_kernel(const
     const bool head = lane_on && (lane % seg) == 0;
     Act fixed;
     if (U <= 32) fixed.init(sh, 128 * u0, nbs);
-    for (int gi = warp; gi < ngroups; gi += NW) {
-        mbar_wait(&bars[gi], 0, p.status);
-        const int r = gi * P + sub_row;
-        const bool valid = lane_on && r < rows;
-        const int64_t n = row0 + r;
-        float acc[1][MT];
+    for (int g0 = warp; g0 < ngroups; g0 += TR * NW) {
+        // TR row groups per iteration: g0, g0 + NW, ...
+        int rr[TR];
+        bool vv[TR];
+        int64_t nn[TR];
+        float acc[TR][MT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) acc[0][m] = 0.f;
-        if (valid) {
-            const int64_t nn[1] = {n};
-            const bool on[1] = {true};
-            if (U <= 32) {
-                FragQ45<QT> f;
-                f.load(tile + (uint32_t)r * sb + (uint32_t)(u0 >> 1) * bb, u0 & 1);
-                const FragQ45<QT>* fr[1] = {&f};
-                unit_q45k<QT, MT, 1, Act, DUMP>(p, fr, fixed, kb0 + (u0 >> 1), u0 & 1, acc, nn, on);
-            } else {
+        for (int t = 0; t < TR; ++t) {
+            const int gi = g0 + t * NW;
+            if (gi < ngroups) mbar_wait(&bars[gi], 0, p.status);
+            rr[t] = gi * P + sub_row;
+            vv[t] = lane_on && gi < ngroups && rr[t] < rows;
+            nn[t] = row0 + rr[t];
+#pragma unroll
+            for (int m = 0; m < MT; ++m) acc[t][m] = 0.f;
+        }
+        if (U <= 32) {
+            FragQ45<QT> f[TR];
+            const FragQ45<QT>* fr[TR];
+#pragma unroll
+            for (int t = 0; t < TR; ++t) {
+                if (vv[t]) f[t].load(tile + (uint32_t)rr[t] * sb + (uint32_t)(u0 >> 1) * bb, u0 & 1);
+                fr[t] = &f[t];
+            }
+            bool any = false;
+#pragma unroll
+            for (int t = 0; t < TR; ++t) any |= vv[t];
+            if (any) unit_q45k<QT, MT, TR, Act, DUMP>(p, fr, fixed, kb0 + (u0 >> 1), u0 & 1, acc, nn, vv);
+        } else {
+#pragma unroll
+            for (int t = 0; t < TR; ++t) {
+                if (!vv[t]) continue;
                 for (int u = u0; u < U; u += 32) {
                     FragQ45<QT> f;
-                    f.load(tile + (uint32_t)r * sb + (uint32_t)(u >> 1) * bb, u & 1);
+                    f.load(tile + (uint32_t)rr[t] * sb + (uint32_t)(u >> 1) * bb, u & 1);
                     ActSlice<MT, false, 8, 4> a;
                     a.init(sh, 128 * u, nbs);
                     const FragQ45<QT>* fr[1] = {&f};
-                    unit_q45k<QT, MT, 1, ActSlice<MT, false, 8, 4>, DUMP>(p, fr, a, kb0 + (u >> 1), u & 1, acc, nn,
-                                                                        on);
+                    float(*a1)[MT] = reinterpret_cast<float(*)[MT]>(&acc[t][0]);
+                    unit_q45k<QT, MT, 1, ActSlice<MT, false, 8, 4>, DUMP>(p, fr, a, kb0 + (u >> 1), u & 1, a1,
+                                                                        &nn[t], &vv[t]);
                 }
             }
         }
-        if (seg == 32) {
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
+        for (int t = 0; t < TR; ++t) {
+            if (seg == 32) {
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[0][m] += __shfl_xor_sync(0xffffffffu, acc[0][m], o);
-            }
-        } else {
+                for (int m = 0; m < MT; ++m) {
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
+                    for (int o = 16; o > 0; o >>= 1) acc[t][m] += __shfl_xor_sync(0xffffffffu, acc[t][m], o);
+                }
+            } else {
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float t = __shfl_down_sync(0xffffffffu, acc[0][m], o);
-                    if (lane + o < seg_end) acc[0][m] += t;
+                for (int m = 0; m < MT; ++m) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const float tt = __shfl_down_sync(0xffffffffu, acc[t][m], o);
+                        if (lane + o < seg_end) acc[t][m] += tt;
+                    }
                 }
             }
-        }
-        if (head && valid) {
-            for (int m = 0; m < p.M && m < MT; ++m) {
-                if (S > 1) {
-                    part[m * p.rows_per_cta + r] = acc[0][m];
-                } else {
-                    float v = acc[0][m];
-                    if (p.residual) v += res[m * p.rows_per_cta + r];
-                    store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
+            if (head && vv[t]) {
+                for (int m = 0; m < p.M && m < MT; ++m) {
+                    if (S > 1) {
+                        part[m * p.rows_per_cta + rr[t]] = acc[t][m];
+                    } else {
+                        float v = acc[t][m];
+                        if (p.residual) v += res[m * p.rows_per_cta + rr[t]];
+                        store_out(p.y, p.ydt, (int64_t)m * p.N + nn[t], v);
+                    }
                 }
             }
         }
