@@ -1179,6 +1179,227 @@ __global__ void __launch_bounds__(tile_warps(MT) * 32, 2) gemv_tile_kernel(const
     }
 }
 
+// ------------------------------------------------------------------ pair kernel (M = 2..8)
+// Q4_K / Q5_K blocks, 2 <= M <= 8, K a multiple of 2048, when a CTA's rows of W
+// and the activation image fit in half of an SM's shared memory.  Rows are
+// staged whole, as in the tile kernel (two CTAs per SM, the next call's weights
+// stream under this call's compute); the image comes from the quantizer kernel.
+// A lane owns one 64-value "pair" of K -- the two 32-value sub-blocks whose
+// codes share the same 32 qs bytes (low / high nibbles) -- for every row of the
+// CTA, so its activation codes and block scales for all M rows are loaded into
+// registers once; a warp covers 2048 values of a row, K/2048 warps span a row,
+// and their partial sums meet in shared memory.  The M sums of a row are
+// reduced across the warp with a transposed butterfly (each step halves the
+// values a lane keeps), far fewer shuffles than M separate reductions.
+constexpr int kPairWarps = 8;
+
+struct PairLayout {
+    int64_t img, res, part, bars, total;
+};
+__host__ __device__ inline PairLayout pair_layout(int64_t M, int64_t K, int64_t rows_per_cta, int64_t rb) {
+    PairLayout L;
+    const int64_t KQ = K / 2048;
+    L.img = ceil_div(rows_per_cta * rb, 128) * 128;
+    L.res = L.img + ceil_div(act_image_bytes(M, K), 16) * 16;
+    L.part = L.res + ceil_div(4 * M * rows_per_cta, 16) * 16;
+    L.bars = L.part + ceil_div(4 * M * rows_per_cta * KQ, 16) * 16;
+    L.total = L.bars + 8 * (rows_per_cta + 1);
+    return L;
+}
+
+// Transposed butterfly over the 32 lanes: on return, lane l (with l % (32/MT)
+// == 0) holds the warp total of value m = l / (32/MT) in v[0].
+template <int MT>
+__device__ __forceinline__ void warp_sum_transposed(float (&v)[MT], int lane) {
+    int n = MT;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        if (n > 1) {
+            const bool upper = (lane & o) != 0;
+            const int h = n >> 1;
+#pragma unroll
+            for (int i = 0; i < MT / 2; ++i) {
+                if (i < h) {
+                    const float keep = upper ? v[h + i] : v[i];
+                    const float send = upper ? v[i] : v[h + i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            n = h;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+    }
+}
+
+template <int QT, int MT, bool DUMP>
+__global__ void __launch_bounds__(kPairWarps * 32, 2) gemv_pair_kernel(const GemvParams p) {
+    constexpr int NW = kPairWarps, NT = NW * 32;
+    constexpr int bb = QT == GGUF_Q4_K ? 144 : 176;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nb = (int)(p.K / 32);
+    const int64_t row0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int rows = (int)min(p.rows_per_cta, p.N - row0);
+    const int KQ = (int)(p.K / 2048), RG = NW / KQ;   // warps per row, row groups
+    const int kq = warp % KQ, rg = warp / KQ;
+    const uint32_t rb = (uint32_t)p.rb;
+    const PairLayout L = pair_layout(p.M, p.K, p.rows_per_cta, p.rb);
+    const uint32_t tile = smem_u32(smem_raw);
+    uint8_t* img = smem_raw + L.img;
+    float* res = reinterpret_cast<float*>(smem_raw + L.res);
+    float* part = reinterpret_cast<float*>(smem_raw + L.part);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bars);   // [rows_per_cta] rows, then the image
+    const uint32_t qa_row = (uint32_t)qa_row_stride(p.K);
+    const uint32_t qa = smem_u32(img), ds = qa + (uint32_t)p.M * qa_row;
+
+    // 1. every row requested at once, before the dependency wait
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int r = 0; r <= (int)p.rows_per_cta; ++r) mbar_init(&bars[r], 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32) {
+            mbar_arrive_expect_tx(&bars[r], rb);
+            bulk_g2s_u32(tile + (uint32_t)r * rb, p.w + (row0 + r) * p.rb, rb, &bars[r]);
+        }
+    }
+    __syncthreads();   // every barrier is initialised before any thread waits on one
+    pdl_launch_dependents();
+
+    // 2. after the producer of X: the quantized image (one bulk copy) and the
+    // tile's residual values
+    pdl_wait();
+    uint64_t* img_bar = &bars[p.rows_per_cta];
+    if (tid == 0) {
+        const uint32_t bytes = (uint32_t)act_image_bytes(p.M, p.K);
+        mbar_arrive_expect_tx(img_bar, bytes);
+        bulk_g2s_u32(qa, p.act_image, bytes, img_bar);
+    }
+    float res0 = 0.f;
+    if (p.residual && tid < p.M * rows)
+        res0 = load_act(p.residual, p.ydt, (int64_t)(tid / rows) * p.N + row0 + tid % rows);
+    mbar_wait(img_bar, 0, p.status);
+    if (p.residual) {
+        if (tid < p.M * rows) res[(tid / rows) * p.rows_per_cta + tid % rows] = res0;
+        for (int i = tid + NT; i < p.M * rows; i += NT)
+            res[(i / rows) * p.rows_per_cta + i % rows] =
+                load_act(p.residual, p.ydt, (int64_t)(i / rows) * p.N + row0 + i % rows);
+    }
+    __syncthreads();
+    if (DUMP && blockIdx.x == 0) {
+        for (int64_t i = tid; i < (int64_t)p.M * p.K; i += NT) {
+            const uint32_t a = qa + (uint32_t)(i / p.K) * qa_row + qa_pos((uint32_t)(i % p.K));
+            if (p.dbg_qa) p.dbg_qa[i] = (int8_t)(lds32(a & ~3u) >> (8 * (a & 3)));
+        }
+        for (int i = tid; i < p.M * nb; i += NT) {
+            const uint4 e = lds128(ds + 16u * i);
+            if (p.dbg_da) p.dbg_da[i] = __uint_as_float(e.x);
+            if (p.dbg_s) p.dbg_s[i] = (int32_t)(e.z + e.w);
+        }
+    }
+
+    // 3. this lane's pair: values 64*pi .. 64*pi + 63 of K, i.e. sub-blocks
+    // jlo = 2*pp (low nibbles) and jlo + 1 (high nibbles) of super-block kb
+    const int pi = kq * 32 + lane;
+    const int kb = pi >> 2, pp = pi & 3, jlo = 2 * pp;
+    uint32_t code[MT][16];
+    float da_lo[MT], da_hi[MT], das_lo[MT], das_hi[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (m < p.M) {
+            const uint32_t a = qa + (uint32_t)m * qa_row + qa_pos((uint32_t)(64 * pi));
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint4 w4 = lds128(a + 16 * c);
+                code[m][4 * c] = w4.x; code[m][4 * c + 1] = w4.y; code[m][4 * c + 2] = w4.z; code[m][4 * c + 3] = w4.w;
+            }
+            const uint4 e0 = lds128(ds + 16u * (uint32_t)(m * nb + 2 * pi));
+            const uint4 e1 = lds128(ds + 16u * (uint32_t)(m * nb + 2 * pi + 1));
+            da_lo[m] = __uint_as_float(e0.x); das_lo[m] = __uint_as_float(e0.y);
+            da_hi[m] = __uint_as_float(e1.x); das_hi[m] = __uint_as_float(e1.y);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) code[m][c] = 0u;
+            da_lo[m] = da_hi[m] = das_lo[m] = das_hi[m] = 0.f;
+        }
+    }
+    const uint32_t rot_lo = (uint32_t)(4 - jlo) & 31u, rot_hi = (uint32_t)(3 - jlo) & 31u;
+    const uint32_t blk_off = (uint32_t)kb * bb;
+
+    // 4. rows of this warp's row group
+    for (int r = rg; r < rows; r += RG) {
+        mbar_wait(&bars[r], 0, p.status);
+        const uint32_t blk = tile + (uint32_t)r * rb + blk_off;
+        const uint4 hdr = lds128(blk);
+        const float d = f16_bits_to_float(hdr.x), dmin = f16_bits_to_float(hdr.x >> 16);
+        // 6-bit scale / min of sub-blocks jlo and jlo + 1 (GGUF packing)
+        int sc0, sc1, mn0, mn1;
+        {
+            const uint32_t s0 = hdr.y, s1 = hdr.z, s2 = hdr.w;   // scale bytes 0-3, 4-7, 8-11
+            const uint32_t scw = pp < 2 ? (s0 & 0x3F3F3F3Fu) : ((s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u));
+            const uint32_t mnw = pp < 2 ? (s1 & 0x3F3F3F3Fu) : (((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u));
+            const int b = jlo & 3;
+            sc0 = (int)((scw >> (8 * b)) & 0xFF); sc1 = (int)((scw >> (8 * b + 8)) & 0xFF);
+            mn0 = (int)((mnw >> (8 * b)) & 0xFF); mn1 = (int)((mnw >> (8 * b + 8)) & 0xFF);
+        }
+        const uint32_t qs = blk + (QT == GGUF_Q5_K ? 48u : 16u) + 32u * (uint32_t)pp;
+        const uint4 q0 = lds128(qs), q1 = lds128(qs + 16);
+        uint4 h0 = make_uint4(0, 0, 0, 0), h1 = h0;
+        if constexpr (QT == GGUF_Q5_K) { h0 = lds128(blk + 16); h1 = lds128(blk + 32); }
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = comp(i < 4 ? q0 : q1, i);
+            lo[i] = w & 0x0F0F0F0Fu;
+            hi[i] = (w >> 4) & 0x0F0F0F0Fu;
+            if constexpr (QT == GGUF_Q5_K) {
+                const uint32_t hb = comp(i < 4 ? h0 : h1, i);
+                lo[i] |= __funnelshift_l(hb, hb, rot_lo) & 0x10101010u;
+                hi[i] |= __funnelshift_l(hb, hb, rot_hi) & 0x10101010u;
+            }
+        }
+        float acc[MT];
+        const float fmn0 = (float)mn0, fmn1 = (float)mn1;
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            int Da = 0, Db = 0, Ea = 0, Eb = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                Da = dp4a(lo[i], code[m][i], Da);
+                Db = dp4a(lo[4 + i], code[m][4 + i], Db);
+                Ea = dp4a(hi[i], code[m][8 + i], Ea);
+                Eb = dp4a(hi[4 + i], code[m][12 + i], Eb);
+            }
+            const int D0 = Da + Db, D1 = Ea + Eb;
+            if (DUMP && p.dbg_D && m < p.M) {
+                dump_D(p, m, row0 + r, 2 * pi, 32, D0);
+                dump_D(p, m, row0 + r, 2 * pi + 1, 32, D1);
+            }
+            const float sd = da_lo[m] * (float)(sc0 * D0) + da_hi[m] * (float)(sc1 * D1);
+            const float sm = das_lo[m] * fmn0 + das_hi[m] * fmn1;
+            acc[m] = d * sd - dmin * sm;
+        }
+        warp_sum_transposed<MT>(acc, lane);
+        const int span = 32 / MT;
+        if (lane % span == 0) {
+            const int m = lane / span;
+            if (m < p.M) part[((int64_t)r * KQ + kq) * p.M + m] = acc[0];
+        }
+    }
+
+    // 5. the K/2048 partials of each row, + residual, stored
+    __syncthreads();
+    for (int i = tid; i < p.M * rows; i += NT) {
+        const int m = i / rows, r = i % rows;
+        float v = 0.f;
+        for (int q = 0; q < KQ; ++q) v += part[((int64_t)r * KQ + q) * p.M + m];
+        if (p.residual) v += res[m * p.rows_per_cta + r];
+        store_out(p.y, p.ydt, (int64_t)m * p.N + row0 + r, v);
+    }
+}
+
 template <int QT, int MT, int LAYOUT, bool DUMP>
 cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
     const int U = (int)(p.K / (QT == GGUF_Q8_0 ? 32 : 128));
@@ -1191,9 +1412,15 @@ cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t 
         if (p.direct) k = gemv_direct_kernel<QT, MT, DUMP>;
     }
     if constexpr ((QT == GGUF_Q4_K || QT == GGUF_Q5_K) && LAYOUT == GGUF_LAYOUT_BLOCKS) {
-        if (p.tile) {
+        if (p.tile == 1) {
             k = gemv_tile_kernel<QT, MT, DUMP>;
             threads = tile_warps(MT) * 32;
+        }
+        if constexpr (MT >= 2 && MT <= 4) {
+            if (p.tile == 2) {
+                k = gemv_pair_kernel<QT, MT, DUMP>;
+                threads = kPairWarps * 32;
+            }
         }
     }
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1285,6 +1512,19 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
         }
     }
     const int64_t rpc = ceil_div(p.N, (int64_t)num_sms);
+    // the pair kernel for 2..4 rows: whole rows staged, codes in registers
+    if ((p.qtype == GGUF_Q4_K || p.qtype == GGUF_Q5_K) && p.layout == GGUF_LAYOUT_BLOCKS && p.M >= 2 && p.M <= 4 &&
+        p.K % 2048 == 0 && kPairWarps % (p.K / 2048) == 0) {
+        const PairLayout L = pair_layout(p.M, p.K, rpc, p.rb);
+        if (L.total <= half) {
+            p.tile = 2;
+            p.direct = 0;
+            p.rows_per_cta = rpc;
+            *grid = (int)ceil_div(p.N, rpc);
+            *smem = (size_t)L.total;
+            return GGUF_OK;
+        }
+    }
     const int64_t groups_per_warp = ceil_div(ceil_div(rpc, P), NW);
     int64_t R = std::min<int64_t>({groups_per_warp, 8, (half - act) / (NW * p.stage_bytes)});
     if (R < 1) R = std::min<int64_t>({groups_per_warp, 8, (max_smem - act) / (NW * p.stage_bytes)});
@@ -1303,7 +1543,7 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
 }
 
 cudaError_t gemv_launch(const GemvParams& p, int grid, size_t smem, bool dump, cudaStream_t stream) {
-    if (p.tile) return dump ? launch_dispatch<true>(p, grid, smem, stream) : launch_dispatch<false>(p, grid, smem, stream);
+    if (p.tile == 1) return dump ? launch_dispatch<true>(p, grid, smem, stream) : launch_dispatch<false>(p, grid, smem, stream);
     // 1. per-32 activation quantizer -> image in the workspace
     const int quarters = 4 * p.M * (int)(p.K / 32);
     cudaLaunchConfig_t cfg = {};

@@ -207,3 +207,35 @@ def test_gemv_activation_quantizer_non_finite_and_extreme_blocks(qtype):
     assert np.array_equal(qa.cpu().numpy(), rqa)
     assert np.array_equal(da.cpu().numpy(), rda, equal_nan=True)
     assert np.array_equal(s.cpu().numpy(), rs_)
+
+
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q5_K])
+@pytest.mark.parametrize("N,K", [(300, 2048), (1000, 4096), (77, 8192)])
+@pytest.mark.parametrize("M", [2, 3, 4])
+def test_gemv_pair_kernel_shapes(qtype, N, K, M):
+    # K a multiple of 2048 and 2..4 rows: the kernel that keeps each lane's
+    # 64-value slice of the activation codes in registers
+    got, ref, _, _ = _case(qtype, N, K, M)
+    U.check_close(got, ref, "bf16", what=f"q{qtype} N{N} K{K} M{M}")
+
+
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q5_K])
+def test_gemv_pair_kernel_integer_terms_bit_exact(qtype):
+    rs = syn.rng(70 + qtype)
+    N, K, M = 41, 2048, 3
+    w = syn.weight_blocks(rs, qtype, N, K)
+    x = syn.normal(rs, (M, K), "bf16")
+    qa = torch.zeros((M, K), dtype=torch.int8, device="cuda")
+    da = torch.zeros((M, K // 32), dtype=torch.float32, device="cuda")
+    s = torch.zeros((M, K // 32), dtype=torch.int32, device="cuda")
+    D = torch.full((M, N, K // 32), -999999, dtype=torch.int32, device="cuda")
+    y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    g.gguf_mm_debug_gemv_terms(U.dev(w), qtype, 0, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, y, g.GGUF_DT_F32,
+                               qa, da, s, D)
+    torch.cuda.synchronize()
+    y_ref, terms = O.gemv_int8_path(w, qtype, N, K, U.act_f32(x, "bf16"), return_terms=True)
+    assert np.array_equal(qa.cpu().numpy(), terms["qa"])
+    assert np.array_equal(da.cpu().numpy(), terms["d_a"])
+    assert np.array_equal(s.cpu().numpy(), terms["s"])
+    assert np.array_equal(D.cpu().numpy().astype(np.int64), terms["D"])
+    U.check_close(U.host64(y), y_ref, "f32")
