@@ -62,9 +62,6 @@ __device__ __forceinline__ uint32_t lds16(uint32_t a) {
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
     return v;
 }
-__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
-}
 __device__ __forceinline__ float i2f(int v) { return (float)v; }
 
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
@@ -939,16 +936,11 @@ __global__ void __launch_bounds__(direct_threads(MT), 1) gemv_direct_kernel(cons
 // resident while this call computes, and its first act is to request all of
 // its weight bytes with bulk copies -- so the next call's weight stream runs
 // under this call's compute and a chain of calls is bound by HBM rather than
-// by per-call latency.
-//
-// Split K: the S CTAs of a thread-block cluster take the S K slices of the same
-// rows.  After its dependency wait each CTA quantizes only its slice of X (no
-// second kernel, no second wait in the chain, and the quantizer work is not
-// repeated by every CTA); the slices' partial row sums meet in distributed
-// shared memory, each CTA adding up an equal share of the rows in slice order.
+// by per-call latency.  After its dependency wait the CTA quantizes the
+// activation row itself (one kernel and one wait per call) and reads its
+// residual values once into shared memory.
 // One mbarrier per group of P rows (the rows a warp pass covers); warps take
-// groups round-robin; a lane's unit is the same for every row, so at M = 1 its
-// activation codes stay in registers.
+// groups round-robin; a lane's unit is the same for every row.
 // warps per CTA -- 16 at M = 1 (more rows in flight; the registers allow it),
 // else 8 -- and row groups per warp iteration (one: measured faster at M = 1
 // than 8 warps taking two rows at a time)
@@ -957,33 +949,17 @@ __host__ __device__ constexpr int tile_rows(int mt) { return 1; }
 
 // Shared-memory layout of the tile kernel (byte offsets).
 struct TileLayout {
-    int64_t img, part, res, bars, total;
+    int64_t img, res, bars, total;
 };
-__host__ __device__ inline TileLayout tile_layout(int64_t M, int64_t klen, int64_t rows_per_cta, int64_t slice_bytes,
-                                                  int S) {
-    const int64_t U = klen / 128;
+__host__ __device__ inline TileLayout tile_layout(int64_t M, int64_t K, int64_t rows_per_cta, int64_t rb) {
+    const int64_t U = K / 128;
     const int64_t P = U < 32 ? 32 / U : 1;
     TileLayout L;
-    L.img = ceil_div(rows_per_cta * slice_bytes, 128) * 128;
-    L.part = L.img + ceil_div(act_image_bytes(M, klen), 16) * 16;
-    L.res = L.part + (S > 1 ? ceil_div(4 * M * rows_per_cta, 16) * 16 : 0);
+    L.img = ceil_div(rows_per_cta * rb, 128) * 128;
+    L.res = L.img + ceil_div(act_image_bytes(M, K), 16) * 16;
     L.bars = L.res + ceil_div(4 * M * rows_per_cta, 16) * 16;
     L.total = L.bars + 8 * ceil_div(rows_per_cta, P);
     return L;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t a) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-    return v;
 }
 
 template <int QT, int MT, bool DUMP>
@@ -994,21 +970,18 @@ __global__ void __launch_bounds__(tile_warps(MT) * 32, 2) gemv_tile_kernel(const
     constexpr bool AREG = false;     // activation codes read from shared memory
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int S = p.ksplit;
-    const int s = (int)(blockIdx.x % S);          // the CTA's rank in its cluster of S
-    const int64_t row0 = (int64_t)(blockIdx.x / S) * p.rows_per_cta;
+    const int64_t row0 = (int64_t)blockIdx.x * p.rows_per_cta;
     const int rows = (int)min(p.rows_per_cta, p.N - row0);
-    const int klen = (int)(p.K / S);              // values in this CTA's K slice
-    const int kb0 = s * (klen / 256);             // its first super-block
-    const int nbs = klen / 32;                    // activation blocks in the slice
-    const int U = klen / 128;                     // units per row slice
+    const int klen = (int)p.K;
+    const int kb0 = 0;
+    const int nbs = klen / 32;                    // activation blocks
+    const int U = klen / 128;                     // units per row
     const int P = U < 32 ? 32 / U : 1;            // rows per warp pass
     const int ngroups = (rows + P - 1) / P;
-    const uint32_t sb = (uint32_t)(klen / 256) * bb;   // bytes of one row slice
-    const TileLayout L = tile_layout(p.M, klen, p.rows_per_cta, sb, S);
+    const uint32_t sb = (uint32_t)p.rb;           // bytes of one row
+    const TileLayout L = tile_layout(p.M, klen, p.rows_per_cta, sb);
     const uint32_t tile = smem_u32(smem_raw);
     uint8_t* img = smem_raw + L.img;
-    float* part = reinterpret_cast<float*>(smem_raw + L.part);
     float* res = reinterpret_cast<float*>(smem_raw + L.res);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + L.bars);
     Shared sh;
@@ -1039,7 +1012,7 @@ __global__ void __launch_bounds__(tile_warps(MT) * 32, 2) gemv_tile_kernel(const
     // now (one round trip for all of them, under the quantizer) and this K
     // slice is quantized
     pdl_wait();
-    const bool res_now = p.residual && S == 1;
+    const bool res_now = p.residual != nullptr;
     float res0 = 0.f;   // this thread's first residual value, held until after the quantizer
     if (res_now && tid < p.M * rows) {
         const int m = tid / rows, r = tid - m * rows;
@@ -1047,9 +1020,9 @@ __global__ void __launch_bounds__(tile_warps(MT) * 32, 2) gemv_tile_kernel(const
     }
     {
         const int rounds = (4 * p.M * (klen / 32) + NT - 1) / NT;   // quarters per thread
-        if (rounds >= 4) quantize_slice<4>(p, (int64_t)s * klen, klen, img, tid, NT);
-        else if (rounds >= 2) quantize_slice<2>(p, (int64_t)s * klen, klen, img, tid, NT);
-        else quantize_slice<1>(p, (int64_t)s * klen, klen, img, tid, NT);
+        if (rounds >= 4) quantize_slice<4>(p, 0, klen, img, tid, NT);
+        else if (rounds >= 2) quantize_slice<2>(p, 0, klen, img, tid, NT);
+        else quantize_slice<1>(p, 0, klen, img, tid, NT);
     }
     if (res_now) {
         if (tid < p.M * rows) res[(tid / rows) * p.rows_per_cta + tid % rows] = res0;
@@ -1063,12 +1036,12 @@ __global__ void __launch_bounds__(tile_warps(MT) * 32, 2) gemv_tile_kernel(const
         for (int i = tid; i < p.M * klen; i += NT) {
             const int m = i / klen, k = i % klen;
             const uint32_t a = sh.qa + (uint32_t)m * sh.qa_row + qa_pos((uint32_t)k);
-            if (p.dbg_qa) p.dbg_qa[(int64_t)m * p.K + (int64_t)s * klen + k] = (int8_t)(lds32(a & ~3u) >> (8 * (a & 3)));
+            if (p.dbg_qa) p.dbg_qa[(int64_t)m * p.K + k] = (int8_t)(lds32(a & ~3u) >> (8 * (a & 3)));
         }
         for (int i = tid; i < p.M * nbs; i += NT) {
             const int m = i / nbs, b = i % nbs;
             const uint4 e = lds128(sh.ds + 16u * i);
-            const int64_t o = (int64_t)m * (p.K / 32) + (int64_t)s * nbs + b;
+            const int64_t o = (int64_t)m * (p.K / 32) + b;
             if (p.dbg_da) p.dbg_da[o] = __uint_as_float(e.x);
             if (p.dbg_s) p.dbg_s[o] = (int32_t)(e.z + e.w);
         }
@@ -1148,35 +1121,14 @@ __global__ void __launch_bounds__(tile_warps(MT) * 32, 2) gemv_tile_kernel(const
             }
             if (head && vv[t]) {
                 for (int m = 0; m < p.M && m < MT; ++m) {
-                    if (S > 1) {
-                        part[m * p.rows_per_cta + rr[t]] = acc[t][m];
-                    } else {
-                        float v = acc[t][m];
-                        if (p.residual) v += res[m * p.rows_per_cta + rr[t]];
-                        store_out(p.y, p.ydt, (int64_t)m * p.N + nn[t], v);
-                    }
+                    float v = acc[t][m];
+                    if (p.residual) v += res[m * p.rows_per_cta + rr[t]];
+                    store_out(p.y, p.ydt, (int64_t)m * p.N + nn[t], v);
                 }
             }
         }
     }
 
-    // 4. split K: the slices' partials meet in distributed shared memory; CTA s
-    // finishes rows [s*share, (s+1)*share) of the group, adding slices in order
-    if (S > 1) {
-        cluster_sync_all();
-        const int share = (rows + S - 1) / S;
-        const int rbeg = min(rows, s * share), cnt = min(rows, rbeg + share) - rbeg;
-        for (int i = tid; i < cnt * p.M; i += NT) {
-            const int m = i / cnt, r = rbeg + i % cnt;
-            const uint32_t la = smem_u32(part + m * p.rows_per_cta + r);
-            float v = 0.f;
-            for (int q = 0; q < S; ++q) v += ld_dsmem_f32(dsmem_map(la, (uint32_t)q));
-            const int64_t n = row0 + r;
-            if (p.residual) v += load_act(p.residual, p.ydt, (int64_t)m * p.N + n);
-            store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
-        }
-        cluster_sync_all();   // every CTA's partials stay in place until all are read
-    }
 }
 
 // ------------------------------------------------------------------ pair kernel (M = 2..8)
@@ -1412,9 +1364,11 @@ cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t 
         if (p.direct) k = gemv_direct_kernel<QT, MT, DUMP>;
     }
     if constexpr ((QT == GGUF_Q4_K || QT == GGUF_Q5_K) && LAYOUT == GGUF_LAYOUT_BLOCKS) {
-        if (p.tile == 1) {
-            k = gemv_tile_kernel<QT, MT, DUMP>;
-            threads = tile_warps(MT) * 32;
+        if constexpr (MT == 1) {
+            if (p.tile == 1) {
+                k = gemv_tile_kernel<QT, MT, DUMP>;
+                threads = tile_warps(MT) * 32;
+            }
         }
         if constexpr (MT >= 2 && MT <= 4) {
             if (p.tile == 2) {
@@ -1430,18 +1384,11 @@ cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t 
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.tile && p.ksplit > 1) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = (unsigned)p.ksplit;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
-    }
     return cudaLaunchKernelEx(&cfg, k, p);
 }
 
@@ -1483,32 +1430,21 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
     // one CTA per SM; it keeps to half of the shared memory so that a CTA of
     // the next call on the stream (programmatic dependent launch) fits beside it
     const int64_t half = std::min<int64_t>(max_smem, 232448 / 2 - 1024);
-    // the tile kernel when a CTA's share of W and its image fit beside a second
-    // CTA: K split over a cluster of ksplit CTAs (2 keeps every SM in use; the
-    // quantizer work per CTA halves) unless one activation row is all there is
+    // one activation row: the tile kernel, when a CTA's rows of W and its image
+    // fit beside a second CTA (the quantizer runs inside it; from two rows on the
+    // stand-alone quantizer kernel, whose work is not repeated by every CTA, wins)
     p.tile = 0;
-    p.ksplit = 1;
-    if ((p.qtype == GGUF_Q4_K || p.qtype == GGUF_Q5_K) && p.layout == GGUF_LAYOUT_BLOCKS) {
-        const int64_t KB = p.K / 256;
-        for (int S : {1}) {
-            if (S == 2 && (p.M < 2 || KB % 2 != 0 || num_sms % 2 != 0)) continue;
-            // the quantizer is repeated by every CTA: worth it for one row,
-            // beaten by the stand-alone quantizer kernel from two rows on
-            if (p.M > 1) continue;
-            const int64_t klen = p.K / S, sb = (klen / 256) * bb;
-            const int64_t G = num_sms / S;
-            const int64_t rpc_t = ceil_div(p.N, G);
-            const TileLayout L = tile_layout(p.M, klen, rpc_t, sb, S);
-            if (L.total <= half) {
-                p.tile = 1;
-                p.ksplit = S;
-                p.direct = 0;
-                p.rows_per_cta = rpc_t;
-                p.stage_bytes = L.img;
-                *grid = (int)(ceil_div(p.N, rpc_t) * S);
-                *smem = (size_t)L.total;
-                return GGUF_OK;
-            }
+    if ((p.qtype == GGUF_Q4_K || p.qtype == GGUF_Q5_K) && p.layout == GGUF_LAYOUT_BLOCKS && p.M == 1) {
+        const int64_t rpc_t = ceil_div(p.N, (int64_t)num_sms);
+        const TileLayout L = tile_layout(p.M, p.K, rpc_t, p.rb);
+        if (L.total <= half) {
+            p.tile = 1;
+            p.direct = 0;
+            p.rows_per_cta = rpc_t;
+            p.stage_bytes = L.img;
+            *grid = (int)ceil_div(p.N, rpc_t);
+            *smem = (size_t)L.total;
+            return GGUF_OK;
         }
     }
     const int64_t rpc = ceil_div(p.N, (int64_t)num_sms);

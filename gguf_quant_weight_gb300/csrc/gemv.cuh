@@ -20,7 +20,6 @@ struct GemvParams {
     void* act_image;       // workspace: the quantized activations (codes + per-block entries)
     int direct;            // unit fields 16-byte aligned: load straight into registers
     int tile;              // rows staged whole in shared memory, two CTAs per SM: 1 tile kernel, 2 pair kernel
-    int ksplit;            // tile kernel: K slices per row group (a cluster of that many CTAs)
     // plan (filled by gemv_plan)
     int64_t rb;            // bytes per weight row (raw layout)
     int64_t rows_per_cta;  // rows owned by one CTA
