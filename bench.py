@@ -432,7 +432,7 @@ def run_gpu(args):
     calls = steps * len(MS)
     achieved = algo * calls / sec / 1e9   # per call: every kernel of gguf_mm_gemv, chained
     # kernels per call: the tile kernel alone at M = 1; the activation quantizer
-    # plus the direct-load kernel at M = 2, 4 (the library's plan for this shape)
+    # plus the pair kernel at M = 2, 4 (the library's plan for this shape)
     launches = steps * sum(1 if m == 1 else 2 for m in MS)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps, "warmup": args.warmup,
@@ -447,7 +447,7 @@ def run_gpu(args):
         "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": recorded_traffic(), "peak_kind": peak_kind,
-                     "kernel": "gguf_mm_gemv: gemv_tile_kernel (M=1); act_quant_kernel + gemv_direct_kernel (M=2,4)",
+                     "kernel": "gguf_mm_gemv: gemv_tile_kernel (M=1); act_quant_kernel + gemv_pair_kernel (M=2,4)",
                      "algorithmic_bytes_per_launch": algo},
         "gpu_launches": launches,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
