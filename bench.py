@@ -215,9 +215,10 @@ def time_graph(fn, reps, stream, calls):
     return e0.elapsed_time(e1) / 1e3 / (reps * calls)
 
 
-def prefill_figures(dev, stream, tc_peak):
-    """Tensor-core figures for the prefill and MoE workloads (context for the
-    second half of the metric); weights rotate over copies larger than L2."""
+def prefill_figures(dev, stream, tc_peak, hbm_peak):
+    """Figures for the other workloads (context for the second half of the
+    metric): the small Q6_K GEMV, the Q6_K / Q5_K and Q8_0 prefill GEMMs and the
+    MoE expert GEMM; weights rotate over copies larger than L2."""
     import torch
     import gguf_quant_weight_gb300 as g
     import gguf_synth as syn
@@ -228,8 +229,22 @@ def prefill_figures(dev, stream, tc_peak):
         c = max(2, int(np.ceil(2.2 * l2 / arr.size)))
         return torch.from_numpy(arr.reshape(-1)).to(dev).repeat(c).view(c, -1), c
 
+    # Q6_K GEMV 256x1024, M = 1, f32 activations and output (no residual)
+    N, K = 256, 1024
+    w = syn.weight_blocks(syn.rng(1005), 14, N, K)
+    W, c = copies_of(w)
+    x = torch.from_numpy(syn.normal(syn.rng(1006), (1, K), "f32")).to(dev)
+    y = torch.empty((1, N), dtype=torch.float32, device=dev)
+    wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 14, N, K, 1)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    t = time_graph(lambda i: g.gguf_mm_gemv(W[i % c], 14, 0, N, K, x, g.GGUF_DT_F32, 1, None, y, g.GGUF_DT_F32,
+                                            ws, wsb, stream=stream), 5, stream, c)
+    out["q6_k_gemv_256x1024_m1_f32"] = {"us": t * 1e6, "weight_gbs": w.size / t / 1e9,
+                                        "hbm_frac": w.size / t / 1e9 / hbm_peak}
     rs = syn.rng(1002)
-    for qt, name, layout in ((14, "q6_k_planes", 1), (13, "q5_k", 0)):
+    for qt, name, layout, ms in ((14, "q6_k_planes", 1, (8, 64, 128, 256, 512, 2048)),
+                                 (13, "q5_k", 0, (8, 64, 128, 256, 512, 2048)),
+                                 (14, "q6_k", 0, (512, 2048))):
         N, K = 14336, 4096
         w = syn.weight_blocks(rs, qt, N, K)
         W, c = copies_of(w)
@@ -239,16 +254,21 @@ def prefill_figures(dev, stream, tc_peak):
                 g.gguf_repack_q6k_planes(W[i], P[i], N * K // 256, 0, stream=stream)
             stream.synchronize()
             W = P
-        for M in (512, 2048):
+        for M in ms:
             x = torch.from_numpy(syn.normal(rs, (M, K), "bf16")).to(dev).view(torch.bfloat16)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qt, N, K, M)
             ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-            t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], qt, layout, N, K, x, g.GGUF_DT_BF16, M, None, y,
-                                                    g.GGUF_DT_BF16, ws, wsb, g.GGUF_PATH_FUSED, stream=stream),
-                           5, stream, c)
-            tf = 2 * M * N * K / t / 1e12
-            out[f"{name}_14336x4096_m{M}_fused"] = {"us": t * 1e6, "tflops": tf, "tc_frac": tf / tc_peak}
+            # M = 8 sits on the border of the two paths: both are timed
+            for path, tag in ((g.GGUF_PATH_FUSED, "fused"), (g.GGUF_PATH_GEMV, "gemv")):
+                if path == g.GGUF_PATH_GEMV and M > 8:
+                    continue
+                t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], qt, layout, N, K, x, g.GGUF_DT_BF16, M, None, y,
+                                                        g.GGUF_DT_BF16, ws, wsb, path, stream=stream),
+                               5, stream, c)
+                tf = 2 * M * N * K / t / 1e12
+                out[f"{name}_14336x4096_m{M}_{tag}"] = {"us": t * 1e6, "tflops": tf, "tc_frac": tf / tc_peak,
+                                                        "weight_gbs": W[0].numel() / t / 1e9}
     # Q8_0 2048x8192: fused vs decode-once (K-padded f16) + dense GEMM
     N, K = 2048, 8192
     w = syn.weight_blocks(syn.rng(1003), 8, N, K)
@@ -279,7 +299,7 @@ def prefill_figures(dev, stream, tc_peak):
     wE = syn.weight_blocks(syn.rng(1004), 12, E * N, K)
     WE, c = copies_of(wE)
     per_expert = N * (K // 256) * 144
-    for T in (32, 512):
+    for T in (32, 64, 256, 512):
         id_sets = [syn.zipf_ids(syn.rng(2000 + T + j), T, E, top_k, 1.1) for j in range(8)]
         IDS = [torch.from_numpy(a).to(dev) for a in id_sets]
         touched = float(np.mean([len(np.unique(a)) for a in id_sets])) * per_expert
@@ -288,12 +308,26 @@ def prefill_figures(dev, stream, tc_peak):
         wsb = g.gguf_mm_workspace_size(g.GGUF_OP_ID, 12, N, K, T, E, top_k)
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
         calls = 8 * c
-        t = time_graph(lambda i: g.gguf_mm_id(WE[i % c], 12, E, N, K, x, g.GGUF_DT_BF16, T, IDS[i % 8], top_k, None,
-                                              y, g.GGUF_DT_BF16, ws, wsb, stream=stream), 3, stream, calls)
         fl = 2 * top_k * T * N * K
-        out[f"q4_k_moe_128x768x2048_top8_t{T}"] = {"us": t * 1e6, "tflops": fl / t / 1e12,
-                                                   "tc_frac": fl / t / 1e12 / tc_peak,
-                                                   "touched_gbs": touched / t / 1e9}
+        rec = {}
+        # second arm: every tile's MMAs at the full tile width, as without the
+        # skip of the tile's empty part (the switch is read when a call is made,
+        # so while the graph is captured)
+        for arm in ("skip", "full_width"):
+            if arm == "full_width":
+                os.environ["GGUF_MM_MOE_FULL_TILES"] = "1"
+            try:
+                t = time_graph(lambda i: g.gguf_mm_id(WE[i % c], 12, E, N, K, x, g.GGUF_DT_BF16, T, IDS[i % 8], top_k,
+                                                      None, y, g.GGUF_DT_BF16, ws, wsb, stream=stream), 3, stream, calls)
+            finally:
+                os.environ.pop("GGUF_MM_MOE_FULL_TILES", None)
+            if arm == "skip":
+                rec.update({"us": t * 1e6, "tflops": fl / t / 1e12, "tc_frac": fl / t / 1e12 / tc_peak,
+                            "touched_gbs": touched / t / 1e9, "hbm_frac": touched / t / 1e9 / hbm_peak,
+                            "experts_touched": touched / per_expert})
+            else:
+                rec["us_full_width_tiles"] = t * 1e6
+        out[f"q4_k_moe_128x768x2048_top8_t{T}"] = rec
     return out
 
 
@@ -454,7 +488,7 @@ def run_gpu(args):
     }
     if rank == 0:
         if not args.no_prefill:
-            line["prefill"] = prefill_figures(dev, stream, tc)
+            line["prefill"] = prefill_figures(dev, stream, tc, hbm)
             line["prefill"]["peak_tflops"] = tc
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()

@@ -25,6 +25,7 @@
 // The MMA never waits on decode of the same stage it consumes: stages ring
 // through S slots, so decode of step i+1.. overlaps the MMAs of step i.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 
 #include "tc_gemm.cuh"
@@ -88,6 +89,7 @@ struct FusedParams {
     const int* ntiles;   // number of work items
     const int* offsets;  // [n_expert + 1] start of each expert's group in the gathered activations
     const int* rows;     // entry (token * top_k + slot) of every gathered row
+    int full_width;      // measurement aid: MMAs always BN wide (no tile-skip)
 };
 
 __device__ __forceinline__ uint4 lds128u(uint32_t a) {
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
     }
     // MMA width: the tile's valid token columns rounded up to 16, so an
     // underfilled tile issues only the MMA columns it needs
-    const int n_mma = min(BN, (cols + 15) & ~15);
+    const int n_mma = fp.full_width ? BN : min(BN, (cols + 15) & ~15);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], DW + 1); mbar_init(&empty[s], 1); }
@@ -604,7 +606,11 @@ int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t
     if ((st = make_tmap_2d(&tb, xg, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)K, (uint64_t)rows_cap,
                            (uint64_t)K * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != GGUF_OK)
         return st;
-    FusedParams fp{N, rows_cap, (int)KB, residual, y, ydt, status, tiles, ntiles, offsets, rows};
+    // GGUF_MM_MOE_FULL_TILES=1: every tile's MMA at the full 128 columns, as
+    // without the tile-skip (a comparison arm for measurement; same output)
+    const char* full = std::getenv("GGUF_MM_MOE_FULL_TILES");
+    FusedParams fp{N, rows_cap, (int)KB, residual, y, ydt, status, tiles, ntiles, offsets, rows,
+                   (full && full[0] == '1') ? 1 : 0};
     const int gy = (int)max_tiles;
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {

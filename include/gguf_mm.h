@@ -123,8 +123,10 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K,
  *   residual [T, top_k, N] of ydt or NULL;  y [T, top_k, N] of ydt (F32, F16, BF16)
  * Rows are grouped by expert on the device; each (expert, 128-row weight tile,
  * token tile) issues MMAs only for round_up(rows, 16) token columns, so the
- * empty part of an underfilled token tile costs nothing.  Ids outside
- * [0, n_expert) are skipped (their Y rows are left untouched).
+ * empty part of an underfilled token tile costs nothing.  (For comparison
+ * runs, the environment variable GGUF_MM_MOE_FULL_TILES=1, read at each call,
+ * issues every tile's MMAs at the full width instead; the output is the same.)
+ * Ids outside [0, n_expert) are skipped (their Y rows are left untouched).
  * Workspace: gguf_mm_workspace_size(GGUF_OP_ID, ...) bytes. */
 int gguf_mm_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K,
                const void* x, int xdt, int64_t T, const int32_t* ids, int64_t top_k,

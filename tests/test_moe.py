@@ -88,3 +88,14 @@ def test_moe_config_128_experts_top8_768x2048(T):
     tok = np.arange(0, T, max(1, T // 8))
     got, ref = _run(syn.Q4_K, E, N, K, T, top_k, ids, seed=1004, token_rows=tok)
     U.check_close(got[tok].reshape(-1, N), ref[tok].reshape(-1, N), "bf16")
+
+
+def test_moe_full_width_tiles_give_the_same_output(monkeypatch):
+    # the comparison switch only widens the MMAs over columns no row fills
+    E, N, K, T, top_k = 16, 256, 512, 40, 4
+    ids = syn.zipf_ids(syn.rng(77), T, E, top_k, 1.1)
+    got, ref = _run(syn.Q4_K, E, N, K, T, top_k, ids)
+    monkeypatch.setenv("GGUF_MM_MOE_FULL_TILES", "1")
+    got_full, _ = _run(syn.Q4_K, E, N, K, T, top_k, ids)
+    U.check_close(got_full.reshape(-1, N), ref.reshape(-1, N), "bf16")
+    assert np.array_equal(got_full, got)
