@@ -170,8 +170,12 @@ size_t gguf_mm_workspace_size(int op, int qtype, int64_t N, int64_t K, int64_t M
     if (N <= 0 || K <= 0 || M <= 0) return 0;
     switch (op) {
         case GGUF_OP_GEMV: return M <= 8 ? gemv_workspace_bytes(M, K) : 0;
-        case GGUF_OP_GEMM:
-            return std::max(gemm_workspace_bytes(qtype, N, K, M), M <= 8 ? gemv_workspace_bytes(M, K) : size_t(0));
+        case GGUF_OP_GEMM: {
+            // sized for the current device's SM count (152 when none is current)
+            int sms = 152, *st = nullptr;
+            if (gg::current_device_launch_facts(&sms, &st) != GGUF_OK) sms = 152;
+            return std::max(gemm_workspace_bytes(qtype, N, K, M, sms), M <= 8 ? gemv_workspace_bytes(M, K) : size_t(0));
+        }
         case GGUF_OP_DENSE: return dense_workspace_bytes(N, K, M);
         case GGUF_OP_ID:
             if (n_expert <= 0 || top_k <= 0) return 0;
@@ -212,11 +216,11 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K, con
         return run_gemv(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace, ws_bytes,
                         (cudaStream_t)stream, nullptr, nullptr, nullptr, nullptr, false);
     if (xdt == GGUF_DT_F32) return GGUF_ERR_UNSUPPORTED;
-    const size_t need = gemm_workspace_bytes(qtype, N, K, M);
-    if (need && (!workspace || ws_bytes < need)) return GGUF_ERR_WORKSPACE;
-    if (workspace && !aligned16(workspace)) return GGUF_ERR_MISALIGNED;
     DeviceFacts* f = nullptr;
     if ((st = facts(&f)) != GGUF_OK) return st;
+    const size_t need = gemm_workspace_bytes(qtype, N, K, M, f->num_sms);
+    if (need && (!workspace || ws_bytes < need)) return GGUF_ERR_WORKSPACE;
+    if (workspace && !aligned16(workspace)) return GGUF_ERR_MISALIGNED;
     return gemm_fused_run(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace, f->num_sms, f->status,
                           (cudaStream_t)stream);
 }

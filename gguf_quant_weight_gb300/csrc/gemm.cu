@@ -30,7 +30,10 @@ namespace gg {
 namespace {
 
 __global__ void convert_act_kernel(const void* __restrict__ x, int xdt, int64_t total, uint16_t* __restrict__ out,
-                                   int odt_bf16) {
+                                   int odt_bf16, uint32_t* __restrict__ zero, int nzero) {
+    // the GEMM that follows on the stream counts on these words being zero
+    if (blockIdx.x == 0)
+        for (int j = threadIdx.x; j < nzero; j += blockDim.x) zero[j] = 0u;
     for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < total;
          i += (int64_t)gridDim.x * blockDim.x * 8) {
         float v[8];
@@ -63,11 +66,11 @@ __global__ void convert_act_kernel(const void* __restrict__ x, int xdt, int64_t 
 }  // namespace
 
 cudaError_t convert_activations(const void* x, int xdt, int64_t M, int64_t K, void* out, int odt, int num_sms,
-                                cudaStream_t s) {
+                                cudaStream_t s, uint32_t* zero, int nzero) {
     const int64_t total = M * K;
     const int64_t blocks = std::min<int64_t>(ceil_div(total, 8 * 256), (int64_t)num_sms * 8);
     convert_act_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(
-        x, xdt, total, static_cast<uint16_t*>(out), odt == GGUF_DT_BF16 ? 1 : 0);
+        x, xdt, total, static_cast<uint16_t*>(out), odt == GGUF_DT_BF16 ? 1 : 0, zero, nzero);
     return cudaGetLastError();
 }
 

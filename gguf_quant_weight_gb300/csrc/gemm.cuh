@@ -7,7 +7,10 @@
 
 namespace gg {
 
-size_t gemm_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t M);
+// Workspace of the fused GEMM on a device with num_sms SMs: the F16
+// activations, plus the split-K partial sums and tickets when the plan for
+// that SM count splits K.
+size_t gemm_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t M, int num_sms);
 size_t dense_workspace_bytes(int64_t N, int64_t K, int64_t M);
 
 int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,

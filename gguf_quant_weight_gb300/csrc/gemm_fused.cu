@@ -13,7 +13,9 @@
 //              Q6_K planes), up to RS super-blocks ahead -- its own warp, so the
 //              weight stream never waits on the MMA's operand stages
 //   warp 1     TMEM allocation and tcgen05.mma issue (128 x BN x 16 per MMA,
-//              f32 accumulators in TMEM), one commit per stage
+//              f32 accumulators in TMEM), one commit per stage; at BN <= 128
+//              one more warp (after the decoders) issues too, half of every
+//              k step's MMAs, into its own accumulator
 //   warp 2     TMA producer of the f16 activation tile of each 64-value k step
 //   warps 3..  decoders (16 warps for Q4_K/Q5_K/Q6_K planes, 8 otherwise):
 //              each k step they turn 128 rows x 64 values of raw bytes into f16
@@ -41,9 +43,21 @@ __host__ __device__ constexpr bool state_decoder(int qt, int layout) {
     return qt == GGUF_Q4_K || qt == GGUF_Q5_K || (qt == GGUF_Q6_K && layout == GGUF_LAYOUT_Q6K_PLANES);
 }
 __host__ __device__ constexpr int decode_warps(int qt, int layout) { return state_decoder(qt, layout) ? 16 : 8; }
-// warp 0: raw-weight TMA producer; warp 1: TMEM + MMA issue; warp 2: activation
-// TMA producer; warps 3..: decoders (and the epilogue)
-__host__ __device__ constexpr int fused_threads(int qt, int layout) { return 96 + 32 * decode_warps(qt, layout); }
+// MMA-issuing threads.  One tcgen05.mma costs the thread that issues it ~60
+// cycles (more beside busy decoder warps) -- at BN <= 128 far longer than the
+// tensor core takes to run it -- while threads in different warps issue in
+// parallel (measured: 1, 2, 4 issuing warps of 128 x 16 x 16 MMAs give 1, 1.7
+// and 3.5 times the rate).  So NI threads, one per warp, split the four MMAs
+// of each k step, each accumulating into its own BN TMEM columns (K split
+// NI ways); the epilogue adds the NI partial sums.  (Two, not four: the TMEM
+// columns are worth more as operand stages.)
+__host__ __device__ constexpr int mma_issuers(int bn) { return bn <= 128 ? 2 : 1; }
+// warp 0: raw-weight TMA producer; warp 1: TMEM + MMA issuer 0; warp 2:
+// activation TMA producer; warps 3 .. 3+DW-1: decoders (and the epilogue);
+// the last NI - 1 warps: MMA issuers 1 .. NI-1
+__host__ __device__ constexpr int fused_threads(int qt, int layout, int bn) {
+    return 96 + 32 * decode_warps(qt, layout) + 32 * (mma_issuers(bn) - 1);
+}
 
 __host__ __device__ constexpr int raw_pitch(int qt, int layout) {
     // bytes per weight row in one raw slot (= the TMA box's inner extent)
@@ -61,20 +75,29 @@ struct FusedCfg {
     // MMA reads it from there, so shared memory carries only the activation
     // tiles (B) and the raw blocks.  One ring of S stages covers both operands
     // of a k step (one "full" barrier: the decoder warps plus the activation
-    // TMA; one "empty" barrier: one commit), which keeps the single MMA-issuing
-    // thread's work per step small -- that thread, not the tensor core, is
-    // what limits the step rate at these tile shapes.
+    // TMA; one "empty" barrier: one commit per issuer), which keeps the
+    // MMA-issuing threads' work per step small.
+    static constexpr int NI = mma_issuers(BN);       // issuers; accumulator j at columns [j*BN, (j+1)*BN)
     static constexpr int A_COLS = 32;                 // TMEM columns per decoded stage
-    static constexpr int A_COL0 = 256;                // first decoded-stage column (after the accumulator)
+    static constexpr int A_COL0 = NI * BN < 32 ? 32 : NI * BN;   // first decoded-stage column
     static constexpr int B_BYTES = BN * 64 * 2;
-    static constexpr int S = BN >= 256 ? 4 : 6;       // stages
+    static constexpr int TMEM_COLS = 512;             // accumulators [0, NI*BN) + decoded stages
+    // Stages: as many as tensor memory holds (up to 12) while shared memory
+    // keeps three raw slots -- the activation tile of a step is requested
+    // when its stage frees, and under the weight stream it lands ~3000 cycles
+    // later, so the ring must reach that far ahead of the MMAs.  BN = 256
+    // keeps four (its tiles are wide enough that the MMAs cover the wait).
+    static constexpr int S_TMEM = (TMEM_COLS - A_COL0) / A_COLS;
+    static constexpr int S_SMEM = (232448 - 2048 - 3 * RAW) / B_BYTES;
+    static constexpr int S_MIN = S_TMEM < S_SMEM ? S_TMEM : S_SMEM;
+    static constexpr int S = BN >= 256 ? 4 : (S_MIN > 12 ? 12 : S_MIN);
     // raw slots: what the activation stages leave (each covers four k steps)
     static constexpr int RS_FIT = (232448 - 2048 - S * B_BYTES) / RAW;
     static constexpr int RS = RS_FIT > 6 ? 6 : RS_FIT;
-    static constexpr int TMEM_COLS = 512;             // accumulator [0, BN) + decoded stages
-    static constexpr int SMEM = S * B_BYTES + RS * RAW + 1024 + 256;
+    static constexpr int SMEM = S * B_BYTES + RS * RAW + 1024 + 512;   // + alignment + barriers
+    static_assert(8 * (2 * S + 2 * RS + 1) + 8 <= 512, "barrier area");
     static_assert(RS >= 2, "raw ring needs two slots");
-    static_assert(A_COL0 + S * A_COLS <= TMEM_COLS && BN <= A_COL0, "TMEM columns");
+    static_assert(A_COL0 + S * A_COLS <= TMEM_COLS && NI * BN <= A_COL0 && 4 % NI == 0, "TMEM columns");
 };
 
 struct FusedParams {
@@ -90,16 +113,20 @@ struct FusedParams {
     const int* offsets;  // [n_expert + 1] start of each expert's group in the gathered activations
     const int* rows;     // entry (token * top_k + slot) of every gathered row
     int full_width;      // measurement aid: MMAs always BN wide (no tile-skip)
+    // split K (dense mode): grid z = ks slices of the super-blocks; every slice
+    // writes its partial tile, the last to finish a tile adds them up
+    int ks;
+    float* partial;      // [tile][ks][BN][128] f32
+    int* tickets;        // [tile], zero at launch
 };
 
+// barrier `id` over the first `threads` threads that reach it (whole warps)
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 __device__ __forceinline__ uint4 lds128u(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ uint32_t lds32u(uint32_t a) {
-    uint32_t v;
-    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
     return v;
 }
 __device__ __forceinline__ uint32_t lds16u(uint32_t a) {
@@ -110,16 +137,9 @@ __device__ __forceinline__ uint32_t lds16u(uint32_t a) {
 __device__ __forceinline__ uint32_t lds_w2(uint32_t a) {   // 32-bit word at a 2-byte aligned address
     return lds16u(a) | (lds16u(a + 2) << 16);
 }
-__device__ __forceinline__ void sts128u(uint32_t a, uint4 v) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
-}
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int i) { return (w >> (8 * i)) & 0xFFu; }
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-    const __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // ---- packed f16 decode
@@ -302,8 +322,10 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
     }
 }
 
-template <int QT, int LAYOUT, int BN, bool MOE>
-__global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
+// SPLIT: the K-split form (a separate instantiation: its epilogue code in the
+// kernel slowed the unsplit form by ~3 %, measured)
+template <int QT, int LAYOUT, int BN, bool MOE, bool SPLIT>
+__global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
     fused_tc_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                     const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW3,
                     const __grid_constant__ CUtensorMap tmB, const FusedParams fp) {
@@ -312,6 +334,12 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
     constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
     constexpr int PITCH = raw_pitch(QT, LAYOUT);
     constexpr int DW = decode_warps(QT, LAYOUT);   // decoder warps
+    constexpr int NI = C::NI;                      // MMA issuers
+    // k steps a decoder warp takes per round: two for Q6_K (measured: raw
+    // blocks 170 -> 101 us, planes 187 -> 182 us at M = 512 / 2048), one for
+    // the others (two cost Q8_0 8 % at M = 4096 and Q5_K 7 % at M = 64)
+    constexpr int DB = QT == GGUF_Q6_K ? 2 : 1;
+    static_assert(4 % DB == 0 && DB <= C::S, "decode rounds");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = align_up_1024(smem_raw);
     uint8_t* sB = base;
@@ -324,7 +352,11 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(tfull + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n0 = (int64_t)blockIdx.x * 128;   // first output feature of the tile
-    const int KB = fp.KB, nk = 4 * KB;
+    // this CTA's super-blocks [kb0, kb0 + nkb) of the K slice blockIdx.z
+    static_assert(!(MOE && SPLIT), "the grouped form does not split K");
+    const int ks = SPLIT ? fp.ks : 1, z = SPLIT ? (int)blockIdx.z : 0;
+    const int kb0 = (int)((int64_t)z * fp.KB / ks);
+    const int nkb = (int)((int64_t)(z + 1) * fp.KB / ks) - kb0, nk = 4 * nkb;
     // tile geometry: weight row coordinate, activation row coordinate, valid token columns
     int64_t wrow0, brow0, t0 = 0;
     int cols, expert = 0, gstart = 0;
@@ -347,9 +379,9 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
     const int n_mma = fp.full_width ? BN : min(BN, (cols + 15) & ~15);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], DW + 1); mbar_init(&empty[s], 1); }
+        for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], DW + 1); mbar_init(&empty[s], NI); }
         for (int s = 0; s < C::RS; ++s) { mbar_init(&rfull[s], 1); mbar_init(&rempty[s], DW); }
-        mbar_init(tfull, 1);
+        mbar_init(tfull, NI);
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tslot, C::TMEM_COLS);
@@ -362,9 +394,9 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
         // raw super-blocks, as far ahead as the raw ring allows
         if (lane == 0) {
             prefetch_tmap(&tmW0);
-            for (int kb = 0; kb < KB; ++kb) {
-                const int rs = kb % C::RS;
-                if (!mbar_wait(&rempty[rs], ((kb / C::RS) & 1) ^ 1, fp.status)) break;
+            for (int kl = 0; kl < nkb; ++kl) {
+                const int kb = kb0 + kl, rs = kl % C::RS;
+                if (!mbar_wait(&rempty[rs], ((kl / C::RS) & 1) ^ 1, fp.status)) break;
                 uint8_t* dst = sR + rs * RAW;
                 mbar_arrive_expect_tx(&rfull[rs], RAW);
                 if constexpr (PLANES) {
@@ -380,18 +412,23 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
             }
         }
     } else if (warp == 2) {
-        // the activation tile of every 64-value k step, one operand stage ahead
+        // the activation tile of every 64-value k step, as far ahead as the ring allows
         if (lane == 0) {
             prefetch_tmap(&tmB);
             for (int i = 0; i < nk; ++i) {
                 const int s = i % C::S;
                 if (!mbar_wait(&empty[s], ((i / C::S) & 1) ^ 1, fp.status)) break;
                 mbar_arrive_expect_tx(&full[s], C::B_BYTES);
-                tma_load_2d(sB + s * C::B_BYTES, &tmB, i * 64, (int)brow0, &full[s]);
+                tma_load_2d(sB + s * C::B_BYTES, &tmB, (4 * kb0 + i) * 64, (int)brow0, &full[s]);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp >= 3 + DW) {
+        // issuer j: the 16-value k slices [j*4/NI, (j+1)*4/NI) of every step,
+        // into accumulator j
         if (lane == 0) {
+            constexpr int KS = 4 / NI;
+            const int j = warp == 1 ? 0 : warp - (2 + DW);
+            const uint32_t d = tmem + (uint32_t)(j * BN);
             const uint32_t idesc = idesc_f16(128, n_mma, 0);
             // B descriptor of stage s, k slice k: the start-address field is
             // linear in the address (+B_BYTES/16 per stage, +2 per 16 values)
@@ -403,7 +440,8 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
                 const uint32_t a0 = tmem + (uint32_t)(C::A_COL0 + s * C::A_COLS);
                 const uint64_t b0 = bdesc0 + (uint64_t)(s * (C::B_BYTES >> 4));
 #pragma unroll
-                for (int k = 0; k < 4; ++k) umma_f16_ts(tmem, a0 + 8 * k, b0 + 2 * k, idesc, (i | k) != 0);
+                for (int k = j * KS; k < (j + 1) * KS; ++k)
+                    umma_f16_ts(d, a0 + 8 * k, b0 + 2 * k, idesc, (i | (k - j * KS)) != 0);
                 umma_commit(&empty[s]);
             }
             umma_commit(tfull);
@@ -417,9 +455,9 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
         const uint32_t t_lane = (uint32_t)(32 * (warp & 3)) << 16;
         int i = 0;
         bool ok = true;
-        for (int kb = 0; kb < KB && ok; ++kb) {
-            const int rs = kb % C::RS;
-            ok = mbar_wait(&rfull[rs], (kb / C::RS) & 1, fp.status);
+        for (int kl = 0; kl < nkb && ok; ++kl) {
+            const int kb = kb0 + kl, rs = kl % C::RS;
+            ok = mbar_wait(&rfull[rs], (kl / C::RS) & 1, fp.status);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             const uint32_t slot = smem_u32(sR + rs * RAW);
             uint32_t row = slot + (uint32_t)(r * PITCH);
@@ -427,49 +465,89 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
             constexpr bool STATE = QT == GGUF_Q4_K || QT == GGUF_Q5_K || PLANES;
             KbState<QT, LAYOUT> st;
             if constexpr (STATE) st.prepare(row, slot, r, hf, kb, DW == 16 ? hh : -1);
+            // DB consecutive k steps per round: their stages are claimed
+            // together and decoded side by side, so one warp's chain of
+            // waits, loads and the TMEM store completion is paid once per DB
+            // steps (the step rate is bound by that chain, not by issue slots)
 #pragma unroll
-            for (int q = 0; q < 4; ++q, ++i) {
-                const int s = i % C::S;
-                ok = mbar_wait(&empty[s], ((i / C::S) & 1) ^ 1, fp.status);
+            for (int q = 0; q < 4; q += DB, i += DB) {
+                bool got = true;
+#pragma unroll
+                for (int d = 0; d < DB; ++d)
+                    got = got && mbar_wait(&empty[(i + d) % C::S], (((i + d) / C::S) & 1) ^ 1, fp.status);
+                ok = got;
                 if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                tc_fence_after();   // the MMAs that read this stage have completed
-                const uint32_t ta = tmem + t_lane + (uint32_t)(C::A_COL0 + s * C::A_COLS);
+                tc_fence_after();   // the MMAs that read these stages have completed
                 if constexpr (DW == 16) {
-                    uint4 out[2];
-                    decode_quarter<QT, LAYOUT>(st, row, slot, r, q, hf, hh, out);
-                    const uint32_t v[8] = {out[0].x, out[0].y, out[0].z, out[0].w,
-                                           out[1].x, out[1].y, out[1].z, out[1].w};
-                    tmem_st8(ta + (uint32_t)(16 * hf + 8 * hh), v);   // values 32hf + 16hh .. +15
+                    uint32_t v[DB][8];
+#pragma unroll
+                    for (int d = 0; d < DB; ++d) {
+                        uint4 out[2];
+                        decode_quarter<QT, LAYOUT>(st, row, slot, r, q + d, hf, hh, out);
+                        v[d][0] = out[0].x; v[d][1] = out[0].y; v[d][2] = out[0].z; v[d][3] = out[0].w;
+                        v[d][4] = out[1].x; v[d][5] = out[1].y; v[d][6] = out[1].z; v[d][7] = out[1].w;
+                    }
+#pragma unroll
+                    for (int d = 0; d < DB; ++d) {   // values 32hf + 16hh .. +15 of step i + d
+                        const uint32_t ta = tmem + t_lane + (uint32_t)(C::A_COL0 + ((i + d) % C::S) * C::A_COLS);
+                        tmem_st8(ta + (uint32_t)(16 * hf + 8 * hh), v[d]);
+                    }
                 } else {
-                    uint4 out[4];
-                    decode32<QT, LAYOUT>(row, slot, r, q, hf, kb, out);
-                    const uint32_t v[16] = {out[0].x, out[0].y, out[0].z, out[0].w, out[1].x, out[1].y,
-                                            out[1].z, out[1].w, out[2].x, out[2].y, out[2].z, out[2].w,
-                                            out[3].x, out[3].y, out[3].z, out[3].w};
-                    tmem_st16(ta + (uint32_t)(16 * hf), v);                // values 32hf .. +31
+#pragma unroll
+                    for (int d = 0; d < DB; ++d) {   // values 32hf .. +31 of step i + d
+                        uint4 out[4];
+                        decode32<QT, LAYOUT>(row, slot, r, q + d, hf, kb, out);
+                        const uint32_t v[16] = {out[0].x, out[0].y, out[0].z, out[0].w, out[1].x, out[1].y,
+                                                out[1].z, out[1].w, out[2].x, out[2].y, out[2].z, out[2].w,
+                                                out[3].x, out[3].y, out[3].z, out[3].w};
+                        const uint32_t ta = tmem + t_lane + (uint32_t)(C::A_COL0 + ((i + d) % C::S) * C::A_COLS);
+                        tmem_st16(ta + (uint32_t)(16 * hf), v);
+                    }
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&full[s]);
+                if (lane == 0) {
+#pragma unroll
+                    for (int d = 0; d < DB; ++d) mbar_arrive(&full[(i + d) % C::S]);
+                }
             }
             __syncwarp();
             if (ok && lane == 0) mbar_arrive(&rempty[rs]);
         }
         // epilogue: decoder warp w reads TMEM lane quarter (w % 4) and column
         // group (w - 3) / 4 of DW / 4 groups of 16-column chunks
-        if (mbar_wait(tfull, 0, fp.status)) {
+        constexpr int G = DW / 4, CH = BN / 16;
+        const int qd = warp & 3, grp = (warp - 3) >> 2;
+        const int64_t n = n0 + 32 * qd + lane;
+        const bool ep_ok = __all_sync(0xffffffffu, mbar_wait(tfull, 0, fp.status));
+        // split K: this slice's sums go to its slot [BN][128] of the tile
+        const int64_t tile = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+        float* const slots = SPLIT ? fp.partial + tile * ks * (BN * 128) : nullptr;
+        if (ep_ok) {
             tc_fence_after();
-            constexpr int G = DW / 4, CH = BN / 16;
-            const int qd = warp & 3, grp = (warp - 3) >> 2;
-            const int64_t n = n0 + 32 * qd + lane;
 #pragma unroll 1
             for (int c = grp * CH / G; c < (grp + 1) * CH / G; ++c) {
                 if (16 * c >= n_mma) break;   // columns past the MMA width hold nothing
                 uint32_t v[16];
                 tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + 16 * c, v);
                 tmem_ld_wait();
-                if (n < fp.N) {
+                tmem_ld_regs(v);
+#pragma unroll
+                for (int j = 1; j < NI; ++j) {   // the other issuers' partial sums, one at a time
+                    uint32_t u[16];
+                    tmem_ld16(tmem + ((uint32_t)(32 * qd) << 16) + j * BN + 16 * c, u);
+                    tmem_ld_wait();
+                    tmem_ld_regs(u);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(u[e]));
+                }
+                if constexpr (SPLIT) {
+                    // column-major slot: a warp's 32 rows of a column are one 128-byte line
+                    float* dst = slots + (int64_t)z * (BN * 128) + (16 * c) * 128 + 32 * qd + lane;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) dst[j * 128] = __uint_as_float(v[j]);
+                } else if (n < fp.N) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int col = 16 * c + j;
@@ -484,6 +562,45 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
                 }
             }
         }
+        if constexpr (SPLIT) {
+            // the last slice to finish the tile adds the slots in slice order
+            // (a fixed order: the result does not depend on which CTA is last)
+            volatile int* ticket = reinterpret_cast<volatile int*>(tslot + 1);
+            __threadfence();
+            named_bar_sync(1, DW * 32);
+            if (warp == 3 && lane == 0) *ticket = ep_ok ? atomicAdd(&fp.tickets[tile], 1) : -1;
+            named_bar_sync(1, DW * 32);
+            if (*ticket == ks - 1) {
+                __threadfence();
+#pragma unroll 1
+                for (int c = grp * CH / G; c < (grp + 1) * CH / G; ++c) {
+                    if (16 * c >= n_mma || n >= fp.N) break;
+                    // a slot's 16 columns are loaded together: one L2 round trip per slot
+                    float acc[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+                    const float* src = slots + (16 * c) * 128 + 32 * qd + lane;
+#pragma unroll 1
+                    for (int q = 0; q < ks; ++q) {
+                        float t[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) t[j] = __ldcg(src + (int64_t)q * (BN * 128) + j * 128);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[j] += t[j];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int col = 16 * c + j;
+                        if (col < cols) {
+                            const int64_t orow = t0 + col;
+                            float o = acc[j];
+                            if (fp.residual) o += load_act(fp.residual, fp.ydt, orow * fp.N + n);
+                            store_out(fp.y, fp.ydt, orow * fp.N + n, o);
+                        }
+                    }
+                }
+            }
+        }
         (void)expert;
     }
     tc_fence_before();
@@ -491,47 +608,89 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT), 1)
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-// Token-tile width: the fewest rounds of CTAs over the SMs; ties keep the
-// smaller tile (fewer zero-filled activation rows staged).  A tile's time is nearly flat in BN (the k-step rate is set by the
-// MMA-issuing thread and the decoders, not by the MMA width): measured about
-// 28 us at BN = 128 and 31 us at BN = 256 for K = 4096, i.e. cost ~ bn + 1150.
-int pick_bn_fused(int64_t N, int64_t M, int num_sms) {
-    int best = 32;
-    double best_cost = 1e30;
-    for (int bn : {32, 64, 128, 256}) {   // ties keep the smaller tile
+// Tile plan: token-tile width BN and K split ks with the least estimated
+// time, in k steps per round of CTAs times the per-step cost.  A step's cost
+// is nearly flat in BN (the step rate is set by the decoder warps, not by the
+// MMA width): ~ (bn + 1150).  Every CTA also pays ~24 steps of fixed cost
+// (start-up until the first blocks are decoded, epilogue, the gap before the
+// next round), and a K split ~8 more (partial tile out, the last slice reads
+// the slots back).  Measured on GB300: splitting pays where the tiles alone
+// leave most SMs idle (N = 2048: 16 row tiles, 49 -> 28 us at M = 128) and
+// loses at N = 14336 (M = 512: 67 us unsplit, 79 us in halves).  A candidate
+// must beat the best so far by 3 %, so ties keep the smaller tile and split.
+struct FusedPlan {
+    int bn, ks;
+};
+FusedPlan plan_fused(int64_t N, int64_t M, int64_t KB, int num_sms) {
+    FusedPlan best{32, 1};
+    double best_cost = 1e300;
+    const int64_t steps = 4 * KB;
+    for (int bn : {32, 64, 128, 256}) {
         const int64_t tiles = ceil_div(N, 128) * ceil_div(M, bn);
-        const double cost = (double)ceil_div(tiles, num_sms) * (std::min<int64_t>(bn, M) + 1150);
-        if (cost < best_cost - 1e-9) { best_cost = cost; best = bn; }
+        for (int ks = 1; ks <= 16; ++ks) {
+            if (ks > KB || (ks > 1 && steps / ks < 8)) break;
+            const double per =
+                (double)(ceil_div(steps, ks) + 24 + (ks > 1 ? 8 : 0)) * (double)(std::min<int64_t>(bn, M) + 1150);
+            const double cost = (double)ceil_div(tiles * ks, num_sms) * per;
+            if (cost < best_cost * 0.97) { best_cost = cost; best = {bn, ks}; }
+        }
     }
     return best;
 }
 
-template <int QT, int LAYOUT, int BN, bool MOE = false>
+// Workspace layout of the fused GEMM: F16 activations | split-K slots | tickets.
+struct FusedWorkspace {
+    size_t act, partial, tickets, total;
+};
+FusedWorkspace fused_workspace(int64_t N, int64_t K, int64_t M, const FusedPlan& pl) {
+    FusedWorkspace w{};
+    w.act = (size_t)(ceil_div(M * K * 2, 256) * 256);
+    w.total = w.act;
+    if (pl.ks > 1) {
+        const int64_t tiles = ceil_div(N, 128) * ceil_div(M, pl.bn);
+        w.partial = w.total;
+        w.total += (size_t)(ceil_div(tiles * pl.ks * pl.bn * 128 * 4, 256) * 256);
+        w.tickets = w.total;
+        w.total += (size_t)(ceil_div(tiles * 4, 256) * 256);
+    }
+    return w;
+}
+
+template <int QT, int LAYOUT, int BN, bool MOE = false, bool SPLIT = false>
 cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const FusedParams& fp, cudaStream_t s,
                          int grid_y = 0) {
     using C = FusedCfg<BN, raw_slot_bytes(QT, LAYOUT)>;
     const int smem = C::SMEM;
-    auto k = fused_tc_kernel<QT, LAYOUT, BN, MOE>;
+    auto k = fused_tc_kernel<QT, LAYOUT, BN, MOE, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)ceil_div(fp.N, 128), MOE ? (unsigned)grid_y : (unsigned)ceil_div(fp.M, BN));
-    k<<<grid, fused_threads(QT, LAYOUT), smem, s>>>(w[0], w[1], w[2], w[3], b, fp);
+    dim3 grid((unsigned)ceil_div(fp.N, 128), MOE ? (unsigned)grid_y : (unsigned)ceil_div(fp.M, BN),
+              SPLIT ? (unsigned)fp.ks : 1u);
+    k<<<grid, fused_threads(QT, LAYOUT, BN), smem, s>>>(w[0], w[1], w[2], w[3], b, fp);
     return cudaGetLastError();
 }
 
 template <int QT, int LAYOUT>
 cudaError_t launch_bn(int bn, const CUtensorMap* w, const CUtensorMap& b, const FusedParams& fp, cudaStream_t s) {
+    const bool split = fp.ks > 1;
     switch (bn) {
-        case 256: return launch_fused<QT, LAYOUT, 256>(w, b, fp, s);
-        case 128: return launch_fused<QT, LAYOUT, 128>(w, b, fp, s);
-        case 64: return launch_fused<QT, LAYOUT, 64>(w, b, fp, s);
-        default: return launch_fused<QT, LAYOUT, 32>(w, b, fp, s);
+        case 256: return split ? launch_fused<QT, LAYOUT, 256, false, true>(w, b, fp, s)
+                               : launch_fused<QT, LAYOUT, 256>(w, b, fp, s);
+        case 128: return split ? launch_fused<QT, LAYOUT, 128, false, true>(w, b, fp, s)
+                               : launch_fused<QT, LAYOUT, 128>(w, b, fp, s);
+        case 64: return split ? launch_fused<QT, LAYOUT, 64, false, true>(w, b, fp, s)
+                              : launch_fused<QT, LAYOUT, 64>(w, b, fp, s);
+        default: return split ? launch_fused<QT, LAYOUT, 32, false, true>(w, b, fp, s)
+                              : launch_fused<QT, LAYOUT, 32>(w, b, fp, s);
     }
 }
 
 }  // namespace
 
-size_t gemm_workspace_bytes(int, int64_t, int64_t K, int64_t M) { return (size_t)(ceil_div(M * K * 2, 256) * 256); }
+size_t gemm_workspace_bytes(int, int64_t N, int64_t K, int64_t M, int num_sms) {
+    if (K % 256 != 0) return (size_t)(ceil_div(M * K * 2, 256) * 256);
+    return fused_workspace(N, K, M, plan_fused(N, M, K / 256, num_sms)).total;
+}
 
 int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
                    const void* residual, void* y, int ydt, void* workspace, int num_sms, int* status,
@@ -540,7 +699,14 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
     const int64_t KB = K / 256;
     if (qtype == GGUF_Q6_K && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;   // 16-byte row strides for TMA
     if (N > INT32_MAX || M > INT32_MAX || KB > (1 << 20)) return GGUF_ERR_UNSUPPORTED;
-    if (convert_activations(x, xdt, M, K, workspace, GGUF_DT_F16, num_sms, stream) != cudaSuccess) return GGUF_ERR_CUDA;
+    const FusedPlan pl = plan_fused(N, M, KB, num_sms);
+    const FusedWorkspace wl = fused_workspace(N, K, M, pl);
+    uint8_t* wsb = static_cast<uint8_t*>(workspace);
+    int* tickets = pl.ks > 1 ? reinterpret_cast<int*>(wsb + wl.tickets) : nullptr;
+    const int ntiles = (int)(ceil_div(N, 128) * ceil_div(M, pl.bn));
+    if (convert_activations(x, xdt, M, K, workspace, GGUF_DT_F16, num_sms, stream,
+                            reinterpret_cast<uint32_t*>(tickets), tickets ? ntiles : 0) != cudaSuccess)
+        return GGUF_ERR_CUDA;
 
     const int bb = block_bytes(qtype) * (qtype == GGUF_Q8_0 ? 8 : 1);   // bytes of one 256-value column
     const int64_t rb = KB * bb;
@@ -567,12 +733,13 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
         if ((st = make_tmap_2d(&tw[0], w, u16, 2, (uint64_t)rb / 2, N, rb, box, 128, none)) != GGUF_OK) return st;
         tw[1] = tw[2] = tw[3] = tw[0];
     }
-    const int bn = pick_bn_fused(N, M, num_sms);
+    const int bn = pl.bn;
     CUtensorMap tb;
     if ((st = make_tmap_2d(&tb, workspace, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (uint64_t)K, (uint64_t)M,
                            (uint64_t)K * 2, 64, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B)) != GGUF_OK)
         return st;
-    FusedParams fp{N, M, (int)KB, residual, y, ydt, status, nullptr, nullptr, nullptr, nullptr};
+    FusedParams fp{N, M, (int)KB, residual, y, ydt, status, nullptr, nullptr, nullptr, nullptr, 0,
+                   pl.ks, pl.ks > 1 ? reinterpret_cast<float*>(wsb + wl.partial) : nullptr, tickets};
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {
         case GGUF_Q8_0: e = launch_bn<GGUF_Q8_0, 0>(bn, tw, tb, fp, stream); break;
@@ -610,7 +777,7 @@ int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t
     // without the tile-skip (a comparison arm for measurement; same output)
     const char* full = std::getenv("GGUF_MM_MOE_FULL_TILES");
     FusedParams fp{N, rows_cap, (int)KB, residual, y, ydt, status, tiles, ntiles, offsets, rows,
-                   (full && full[0] == '1') ? 1 : 0};
+                   (full && full[0] == '1') ? 1 : 0, 1, nullptr, nullptr};
     const int gy = (int)max_tiles;
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {

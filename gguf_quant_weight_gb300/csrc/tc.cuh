@@ -92,6 +92,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t v[16]) {
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Placed after tmem_ld_wait: ties the loaded registers to a point after the
+// wait, so no use of them can be scheduled before it.
+__device__ __forceinline__ void tmem_ld_regs(uint32_t v[16]) {
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15]));
+}
 
 // Thread t of the warp writes 8 (16) consecutive 32-bit columns of lane
 // (taddr.lane + t), starting at column taddr.col.

@@ -56,8 +56,10 @@ __device__ __forceinline__ void tc_epilogue(const TcEpilogue& ep, uint32_t tmem,
 int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t inner,
                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                  CUtensorMapSwizzle swz);
+// X (F32/F16/BF16) -> odt (F16/BF16) into out; also zeroes nzero 32-bit words
+// at `zero` (the split-K tickets of the GEMM that follows).
 cudaError_t convert_activations(const void* x, int xdt, int64_t M, int64_t K, void* out, int odt, int num_sms,
-                                cudaStream_t s);
+                                cudaStream_t s, uint32_t* zero = nullptr, int nzero = 0);
 int pick_bn(int64_t N, int64_t M, int num_sms);
 
 }  // namespace gg

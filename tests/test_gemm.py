@@ -110,3 +110,28 @@ def test_fused_rejects_q6k_rows_without_16_byte_stride():
         g.gguf_mm_gemm(w, syn.Q6_K, 0, 256, 256, x, g.GGUF_DT_BF16, 16, None, y, g.GGUF_DT_BF16, ws, 1 << 16,
                        g.GGUF_PATH_FUSED)
     assert e.value.status == g.GGUF_ERR_UNSUPPORTED
+
+
+def test_fused_split_k_residual_exact_and_deterministic():
+    # 2 row tiles and K = 4096 leave most SMs idle, so the plan splits K; the
+    # slices' sums meet in the workspace and the last slice adds them in a
+    # fixed order: two runs agree bit for bit, and both match the oracle
+    qtype, N, K, M = syn.Q4_K, 256, 4096, 40
+    rs = syn.rng(4242)
+    w = syn.weight_blocks(rs, qtype, N, K)
+    x = syn.normal(rs, (M, K), "bf16")
+    r = syn.normal(rs, (M, N), "bf16")
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qtype, N, K, M)
+    assert ws_bytes > M * K * 2   # room for the partial tiles
+    outs = []
+    for fill in (0x00, 0xFF):   # stale workspace bytes (tickets included) must not matter
+        ws = torch.full((ws_bytes,), fill, dtype=torch.uint8, device="cuda")
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        g.gguf_mm_gemm(U.dev(w), qtype, 0, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, U.dev(r, "bf16"), y,
+                       g.GGUF_DT_BF16, ws, ws_bytes, g.GGUF_PATH_FUSED)
+        torch.cuda.synchronize()
+        assert g.gguf_mm_check_errors() == 0
+        outs.append(U.host64(y))
+    assert np.array_equal(outs[0], outs[1])
+    ref = O.matmul_exact(U.act_f64(x, "bf16"), O.dequant(w, qtype, N, K), U.act_f64(r, "bf16"))
+    U.check_close(outs[0], ref, "bf16")
