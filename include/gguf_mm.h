@@ -71,7 +71,10 @@ typedef enum { GGUF_OP_GEMV = 0, GGUF_OP_GEMM = 1, GGUF_OP_ID = 2, GGUF_OP_DENSE
 /* Bytes of device workspace the given call needs (0 = none; pass NULL then).
  * op GGUF_OP_GEMV/GEMM take (t, N, K, M) -- the GEMM figure also covers the
  * GEMV path that GGUF_PATH_AUTO/GEMV may take for M <= 8; GGUF_OP_ID takes all arguments with M
- * the token count T; GGUF_OP_DENSE takes (N, K, M).  Returns 0 for invalid input. */
+ * the token count T; GGUF_OP_DENSE takes (N, K, M).  Returns 0 for invalid input.
+ * The GGUF_OP_GEMM figure depends on the current device's SM count (152 is
+ * assumed when no device is current): query it on the device that runs the
+ * call. */
 size_t gguf_mm_workspace_size(int op, int qtype, int64_t N, int64_t K, int64_t M,
                               int64_t n_expert, int64_t top_k);
 
@@ -109,7 +112,11 @@ int gguf_mm_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K,
  * feeds it to tcgen05 tensor-core MMAs with TMEM accumulators; activations are
  * converted to f16 into the workspace first (OpenVINO PR #39119,
  * "Implementation", DPAS prefill row: decode each block once, reuse it across
- * activation rows, overlap loading with decoding, tile grows with M).
+ * activation rows, overlap loading with decoding, tile grows with M).  When
+ * the weight's row tiles are too few to occupy the GPU (small N), K is split
+ * across CTAs: each slice's partial sums go to the workspace and the last
+ * slice to finish a tile adds them in slice order (the result does not depend
+ * on timing).
  * Workspace: gguf_mm_workspace_size(GGUF_OP_GEMM, ...) bytes. */
 int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K,
                  const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
