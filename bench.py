@@ -215,37 +215,50 @@ def time_graph(fn, reps, stream, calls):
     return e0.elapsed_time(e1) / 1e3 / (reps * calls)
 
 
-def prefill_figures(dev, stream, tc_peak, hbm_peak):
+def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
     """Figures for the other workloads (context for the second half of the
     metric): the small Q6_K GEMV, the Q6_K / Q5_K and Q8_0 prefill GEMMs and the
-    MoE expert GEMM; weights rotate over copies larger than L2."""
+    MoE expert GEMM; weights rotate over copies larger than L2.  `only`: a
+    regular expression; just the entries whose key it matches are run."""
+    import re
     import torch
     import gguf_quant_weight_gb300 as g
     import gguf_synth as syn
     out = {}
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
+    def want(key):
+        return only is None or re.search(only, key) is not None
+
     def copies_of(arr):
         c = max(2, int(np.ceil(2.2 * l2 / arr.size)))
         return torch.from_numpy(arr.reshape(-1)).to(dev).repeat(c).view(c, -1), c
 
     # Q6_K GEMV 256x1024, M = 1, f32 activations and output (no residual)
-    N, K = 256, 1024
-    w = syn.weight_blocks(syn.rng(1005), 14, N, K)
-    W, c = copies_of(w)
-    x = torch.from_numpy(syn.normal(syn.rng(1006), (1, K), "f32")).to(dev)
-    y = torch.empty((1, N), dtype=torch.float32, device=dev)
-    wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 14, N, K, 1)
-    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-    t = time_graph(lambda i: g.gguf_mm_gemv(W[i % c], 14, 0, N, K, x, g.GGUF_DT_F32, 1, None, y, g.GGUF_DT_F32,
-                                            ws, wsb, stream=stream), 5, stream, c)
-    out["q6_k_gemv_256x1024_m1_f32"] = {"us": t * 1e6, "weight_gbs": w.size / t / 1e9,
-                                        "hbm_frac": w.size / t / 1e9 / hbm_peak}
+    key = "q6_k_gemv_256x1024_m1_f32"
+    if want(key):
+        N, K = 256, 1024
+        w = syn.weight_blocks(syn.rng(1005), 14, N, K)
+        W, c = copies_of(w)
+        x = torch.from_numpy(syn.normal(syn.rng(1006), (1, K), "f32")).to(dev)
+        y = torch.empty((1, N), dtype=torch.float32, device=dev)
+        wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 14, N, K, 1)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        t = time_graph(lambda i: g.gguf_mm_gemv(W[i % c], 14, 0, N, K, x, g.GGUF_DT_F32, 1, None, y, g.GGUF_DT_F32,
+                                                ws, wsb, stream=stream), 5, stream, c)
+        out[key] = {"us": t * 1e6, "weight_gbs": w.size / t / 1e9, "hbm_frac": w.size / t / 1e9 / hbm_peak}
+
+    # Q6_K (planes and raw blocks) and Q5_K prefill, 14336x4096
     rs = syn.rng(1002)
     for qt, name, layout, ms in ((14, "q6_k_planes", 1, (8, 64, 128, 256, 512, 2048)),
                                  (13, "q5_k", 0, (8, 64, 128, 256, 512, 2048)),
                                  (14, "q6_k", 0, (512, 2048))):
         N, K = 14336, 4096
+        # M = 8 sits on the border of the two paths: both are timed
+        runs = [(M, path, tag) for M in ms for path, tag in ((g.GGUF_PATH_FUSED, "fused"), (g.GGUF_PATH_GEMV, "gemv"))
+                if (path == g.GGUF_PATH_FUSED or M <= 8) and want(f"{name}_14336x4096_m{M}_{tag}")]
+        if not runs:
+            continue
         w = syn.weight_blocks(rs, qt, N, K)
         W, c = copies_of(w)
         if layout:   # regroup every copy into the QL | QH | SC | D planes on the GPU
@@ -254,52 +267,60 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak):
                 g.gguf_repack_q6k_planes(W[i], P[i], N * K // 256, 0, stream=stream)
             stream.synchronize()
             W = P
-        for M in ms:
+        for M, path, tag in runs:
             x = torch.from_numpy(syn.normal(rs, (M, K), "bf16")).to(dev).view(torch.bfloat16)
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qt, N, K, M)
             ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-            # M = 8 sits on the border of the two paths: both are timed
-            for path, tag in ((g.GGUF_PATH_FUSED, "fused"), (g.GGUF_PATH_GEMV, "gemv")):
-                if path == g.GGUF_PATH_GEMV and M > 8:
-                    continue
-                t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], qt, layout, N, K, x, g.GGUF_DT_BF16, M, None, y,
-                                                        g.GGUF_DT_BF16, ws, wsb, path, stream=stream),
-                               5, stream, c)
-                tf = 2 * M * N * K / t / 1e12
-                out[f"{name}_14336x4096_m{M}_{tag}"] = {"us": t * 1e6, "tflops": tf, "tc_frac": tf / tc_peak,
-                                                        "weight_gbs": W[0].numel() / t / 1e9}
+            t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], qt, layout, N, K, x, g.GGUF_DT_BF16, M, None, y,
+                                                    g.GGUF_DT_BF16, ws, wsb, path, stream=stream), 5, stream, c)
+            tf = 2 * M * N * K / t / 1e12
+            out[f"{name}_14336x4096_m{M}_{tag}"] = {"us": t * 1e6, "tflops": tf, "tc_frac": tf / tc_peak,
+                                                    "weight_gbs": W[0].numel() / t / 1e9}
+
     # Q8_0 2048x8192: fused vs decode-once (K-padded f16) + dense GEMM
     N, K = 2048, 8192
-    w = syn.weight_blocks(syn.rng(1003), 8, N, K)
-    W, c = copies_of(w)
-    ld = K + 64
-    wd = torch.empty((N, ld), dtype=torch.float16, device=dev)
-    g.gguf_dequant_padded(W[0], 8, 0, N, K, wd, g.GGUF_DT_F16, ld, stream=stream)
-    cd = max(2, int(np.ceil(2.2 * l2 / (wd.numel() * 2))))
-    WD = wd.unsqueeze(0).repeat(cd, 1, 1)
-    t_dec = time_graph(lambda i: g.gguf_dequant_padded(W[i % c], 8, 0, N, K, wd, g.GGUF_DT_F16, ld, stream=stream),
-                       5, stream, c)
-    out["q8_0_2048x8192_decode_once"] = {"us": t_dec * 1e6, "gbs": (w.size + N * ld * 2) / t_dec / 1e9}
-    for M in (128, 512, 4096):
-        x = torch.from_numpy(syn.normal(rs, (M, K), "bf16")).to(dev).view(torch.bfloat16)
-        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 8, N, K, M)
-        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-        t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], 8, 0, N, K, x, g.GGUF_DT_BF16, M, None, y, g.GGUF_DT_BF16,
-                                                ws, wsb, g.GGUF_PATH_FUSED, stream=stream), 5, stream, c)
-        t2 = time_graph(lambda i: g.gguf_dense_gemm(WD[i % cd], g.GGUF_DT_F16, ld, N, K, x, g.GGUF_DT_BF16, M, None,
-                                                    y, g.GGUF_DT_BF16, ws, wsb, stream=stream), 5, stream, cd)
-        fl = 2 * M * N * K
-        out[f"q8_0_2048x8192_m{M}_fused"] = {"us": t * 1e6, "tflops": fl / t / 1e12, "tc_frac": fl / t / 1e12 / tc_peak}
-        out[f"q8_0_2048x8192_m{M}_dense_after_decode_once"] = {"us": t2 * 1e6, "tflops": fl / t2 / 1e12,
-                                                                 "tc_frac": fl / t2 / 1e12 / tc_peak}
+    ms = [M for M in (128, 512, 4096) if want(f"q8_0_2048x8192_m{M}_fused") or
+          want(f"q8_0_2048x8192_m{M}_dense_after_decode_once")]
+    if ms or want("q8_0_2048x8192_decode_once"):
+        w = syn.weight_blocks(syn.rng(1003), 8, N, K)
+        W, c = copies_of(w)
+        ld = K + 64
+        wd = torch.empty((N, ld), dtype=torch.float16, device=dev)
+        g.gguf_dequant_padded(W[0], 8, 0, N, K, wd, g.GGUF_DT_F16, ld, stream=stream)
+        cd = max(2, int(np.ceil(2.2 * l2 / (wd.numel() * 2))))
+        WD = wd.unsqueeze(0).repeat(cd, 1, 1)
+        if want("q8_0_2048x8192_decode_once"):
+            t_dec = time_graph(lambda i: g.gguf_dequant_padded(W[i % c], 8, 0, N, K, wd, g.GGUF_DT_F16, ld,
+                                                               stream=stream), 5, stream, c)
+            out["q8_0_2048x8192_decode_once"] = {"us": t_dec * 1e6, "gbs": (w.size + N * ld * 2) / t_dec / 1e9}
+        for M in ms:
+            x = torch.from_numpy(syn.normal(rs, (M, K), "bf16")).to(dev).view(torch.bfloat16)
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 8, N, K, M)
+            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            fl = 2 * M * N * K
+            if want(f"q8_0_2048x8192_m{M}_fused"):
+                t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], 8, 0, N, K, x, g.GGUF_DT_BF16, M, None, y,
+                                                        g.GGUF_DT_BF16, ws, wsb, g.GGUF_PATH_FUSED, stream=stream),
+                               5, stream, c)
+                out[f"q8_0_2048x8192_m{M}_fused"] = {"us": t * 1e6, "tflops": fl / t / 1e12,
+                                                     "tc_frac": fl / t / 1e12 / tc_peak}
+            if want(f"q8_0_2048x8192_m{M}_dense_after_decode_once"):
+                t2 = time_graph(lambda i: g.gguf_dense_gemm(WD[i % cd], g.GGUF_DT_F16, ld, N, K, x, g.GGUF_DT_BF16, M,
+                                                            None, y, g.GGUF_DT_BF16, ws, wsb, stream=stream),
+                                5, stream, cd)
+                out[f"q8_0_2048x8192_m{M}_dense_after_decode_once"] = {"us": t2 * 1e6, "tflops": fl / t2 / 1e12,
+                                                                         "tc_frac": fl / t2 / 1e12 / tc_peak}
+
     # MoE: 128 experts top-8, Q4_K 768x2048; ids rotate over 8 Zipf(1.1) draws
     E, N, K, top_k = 128, 768, 2048, 8
-    wE = syn.weight_blocks(syn.rng(1004), 12, E * N, K)
-    WE, c = copies_of(wE)
+    ts = [T for T in (32, 64, 256, 512) if want(f"q4_k_moe_128x768x2048_top8_t{T}")]
+    if ts:
+        wE = syn.weight_blocks(syn.rng(1004), 12, E * N, K)
+        WE, c = copies_of(wE)
     per_expert = N * (K // 256) * 144
-    for T in (32, 64, 256, 512):
+    for T in ts:
         id_sets = [syn.zipf_ids(syn.rng(2000 + T + j), T, E, top_k, 1.1) for j in range(8)]
         IDS = [torch.from_numpy(a).to(dev) for a in id_sets]
         touched = float(np.mean([len(np.unique(a)) for a in id_sets])) * per_expert
@@ -488,7 +509,7 @@ def run_gpu(args):
     }
     if rank == 0:
         if not args.no_prefill:
-            line["prefill"] = prefill_figures(dev, stream, tc, hbm)
+            line["prefill"] = prefill_figures(dev, stream, tc, hbm, args.prefill_only)
             line["prefill"]["peak_tflops"] = tc
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline()
@@ -505,6 +526,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-only", default=None, metavar="REGEX",
+                    help="run only the prefill figures whose key matches (e.g. q6_k_planes_14336x4096_m512)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

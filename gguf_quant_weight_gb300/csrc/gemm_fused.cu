@@ -285,6 +285,21 @@ __device__ __forceinline__ void decode_quarter(const KbState<QT, LAYOUT>& st, ui
     }
 }
 
+// Q8_0 block J (0..7) of a 272-byte raw row: its f16 scale bits and its 32
+// codes as 8 words.  The 34-byte blocks sit at 2-byte alignment, so the row is
+// read as three aligned 16-byte pieces and the words are cut out with funnel
+// shifts: with rows 272 = 17 x 16 bytes apart, 16-byte reads of 32 rows are
+// free of bank conflicts (2-byte reads hit 8 distinct banks: 4-way).
+template <int J>
+__device__ __forceinline__ void q8_block(uint32_t row, uint32_t& d_bits, uint32_t q4[8]) {
+    constexpr int B = (34 * J) & ~15, S = (34 * J) & 15, T = S + 2;   // piece start, scale and code offsets
+    const uint4 c0 = lds128u(row + B), c1 = lds128u(row + B + 16), c2 = lds128u(row + B + 32);
+    const uint32_t w[12] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w, c2.x, c2.y, c2.z, c2.w};
+    d_bits = (S & 2) ? (w[S / 4] >> 16) : (w[S / 4] & 0xFFFFu);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q4[i] = (T & 2) ? __funnelshift_r(w[T / 4 + i], w[T / 4 + i + 1], 16) : w[T / 4 + i];
+}
+
 // Decode values 32*hf .. 32*hf+31 of k step q (values 64q .. 64q+63 of the
 // super-block) of one weight row whose raw bytes start at shared address `row`.
 template <int QT, int LAYOUT>
@@ -295,11 +310,20 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
     const __half2 zero2 = __float2half2_rn(0.f);
     if constexpr (QT == GGUF_Q8_0) {
         // signed codes: flipping the sign bit gives b = q + 128 in 0..255
-        const uint32_t blk = row + 34u * (uint32_t)(2 * q + hf);   // 2-byte aligned
-        const __half2 d2 = h2_bits(lds16u(blk) * 0x10001u);
-        uint32_t q4[8];
+        uint32_t db, q4[8];
+        switch (2 * q + hf) {
+            case 0: q8_block<0>(row, db, q4); break;
+            case 1: q8_block<1>(row, db, q4); break;
+            case 2: q8_block<2>(row, db, q4); break;
+            case 3: q8_block<3>(row, db, q4); break;
+            case 4: q8_block<4>(row, db, q4); break;
+            case 5: q8_block<5>(row, db, q4); break;
+            case 6: q8_block<6>(row, db, q4); break;
+            default: q8_block<7>(row, db, q4); break;
+        }
+        const __half2 d2 = h2_bits(db * 0x10001u);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q4[i] = lds_w2(blk + 2 + 4 * i) ^ 0x80808080u;
+        for (int i = 0; i < 8; ++i) q4[i] ^= 0x80808080u;
         emit32_h(q4, __float2half2_rn(1152.f), d2, zero2, d2, zero2, out);
     } else {
         // raw Q6_K: values 64q + 32hf + l = 128h + 32g + l with h = q/2, g = 2(q%2) + hf
