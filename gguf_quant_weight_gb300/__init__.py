@@ -38,6 +38,8 @@ _SIGS = {
                               _c_int, _c_vp, _c_sz, _c_int, _c_vp]),
     "gguf_mm_id": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_i64,
                             _c_vp, _c_vp, _c_int, _c_vp, _c_sz, _c_vp]),
+    "gguf_mm_id_slots": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_i64,
+                                  _c_vp, _c_vp, _c_int, _c_vp, _c_sz, _c_vp]),
     "gguf_repack_q6k_planes": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_vp]),
     "gguf_dequant_padded": (_c_int, [_c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp]),
     "gguf_dense_gemm": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_vp,
@@ -131,6 +133,13 @@ def gguf_mm_gemm(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace=
 def gguf_mm_id(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace=None,
                ws_bytes=0, stream=None):
     return _check("gguf_mm_id", load_library().gguf_mm_id(
+        _p(w_experts), qtype, n_expert, N, K, _p(x), xdt, T, _p(ids), top_k, _p(residual), _p(y), ydt,
+        _p(workspace), ws_bytes, _s(stream)))
+
+
+def gguf_mm_id_slots(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace=None,
+                     ws_bytes=0, stream=None):
+    return _check("gguf_mm_id_slots", load_library().gguf_mm_id_slots(
         _p(w_experts), qtype, n_expert, N, K, _p(x), xdt, T, _p(ids), top_k, _p(residual), _p(y), ydt,
         _p(workspace), ws_bytes, _s(stream)))
 

@@ -225,9 +225,9 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K, con
                           (cudaStream_t)stream);
 }
 
-int gguf_mm_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
-               int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt,
-               void* workspace, size_t ws_bytes, gguf_stream_t stream) {
+static int run_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
+                  int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt,
+                  void* workspace, size_t ws_bytes, gguf_stream_t stream, bool per_slot) {
     if (!ids || n_expert <= 0 || top_k <= 0) return GGUF_ERR_INVALID_ARG;
     int st = check_common(w_experts, qtype, GGUF_LAYOUT_BLOCKS, N, K, x, xdt, T, residual, y, ydt);
     if (st != GGUF_OK) return st;
@@ -239,7 +239,21 @@ int gguf_mm_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, in
     DeviceFacts* f = nullptr;
     if ((st = facts(&f)) != GGUF_OK) return st;
     return moe_run(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace,
-                   f->num_sms, f->status, (cudaStream_t)stream);
+                   f->num_sms, f->status, (cudaStream_t)stream, per_slot);
+}
+
+int gguf_mm_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
+               int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt,
+               void* workspace, size_t ws_bytes, gguf_stream_t stream) {
+    return run_id(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace, ws_bytes,
+                  stream, false);
+}
+
+int gguf_mm_id_slots(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x,
+                     int xdt, int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt,
+                     void* workspace, size_t ws_bytes, gguf_stream_t stream) {
+    return run_id(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace, ws_bytes,
+                  stream, true);
 }
 
 int gguf_repack_q6k_planes(const void* src, void* dst, int64_t nblk, int inverse, gguf_stream_t stream) {

@@ -131,15 +131,17 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const int32_t*
     }
 }
 
-// One warp per grouped row: x[token] -> f16, 8 values per lane step.
-__global__ void __launch_bounds__(256) moe_gather_kernel(const void* __restrict__ x, int xdt, int64_t K, int top_k,
+// One warp per grouped row: its activation row -> f16, 8 values per lane
+// step.  The row is x[token] (one row per token, shared by its slots) or, in
+// the per-slot form, x[token * top_k + slot] (row_div = 1).
+__global__ void __launch_bounds__(256) moe_gather_kernel(const void* __restrict__ x, int xdt, int64_t K, int row_div,
                                                          const int* __restrict__ row_count,
                                                          const int* __restrict__ rows, int64_t cap,
                                                          uint16_t* __restrict__ xg) {
     const int lane = threadIdx.x & 31;
     const int64_t p = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (p >= cap || p >= *row_count) return;
-    const int64_t t = rows[p] / top_k;
+    const int64_t t = rows[p] / row_div;
     const uint16_t* src = static_cast<const uint16_t*>(x) + t * K;
     uint16_t* dst = xg + p * K;
     for (int64_t k = 8 * lane; k < K; k += 256) {
@@ -169,7 +171,7 @@ size_t moe_workspace_bytes(int, int64_t n_expert, int64_t N, int64_t K, int64_t 
 
 int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
             int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
-            int num_sms, int* status, cudaStream_t stream) {
+            int num_sms, int* status, cudaStream_t stream, bool per_slot) {
     (void)num_sms;
     if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
     const int64_t entries = T * top_k;
@@ -183,7 +185,7 @@ int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64
     moe_route_kernel<<<1, kRouteThreads, route_smem, stream>>>(ids, (int)entries, (int)n_expert, (int)L.max_tiles,
                                                               L.offsets, L.ntiles, L.tiles, L.rows);
     if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;
-    moe_gather_kernel<<<(unsigned)ceil_div(entries, 8), 256, 0, stream>>>(x, xdt, K, (int)top_k,
+    moe_gather_kernel<<<(unsigned)ceil_div(entries, 8), 256, 0, stream>>>(x, xdt, K, per_slot ? 1 : (int)top_k,
                                                                            L.offsets + n_expert, L.rows, entries,
                                                                            L.xg);
     if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;

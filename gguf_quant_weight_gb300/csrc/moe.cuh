@@ -10,6 +10,6 @@ size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, in
 
 int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
             int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
-            int num_sms, int* status, cudaStream_t stream);
+            int num_sms, int* status, cudaStream_t stream, bool per_slot = false);
 
 }  // namespace gg

@@ -140,6 +140,18 @@ int gguf_mm_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, in
                const void* residual, void* y, int ydt,
                void* workspace, size_t ws_bytes, gguf_stream_t stream);
 
+/* The same expert GEMM with one activation row per (token, slot) -- the
+ * down-projection form of mul_mm_id, where each slot's input is that
+ * expert's own up-projection output (llama.cpp PR #28301, "Overview": every
+ * routed row multiplies its expert's weight):
+ *   Y[t, k, :] = X[t, k, :] . W_{ids[t, k]}^T (+ residual[t, k, :]),
+ *   x [T, top_k, K] of xdt (F16 or BF16); all other arguments, the workspace
+ *   size (gguf_mm_workspace_size(GGUF_OP_ID, ...)) and the errors as gguf_mm_id. */
+int gguf_mm_id_slots(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K,
+                     const void* x, int xdt, int64_t T, const int32_t* ids, int64_t top_k,
+                     const void* residual, void* y, int ydt,
+                     void* workspace, size_t ws_bytes, gguf_stream_t stream);
+
 /* Q6_K plane regrouping (OpenVINO PR #39119, "Transformation"): blocks ->
  * QL[nblk][128] | QH[nblk][64] | SC[nblk][16] | D[nblk][2] (inverse = 0), or
  * back (inverse = 1).  src and dst are 210*nblk bytes each and must not

@@ -378,7 +378,8 @@ def moe_mm_id_exact(w_experts, qtype: int, n_expert: int, N: int, K: int, x: np.
                     ids: np.ndarray, residual: np.ndarray | None = None,
                     token_rows: np.ndarray | None = None) -> np.ndarray:
     """y[t, k, :] = x[t, :] . W_{ids[t, k]}^T (+ residual[t, k, :]), float64.
-    x [T, K] (the same activation row for all of a token's slots); ids [T, top_k].
+    x [T, K] (the same activation row for all of a token's slots) or [T, top_k, K]
+    (one row per slot: y[t, k, :] = x[t, k, :] . W_{ids[t, k]}^T); ids [T, top_k].
     An id outside [0, n_expert) selects no expert: that row stays NaN (reading:
     the pages route every slot to a real expert; the library leaves such rows
     unwritten).  token_rows optionally restricts the evaluation to those tokens
@@ -397,7 +398,7 @@ def moe_mm_id_exact(w_experts, qtype: int, n_expert: int, N: int, K: int, x: np.
                 continue
             if e not in decoded:
                 decoded[e] = dequant(wE[e], qtype, N, K)
-            y[t, k] = decoded[e] @ x64[t]
+            y[t, k] = decoded[e] @ (x64[t, k] if x64.ndim == 3 else x64[t])
     if residual is not None:
         y = y + np.asarray(residual, dtype=np.float64)
     return y

@@ -27,7 +27,8 @@ def lib():
 
 def test_header_lists_the_entry_points():
     names = _declared()
-    for n in ("gguf_mm_gemv", "gguf_mm_gemm", "gguf_mm_id", "gguf_repack_q6k_planes", "gguf_dequant_padded",
+    for n in ("gguf_mm_gemv", "gguf_mm_gemm", "gguf_mm_id", "gguf_mm_id_slots", "gguf_repack_q6k_planes",
+              "gguf_dequant_padded",
               "gguf_dense_gemm", "gguf_mm_check_errors", "gguf_mm_workspace_size"):
         assert n in names
 

@@ -99,3 +99,43 @@ def test_moe_full_width_tiles_give_the_same_output(monkeypatch):
     got_full, _ = _run(syn.Q4_K, E, N, K, T, top_k, ids)
     U.check_close(got_full.reshape(-1, N), ref.reshape(-1, N), "bf16")
     assert np.array_equal(got_full, got)
+
+
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q8_0])
+def test_moe_per_slot_activations(qtype):
+    # down-projection form: every (token, slot) row has its own activations
+    E, N, K, T, top_k = 8, 256, 512, 37, 4
+    rs = syn.rng(91 + qtype)
+    wE = syn.weight_blocks(rs, qtype, E * N, K)
+    x = syn.normal(rs, (T, top_k, K), "bf16")
+    r = syn.normal(rs, (T, top_k, N), "bf16")
+    ids = _distinct_ids(syn.rng(92), T, E, top_k)
+    y = torch.full((T, top_k, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    g.gguf_mm_id_slots(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids), top_k,
+                       U.dev(r, "bf16"), y, g.GGUF_DT_BF16, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert g.gguf_mm_check_errors() == 0
+    ref = O.moe_mm_id_exact(wE, qtype, E, N, K, U.act_f64(x, "bf16"), ids, U.act_f64(r, "bf16"))
+    U.check_close(U.host64(y).reshape(-1, N), ref.reshape(-1, N), "bf16")
+
+
+def test_moe_per_slot_with_repeated_rows_equals_shared_rows():
+    E, N, K, T, top_k = 8, 128, 256, 20, 3
+    rs = syn.rng(93)
+    wE = U.dev(syn.weight_blocks(rs, syn.Q5_K, E * N, K))
+    x = syn.normal(rs, (T, K), "bf16")
+    xs = np.repeat(x[:, None, :], top_k, axis=1)
+    ids = U.dev(_distinct_ids(syn.rng(94), T, E, top_k))
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, syn.Q5_K, N, K, T, E, top_k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    ys = []
+    for fn, xin in ((g.gguf_mm_id, x), (g.gguf_mm_id_slots, xs)):
+        y = torch.empty((T, top_k, N), dtype=torch.bfloat16, device="cuda")
+        fn(wE, syn.Q5_K, E, N, K, U.dev(xin, "bf16"), g.GGUF_DT_BF16, T, ids, top_k, None, y, g.GGUF_DT_BF16, ws,
+           ws_bytes)
+        torch.cuda.synchronize()
+        ys.append(U.host64(y))
+    assert g.gguf_mm_check_errors() == 0
+    assert np.array_equal(ys[0], ys[1])

@@ -312,3 +312,23 @@ def test_moe_out_of_range_ids_select_no_expert():
     ids = np.array([[0], [-1], [E]], np.int32)
     y = O.moe_mm_id_exact(wE, O.Q8_0, E, N, K, x, ids)
     assert np.all(np.isfinite(y[0])) and np.all(np.isnan(y[1])) and np.all(np.isnan(y[2]))
+
+
+def test_moe_per_slot_rows_reduce_to_shared_rows_and_to_dense():
+    # per-slot activations that repeat the token's row give the shared-row
+    # result; each slot's own row multiplies its own expert
+    g = syn.rng(31)
+    E, N, K, T, top_k = 3, 8, 256, 4, 2
+    wE = syn.weight_blocks(g, O.Q4_K, E * N, K)
+    x = syn.normal(g, (T, K), "f32")
+    ids = np.array([[0, 2], [1, 0], [2, 1], [0, 1]], np.int32)
+    shared = O.moe_mm_id_exact(wE, O.Q4_K, E, N, K, x, ids)
+    assert np.array_equal(O.moe_mm_id_exact(wE, O.Q4_K, E, N, K, np.repeat(x[:, None, :], top_k, 1), ids), shared)
+    xs = syn.normal(g, (T, top_k, K), "f32")
+    y = O.moe_mm_id_exact(wE, O.Q4_K, E, N, K, xs, ids)
+    rb = wE.shape[1]
+    for t in range(T):
+        for k in range(top_k):
+            e = ids[t, k]
+            dense = O.matmul_exact(xs[t, k][None, :], O.dequant(wE[e * N:(e + 1) * N].reshape(N, rb), O.Q4_K, N, K))
+            assert np.max(np.abs(y[t, k] - dense[0])) <= 1e-12 * np.max(np.abs(dense))
