@@ -313,9 +313,11 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
                 out[f"q8_0_2048x8192_m{M}_dense_after_decode_once"] = {"us": t2 * 1e6, "tflops": fl / t2 / 1e12,
                                                                          "tc_frac": fl / t2 / 1e12 / tc_peak}
 
-    # MoE: 128 experts top-8, Q4_K 768x2048; ids rotate over 8 Zipf(1.1) draws
+    # MoE: 128 experts top-8, Q4_K 768x2048; ids rotate over 8 Zipf(1.1) draws.
+    # T = 32..512 is the prefill batch; T = 1, 2, 4 the decode form (one int8
+    # GEMV per routed row), timed against the routed path as well
     E, N, K, top_k = 128, 768, 2048, 8
-    ts = [T for T in (32, 64, 256, 512) if want(f"q4_k_moe_128x768x2048_top8_t{T}")]
+    ts = [T for T in (1, 2, 4, 32, 64, 256, 512) if want(f"q4_k_moe_128x768x2048_top8_t{T}")]
     if ts:
         wE = syn.weight_blocks(syn.rng(1004), 12, E * N, K)
         WE, c = copies_of(wE)
@@ -331,23 +333,26 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
         calls = 8 * c
         fl = 2 * top_k * T * N * K
         rec = {}
-        # second arm: every tile's MMAs at the full tile width, as without the
-        # skip of the tile's empty part (the switch is read when a call is made,
-        # so while the graph is captured)
-        for arm in ("skip", "full_width"):
-            if arm == "full_width":
-                os.environ["GGUF_MM_MOE_FULL_TILES"] = "1"
+        # comparison arms (the switches are read when a call is made, so while
+        # the graph is captured): the decode form off (T <= 4), and every
+        # tile's MMAs at the full tile width instead of the tile-skip (T >= 32)
+        arms = [("default", {})]
+        arms.append(("routed_path", {"GGUF_MM_MOE_MV": "0"}) if T * top_k <= 32 else
+                    ("full_width_tiles", {"GGUF_MM_MOE_FULL_TILES": "1"}))
+        for arm, env in arms:
+            os.environ.update(env)
             try:
                 t = time_graph(lambda i: g.gguf_mm_id(WE[i % c], 12, E, N, K, x, g.GGUF_DT_BF16, T, IDS[i % 8], top_k,
                                                       None, y, g.GGUF_DT_BF16, ws, wsb, stream=stream), 3, stream, calls)
             finally:
-                os.environ.pop("GGUF_MM_MOE_FULL_TILES", None)
-            if arm == "skip":
+                for k in env:
+                    os.environ.pop(k, None)
+            if arm == "default":
                 rec.update({"us": t * 1e6, "tflops": fl / t / 1e12, "tc_frac": fl / t / 1e12 / tc_peak,
                             "touched_gbs": touched / t / 1e9, "hbm_frac": touched / t / 1e9 / hbm_peak,
                             "experts_touched": touched / per_expert})
             else:
-                rec["us_full_width_tiles"] = t * 1e6
+                rec["us_" + arm] = t * 1e6
         out[f"q4_k_moe_128x768x2048_top8_t{T}"] = rec
     return out
 

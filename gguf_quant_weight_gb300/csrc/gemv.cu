@@ -1414,6 +1414,120 @@ cudaError_t launch_dispatch(const GemvParams& p, int grid, size_t smem, cudaStre
     return cudaErrorInvalidValue;
 }
 
+// ------------------------------------------------------------------ MoE decode form (mul_mv_id)
+// A few routed rows (decode: one token, top_k experts): each row is its own
+// GEMV against its expert's blocks, so the rows skip routing and grouping and
+// go straight through the int8 path -- the activation row quantized once (the
+// act_quant image), each CTA taking kMvRows weight rows of one routed row's
+// expert, every fragment of those rows requested before any is used.
+constexpr int kMvThreads = 256, kMvRows = 32;
+
+template <int QT>
+__global__ void __launch_bounds__(kMvThreads) moe_mv_kernel(const MoeMvParams mp) {
+    constexpr int bb = QT == GGUF_Q4_K ? 144 : 176;
+    constexpr int NW = kMvThreads / 32;
+    const int p = (int)blockIdx.y;                      // routed row: token * top_k + slot
+    const int e = mp.ids[p];
+    if (e < 0 || e >= mp.n_expert) return;              // no expert: the row is left untouched
+    const int64_t arow = mp.per_slot ? p : p / mp.top_k;   // its activation row in the image
+    const int64_t row0 = (int64_t)blockIdx.x * kMvRows;
+    const int64_t row_end = min(mp.N, row0 + kMvRows);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nb = (int)(mp.K / 32);
+    const uint32_t qa_row = (uint32_t)qa_row_stride(mp.K);
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    {
+        const uint4* sc = reinterpret_cast<const uint4*>(mp.image + arow * qa_row);
+        const uint4* se = reinterpret_cast<const uint4*>(mp.image + mp.rows * (int64_t)qa_row + arow * nb * 16);
+        uint4* dc = reinterpret_cast<uint4*>(smem_raw);
+        uint4* de = reinterpret_cast<uint4*>(smem_raw + qa_row);
+        for (int i = threadIdx.x; i < (int)(qa_row / 16); i += kMvThreads) dc[i] = sc[i];
+        for (int i = threadIdx.x; i < nb; i += kMvThreads) de[i] = se[i];
+    }
+    const int U = (int)(mp.K / 128);                    // units per row
+    const int seg = U < 32 ? U : 32;
+    const int P = U < 32 ? 32 / U : 1;                  // rows per warp pass
+    const int u0 = U < 32 ? lane % U : lane;
+    const int sub_row = U < 32 ? lane / U : 0;
+    const bool lane_on = U >= 32 || lane < P * U;
+    const int groups = (int)ceil_div(row_end - row0, P);
+    const uint8_t* we = mp.w + (int64_t)e * mp.N * mp.rb;
+    auto row_of = [&](int g) { return row0 + (int64_t)g * P + sub_row; };
+    auto fetch = [&](FragQ45<QT>& f, int g, int u) {
+        if (g < groups && lane_on && row_of(g) < row_end)
+            load_global<QT>(f, we + row_of(g) * mp.rb + (int64_t)(u >> 1) * bb, u & 1);
+    };
+    // one unit per lane and row (K <= 4096): this warp's first two row groups
+    // are requested together, before the activation row has landed
+    FragQ45<QT> f0, f1;
+    if (U <= 32) {
+        fetch(f0, warp, u0);
+        fetch(f1, warp + NW, u0);
+    }
+    __syncthreads();
+    Shared sh;
+    sh.qa = smem_u32(smem_raw);
+    sh.qa_row = qa_row;
+    sh.ds = sh.qa + qa_row;
+    sh.stage = 0;
+    GemvParams gp{};
+    gp.M = 1;
+    gp.K = mp.K;
+    gp.N = mp.N;
+    const int seg_end = (lane / seg) * seg + seg;
+    const bool head = lane_on && (lane % seg) == 0;
+    using Act = ActSlice<1, false, 8, 4>;
+    auto compute = [&](const FragQ45<QT>& f, int g, int u, float (&acc)[1][1]) {
+        if (!(g < groups && lane_on && row_of(g) < row_end)) return;
+        Act a;
+        a.init(sh, 128 * u, nb);
+        const FragQ45<QT>* fr[1] = {&f};
+        const int64_t nn[1] = {row_of(g)};
+        const bool on[1] = {true};
+        unit_q45k<QT, 1, 1, Act, false>(gp, fr, a, u >> 1, u & 1, acc, nn, on);
+    };
+    auto finish = [&](float (&acc)[1][1], int g) {
+        if (seg == 32) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[0][0] += __shfl_xor_sync(0xffffffffu, acc[0][0], o);
+        } else {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float t = __shfl_down_sync(0xffffffffu, acc[0][0], o);
+                if (lane + o < seg_end) acc[0][0] += t;
+            }
+        }
+        const int64_t n = row_of(g);
+        if (head && g < groups && n < row_end) {
+            const int64_t o = (int64_t)p * mp.N + n;
+            float v = acc[0][0];
+            if (mp.residual) v += load_act(mp.residual, mp.ydt, o);
+            store_out(mp.y, mp.ydt, o, v);
+        }
+    };
+    if (U <= 32) {
+        for (int g = warp; g < groups; g += 2 * NW) {
+            float acc[1][1] = {{0.f}};
+            compute(f0, g, u0, acc);
+            fetch(f0, g + 2 * NW, u0);
+            finish(acc, g);
+            acc[0][0] = 0.f;
+            compute(f1, g + NW, u0, acc);
+            fetch(f1, g + 3 * NW, u0);
+            finish(acc, g + NW);
+        }
+    } else {
+        for (int g = warp; g < groups; g += NW) {
+            float acc[1][1] = {{0.f}};
+            for (int u = u0; u < U; u += 32) {
+                fetch(f0, g, u);
+                compute(f0, g, u, acc);
+            }
+            finish(acc, g);
+        }
+    }
+}
+
 }  // namespace
 
 int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem) {
@@ -1498,5 +1612,32 @@ cudaError_t gemv_launch(const GemvParams& p, int grid, size_t smem, bool dump, c
 }
 
 size_t gemv_workspace_bytes(int64_t M, int64_t K) { return (size_t)(ceil_div(act_image_bytes(M, K), 256) * 256); }
+
+// ------------------------------------------------------------------ MoE decode form entry
+size_t moe_mv_image_bytes(int64_t rows, int64_t K) { return (size_t)(ceil_div(act_image_bytes(rows, K), 256) * 256); }
+
+cudaError_t moe_mv_launch(const MoeMvParams& mp, const void* x, int xdt, cudaStream_t stream) {
+    // 1. the activation rows quantized once (the decode GEMV's image)
+    GemvParams q{};
+    q.x = x;
+    q.xdt = xdt;
+    q.M = (int)mp.rows;
+    q.K = mp.K;
+    q.act_image = const_cast<uint8_t*>(mp.image);
+    q.status = mp.status;
+    const int quarters = 4 * q.M * (int)(mp.K / 32);
+    act_quant_kernel<<<(unsigned)ceil_div(quarters, 256), 256, 0, stream>>>(q);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // 2. one CTA per (kMvRows weight rows, routed row)
+    const size_t smem = (size_t)(qa_row_stride(mp.K) + (mp.K / 32) * 16);
+    auto k = mp.qtype == GGUF_Q4_K ? moe_mv_kernel<GGUF_Q4_K> : moe_mv_kernel<GGUF_Q5_K>;
+    if (smem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+        return e;
+    dim3 grid((unsigned)ceil_div(mp.N, kMvRows), (unsigned)mp.entries);
+    k<<<grid, kMvThreads, smem, stream>>>(mp);
+    return cudaGetLastError();
+}
 
 }  // namespace gg

@@ -40,4 +40,23 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
 size_t gemv_workspace_bytes(int64_t M, int64_t K);
 cudaError_t gemv_launch(const GemvParams& p, int grid, size_t smem, bool dump, cudaStream_t stream);
 
+// MoE decode form (a few routed rows, Q4_K / Q5_K): every routed row p =
+// token * top_k + slot is a GEMV of its activation row (x[token], or x[p] in the
+// per-slot form) against expert ids[p]'s blocks, on the int8 path.
+struct MoeMvParams {
+    const uint8_t* w;       // expert weights back to back: [E * N, rb]
+    int qtype;
+    int64_t n_expert, N, K, rb;
+    const int32_t* ids;     // [entries]
+    int entries, top_k, per_slot;
+    const uint8_t* image;   // workspace: act_quant image of the `rows` activation rows
+    int64_t rows;           // activation rows (T, or T * top_k in the per-slot form)
+    const void* residual;
+    void* y;
+    int ydt;
+    int* status;
+};
+size_t moe_mv_image_bytes(int64_t rows, int64_t K);
+cudaError_t moe_mv_launch(const MoeMvParams& mp, const void* x, int xdt, cudaStream_t stream);
+
 }  // namespace gg

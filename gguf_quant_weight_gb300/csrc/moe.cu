@@ -18,9 +18,19 @@
 //      MMAs issued for round_up(rows, 16) token columns only.
 // Nothing waits on the host: the counts never leave the device, so the GEMM
 // grid is the upper bound on work items and surplus CTAs exit at once.
+//
+// Decode form (mul_mv_id): with at most kMoeMvRows routed rows (Q4_K / Q5_K)
+// every row is a GEMV of its own, on the int8 path of the decode GEMV
+// (ov39119's path table sends small batches to the GEMV): no routing, no
+// grouping, and one CTA per (32 weight rows, routed row) instead of a tile per
+// expert that decodes 128 rows to f16 for one token column.
+#include <algorithm>
+#include <cstdlib>
+
 #include "common.cuh"
 #include "formats.cuh"
 #include "gemm.cuh"
+#include "gemv.cuh"
 #include "moe.cuh"
 
 namespace gg {
@@ -29,6 +39,14 @@ namespace {
 
 constexpr int kRouteThreads = 1024;
 constexpr int kMoeTile = 128;   // token rows per work item (the GEMM's BN)
+
+// GGUF_MM_MOE_MV=0 in the environment (read at each call) keeps every batch
+// on the routed path, for comparison runs
+bool mv_form(int qtype, int64_t entries) {
+    const char* env = std::getenv("GGUF_MM_MOE_MV");
+    if (env && env[0] == '0') return false;
+    return (qtype == GGUF_Q4_K || qtype == GGUF_Q5_K) && entries <= kMoeMvRows;
+}
 
 struct MoeLayout {
     int* offsets;   // [E + 1]
@@ -164,9 +182,13 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const void* __restrict_
 
 }  // namespace
 
-size_t moe_workspace_bytes(int, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k) {
+size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k) {
     (void)N;
-    return moe_layout(nullptr, n_expert, K, T, top_k).bytes;
+    // enough for either form, so a comparison run may switch between them
+    const size_t routed = moe_layout(nullptr, n_expert, K, T, top_k).bytes;
+    if ((qtype == GGUF_Q4_K || qtype == GGUF_Q5_K) && T * top_k <= kMoeMvRows)
+        return std::max(routed, moe_mv_image_bytes(T * top_k, K));
+    return routed;
 }
 
 int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
@@ -176,6 +198,26 @@ int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64
     if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
     const int64_t entries = T * top_k;
     if (entries > INT32_MAX / 2 || n_expert * N > INT32_MAX) return GGUF_ERR_UNSUPPORTED;
+    if (mv_form(qtype, entries)) {
+        MoeMvParams mp{};
+        mp.w = static_cast<const uint8_t*>(w_experts);
+        mp.qtype = qtype;
+        mp.n_expert = n_expert;
+        mp.N = N;
+        mp.K = K;
+        mp.rb = K / 256 * block_bytes(qtype);
+        mp.ids = ids;
+        mp.entries = (int)entries;
+        mp.top_k = (int)top_k;
+        mp.per_slot = per_slot ? 1 : 0;
+        mp.image = static_cast<const uint8_t*>(workspace);
+        mp.rows = per_slot ? entries : T;
+        mp.residual = residual;
+        mp.y = y;
+        mp.ydt = ydt;
+        mp.status = status;
+        return moe_mv_launch(mp, x, xdt, stream) == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
+    }
     const MoeLayout L = moe_layout(workspace, n_expert, K, T, top_k);
     const size_t route_smem = (size_t)(2 * n_expert + 128) * sizeof(int);
     if (route_smem > 48 * 1024 &&

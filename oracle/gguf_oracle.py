@@ -404,6 +404,29 @@ def moe_mm_id_exact(w_experts, qtype: int, n_expert: int, N: int, K: int, x: np.
     return y
 
 
+def moe_mv_id_int8(w_experts, qtype: int, n_expert: int, N: int, K: int, x32: np.ndarray,
+                   ids: np.ndarray, residual: np.ndarray | None = None) -> np.ndarray:
+    """The expert GEMM's decode form (mul_mv_id): every routed row (t, k) is
+    the int8-path GEMV (gemv_int8_path, OpenVINO PR #39119 "Implementation",
+    GEMV row) of its activation row -- x32[t] ([T, K]) or x32[t, k]
+    ([T, top_k, K]) -- against expert ids[t, k].  Rows without a valid expert
+    stay NaN, as in moe_mm_id_exact."""
+    T, top_k = ids.shape
+    rb = K // BLOCK_VALUES[qtype] * BLOCK_BYTES[qtype]
+    wE = np.asarray(w_experts, dtype=np.uint8).reshape(n_expert, N, rb)
+    x32 = np.asarray(x32, dtype=np.float32)
+    y = np.full((T, top_k, N), np.nan)
+    for t in range(T):
+        for k in range(top_k):
+            e = int(ids[t, k])
+            if not 0 <= e < n_expert:
+                continue
+            row = x32[t, k] if x32.ndim == 3 else x32[t]
+            r = None if residual is None else np.asarray(residual, dtype=np.float64)[t, k][None, :]
+            y[t, k] = gemv_int8_path(wE[e], qtype, N, K, row[None, :], r)[0]
+    return y
+
+
 def moe_routing(ids: np.ndarray, n_expert: int):
     """Routing facts that any valid grouping must reproduce: per-expert row count
     and exclusive prefix offsets; rows of expert e are the (t, k) with ids == e."""

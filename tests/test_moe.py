@@ -30,9 +30,18 @@ def _run(qtype, E, N, K, T, top_k, ids, residual=False, ydt="bf16", seed=0, toke
                  top_k, None if r is None else U.dev(r, ydt), y, U.DT[ydt], ws, ws_bytes)
     torch.cuda.synchronize()
     assert g.gguf_mm_check_errors() == 0
-    ref = O.moe_mm_id_exact(wE, qtype, E, N, K, U.act_f64(x, "bf16"), ids,
-                            None if r is None else U.act_f64(r, ydt), token_rows=token_rows)
+    rr = None if r is None else U.act_f64(r, ydt)
+    if mv_form(qtype, T * top_k):
+        ref = O.moe_mv_id_int8(wE, qtype, E, N, K, U.act_f32(x, "bf16"), ids, rr)
+    else:
+        ref = O.moe_mm_id_exact(wE, qtype, E, N, K, U.act_f64(x, "bf16"), ids, rr, token_rows=token_rows)
     return U.host64(y), ref
+
+
+def mv_form(qtype, entries):
+    # the library's decode form: at most 32 routed rows of Q4_K / Q5_K experts
+    # are computed one int8 GEMV per row (the GEMV's arithmetic)
+    return qtype in (syn.Q4_K, syn.Q5_K) and entries <= 32
 
 
 def _distinct_ids(rs, T, E, top_k):
@@ -117,7 +126,10 @@ def test_moe_per_slot_activations(qtype):
                        U.dev(r, "bf16"), y, g.GGUF_DT_BF16, ws, ws_bytes)
     torch.cuda.synchronize()
     assert g.gguf_mm_check_errors() == 0
-    ref = O.moe_mm_id_exact(wE, qtype, E, N, K, U.act_f64(x, "bf16"), ids, U.act_f64(r, "bf16"))
+    if mv_form(qtype, T * top_k):
+        ref = O.moe_mv_id_int8(wE, qtype, E, N, K, U.act_f32(x, "bf16"), ids, U.act_f64(r, "bf16"))
+    else:
+        ref = O.moe_mm_id_exact(wE, qtype, E, N, K, U.act_f64(x, "bf16"), ids, U.act_f64(r, "bf16"))
     U.check_close(U.host64(y).reshape(-1, N), ref.reshape(-1, N), "bf16")
 
 
@@ -139,3 +151,26 @@ def test_moe_per_slot_with_repeated_rows_equals_shared_rows():
         ys.append(U.host64(y))
     assert g.gguf_mm_check_errors() == 0
     assert np.array_equal(ys[0], ys[1])
+
+
+@pytest.mark.parametrize("T,top_k,per_slot", [(1, 8, False), (2, 8, True), (4, 8, False), (3, 5, True)])
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q5_K])
+def test_moe_decode_form_128_experts_768x2048(qtype, T, top_k, per_slot):
+    # decode: a few routed rows, each its own int8 GEMV (no routing)
+    E, N, K = 128, 768, 2048
+    rs = syn.rng(300 + T * top_k + qtype)
+    wE = syn.weight_blocks(rs, qtype, E * N, K)
+    x = syn.normal(rs, (T, top_k, K) if per_slot else (T, K), "bf16")
+    r = syn.normal(rs, (T, top_k, N), "bf16")
+    ids = syn.zipf_ids(syn.rng(301 + T), T, E, top_k, 1.1)
+    assert mv_form(qtype, T * top_k)
+    y = torch.full((T, top_k, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    fn = g.gguf_mm_id_slots if per_slot else g.gguf_mm_id
+    fn(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids), top_k, U.dev(r, "bf16"), y,
+       g.GGUF_DT_BF16, ws, ws_bytes)
+    torch.cuda.synchronize()
+    assert g.gguf_mm_check_errors() == 0
+    ref = O.moe_mv_id_int8(wE, qtype, E, N, K, U.act_f32(x, "bf16"), ids, U.act_f64(r, "bf16"))
+    U.check_close(U.host64(y).reshape(-1, N), ref.reshape(-1, N), "bf16")

@@ -332,3 +332,25 @@ def test_moe_per_slot_rows_reduce_to_shared_rows_and_to_dense():
             e = ids[t, k]
             dense = O.matmul_exact(xs[t, k][None, :], O.dequant(wE[e * N:(e + 1) * N].reshape(N, rb), O.Q4_K, N, K))
             assert np.max(np.abs(y[t, k] - dense[0])) <= 1e-12 * np.max(np.abs(dense))
+
+
+def test_moe_decode_form_reduces_to_the_int8_gemv():
+    # all slots on one expert with the token's shared row: every slot is that
+    # expert's int8-path GEMV of the row; a per-slot row changes only its slot
+    g = syn.rng(37)
+    E, N, K, T, top_k = 3, 8, 256, 2, 2
+    wE = syn.weight_blocks(g, O.Q5_K, E * N, K)
+    x = syn.normal(g, (T, K), "f32")
+    ids = np.full((T, top_k), 1, np.int32)
+    y = O.moe_mv_id_int8(wE, O.Q5_K, E, N, K, x, ids)
+    w1 = wE[N:2 * N]
+    ref = O.gemv_int8_path(w1, O.Q5_K, N, K, x)
+    for k in range(top_k):
+        assert np.array_equal(y[:, k], ref)
+    xs = np.repeat(x[:, None, :], top_k, 1)
+    xs[1, 1] = syn.normal(g, (K,), "f32")
+    ys = O.moe_mv_id_int8(wE, O.Q5_K, E, N, K, xs, ids)
+    assert np.array_equal(ys[0], y[0]) and np.array_equal(ys[1, 0], y[1, 0])
+    assert np.array_equal(ys[1, 1], O.gemv_int8_path(w1, O.Q5_K, N, K, xs[1, 1][None, :])[0])
+    ids[0, 1] = -1
+    assert np.all(np.isnan(O.moe_mv_id_int8(wE, O.Q5_K, E, N, K, x, ids)[0, 1]))
