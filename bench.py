@@ -314,10 +314,10 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
                                                                          "tc_frac": fl / t2 / 1e12 / tc_peak}
 
     # MoE: 128 experts top-8, Q4_K 768x2048; ids rotate over 8 Zipf(1.1) draws.
-    # T = 32..512 is the prefill batch; T = 1, 2, 4 the decode form (one int8
+    # T = 32..512 is the prefill batch; T = 1, 4, 16 the decode form (one int8
     # GEMV per routed row), timed against the routed path as well
     E, N, K, top_k = 128, 768, 2048, 8
-    ts = [T for T in (1, 2, 4, 32, 64, 256, 512) if want(f"q4_k_moe_128x768x2048_top8_t{T}")]
+    ts = [T for T in (1, 4, 16, 32, 64, 256, 512) if want(f"q4_k_moe_128x768x2048_top8_t{T}")]
     if ts:
         wE = syn.weight_blocks(syn.rng(1004), 12, E * N, K)
         WE, c = copies_of(wE)
@@ -334,10 +334,10 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
         fl = 2 * top_k * T * N * K
         rec = {}
         # comparison arms (the switches are read when a call is made, so while
-        # the graph is captured): the decode form off (T <= 4), and every
+        # the graph is captured): the decode form off (T <= 16), and every
         # tile's MMAs at the full tile width instead of the tile-skip (T >= 32)
         arms = [("default", {})]
-        arms.append(("routed_path", {"GGUF_MM_MOE_MV": "0"}) if T * top_k <= 32 else
+        arms.append(("routed_path", {"GGUF_MM_MOE_MV": "0"}) if T * top_k <= 128 else
                     ("full_width_tiles", {"GGUF_MM_MOE_FULL_TILES": "1"}))
         for arm, env in arms:
             os.environ.update(env)

@@ -19,7 +19,9 @@
 // Nothing waits on the host: the counts never leave the device, so the GEMM
 // grid is the upper bound on work items and surplus CTAs exit at once.
 //
-// Decode form (mul_mv_id): with at most kMoeMvRows routed rows (Q4_K / Q5_K)
+// Decode form (mul_mv_id): with at most kMoeMvRows routed rows (Q4_K / Q5_K;
+// 128: measured against the routed path, 23 vs 33 us at 64 rows, 38 vs 44 at
+// 128, 66 vs 54 at 256, Q4_K 128 x 768 x 2048)
 // every row is a GEMV of its own, on the int8 path of the decode GEMV
 // (ov39119's path table sends small batches to the GEMV): no routing, no
 // grouping, and one CTA per (32 weight rows, routed row) instead of a tile per

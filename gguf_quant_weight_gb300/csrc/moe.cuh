@@ -8,7 +8,7 @@ namespace gg {
 
 // At most this many routed rows (T * top_k) of Q4_K / Q5_K experts take the
 // decode form: one int8 GEMV per row, no routing.
-constexpr int kMoeMvRows = 32;
+constexpr int kMoeMvRows = 128;
 
 size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k);
 

@@ -134,7 +134,7 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K,
  * runs, the environment variable GGUF_MM_MOE_FULL_TILES=1, read at each call,
  * issues every tile's MMAs at the full width instead; the output is the same.)
  * Ids outside [0, n_expert) are skipped (their Y rows are left untouched).
- * Decode form (mul_mv_id): when T * top_k <= 32 and the experts are Q4_K or
+ * Decode form (mul_mv_id): when T * top_k <= 128 and the experts are Q4_K or
  * Q5_K, every routed row is instead one GEMV of the decode path (int8
  * activation codes, integer sub-block dots; the results are those of
  * gguf_mm_gemv on that expert and row), with no routing step.
