@@ -118,6 +118,9 @@ struct FusedParams {
     int ks;
     float* partial;      // [tile][ks][BN][128] f32
     int* tickets;        // [tile], zero at launch
+    // split form's tiles in launch order (1-D grid): the first n_full whole,
+    // then every further tile as ks consecutive K slices
+    int n_full, ntile_n;
 };
 
 // barrier `id` over the first `threads` threads that reach it (whole warps)
@@ -375,10 +378,27 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
     uint64_t* tfull = rempty + C::RS;
     uint32_t* tslot = reinterpret_cast<uint32_t*>(tfull + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t n0 = (int64_t)blockIdx.x * 128;   // first output feature of the tile
-    // this CTA's super-blocks [kb0, kb0 + nkb) of the K slice blockIdx.z
     static_assert(!(MOE && SPLIT), "the grouped form does not split K");
-    const int ks = SPLIT ? fp.ks : 1, z = SPLIT ? (int)blockIdx.z : 0;
+    // tile (row tile bx, token tile by) and K slice z of ks; the split form
+    // walks a 1-D grid: n_full whole tiles, then the rest in ks slices each
+    int bx = (int)blockIdx.x, by = (int)blockIdx.y, z = 0, ks = 1;
+    int64_t split_tile = 0;   // the tile's index among the split ones
+    if constexpr (SPLIT) {
+        const int64_t b = blockIdx.x;
+        int64_t t;
+        if (b < fp.n_full) {
+            t = b;
+        } else {
+            ks = fp.ks;
+            split_tile = (b - fp.n_full) / ks;
+            z = (int)((b - fp.n_full) % ks);
+            t = fp.n_full + split_tile;
+        }
+        bx = (int)(t % fp.ntile_n);
+        by = (int)(t / fp.ntile_n);
+    }
+    const int64_t n0 = (int64_t)bx * 128;   // first output feature of the tile
+    // this CTA's super-blocks [kb0, kb0 + nkb) of the K slice z
     const int kb0 = (int)((int64_t)z * fp.KB / ks);
     const int nkb = (int)((int64_t)(z + 1) * fp.KB / ks) - kb0, nk = 4 * nkb;
     // tile geometry: weight row coordinate, activation row coordinate, valid token columns
@@ -393,7 +413,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
         brow0 = gstart;
         cols = tl.z;
     } else {
-        t0 = (int64_t)blockIdx.y * BN;
+        t0 = (int64_t)by * BN;
         wrow0 = n0;
         brow0 = t0;
         cols = (int)min((int64_t)BN, fp.M - t0);
@@ -546,8 +566,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
         const int64_t n = n0 + 32 * qd + lane;
         const bool ep_ok = __all_sync(0xffffffffu, mbar_wait(tfull, 0, fp.status));
         // split K: this slice's sums go to its slot [BN][128] of the tile
-        const int64_t tile = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
-        float* const slots = SPLIT ? fp.partial + tile * ks * (BN * 128) : nullptr;
+        float* const slots = SPLIT ? fp.partial + split_tile * ks * (BN * 128) : nullptr;
         if (ep_ok) {
             tc_fence_after();
 #pragma unroll 1
@@ -566,7 +585,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
 #pragma unroll
                     for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(u[e]));
                 }
-                if constexpr (SPLIT) {
+                if (SPLIT && ks > 1) {
                     // column-major slot: a warp's 32 rows of a column are one 128-byte line
                     float* dst = slots + (int64_t)z * (BN * 128) + (16 * c) * 128 + 32 * qd + lane;
 #pragma unroll
@@ -586,13 +605,13 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
                 }
             }
         }
-        if constexpr (SPLIT) {
+        if (SPLIT && ks > 1) {   // uniform across the CTA
             // the last slice to finish the tile adds the slots in slice order
             // (a fixed order: the result does not depend on which CTA is last)
             volatile int* ticket = reinterpret_cast<volatile int*>(tslot + 1);
             __threadfence();
             named_bar_sync(1, DW * 32);
-            if (warp == 3 && lane == 0) *ticket = ep_ok ? atomicAdd(&fp.tickets[tile], 1) : -1;
+            if (warp == 3 && lane == 0) *ticket = ep_ok ? atomicAdd(&fp.tickets[split_tile], 1) : -1;
             named_bar_sync(1, DW * 32);
             if (*ticket == ks - 1) {
                 __threadfence();
@@ -642,21 +661,36 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
 // leave most SMs idle (N = 2048: 16 row tiles, 49 -> 28 us at M = 128) and
 // loses at N = 14336 (M = 512: 67 us unsplit, 79 us in halves).  A candidate
 // must beat the best so far by 3 %, so ties keep the smaller tile and split.
+// Two kinds of split: every tile in ks slices (n_full = 0), or only the tiles
+// of the last, partial round (the first n_full whole, the rest in ks slices,
+// which fill the SMs the partial round would leave idle: 224 tiles at M = 512
+// are one round of 152 whole tiles and 72 tiles in halves).
 struct FusedPlan {
     int bn, ks;
+    int64_t n_full;   // tiles kept whole (in launch order) when ks > 1
 };
 FusedPlan plan_fused(int64_t N, int64_t M, int64_t KB, int num_sms) {
-    FusedPlan best{32, 1};
+    FusedPlan best{32, 1, 0};
     double best_cost = 1e300;
     const int64_t steps = 4 * KB;
+    auto consider = [&](double cost, FusedPlan p) {
+        if (cost < best_cost * 0.97) { best_cost = cost; best = p; }
+    };
     for (int bn : {32, 64, 128, 256}) {
+        const double step_cost = (double)(std::min<int64_t>(bn, M) + 1150);
         const int64_t tiles = ceil_div(N, 128) * ceil_div(M, bn);
         for (int ks = 1; ks <= 16; ++ks) {
             if (ks > KB || (ks > 1 && steps / ks < 8)) break;
-            const double per =
-                (double)(ceil_div(steps, ks) + 24 + (ks > 1 ? 8 : 0)) * (double)(std::min<int64_t>(bn, M) + 1150);
-            const double cost = (double)ceil_div(tiles * ks, num_sms) * per;
-            if (cost < best_cost * 0.97) { best_cost = cost; best = {bn, ks}; }
+            const double per = (double)(ceil_div(steps, ks) + 24 + (ks > 1 ? 8 : 0)) * step_cost;
+            consider((double)ceil_div(tiles * ks, num_sms) * per, {bn, ks, 0});
+        }
+        // whole rounds, then the partial round's tiles split to fill the SMs
+        const int64_t rounds = tiles / num_sms, tail = tiles - rounds * num_sms;
+        if (rounds >= 1 && tail > 0) {
+            for (int ks = 2; ks <= 16 && ks <= KB && steps / ks >= 8 && tail * ks <= num_sms; ++ks) {
+                const double cost = ((double)rounds * (steps + 24) + (double)(ceil_div(steps, ks) + 24 + 8)) * step_cost;
+                consider(cost, {bn, ks, rounds * num_sms});
+            }
         }
     }
     return best;
@@ -671,11 +705,11 @@ FusedWorkspace fused_workspace(int64_t N, int64_t K, int64_t M, const FusedPlan&
     w.act = (size_t)(ceil_div(M * K * 2, 256) * 256);
     w.total = w.act;
     if (pl.ks > 1) {
-        const int64_t tiles = ceil_div(N, 128) * ceil_div(M, pl.bn);
+        const int64_t split = ceil_div(N, 128) * ceil_div(M, pl.bn) - pl.n_full;   // tiles in slices
         w.partial = w.total;
-        w.total += (size_t)(ceil_div(tiles * pl.ks * pl.bn * 128 * 4, 256) * 256);
+        w.total += (size_t)(ceil_div(split * pl.ks * pl.bn * 128 * 4, 256) * 256);
         w.tickets = w.total;
-        w.total += (size_t)(ceil_div(tiles * 4, 256) * 256);
+        w.total += (size_t)(ceil_div(split * 4, 256) * 256);
     }
     return w;
 }
@@ -688,8 +722,11 @@ cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const Fused
     auto k = fused_tc_kernel<QT, LAYOUT, BN, MOE, SPLIT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)ceil_div(fp.N, 128), MOE ? (unsigned)grid_y : (unsigned)ceil_div(fp.M, BN),
-              SPLIT ? (unsigned)fp.ks : 1u);
+    dim3 grid((unsigned)ceil_div(fp.N, 128), MOE ? (unsigned)grid_y : (unsigned)ceil_div(fp.M, BN));
+    if (SPLIT) {
+        const int64_t tiles = ceil_div(fp.N, 128) * ceil_div(fp.M, BN);
+        grid = dim3((unsigned)(fp.n_full + (tiles - fp.n_full) * fp.ks));
+    }
     k<<<grid, fused_threads(QT, LAYOUT, BN), smem, s>>>(w[0], w[1], w[2], w[3], b, fp);
     return cudaGetLastError();
 }
@@ -727,7 +764,7 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
     const FusedWorkspace wl = fused_workspace(N, K, M, pl);
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     int* tickets = pl.ks > 1 ? reinterpret_cast<int*>(wsb + wl.tickets) : nullptr;
-    const int ntiles = (int)(ceil_div(N, 128) * ceil_div(M, pl.bn));
+    const int ntiles = (int)(ceil_div(N, 128) * ceil_div(M, pl.bn) - pl.n_full);   // tiles in slices
     if (convert_activations(x, xdt, M, K, workspace, GGUF_DT_F16, num_sms, stream,
                             reinterpret_cast<uint32_t*>(tickets), tickets ? ntiles : 0) != cudaSuccess)
         return GGUF_ERR_CUDA;
@@ -763,7 +800,8 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
                            (uint64_t)K * 2, 64, (uint32_t)bn, CU_TENSOR_MAP_SWIZZLE_128B)) != GGUF_OK)
         return st;
     FusedParams fp{N, M, (int)KB, residual, y, ydt, status, nullptr, nullptr, nullptr, nullptr, 0,
-                   pl.ks, pl.ks > 1 ? reinterpret_cast<float*>(wsb + wl.partial) : nullptr, tickets};
+                   pl.ks, pl.ks > 1 ? reinterpret_cast<float*>(wsb + wl.partial) : nullptr, tickets,
+                   (int)pl.n_full, (int)ceil_div(N, 128)};
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {
         case GGUF_Q8_0: e = launch_bn<GGUF_Q8_0, 0>(bn, tw, tb, fp, stream); break;

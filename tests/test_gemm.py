@@ -135,3 +135,27 @@ def test_fused_split_k_residual_exact_and_deterministic():
     assert np.array_equal(outs[0], outs[1])
     ref = O.matmul_exact(U.act_f64(x, "bf16"), O.dequant(w, qtype, N, K), U.act_f64(r, "bf16"))
     U.check_close(outs[0], ref, "bf16")
+
+
+def test_fused_tail_split_whole_then_halves():
+    # 224 tiles on a 152-SM GB300: the plan keeps one round of 152 tiles whole
+    # and splits the other 72 into K halves; stale workspace bytes must not
+    # matter and two runs agree bit for bit
+    qtype, N, K, M = syn.Q4_K, 14336, 1024, 512
+    rs = syn.rng(4343)
+    w = syn.weight_blocks(rs, qtype, N, K)
+    x = syn.normal(rs, (M, K), "bf16")
+    r = syn.normal(rs, (M, N), "bf16")
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qtype, N, K, M)
+    outs = []
+    for fill in (0x00, 0xFF):
+        ws = torch.full((ws_bytes,), fill, dtype=torch.uint8, device="cuda")
+        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        g.gguf_mm_gemm(U.dev(w), qtype, 0, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, U.dev(r, "bf16"), y,
+                       g.GGUF_DT_BF16, ws, ws_bytes, g.GGUF_PATH_FUSED)
+        torch.cuda.synchronize()
+        assert g.gguf_mm_check_errors() == 0
+        outs.append(U.host64(y))
+    assert np.array_equal(outs[0], outs[1])
+    ref = O.matmul_exact(U.act_f64(x, "bf16"), O.dequant(w, qtype, N, K), U.act_f64(r, "bf16"))
+    U.check_close(outs[0], ref, "bf16")
