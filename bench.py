@@ -168,6 +168,25 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ ranks
+
+def max_over_ranks(values, device):
+    """Each timed duration, maxed over the ranks of the process group (a
+    barrier-bracketed region ends when its slowest rank ends)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_gbs(steps, world_size, seconds):
+    """Whole-job weight GB/s: every rank (an independent replica) streams
+    steps x |MS| weight matrices in the same max-over-ranks time."""
+    return steps * len(MS) * W_BYTES * world_size / seconds / 1e9
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def kernel_source_hash():
@@ -479,14 +498,10 @@ def run_gpu(args):
         raise RuntimeError(f"device status {status}")
 
     # max over ranks; value sums the replicas
-    t = torch.tensor([sec, esec], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    sec, esec = float(t[0]), float(t[1])
+    sec, esec = max_over_ranks([sec, esec], dev)
     steps = args.steps
-    weight_bytes = steps * len(MS) * W_BYTES * ws
-    value = weight_bytes / sec / 1e9
-    e2e = weight_bytes / esec / 1e9
+    value = job_gbs(steps, ws, sec)
+    e2e = job_gbs(steps, ws, esec)
     hbm, tc, tc_sus, peak_kind = peaks()
     algo = sum(W_BYTES + m * K * 2 + 2 * m * N * 2 for m in MS) / len(MS)   # weights + x + residual + y
     calls = steps * len(MS)
