@@ -21,11 +21,14 @@
 //              each k step they turn 128 rows x 64 values of raw bytes into f16
 //              (packed f16 math: w = fl16(d*sc)*q - fl16(dmin*m) in one fused
 //              multiply-add per value pair; the scales of a super-block are
-//              computed once, at its first k step), written straight into the
-//              128-byte-swizzled K-major operand layout the MMA reads; then the
-//              epilogue (TMEM -> registers, + residual, store)
+//              computed once, at its first k step), written into tensor
+//              memory with tcgen05.st, where the MMA reads its A operand; then
+//              the epilogue (TMEM -> registers, + residual, store)
 // The MMA never waits on decode of the same stage it consumes: stages ring
 // through S slots, so decode of step i+1.. overlaps the MMAs of step i.
+// When the tiles would leave SMs idle, K is split across CTAs (all tiles, or
+// only those of the last, partial round); the slices' partial tiles meet in the
+// workspace and the last slice of a tile adds them in slice order.
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>

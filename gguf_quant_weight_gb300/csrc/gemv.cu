@@ -1417,33 +1417,30 @@ cudaError_t launch_dispatch(const GemvParams& p, int grid, size_t smem, cudaStre
 // ------------------------------------------------------------------ MoE decode form (mul_mv_id)
 // A few routed rows (decode: one token, top_k experts): each row is its own
 // GEMV against its expert's blocks, so the rows skip routing and grouping and
-// go straight through the int8 path -- the activation row quantized once (the
-// act_quant image), each CTA taking kMvRows weight rows of one routed row's
-// expert, every fragment of those rows requested before any is used.
-constexpr int kMvThreads = 256, kMvRows = 32;
+// go straight through the int8 path -- each CTA takes kMvRows weight rows of
+// one routed row's expert and requests its first fragments before it needs
+// the activation row.  With at most kMvFuseRows routed rows (QUANT) the CTA
+// quantizes its activation row into shared memory itself while they arrive
+// (one kernel per call); with more, the rows are quantized once by the
+// quantizer kernel and each CTA copies its row's image (the in-CTA quantizer
+// repeated by every CTA of a row costs more than the second kernel: 44 vs 36
+// us at 128 rows; 5.5 vs 6.5 us at 8).
+constexpr int kMvThreads = 256, kMvRows = 32, kMvFuseRows = 8;
 
-template <int QT>
+template <int QT, bool QUANT>
 __global__ void __launch_bounds__(kMvThreads) moe_mv_kernel(const MoeMvParams mp) {
     constexpr int bb = QT == GGUF_Q4_K ? 144 : 176;
     constexpr int NW = kMvThreads / 32;
     const int p = (int)blockIdx.y;                      // routed row: token * top_k + slot
     const int e = mp.ids[p];
     if (e < 0 || e >= mp.n_expert) return;              // no expert: the row is left untouched
-    const int64_t arow = mp.per_slot ? p : p / mp.top_k;   // its activation row in the image
+    const int64_t arow = mp.per_slot ? p : p / mp.top_k;   // its activation row
     const int64_t row0 = (int64_t)blockIdx.x * kMvRows;
     const int64_t row_end = min(mp.N, row0 + kMvRows);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nb = (int)(mp.K / 32);
     const uint32_t qa_row = (uint32_t)qa_row_stride(mp.K);
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    {
-        const uint4* sc = reinterpret_cast<const uint4*>(mp.image + arow * qa_row);
-        const uint4* se = reinterpret_cast<const uint4*>(mp.image + mp.rows * (int64_t)qa_row + arow * nb * 16);
-        uint4* dc = reinterpret_cast<uint4*>(smem_raw);
-        uint4* de = reinterpret_cast<uint4*>(smem_raw + qa_row);
-        for (int i = threadIdx.x; i < (int)(qa_row / 16); i += kMvThreads) dc[i] = sc[i];
-        for (int i = threadIdx.x; i < nb; i += kMvThreads) de[i] = se[i];
-    }
     const int U = (int)(mp.K / 128);                    // units per row
     const int seg = U < 32 ? U : 32;
     const int P = U < 32 ? 32 / U : 1;                  // rows per warp pass
@@ -1457,12 +1454,33 @@ __global__ void __launch_bounds__(kMvThreads) moe_mv_kernel(const MoeMvParams mp
         if (g < groups && lane_on && row_of(g) < row_end)
             load_global<QT>(f, we + row_of(g) * mp.rb + (int64_t)(u >> 1) * bb, u & 1);
     };
+    if constexpr (!QUANT) {
+        // this row's image (codes [qa_row] then entries [nb]) from the workspace
+        const uint4* sc = reinterpret_cast<const uint4*>(mp.image + arow * qa_row);
+        const uint4* se = reinterpret_cast<const uint4*>(mp.image + mp.rows * (int64_t)qa_row + arow * nb * 16);
+        uint4* dc = reinterpret_cast<uint4*>(smem_raw);
+        uint4* de = reinterpret_cast<uint4*>(smem_raw + qa_row);
+        for (int i = threadIdx.x; i < (int)(qa_row / 16); i += kMvThreads) dc[i] = sc[i];
+        for (int i = threadIdx.x; i < nb; i += kMvThreads) de[i] = se[i];
+    }
     // one unit per lane and row (K <= 4096): this warp's first two row groups
     // are requested together, before the activation row has landed
     FragQ45<QT> f0, f1;
     if (U <= 32) {
         fetch(f0, warp, u0);
         fetch(f1, warp + NW, u0);
+    }
+    if constexpr (QUANT) {
+        // the activation row -> codes [qa_row] then entries [nb] in shared memory
+        GemvParams q{};
+        q.x = static_cast<const uint8_t*>(mp.x) + arow * mp.K * (mp.xdt == GGUF_DT_F32 ? 4 : 2);
+        q.xdt = mp.xdt;
+        q.M = 1;
+        q.K = mp.K;
+        const int rounds = (4 * nb + kMvThreads - 1) / kMvThreads;   // quarters per thread
+        if (rounds >= 4) quantize_slice<4>(q, 0, (int)mp.K, smem_raw, threadIdx.x, kMvThreads);
+        else if (rounds >= 2) quantize_slice<2>(q, 0, (int)mp.K, smem_raw, threadIdx.x, kMvThreads);
+        else quantize_slice<1>(q, 0, (int)mp.K, smem_raw, threadIdx.x, kMvThreads);
     }
     __syncthreads();
     Shared sh;
@@ -1616,22 +1634,26 @@ size_t gemv_workspace_bytes(int64_t M, int64_t K) { return (size_t)(ceil_div(act
 // ------------------------------------------------------------------ MoE decode form entry
 size_t moe_mv_image_bytes(int64_t rows, int64_t K) { return (size_t)(ceil_div(act_image_bytes(rows, K), 256) * 256); }
 
-cudaError_t moe_mv_launch(const MoeMvParams& mp, const void* x, int xdt, cudaStream_t stream) {
-    // 1. the activation rows quantized once (the decode GEMV's image)
-    GemvParams q{};
-    q.x = x;
-    q.xdt = xdt;
-    q.M = (int)mp.rows;
-    q.K = mp.K;
-    q.act_image = const_cast<uint8_t*>(mp.image);
-    q.status = mp.status;
-    const int quarters = 4 * q.M * (int)(mp.K / 32);
-    act_quant_kernel<<<(unsigned)ceil_div(quarters, 256), 256, 0, stream>>>(q);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    // 2. one CTA per (kMvRows weight rows, routed row)
+cudaError_t moe_mv_launch(const MoeMvParams& mp, cudaStream_t stream) {
+    cudaError_t e = cudaSuccess;
+    const bool quant = mp.entries <= kMvFuseRows;
+    if (!quant) {
+        // the activation rows quantized once, into the workspace image
+        GemvParams q{};
+        q.x = mp.x;
+        q.xdt = mp.xdt;
+        q.M = (int)mp.rows;
+        q.K = mp.K;
+        q.act_image = const_cast<uint8_t*>(mp.image);
+        q.status = mp.status;
+        const int quarters = 4 * q.M * (int)(mp.K / 32);
+        act_quant_kernel<<<(unsigned)ceil_div(quarters, 256), 256, 0, stream>>>(q);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // one CTA per (kMvRows weight rows, routed row); the activation row's image in shared memory
     const size_t smem = (size_t)(qa_row_stride(mp.K) + (mp.K / 32) * 16);
-    auto k = mp.qtype == GGUF_Q4_K ? moe_mv_kernel<GGUF_Q4_K> : moe_mv_kernel<GGUF_Q5_K>;
+    auto k = mp.qtype == GGUF_Q4_K ? (quant ? moe_mv_kernel<GGUF_Q4_K, true> : moe_mv_kernel<GGUF_Q4_K, false>)
+                                   : (quant ? moe_mv_kernel<GGUF_Q5_K, true> : moe_mv_kernel<GGUF_Q5_K, false>);
     if (smem > 48 * 1024 &&
         (e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;

@@ -49,14 +49,16 @@ struct MoeMvParams {
     int64_t n_expert, N, K, rb;
     const int32_t* ids;     // [entries]
     int entries, top_k, per_slot;
-    const uint8_t* image;   // workspace: act_quant image of the `rows` activation rows
-    int64_t rows;           // activation rows (T, or T * top_k in the per-slot form)
+    const void* x;          // activation rows [T, K] (per-slot form: [T * top_k, K])
+    int xdt;
+    const uint8_t* image;   // workspace for their act_quant image (more than a few routed rows)
+    int64_t rows;           // activation rows: T, or T * top_k in the per-slot form
     const void* residual;
     void* y;
     int ydt;
     int* status;
 };
 size_t moe_mv_image_bytes(int64_t rows, int64_t K);
-cudaError_t moe_mv_launch(const MoeMvParams& mp, const void* x, int xdt, cudaStream_t stream);
+cudaError_t moe_mv_launch(const MoeMvParams& mp, cudaStream_t stream);
 
 }  // namespace gg

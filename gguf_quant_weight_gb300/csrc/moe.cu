@@ -212,13 +212,15 @@ int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64
         mp.entries = (int)entries;
         mp.top_k = (int)top_k;
         mp.per_slot = per_slot ? 1 : 0;
+        mp.x = x;
+        mp.xdt = xdt;
         mp.image = static_cast<const uint8_t*>(workspace);
         mp.rows = per_slot ? entries : T;
         mp.residual = residual;
         mp.y = y;
         mp.ydt = ydt;
         mp.status = status;
-        return moe_mv_launch(mp, x, xdt, stream) == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
+        return moe_mv_launch(mp, stream) == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
     }
     const MoeLayout L = moe_layout(workspace, n_expert, K, T, top_k);
     const size_t route_smem = (size_t)(2 * n_expert + 128) * sizeof(int);
