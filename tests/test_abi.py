@@ -72,3 +72,28 @@ def test_workspace_sizes_are_consistent(lib):
         assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 13, 4096, K, M) >= -(-img // 256) * 256
     assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 13, 4096, 4096, 9) == 0
     assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 13, 4096, 4096, 0) == 0
+
+
+def test_per_slot_moe_rejects_bad_arguments_without_a_gpu(lib):
+    f = g.raw_status
+    assert f("gguf_mm_id_slots", 16, 12, 0, 4, 256, 16, 2, 8, None, 8, None, 16, 2, None, 0, None) == \
+        g.GGUF_ERR_INVALID_ARG
+
+
+def _r256(b):
+    return -(-b // 256) * 256
+
+
+def test_gemm_workspace_follows_the_tile_plan(lib):
+    # (sized for 152 SMs when no device is current) activations in f16, then,
+    # when the plan splits K, one f32 [BN][128] slot per slice of every split
+    # tile and one ticket per split tile
+    act = lambda M, K: _r256(M * K * 2)
+    # 2048 rows (16 row tiles) leave most SMs idle: every tile in 8 K slices at BN = 128
+    assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 8, 2048, 8192, 128) == \
+        act(128, 8192) + _r256(16 * 8 * 128 * 128 * 4) + _r256(16 * 4)
+    # 224 tiles at BN = 256: one round of 152 whole tiles, the other 72 in K halves
+    assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 13, 14336, 4096, 512) == \
+        act(512, 4096) + _r256(72 * 2 * 256 * 128 * 4) + _r256(72 * 4)
+    # 896 tiles: whole rounds only, no split
+    assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 13, 14336, 4096, 2048) == act(2048, 4096)
