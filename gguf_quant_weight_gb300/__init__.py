@@ -50,7 +50,10 @@ _SIGS = {
     "gguf_mm_status_string": (ctypes.c_char_p, [_c_int]),
     "gguf_mm_version": (_c_int, []),
     "gguf_mm_debug_gemv_terms": (_c_int, [_c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp,
-                                          _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp]),
+                                          _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_int,
+                                          ctypes.POINTER(_c_int), _c_vp]),
+    "gguf_mm_gemv_kernel": (_c_int, [_c_int, _c_int, _c_i64, _c_i64, _c_i64, _c_int]),
+    "gguf_mm_debug_moe_route": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp]),
     "gguf_mm_debug_timeout": (_c_int, [_c_i64, _c_vp]),
 }
 
@@ -169,10 +172,27 @@ def gguf_mm_check_errors(stream=None) -> int:
     return load_library().gguf_mm_check_errors(_s(stream))
 
 
-def gguf_mm_debug_gemv_terms(w, qtype, layout, N, K, x, xdt, M, y, ydt, qa=None, d_a=None, s=None, D=None,
-                             stream=None):
-    return _check("gguf_mm_debug_gemv_terms", load_library().gguf_mm_debug_gemv_terms(
-        _p(w), qtype, layout, N, K, _p(x), xdt, M, _p(y), ydt, _p(qa), _p(d_a), _p(s), _p(D), _s(stream)))
+GEMV_KERNELS = {0: "staged", 1: "direct", 2: "tile", 3: "pair", 4: "rowlane"}
+
+
+def gguf_mm_debug_gemv_terms(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, qa=None, d_a=None, s=None,
+                             D=None, workspace=None, ws_bytes=0, kernel=-1, stream=None) -> int:
+    """Runs the GEMV with its integer intermediates dumped; returns the id of the kernel that ran."""
+    out = _c_int(-1)
+    _check("gguf_mm_debug_gemv_terms", load_library().gguf_mm_debug_gemv_terms(
+        _p(w), qtype, layout, N, K, _p(x), xdt, M, _p(residual), _p(y), ydt, _p(qa), _p(d_a), _p(s), _p(D),
+        _p(workspace), ws_bytes, kernel, ctypes.byref(out), _s(stream)))
+    return out.value
+
+
+def gguf_mm_gemv_kernel(qtype, layout, N, K, M, xdt=GGUF_DT_BF16) -> int:
+    """The id of the GEMV kernel gguf_mm_gemv picks for this shape (negative status on error)."""
+    return load_library().gguf_mm_gemv_kernel(qtype, layout, N, K, M, xdt)
+
+
+def gguf_mm_debug_moe_route(ids, entries, n_expert, offsets, ntiles, tiles, max_tiles, rows, stream=None):
+    return _check("gguf_mm_debug_moe_route", load_library().gguf_mm_debug_moe_route(
+        _p(ids), entries, n_expert, _p(offsets), _p(ntiles), _p(tiles), max_tiles, _p(rows), _s(stream)))
 
 
 def gguf_mm_debug_timeout(spin_limit, stream=None):

@@ -90,9 +90,19 @@ int check_common(const void* w, int qtype, int layout, int64_t N, int64_t K, con
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA; }
 
+// GGUF_PATH_AUTO's choice (OpenVINO PR #39119, "Implementation", path table:
+// fewer than 8 rows or f32 activations -> GEMV, otherwise the prefill GEMM).
+int auto_path(int qtype, int layout, int64_t N, int64_t K, int64_t M, int xdt) {
+    (void)qtype; (void)layout; (void)N; (void)K;
+    if (M < 8) return GGUF_PATH_GEMV;
+    if (xdt == GGUF_DT_F32 && M <= 8) return GGUF_PATH_GEMV;
+    return GGUF_PATH_FUSED;
+}
+
 int run_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
              const void* residual, void* y, int ydt, void* workspace, size_t ws_bytes, cudaStream_t stream,
-             int8_t* qa, float* da, int32_t* s, int32_t* D, bool dump) {
+             int8_t* qa, float* da, int32_t* s, int32_t* D, bool dump, int force = -1, int* kind = nullptr,
+             bool launch = true) {
     int st = check_common(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt);
     if (st != GGUF_OK) return st;
     if (M > 8) return GGUF_ERR_UNSUPPORTED;
@@ -119,9 +129,12 @@ int run_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K, const v
     p.dbg_da = da;
     p.dbg_s = s;
     p.dbg_D = D;
+    p.force = force;
     int grid = 0;
     size_t smem = 0;
     if ((st = gemv_plan(p, f->num_sms, f->max_smem_optin, &grid, &smem)) != GGUF_OK) return st;
+    if (kind) *kind = gemv_kind(p);
+    if (!launch) return GGUF_OK;
     return cuda_status(gemv_launch(p, grid, smem, dump, stream));
 }
 
@@ -192,17 +205,22 @@ int gguf_mm_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K, con
 }
 
 int gguf_mm_debug_gemv_terms(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt,
-                             int64_t M, void* y, int ydt, int8_t* qa, float* d_a, int32_t* s, int32_t* D,
+                             int64_t M, const void* residual, void* y, int ydt, int8_t* qa, float* d_a, int32_t* s,
+                             int32_t* D, void* workspace, size_t ws_bytes, int kernel, int* kernel_out,
                              gguf_stream_t stream) {
-    // a debugging aid: it owns a stream-ordered workspace for the one call
-    if (M <= 0 || M > 8 || K <= 0) return GGUF_ERR_UNSUPPORTED;
-    const size_t ws = gemv_workspace_bytes(M, K);
-    void* buf = nullptr;
-    if (cudaMallocAsync(&buf, ws, (cudaStream_t)stream) != cudaSuccess) return GGUF_ERR_CUDA;
-    const int st = run_gemv(w, qtype, layout, N, K, x, xdt, M, nullptr, y, ydt, buf, ws, (cudaStream_t)stream, qa,
-                            d_a, s, D, true);
-    const cudaError_t e = cudaFreeAsync(buf, (cudaStream_t)stream);
-    return st != GGUF_OK ? st : cuda_status(e);
+    return run_gemv(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace, ws_bytes, (cudaStream_t)stream,
+                    qa, d_a, s, D, true, kernel, kernel_out);
+}
+
+int gguf_mm_gemv_kernel(int qtype, int layout, int64_t N, int64_t K, int64_t M, int xdt) {
+    // the plan for dummy (aligned, non-null) pointers: nothing is launched
+    static const uint8_t dummy[16] __attribute__((aligned(16))) = {};
+    const void* d = dummy;
+    int kind = -1;
+    const int st = run_gemv(d, qtype, layout, N, K, d, xdt, M, nullptr, const_cast<void*>(d), GGUF_DT_F32,
+                            const_cast<void*>(d), gemv_workspace_bytes(M > 0 && M <= 8 ? M : 1, K > 0 ? K : 32),
+                            nullptr, nullptr, nullptr, nullptr, nullptr, false, -1, &kind, false);
+    return st == GGUF_OK ? kind : st;
 }
 
 int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
@@ -211,11 +229,13 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K, con
     int st = check_common(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt);
     if (st != GGUF_OK) return st;
     if (path != GGUF_PATH_AUTO && path != GGUF_PATH_GEMV && path != GGUF_PATH_FUSED) return GGUF_ERR_INVALID_ARG;
-    if (path == GGUF_PATH_AUTO) path = (M < 8 || xdt == GGUF_DT_F32) ? GGUF_PATH_GEMV : GGUF_PATH_FUSED;
+    // the pages' path table: fewer than 8 rows, or f32 activations, to the
+    // GEMV; the GEMV takes at most 8 rows, so larger f32 batches go to the
+    // fused path (which converts them to f16 row by row)
+    if (path == GGUF_PATH_AUTO) path = auto_path(qtype, layout, N, K, M, xdt);
     if (path == GGUF_PATH_GEMV)
         return run_gemv(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace, ws_bytes,
                         (cudaStream_t)stream, nullptr, nullptr, nullptr, nullptr, false);
-    if (xdt == GGUF_DT_F32) return GGUF_ERR_UNSUPPORTED;
     DeviceFacts* f = nullptr;
     if ((st = facts(&f)) != GGUF_OK) return st;
     const size_t need = gemm_workspace_bytes(qtype, N, K, M, f->num_sms);
@@ -314,6 +334,19 @@ int gguf_mm_check_errors(gguf_stream_t stream) {
     }
     if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;
     return h;
+}
+
+int gguf_mm_debug_moe_route(const int32_t* ids, int64_t entries, int64_t n_expert, int32_t* offsets,
+                            int32_t* ntiles, int32_t* tiles, int64_t max_tiles, int32_t* rows, gguf_stream_t stream) {
+    if (!ids || !offsets || !ntiles || !tiles || !rows || entries <= 0 || n_expert <= 0) return GGUF_ERR_INVALID_ARG;
+    if (entries > INT32_MAX / 2 || n_expert > 4096) return GGUF_ERR_UNSUPPORTED;
+    if (max_tiles < moe_max_tiles(n_expert, entries)) return GGUF_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(tiles) & 15u) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return GGUF_ERR_MISALIGNED;
+    DeviceFacts* f = nullptr;
+    int st = facts(&f);
+    if (st != GGUF_OK) return st;
+    return moe_route_debug(ids, entries, n_expert, offsets, ntiles, reinterpret_cast<int4*>(tiles), max_tiles, rows,
+                           (cudaStream_t)stream);
 }
 
 int gguf_mm_debug_timeout(int64_t spin_limit, gguf_stream_t stream) {

@@ -46,8 +46,24 @@ __device__ __forceinline__ int q6k_code(const uint8_t* ql, const uint8_t* qh, in
     return lo | (hi << 4);
 }
 
-// Weight value of element e of one block, as f32 (the products are exact in
-// f32; a K-quant's "- dmin*m" is the one rounding step).
+// a - b for exact f32 operands, rounded to odd: toward zero, then the last
+// bit set when the difference was not exact (Knuth's two-sum gives the exact
+// error of the nearest-rounded difference).  A value rounded to odd in f32 and
+// then to nearest in a type with at least two fewer significant bits (f16: 11,
+// bf16: 8 against f32's 24) is the correctly rounded exact difference -- one
+// rounding, not two.
+__device__ __forceinline__ float sub_round_odd(float a, float b) {
+    const float s = __fsub_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(-b, bb));
+    const float t = __fsub_rz(a, b);
+    return (err != 0.f && isfinite(t)) ? __uint_as_float(__float_as_uint(t) | 1u) : t;   // inf, NaN pass as they are
+}
+
+// Weight value of element e of one block as f32.  Every product is exact in
+// f32 (d, dmin: 11 significant bits; sc, m: 6; q: at most 6); a K-quant's
+// "- dmin*m" is rounded to odd (sub_round_odd), so that the one rounding to
+// the output type is the correct rounding of the exact weight.
 template <int QT>
 __device__ __forceinline__ float decode_elem(const uint8_t* blk, int e) {
     if (QT == GGUF_Q8_0) {
@@ -62,7 +78,7 @@ __device__ __forceinline__ float decode_elem(const uint8_t* blk, int e) {
         } else {
             q = kquant_nibble(blk + 48, e) + 16 * ((blk[16 + (e & 31)] >> j) & 1);
         }
-        return (d * (float)kquant_6bit(s, j)) * (float)q - dmin * (float)kquant_6bit(s, j + 8);
+        return sub_round_odd((d * (float)kquant_6bit(s, j)) * (float)q, dmin * (float)kquant_6bit(s, j + 8));
     } else {
         const float d = ld_f16_bytes(blk + 208);
         const int8_t sc = static_cast<int8_t>(blk[192 + (e >> 4)]);

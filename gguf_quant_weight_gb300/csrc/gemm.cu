@@ -29,48 +29,97 @@ namespace gg {
 
 namespace {
 
-__global__ void convert_act_kernel(const void* __restrict__ x, int xdt, int64_t total, uint16_t* __restrict__ out,
-                                   int odt_bf16, uint32_t* __restrict__ zero, int nzero) {
+// One warp per activation row.  For an f16 copy the row is scaled by 2^-s
+// first, with s = floor(log2(max |x|)) - 14, so that its largest magnitude
+// lands in [2^14, 2^15): a bf16 or f32 row whose values exceed f16's range
+// (65504) or sit below its normal range (2^-14) keeps its 8 (bf16) or 11
+// (f32, rounded) significant bits instead of turning into inf or losing bits
+// in f16 subnormals.  The scale 2^s goes to scale[m]; the GEMM's epilogue
+// multiplies row m's sums by it.  A power of two is exact, so rows already in
+// range give the same result bit for bit as an unscaled copy.  (A row holding
+// inf or NaN is left unscaled: those values pass through as they are.)  A
+// bf16 copy keeps f32's range and is never scaled.
+template <int XDT>
+__device__ __forceinline__ void load8(const void* x, int64_t off, float v[8]) {
+    if (XDT == GGUF_DT_F32) {
+        const float4 a = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + off);
+        const float4 b = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + off + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+        const uint4 t = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + off);
+        const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = w4[j] & 0xFFFFu, hi = w4[j] >> 16;
+            if (XDT == GGUF_DT_BF16) { v[2 * j] = __uint_as_float(lo << 16); v[2 * j + 1] = __uint_as_float(hi << 16); }
+            else { v[2 * j] = f16_bits_to_float(lo); v[2 * j + 1] = f16_bits_to_float(hi); }
+        }
+    }
+}
+
+template <int XDT>
+__global__ void __launch_bounds__(256) convert_rows_kernel(const void* __restrict__ x, int64_t M, int64_t K,
+                                                           uint16_t* __restrict__ out, int odt_bf16,
+                                                           float* __restrict__ scale, uint32_t* __restrict__ zero,
+                                                           int nzero) {
     // the GEMM that follows on the stream counts on these words being zero
     if (blockIdx.x == 0)
         for (int j = threadIdx.x; j < nzero; j += blockDim.x) zero[j] = 0u;
-    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < total;
-         i += (int64_t)gridDim.x * blockDim.x * 8) {
-        float v[8];
-        if (i + 8 <= total && xdt != GGUF_DT_F32) {
-            const uint4 t = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + i);
-            const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+    const int lane = threadIdx.x & 31;
+    for (int64_t m = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); m < M; m += (int64_t)gridDim.x * 8) {
+        const int64_t base = m * K;
+        float mul = 1.f, back = 1.f;
+        if (!odt_bf16) {
+            float amax = 0.f;   // largest finite magnitude; a non-finite value marks the row
+            bool finite = true;
+            for (int64_t k = 8 * lane; k < K; k += 256) {
+                float v[8];
+                load8<XDT>(x, base + k, v);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t lo = w4[j] & 0xFFFFu, hi = w4[j] >> 16;
-                if (xdt == GGUF_DT_BF16) { v[2 * j] = __uint_as_float(lo << 16); v[2 * j + 1] = __uint_as_float(hi << 16); }
-                else { v[2 * j] = f16_bits_to_float(lo); v[2 * j + 1] = f16_bits_to_float(hi); }
+                for (int j = 0; j < 8; ++j) {
+                    finite = finite && isfinite(v[j]);
+                    amax = fmaxf(amax, fabsf(v[j]));
+                }
             }
-        } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = i + j < total ? load_act(x, xdt, i + j) : 0.f;
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            finite = __all_sync(0xffffffffu, finite);
+            if (finite && amax > 0.f) {
+                const int s = max(-100, min(100, ilogbf(amax) - 14));
+                mul = ldexpf(1.f, -s);
+                back = ldexpf(1.f, s);
+            }
         }
-        uint16_t o[8];
+        for (int64_t k = 8 * lane; k < K; k += 256) {
+            float v[8];
+            load8<XDT>(x, base + k, v);
+            uint16_t o[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            o[j] = odt_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v[j])) : __half_as_ushort(__float2half_rn(v[j]));
-        if (i + 8 <= total) {
-            *reinterpret_cast<uint4*>(out + i) = make_uint4(o[0] | (uint32_t)o[1] << 16, o[2] | (uint32_t)o[3] << 16,
-                                                            o[4] | (uint32_t)o[5] << 16, o[6] | (uint32_t)o[7] << 16);
-        } else {
-            for (int j = 0; j < 8 && i + j < total; ++j) out[i + j] = o[j];
+            for (int j = 0; j < 8; ++j)
+                o[j] = odt_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v[j]))
+                                : __half_as_ushort(__float2half_rn(v[j] * mul));
+            *reinterpret_cast<uint4*>(out + base + k) =
+                make_uint4(o[0] | (uint32_t)o[1] << 16, o[2] | (uint32_t)o[3] << 16, o[4] | (uint32_t)o[5] << 16,
+                           o[6] | (uint32_t)o[7] << 16);
         }
+        if (lane == 0 && scale) scale[m] = back;
     }
 }
 
 }  // namespace
 
-cudaError_t convert_activations(const void* x, int xdt, int64_t M, int64_t K, void* out, int odt, int num_sms,
-                                cudaStream_t s, uint32_t* zero, int nzero) {
-    const int64_t total = M * K;
-    const int64_t blocks = std::min<int64_t>(ceil_div(total, 8 * 256), (int64_t)num_sms * 8);
-    convert_act_kernel<<<(unsigned)std::max<int64_t>(blocks, 1), 256, 0, s>>>(
-        x, xdt, total, static_cast<uint16_t*>(out), odt == GGUF_DT_BF16 ? 1 : 0, zero, nzero);
+cudaError_t convert_activations(const void* x, int xdt, int64_t M, int64_t K, void* out, int odt, float* scale,
+                                int num_sms, cudaStream_t s, uint32_t* zero, int nzero) {
+    if (K % 8 != 0) return cudaErrorInvalidValue;
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(ceil_div(M, 8), (int64_t)num_sms * 16));
+    const int bf = odt == GGUF_DT_BF16 ? 1 : 0;
+    uint16_t* o = static_cast<uint16_t*>(out);
+    if (xdt == GGUF_DT_F32)
+        convert_rows_kernel<GGUF_DT_F32><<<(unsigned)blocks, 256, 0, s>>>(x, M, K, o, bf, scale, zero, nzero);
+    else if (xdt == GGUF_DT_F16)
+        convert_rows_kernel<GGUF_DT_F16><<<(unsigned)blocks, 256, 0, s>>>(x, M, K, o, bf, scale, zero, nzero);
+    else
+        convert_rows_kernel<GGUF_DT_BF16><<<(unsigned)blocks, 256, 0, s>>>(x, M, K, o, bf, scale, zero, nzero);
     return cudaGetLastError();
 }
 
@@ -202,7 +251,7 @@ int pick_bn(int64_t N, int64_t M, int num_sms) {
 
 size_t dense_workspace_bytes(int64_t N, int64_t K, int64_t M) {
     (void)N;
-    return (size_t)(ceil_div(M * K * 2, 256) * 256);
+    return (size_t)(act_copy_bytes(M, K) + act_scale_bytes(M));   // converted activations, then their row scales
 }
 
 int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
@@ -210,8 +259,11 @@ int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K
                    cudaStream_t stream) {
     if (N > (int64_t)INT32_MAX || M > (int64_t)INT32_MAX) return GGUF_ERR_UNSUPPORTED;
     const void* xb = x;
+    float* xscale = nullptr;
     if (xdt != wdt) {
-        if (convert_activations(x, xdt, M, K, workspace, wdt, num_sms, stream) != cudaSuccess) return GGUF_ERR_CUDA;
+        xscale = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + act_copy_bytes(M, K));
+        if (convert_activations(x, xdt, M, K, workspace, wdt, xscale, num_sms, stream) != cudaSuccess)
+            return GGUF_ERR_CUDA;
         xb = workspace;
     }
     const CUtensorMapDataType dt = wdt == GGUF_DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -223,7 +275,7 @@ int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K
     st = make_tmap_2d(&tb, xb, dt, 2, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, (uint32_t)bn,
                       CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != GGUF_OK) return st;
-    TcEpilogue ep{residual, y, ydt, N, M};
+    TcEpilogue ep{residual, y, ydt, N, M, xscale};
     const int nk = (int)(K / 64), bf = wdt == GGUF_DT_BF16 ? 1 : 0;
     cudaError_t e;
     switch (bn) {

@@ -24,8 +24,9 @@ int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K
 // Grouped (MoE) form of the fused GEMM: work items (expert, token tile) and
 // the grouped activation rows come from the routing kernel (moe.cu).
 int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* xg,
-                     int64_t rows_cap, const int4* tiles, const int* ntiles, const int* offsets, const int* rows,
-                     int64_t max_tiles, const void* residual, void* y, int ydt, int* status, cudaStream_t stream);
+                     const float* xscale, int64_t rows_cap, const int4* tiles, const int* ntiles, const int* offsets,
+                     const int* rows, int64_t max_tiles, const void* residual, void* y, int ydt, int* status,
+                     cudaStream_t stream);
 
 // Launch facts of the current device (SM count, device address of the status
 // word), as the C entry points use them.

@@ -124,6 +124,9 @@ struct FusedParams {
     // split form's tiles in launch order (1-D grid): the first n_full whole,
     // then every further tile as ks consecutive K slices
     int n_full, ntile_n;
+    // power-of-two scale of each activation row's f16 copy (dense: row t0 +
+    // col; grouped: gathered row gstart + col); the epilogue multiplies by it
+    const float* xscale;
 };
 
 // barrier `id` over the first `threads` threads that reach it (whole warps)
@@ -600,7 +603,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
                         if (col < cols) {
                             // output row: token m (dense) or the routed entry (grouped)
                             const int64_t orow = MOE ? (int64_t)fp.rows[gstart + col] : t0 + col;
-                            float o = __uint_as_float(v[j]);
+                            float o = __uint_as_float(v[j]) * fp.xscale[MOE ? gstart + col : t0 + col];
                             if (fp.residual) o += load_act(fp.residual, fp.ydt, orow * fp.N + n);
                             store_out(fp.y, fp.ydt, orow * fp.N + n, o);
                         }
@@ -639,7 +642,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
                         const int col = 16 * c + j;
                         if (col < cols) {
                             const int64_t orow = t0 + col;
-                            float o = acc[j];
+                            float o = acc[j] * fp.xscale[orow];
                             if (fp.residual) o += load_act(fp.residual, fp.ydt, orow * fp.N + n);
                             store_out(fp.y, fp.ydt, orow * fp.N + n, o);
                         }
@@ -701,12 +704,13 @@ FusedPlan plan_fused(int64_t N, int64_t M, int64_t KB, int num_sms) {
 
 // Workspace layout of the fused GEMM: F16 activations | split-K slots | tickets.
 struct FusedWorkspace {
-    size_t act, partial, tickets, total;
+    size_t act, scale, partial, tickets, total;   // act: bytes of the f16 copy; the others are offsets
 };
 FusedWorkspace fused_workspace(int64_t N, int64_t K, int64_t M, const FusedPlan& pl) {
     FusedWorkspace w{};
-    w.act = (size_t)(ceil_div(M * K * 2, 256) * 256);
-    w.total = w.act;
+    w.act = (size_t)act_copy_bytes(M, K);
+    w.scale = w.act;
+    w.total = w.act + (size_t)act_scale_bytes(M);
     if (pl.ks > 1) {
         const int64_t split = ceil_div(N, 128) * ceil_div(M, pl.bn) - pl.n_full;   // tiles in slices
         w.partial = w.total;
@@ -768,7 +772,8 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
     uint8_t* wsb = static_cast<uint8_t*>(workspace);
     int* tickets = pl.ks > 1 ? reinterpret_cast<int*>(wsb + wl.tickets) : nullptr;
     const int ntiles = (int)(ceil_div(N, 128) * ceil_div(M, pl.bn) - pl.n_full);   // tiles in slices
-    if (convert_activations(x, xdt, M, K, workspace, GGUF_DT_F16, num_sms, stream,
+    float* xscale = reinterpret_cast<float*>(wsb + wl.scale);
+    if (convert_activations(x, xdt, M, K, workspace, GGUF_DT_F16, xscale, num_sms, stream,
                             reinterpret_cast<uint32_t*>(tickets), tickets ? ntiles : 0) != cudaSuccess)
         return GGUF_ERR_CUDA;
 
@@ -804,7 +809,7 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
         return st;
     FusedParams fp{N, M, (int)KB, residual, y, ydt, status, nullptr, nullptr, nullptr, nullptr, 0,
                    pl.ks, pl.ks > 1 ? reinterpret_cast<float*>(wsb + wl.partial) : nullptr, tickets,
-                   (int)pl.n_full, (int)ceil_div(N, 128)};
+                   (int)pl.n_full, (int)ceil_div(N, 128), xscale};
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {
         case GGUF_Q8_0: e = launch_bn<GGUF_Q8_0, 0>(bn, tw, tb, fp, stream); break;
@@ -819,8 +824,9 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
 }
 
 int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* xg,
-                     int64_t rows_cap, const int4* tiles, const int* ntiles, const int* offsets, const int* rows,
-                     int64_t max_tiles, const void* residual, void* y, int ydt, int* status, cudaStream_t stream) {
+                     const float* xscale, int64_t rows_cap, const int4* tiles, const int* ntiles, const int* offsets,
+                     const int* rows, int64_t max_tiles, const void* residual, void* y, int ydt, int* status,
+                     cudaStream_t stream) {
     const int64_t KB = K / 256;
     if (qtype == GGUF_Q6_K && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;   // 16-byte row strides for TMA
     if (max_tiles > 65535 || KB > (1 << 20)) return GGUF_ERR_UNSUPPORTED;
@@ -842,7 +848,7 @@ int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t
     // without the tile-skip (a comparison arm for measurement; same output)
     const char* full = std::getenv("GGUF_MM_MOE_FULL_TILES");
     FusedParams fp{N, rows_cap, (int)KB, residual, y, ydt, status, tiles, ntiles, offsets, rows,
-                   (full && full[0] == '1') ? 1 : 0, 1, nullptr, nullptr};
+                   (full && full[0] == '1') ? 1 : 0, 1, nullptr, nullptr, 0, 0, xscale};
     const int gy = (int)max_tiles;
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {

@@ -1352,6 +1352,157 @@ __global__ void __launch_bounds__(kPairWarps * 32, 2) gemv_pair_kernel(const Gem
     }
 }
 
+// ------------------------------------------------------------------ row-lane kernel (M = 1..4)
+// Q4_K / Q5_K blocks, when a CTA's rows of W (at most 64) and the activation
+// image fit in half of an SM's shared memory.  As in the tile kernel, the
+// CTA requests all of its rows with bulk copies at launch (two CTAs share an
+// SM, so the next call's weights stream in under this call's compute) and,
+// after its dependency wait, quantizes the M activation rows itself: one
+// kernel and one wait per call for every M up to 4.
+// The mapping is transposed with respect to the other kernels: a lane owns a
+// weight ROW and a warp owns a set of 128-value units along K (unit u goes to
+// warp u % NW).  All lanes of a warp therefore read the same activation codes
+// and block entries at the same time (warp-uniform shared-memory addresses,
+// served as broadcasts), every row of the CTA is handled in one round instead
+// of one row per warp per round, and the rows' bytes sit at a pitch of an odd
+// number of 16-byte chunks, so the eight lanes of a quarter-warp reading the
+// same field of eight consecutive rows hit eight different bank groups.
+// Each warp leaves one partial sum per (row, activation row) in shared
+// memory; the last phase adds the warps' partials in warp order, then the
+// residual, and stores.
+__host__ __device__ constexpr int rowlane_warps(int mt) { return mt == 1 ? 16 : mt == 2 ? 16 : 8; }
+
+struct RowLaneLayout {
+    int64_t pitch, img, part, res, bar, total;
+};
+__host__ __device__ inline RowLaneLayout rowlane_layout(int64_t M, int64_t K, int64_t rows_per_cta, int64_t rb,
+                                                        int nw) {
+    RowLaneLayout L;
+    L.pitch = ((rb / 16) % 2 == 0) ? rb + 16 : rb;      // odd number of 16-byte chunks per row
+    L.img = ceil_div(rows_per_cta * L.pitch, 128) * 128;
+    L.part = L.img + ceil_div(act_image_bytes(M, K), 16) * 16;
+    const int64_t mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : 8;   // the kernel's row stride of partials
+    L.res = L.part + ceil_div(4 * (int64_t)nw * rows_per_cta * mt, 16) * 16;
+    L.bar = L.res + ceil_div(4 * M * rows_per_cta, 16) * 16;
+    L.total = L.bar + 16;
+    return L;
+}
+
+template <int QT, int MT, int RI, bool DUMP>
+__global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel(const GemvParams p) {
+    constexpr int NW = rowlane_warps(MT), NT = NW * 32;
+    constexpr int bb = QT == GGUF_Q4_K ? 144 : 176;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row0 = (int64_t)blockIdx.x * p.rows_per_cta;
+    const int rows = (int)min(p.rows_per_cta, p.N - row0);   // 1 .. 32 * RI
+    const int rpc = (int)p.rows_per_cta;
+    const int nb = (int)(p.K / 32), U = (int)(p.K / 128);
+    const RowLaneLayout L = rowlane_layout(p.M, p.K, p.rows_per_cta, p.rb, NW);
+    const uint32_t tile = smem_u32(smem_raw);
+    const uint32_t pitch = (uint32_t)L.pitch, rb = (uint32_t)p.rb;
+    uint8_t* img = smem_raw + L.img;
+    float* part = reinterpret_cast<float*>(smem_raw + L.part);   // [NW][rows_per_cta][MT]
+    float* res = reinterpret_cast<float*>(smem_raw + L.res);     // [M][rows_per_cta]
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
+
+    // 1. every row of the CTA requested at once, before the dependency wait
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(bar, (uint32_t)rows * rb);
+        }
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32)
+            bulk_g2s_u32(tile + (uint32_t)r * pitch, p.w + (row0 + r) * p.rb, rb, bar);
+    }
+    pdl_launch_dependents();
+
+    // 2. after the producer of X: the tile's residual values (one load per
+    // thread, issued before the quantizer) and the activation image
+    pdl_wait();
+    const bool has_res = p.residual != nullptr;
+    float res0 = 0.f;
+    if (has_res && tid < p.M * rows) res0 = load_act(p.residual, p.ydt, (int64_t)(tid / rows) * p.N + row0 + tid % rows);
+    {
+        const int rounds = (4 * p.M * nb + NT - 1) / NT;   // quarters per thread
+        if (rounds >= 4) quantize_slice<4>(p, 0, (int)p.K, img, tid, NT);
+        else if (rounds >= 2) quantize_slice<2>(p, 0, (int)p.K, img, tid, NT);
+        else quantize_slice<1>(p, 0, (int)p.K, img, tid, NT);
+    }
+    if (has_res) {
+        if (tid < p.M * rows) res[(tid / rows) * rpc + tid % rows] = res0;
+        for (int i = tid + NT; i < p.M * rows; i += NT)
+            res[(i / rows) * rpc + i % rows] = load_act(p.residual, p.ydt, (int64_t)(i / rows) * p.N + row0 + i % rows);
+    }
+    __syncthreads();   // the image, the residual values and the barrier's initialisation are visible
+    Shared sh;
+    sh.qa_row = (uint32_t)qa_row_stride(p.K);
+    sh.qa = smem_u32(img);
+    sh.ds = sh.qa + (uint32_t)p.M * sh.qa_row;
+    sh.stage = tile;
+    if (DUMP && blockIdx.x == 0) {
+        for (int64_t i = tid; i < (int64_t)p.M * p.K; i += NT) {
+            const uint32_t a = sh.qa + (uint32_t)(i / p.K) * sh.qa_row + qa_pos((uint32_t)(i % p.K));
+            if (p.dbg_qa) p.dbg_qa[i] = (int8_t)(lds32(a & ~3u) >> (8 * (a & 3)));
+        }
+        for (int i = tid; i < p.M * nb; i += NT) {
+            const uint4 e = lds128(sh.ds + 16u * i);
+            if (p.dbg_da) p.dbg_da[i] = __uint_as_float(e.x);
+            if (p.dbg_s) p.dbg_s[i] = (int32_t)(e.z + e.w);
+        }
+    }
+
+    // 3. lane = row (lane, lane + 32, ...), warp = units warp, warp + NW, ...
+    float acc[RI][MT];
+#pragma unroll
+    for (int i = 0; i < RI; ++i)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[i][m] = 0.f;
+    const bool ok = __syncthreads_and(mbar_wait(bar, 0, p.status) ? 1 : 0) != 0;
+    if (ok) {
+        using Act = ActSlice<MT, false, 8, 4>;
+        for (int u = warp; u < U; u += NW) {
+            Act a;
+            a.init(sh, 128 * u, nb);
+            const uint32_t ub = (uint32_t)(u >> 1) * bb;
+#pragma unroll
+            for (int i = 0; i < RI; ++i) {
+                const int r = lane + 32 * i;
+                if (r < rows) {
+                    FragQ45<QT> f;
+                    f.load(tile + (uint32_t)r * pitch + ub, u & 1);
+                    const FragQ45<QT>* fr[1] = {&f};
+                    const int64_t nn[1] = {row0 + r};
+                    const bool on[1] = {true};
+                    float(*a1)[MT] = reinterpret_cast<float(*)[MT]>(&acc[i][0]);
+                    unit_q45k<QT, MT, 1, Act, DUMP>(p, fr, a, u >> 1, u & 1, a1, nn, on);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < RI; ++i) {
+        const int r = lane + 32 * i;
+        if (r < rows) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m) part[(warp * rpc + r) * MT + m] = acc[i][m];
+        }
+    }
+    __syncthreads();
+
+    // 4. the warps' partial sums of each (row, activation row), in warp order, + residual
+    const int nwu = U < NW ? U : NW;   // warps that owned units
+    for (int t = tid; t < p.M * rows; t += NT) {
+        const int m = t / rows, r = t - m * rows;
+        float v = 0.f;
+        for (int w = 0; w < nwu; ++w) v += part[(w * rpc + r) * MT + m];
+        if (has_res) v += res[m * rpc + r];
+        store_out(p.y, p.ydt, (int64_t)m * p.N + row0 + r, v);
+    }
+}
+
 template <int QT, int MT, int LAYOUT, bool DUMP>
 cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
     const int U = (int)(p.K / (QT == GGUF_Q8_0 ? 32 : 128));
@@ -1374,6 +1525,12 @@ cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t 
             if (p.tile == 2) {
                 k = gemv_pair_kernel<QT, MT, DUMP>;
                 threads = kPairWarps * 32;
+            }
+        }
+        if constexpr (MT <= 4) {
+            if (p.tile == 3) {
+                k = p.rows_per_cta <= 32 ? gemv_rowlane_kernel<QT, MT, 1, DUMP> : gemv_rowlane_kernel<QT, MT, 2, DUMP>;
+                threads = rowlane_warps(MT) * 32;
             }
         }
     }
@@ -1566,7 +1723,25 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
     // fit beside a second CTA (the quantizer runs inside it; from two rows on the
     // stand-alone quantizer kernel, whose work is not repeated by every CTA, wins)
     p.tile = 0;
-    if ((p.qtype == GGUF_Q4_K || p.qtype == GGUF_Q5_K) && p.layout == GGUF_LAYOUT_BLOCKS && p.M == 1) {
+    const bool q45 = (p.qtype == GGUF_Q4_K || p.qtype == GGUF_Q5_K) && p.layout == GGUF_LAYOUT_BLOCKS;
+    // up to four rows: the row-lane kernel, when a CTA's rows (at most 64, and
+    // enough of them to occupy most lanes) and the image fit beside a second CTA
+    if (q45 && p.M <= 4 && (p.force < 0 || p.force == GEMV_ROWLANE)) {
+        const int64_t rpc_t = ceil_div(p.N, (int64_t)num_sms);
+        const int mt = p.M <= 1 ? 1 : p.M <= 2 ? 2 : 4;
+        const RowLaneLayout L = rowlane_layout(p.M, p.K, rpc_t, p.rb, rowlane_warps(mt));
+        if (rpc_t <= 64 && (rpc_t >= 16 || p.force == GEMV_ROWLANE) && L.total <= half &&
+            rpc_t * p.rb < (int64_t(1) << 20)) {
+            p.tile = 3;
+            p.direct = 0;
+            p.rows_per_cta = rpc_t;
+            *grid = (int)ceil_div(p.N, rpc_t);
+            *smem = (size_t)L.total;
+            return GGUF_OK;
+        }
+    }
+    if (p.force == GEMV_ROWLANE) return GGUF_ERR_UNSUPPORTED;
+    if (q45 && p.M == 1 && (p.force < 0 || p.force == GEMV_TILE)) {
         const int64_t rpc_t = ceil_div(p.N, (int64_t)num_sms);
         const TileLayout L = tile_layout(p.M, p.K, rpc_t, p.rb);
         if (L.total <= half) {
@@ -1581,8 +1756,9 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
     }
     const int64_t rpc = ceil_div(p.N, (int64_t)num_sms);
     // the pair kernel for 2..4 rows: whole rows staged, codes in registers
-    if ((p.qtype == GGUF_Q4_K || p.qtype == GGUF_Q5_K) && p.layout == GGUF_LAYOUT_BLOCKS && p.M >= 2 && p.M <= 4 &&
-        p.K % 2048 == 0 && kPairWarps % (p.K / 2048) == 0) {
+    if (p.force == GEMV_TILE) return GGUF_ERR_UNSUPPORTED;
+    if (q45 && p.M >= 2 && p.M <= 4 && p.K % 2048 == 0 && kPairWarps % (p.K / 2048) == 0 &&
+        (p.force < 0 || p.force == GEMV_PAIR)) {
         const PairLayout L = pair_layout(p.M, p.K, rpc, p.rb);
         if (L.total <= half) {
             p.tile = 2;
@@ -1593,6 +1769,7 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
             return GGUF_OK;
         }
     }
+    if (p.force == GEMV_PAIR) return GGUF_ERR_UNSUPPORTED;
     const int64_t groups_per_warp = ceil_div(ceil_div(rpc, P), NW);
     int64_t R = std::min<int64_t>({groups_per_warp, 8, (half - act) / (NW * p.stage_bytes)});
     if (R < 1) R = std::min<int64_t>({groups_per_warp, 8, (max_smem - act) / (NW * p.stage_bytes)});
@@ -1600,6 +1777,8 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
     p.stages = (int)R;
     p.direct = (p.qtype == GGUF_Q4_K || p.qtype == GGUF_Q5_K ||
                 (p.qtype == GGUF_Q6_K && p.layout == GGUF_LAYOUT_Q6K_PLANES)) ? 1 : 0;
+    if (p.force == GEMV_STAGED) p.direct = 0;
+    if (p.force == GEMV_DIRECT && !p.direct) return GGUF_ERR_UNSUPPORTED;
     p.rows_per_cta = rpc;
     p.chunk_rows = 0;
     *grid = (int)ceil_div(p.N, rpc);
@@ -1610,8 +1789,13 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
     return GGUF_OK;
 }
 
+int gemv_kind(const GemvParams& p) {
+    return p.tile == 1 ? GEMV_TILE : p.tile == 2 ? GEMV_PAIR : p.tile == 3 ? GEMV_ROWLANE
+                                                                           : p.direct ? GEMV_DIRECT : GEMV_STAGED;
+}
+
 cudaError_t gemv_launch(const GemvParams& p, int grid, size_t smem, bool dump, cudaStream_t stream) {
-    if (p.tile == 1) return dump ? launch_dispatch<true>(p, grid, smem, stream) : launch_dispatch<false>(p, grid, smem, stream);
+    if (p.tile == 1 || p.tile == 3) return dump ? launch_dispatch<true>(p, grid, smem, stream) : launch_dispatch<false>(p, grid, smem, stream);
     // 1. per-32 activation quantizer -> image in the workspace
     const int quarters = 4 * p.M * (int)(p.K / 32);
     cudaLaunchConfig_t cfg = {};

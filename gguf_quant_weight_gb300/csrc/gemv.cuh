@@ -19,7 +19,8 @@ struct GemvParams {
     int pdl;               // launch with programmatic stream serialization
     void* act_image;       // workspace: the quantized activations (codes + per-block entries)
     int direct;            // unit fields 16-byte aligned: load straight into registers
-    int tile;              // rows staged whole in shared memory, two CTAs per SM: 1 tile kernel, 2 pair kernel
+    int tile;              // rows staged whole in shared memory, two CTAs per SM: 1 tile, 2 pair, 3 row-lane kernel
+    int force;             // -1: the plan's choice; else one of the GEMV_* kernels (test hook)
     // plan (filled by gemv_plan)
     int64_t rb;            // bytes per weight row (raw layout)
     int64_t rows_per_cta;  // rows owned by one CTA
@@ -32,6 +33,11 @@ struct GemvParams {
     int32_t* dbg_s;
     int32_t* dbg_D;
 };
+
+// GEMV kernels a plan can choose (ids reported by the test hooks).
+enum { GEMV_STAGED = 0, GEMV_DIRECT = 1, GEMV_TILE = 2, GEMV_PAIR = 3, GEMV_ROWLANE = 4 };
+// The kernel a filled plan launches.
+int gemv_kind(const GemvParams& p);
 
 // Fills the plan fields; returns GGUF_OK or GGUF_ERR_UNSUPPORTED when the
 // activations and one chunk do not fit in max_smem bytes of shared memory.

@@ -55,6 +55,7 @@ struct MoeLayout {
     int* ntiles;    // [1]
     int4* tiles;    // [max_tiles]
     int* rows;      // [T * top_k]
+    float* xscale;  // [T * top_k] power-of-two scale of each gathered f16 row
     uint16_t* xg;   // [T * top_k, K] f16
     int64_t max_tiles;
     size_t bytes;
@@ -72,6 +73,7 @@ MoeLayout moe_layout(void* base, int64_t E, int64_t K, int64_t T, int64_t top_k)
     L.ntiles = reinterpret_cast<int*>(take(4));
     L.tiles = reinterpret_cast<int4*>(take(16 * L.max_tiles));
     L.rows = reinterpret_cast<int*>(take(4 * entries));
+    L.xscale = reinterpret_cast<float*>(take(4 * entries));
     L.xg = reinterpret_cast<uint16_t*>(take(2 * entries * K));
     L.bytes = (size_t)off;
     return L;
@@ -152,37 +154,87 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const int32_t*
 }
 
 // One warp per grouped row: its activation row -> f16, 8 values per lane
-// step.  The row is x[token] (one row per token, shared by its slots) or, in
-// the per-slot form, x[token * top_k + slot] (row_div = 1).
+// step, scaled by 2^-s with s = floor(log2(max |x|)) - 14 so that the row's
+// largest magnitude lands in [2^14, 2^15) (a bf16 row beyond f16's range
+// stays finite; a row below its normal range keeps its bits); 2^s goes to
+// xscale[p] for the GEMM's epilogue.  A power of two is exact; a row holding
+// inf or NaN is left unscaled.  The row is x[token] (one row per token,
+// shared by its slots) or, in the per-slot form, x[token * top_k + slot]
+// (row_div = 1).
+__device__ __forceinline__ void load8_16(const uint16_t* src, int xdt, float v[8]) {
+    const uint4 t = *reinterpret_cast<const uint4*>(src);
+    const uint32_t w4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (xdt == GGUF_DT_F16) {
+            v[2 * j] = f16_bits_to_float(w4[j] & 0xFFFFu);
+            v[2 * j + 1] = f16_bits_to_float(w4[j] >> 16);
+        } else {
+            v[2 * j] = __uint_as_float(w4[j] << 16);
+            v[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(256) moe_gather_kernel(const void* __restrict__ x, int xdt, int64_t K, int row_div,
                                                          const int* __restrict__ row_count,
                                                          const int* __restrict__ rows, int64_t cap,
-                                                         uint16_t* __restrict__ xg) {
+                                                         uint16_t* __restrict__ xg, float* __restrict__ xscale) {
     const int lane = threadIdx.x & 31;
     const int64_t p = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (p >= cap || p >= *row_count) return;
     const int64_t t = rows[p] / row_div;
     const uint16_t* src = static_cast<const uint16_t*>(x) + t * K;
     uint16_t* dst = xg + p * K;
+    float amax = 0.f;
+    bool finite = true;
     for (int64_t k = 8 * lane; k < K; k += 256) {
-        const uint4 v = *reinterpret_cast<const uint4*>(src + k);
-        if (xdt == GGUF_DT_F16) {
-            *reinterpret_cast<uint4*>(dst + k) = v;
-        } else {
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[4];
+        float v[8];
+        load8_16(src + k, xdt, v);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float a = __uint_as_float(w4[j] << 16), b = __uint_as_float(w4[j] & 0xFFFF0000u);
-                const __half2 h = __floats2half2_rn(a, b);
-                o[j] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[0], o[1], o[2], o[3]);
+        for (int j = 0; j < 8; ++j) {
+            finite = finite && isfinite(v[j]);
+            amax = fmaxf(amax, fabsf(v[j]));
         }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    finite = __all_sync(0xffffffffu, finite);
+    float mul = 1.f, back = 1.f;
+    if (finite && amax > 0.f) {
+        const int s = max(-100, min(100, ilogbf(amax) - 14));
+        mul = ldexpf(1.f, -s);
+        back = ldexpf(1.f, s);
+    }
+    for (int64_t k = 8 * lane; k < K; k += 256) {
+        float v[8];
+        load8_16(src + k, xdt, v);
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half2 h = __floats2half2_rn(v[2 * j] * mul, v[2 * j + 1] * mul);
+            o[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (lane == 0) xscale[p] = back;
 }
 
 }  // namespace
+
+int moe_route_debug(const int32_t* ids, int64_t entries, int64_t n_expert, int* offsets, int* ntiles, int4* tiles,
+                    int64_t max_tiles, int* rows, cudaStream_t stream) {
+    const size_t route_smem = (size_t)(2 * n_expert + 128) * sizeof(int);
+    if (route_smem > 48 * 1024 &&
+        cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)route_smem) !=
+            cudaSuccess)
+        return GGUF_ERR_CUDA;
+    moe_route_kernel<<<1, kRouteThreads, route_smem, stream>>>(ids, (int)entries, (int)n_expert, (int)max_tiles,
+                                                              offsets, ntiles, tiles, rows);
+    return cudaGetLastError() == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
+}
+
+int64_t moe_max_tiles(int64_t n_expert, int64_t entries) { return std::min(n_expert, entries) + ceil_div(entries, kMoeTile); }
 
 size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k) {
     (void)N;
@@ -233,10 +285,10 @@ int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64
     if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;
     moe_gather_kernel<<<(unsigned)ceil_div(entries, 8), 256, 0, stream>>>(x, xdt, K, per_slot ? 1 : (int)top_k,
                                                                            L.offsets + n_expert, L.rows, entries,
-                                                                           L.xg);
+                                                                           L.xg, L.xscale);
     if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;
-    return grouped_gemm_run(w_experts, qtype, n_expert, N, K, L.xg, entries, L.tiles, L.ntiles, L.offsets, L.rows,
-                            L.max_tiles, residual, y, ydt, status, stream);
+    return grouped_gemm_run(w_experts, qtype, n_expert, N, K, L.xg, L.xscale, entries, L.tiles, L.ntiles, L.offsets,
+                            L.rows, L.max_tiles, residual, y, ydt, status, stream);
 }
 
 }  // namespace gg

@@ -16,4 +16,12 @@ int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64
             int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
             int num_sms, int* status, cudaStream_t stream, bool per_slot = false);
 
+// The routing step alone (test hook): per-expert group offsets [E + 1], the
+// number of (expert, token tile) work items, the items {expert, first row,
+// rows, 0} (at most max_tiles) and the grouped entry list [entries].
+int moe_route_debug(const int32_t* ids, int64_t entries, int64_t n_expert, int* offsets, int* ntiles, int4* tiles,
+                    int64_t max_tiles, int* rows, cudaStream_t stream);
+// Work items the routing step can produce for this many experts and routed rows.
+int64_t moe_max_tiles(int64_t n_expert, int64_t entries);
+
 }  // namespace gg

@@ -22,6 +22,7 @@ struct TcEpilogue {
     void* y;               // [M][N]
     int ydt;
     int64_t N, M;          // output features, tokens
+    const float* xscale;   // [M] power-of-two scale of each activation row's f16 copy, or null (1)
 };
 
 __device__ __forceinline__ uint8_t* align_up_1024(uint8_t* p) {
@@ -45,6 +46,7 @@ __device__ __forceinline__ void tc_epilogue(const TcEpilogue& ep, uint32_t tmem,
                 const int64_t m = t0 + 16 * c + j;
                 if (m < ep.M) {
                     float o = __uint_as_float(v[j]);
+                    if (ep.xscale) o *= ep.xscale[m];
                     if (ep.residual) o += load_act(ep.residual, ep.ydt, m * ep.N + n);
                     store_out(ep.y, ep.ydt, m * ep.N + n, o);
                 }
@@ -56,10 +58,15 @@ __device__ __forceinline__ void tc_epilogue(const TcEpilogue& ep, uint32_t tmem,
 int make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, uint64_t inner,
                  uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
                  CUtensorMapSwizzle swz);
-// X (F32/F16/BF16) -> odt (F16/BF16) into out; also zeroes nzero 32-bit words
-// at `zero` (the split-K tickets of the GEMM that follows).
-cudaError_t convert_activations(const void* x, int xdt, int64_t M, int64_t K, void* out, int odt, int num_sms,
-                                cudaStream_t s, uint32_t* zero = nullptr, int nzero = 0);
+// X [M, K] (F32/F16/BF16) -> odt (F16/BF16) into out, row by row; an F16 copy
+// of row m holds x * 2^-s_m (scale[m] = 2^s_m, see the kernel), a BF16 copy x
+// itself (scale[m] = 1).  scale may be null.  Also zeroes nzero 32-bit words at
+// `zero` (the split-K tickets of the GEMM that follows).  K % 8 == 0.
+cudaError_t convert_activations(const void* x, int xdt, int64_t M, int64_t K, void* out, int odt, float* scale,
+                                int num_sms, cudaStream_t s, uint32_t* zero = nullptr, int nzero = 0);
+// Bytes of the activation copy that precedes the row scales in a workspace.
+__host__ __device__ inline int64_t act_copy_bytes(int64_t M, int64_t K) { return (M * K * 2 + 255) / 256 * 256; }
+__host__ __device__ inline int64_t act_scale_bytes(int64_t M) { return (M * 4 + 255) / 256 * 256; }
 int pick_bn(int64_t N, int64_t M, int num_sms);
 
 }  // namespace gg

@@ -209,18 +209,46 @@ const char* gguf_mm_status_string(int status);
 /* Library ABI version (major*100 + minor). */
 int gguf_mm_version(void);
 
-/* Test hook: runs the GEMV kernel of gguf_mm_gemv in a build that also writes
- * its integer intermediates, so they can be compared bit for bit with a CPU
- * restatement: qa [M, K] i8, d_a [M, K/32] f32 and s [M, K/32] i32 from the
- * activation quantizer (taken from the first CTA), and the integer sub-block
- * dots D [M, N, K/sub] i32, sub = 16 for Q6_K and 32 otherwise.  Q6_K dots are
- * of (q6 - 32), Q4_K/Q5_K of the unsigned quant, Q8_0 of the signed quant.
- * Any debug pointer may be NULL.  Also writes y like gguf_mm_gemv.  It takes
- * no workspace: it allocates one stream-ordered for the call (cudaMallocAsync). */
+/* Test hook: runs gguf_mm_gemv (same arguments and workspace rules) with a
+ * build of its GEMV kernel that also writes the integer intermediates, so they
+ * can be compared bit for bit with a CPU restatement: qa [M, K] i8, d_a
+ * [M, K/32] f32 and s [M, K/32] i32 from the activation quantizer (taken from
+ * the first CTA), and the integer sub-block dots D [M, N, K/sub] i32, sub = 16
+ * for Q6_K and 32 otherwise.  Q6_K dots are of (q6 - 32), Q4_K/Q5_K of the
+ * unsigned quant, Q8_0 of the signed quant.  Any debug pointer may be NULL.
+ *   kernel      -1: the kernel gguf_mm_gemv would choose; else one of the
+ *               GEMV kernel ids below, forced (UNSUPPORTED if it cannot run
+ *               this shape)
+ *   kernel_out  host int* or NULL: receives the id of the kernel that ran
+ * Kernel ids: 0 staged rows (per-warp ring of row slots), 1 direct register
+ * loads, 2 tile (M = 1, whole rows in shared memory, quantizer inside), 3 pair
+ * (M = 2..4, activation codes in registers), 4 row-lane (M = 1..4, a lane per
+ * weight row, quantizer inside).  Allocates nothing. */
 int gguf_mm_debug_gemv_terms(const void* w, int qtype, int layout, int64_t N, int64_t K,
-                             const void* x, int xdt, int64_t M, void* y, int ydt,
+                             const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
                              int8_t* qa, float* d_a, int32_t* s, int32_t* D,
+                             void* workspace, size_t ws_bytes, int kernel, int* kernel_out,
                              gguf_stream_t stream);
+
+/* The GEMV kernel id (as above) that gguf_mm_gemv chooses for this shape on the
+ * current device, or a negative status.  Launches nothing. */
+int gguf_mm_gemv_kernel(int qtype, int layout, int64_t N, int64_t K, int64_t M, int xdt);
+
+/* Test hook: the MoE routing step of gguf_mm_id alone, writing its tables
+ * into caller buffers (device memory) so that they can be compared with a CPU
+ * restatement: for ids [entries] int32 (entries = T * top_k; ids outside
+ * [0, n_expert) are skipped),
+ *   offsets [n_expert + 1]  start of each expert's group of rows; offsets[E]
+ *                           = number of routed rows (integer, exact)
+ *   ntiles  [1]             number of (expert, token tile of <= 128 rows) items
+ *   tiles   [max_tiles][4]  the items {expert, first row in the group, rows, 0}
+ *   rows    [entries]       the routed entries (token * top_k + slot), grouped
+ *                           by expert; the order inside a group is unspecified
+ * max_tiles must be at least min(n_expert, entries) + ceil(entries / 128)
+ * (else WORKSPACE); tiles must be 16-byte aligned. */
+int gguf_mm_debug_moe_route(const int32_t* ids, int64_t entries, int64_t n_expert, int32_t* offsets,
+                            int32_t* ntiles, int32_t* tiles, int64_t max_tiles, int32_t* rows,
+                            gguf_stream_t stream);
 
 /* Test hook for the bounded device waits: launches a kernel whose wait on an
  * mbarrier that nothing completes gives up after about `spin_limit` polls and

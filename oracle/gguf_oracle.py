@@ -75,7 +75,7 @@ def round_f64_to_bf16_bits(v: np.ndarray) -> np.ndarray:
     ties to even.  Values beyond the bf16 range are not expected here.
     """
     v = np.asarray(v, dtype=np.float64)
-    out = np.zeros(v.shape, dtype=np.float64)
+    out = np.array(v * 0.0)                       # zeros that keep v's sign (IEEE: rounding -0 gives -0)
     nz = v != 0
     _, ex = np.frexp(v[nz])                       # |v| = m * 2**ex, 0.5 <= m < 1
     e = np.maximum(ex - 1, -126)                  # bf16 subnormal spacing 2**-133
@@ -429,7 +429,10 @@ def moe_mv_id_int8(w_experts, qtype: int, n_expert: int, N: int, K: int, x32: np
 
 def moe_routing(ids: np.ndarray, n_expert: int):
     """Routing facts that any valid grouping must reproduce: per-expert row count
-    and exclusive prefix offsets; rows of expert e are the (t, k) with ids == e."""
-    counts = np.bincount(np.asarray(ids).ravel(), minlength=n_expert).astype(np.int64)
+    and exclusive prefix offsets; rows of expert e are the (t, k) with ids == e.
+    Ids outside [0, n_expert) select no expert and are not counted."""
+    flat = np.asarray(ids).ravel()
+    valid = flat[(flat >= 0) & (flat < n_expert)]
+    counts = np.bincount(valid, minlength=n_expert).astype(np.int64)
     offsets = np.concatenate([[0], np.cumsum(counts)[:-1]])
     return counts, offsets

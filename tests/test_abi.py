@@ -85,10 +85,10 @@ def _r256(b):
 
 
 def test_gemm_workspace_follows_the_tile_plan(lib):
-    # (sized for 152 SMs when no device is current) activations in f16, then,
-    # when the plan splits K, one f32 [BN][128] slot per slice of every split
-    # tile and one ticket per split tile
-    act = lambda M, K: _r256(M * K * 2)
+    # (sized for 152 SMs when no device is current) activations in f16 and
+    # their per-row f32 scales, then, when the plan splits K, one f32 [BN][128]
+    # slot per slice of every split tile and one ticket per split tile
+    act = lambda M, K: _r256(M * K * 2) + _r256(M * 4)
     # 2048 rows (16 row tiles) leave most SMs idle: every tile in 8 K slices at BN = 128
     assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 8, 2048, 8192, 128) == \
         act(128, 8192) + _r256(16 * 8 * 128 * 128 * 4) + _r256(16 * 4)

@@ -17,61 +17,99 @@ def _gpu():
     U.require_gpu()
 
 
-def _dense(qtype, N, K, M, wdt="f16", ydt="bf16", residual=True, seed=0):
+def _dense(qtype, N, K, M, wdt="f16", ydt="bf16", residual=True, seed=0, rows=None):
+    """Decode once to wdt, then the dense GEMM; returns (got, exact oracle, oracle
+    on the weights rounded to wdt) for the sampled activation rows."""
     rs = syn.rng(seed + N + 3 * K + 7 * M + qtype)
     w = syn.weight_blocks(rs, qtype, N, K)
     x = syn.normal(rs, (M, K), "bf16")
     r = syn.normal(rs, (M, N), ydt) if residual else None
     ld = K + 64
-    wd = torch.empty((N, ld), dtype=U.TORCH_DT[wdt], device="cuda")
-    g.gguf_dequant_padded(U.dev(w), qtype, 0, N, K, wd, U.DT[wdt], ld)
-    y = torch.empty((M, N), dtype=U.TORCH_DT[ydt], device="cuda")
+    wd = U.guarded((N, ld), U.TORCH_DT[wdt])
+    g.gguf_dequant_padded(U.dev(w), qtype, 0, N, K, wd.t, U.DT[wdt], ld)
+    y = U.guarded((M, N), U.TORCH_DT[ydt])
     ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_DENSE, 0, N, K, M)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    g.gguf_dense_gemm(wd, U.DT[wdt], ld, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M,
-                      None if r is None else U.dev(r, ydt), y, U.DT[ydt], ws, ws_bytes)
+    ws = U.workspace(ws_bytes, 0xEE)
+    g.gguf_dense_gemm(wd.t, U.DT[wdt], ld, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M,
+                      None if r is None else U.dev(r, ydt), y.t, U.DT[ydt], ws.t, ws_bytes)
     torch.cuda.synchronize()
-    ref = O.matmul_exact(U.act_f64(x, "bf16"), O.dequant(w, qtype, N, K), None if r is None else U.act_f64(r, ydt))
-    return U.host64(y), ref
+    for b, nm in ((wd, "decoded"), (y, "y"), (ws, "workspace")):
+        b.check(nm)
+    assert g.gguf_mm_check_errors() == 0
+    sel = slice(None) if rows is None else rows
+    xs = U.act_f64(x[sel], "bf16")
+    rr = None if r is None else U.act_f64(r[sel], ydt)
+    w64 = O.dequant(w, qtype, N, K)
+    ref = O.matmul_exact(xs, w64, rr)
+    bits = O.dequant_padded_bits(w, qtype, N, K, K, wdt)
+    wr = bits.view(np.float16).astype(np.float64) if wdt == "f16" else O.bf16_bits_to_f64(bits)
+    ref_rounded = O.matmul_exact(xs, wr, rr)
+    return U.host64(y.t)[sel], ref, ref_rounded
 
 
 @pytest.mark.parametrize("N,K,M", [(128, 256, 16), (200, 512, 33), (256, 1024, 300), (130, 768, 1),
                                    (384, 512, 257), (1000, 256, 64)])
 @pytest.mark.parametrize("qtype", [syn.Q8_0, syn.Q4_K])
 def test_dense_gemm_f16(qtype, N, K, M):
-    got, ref = _dense(qtype, N, K, M)
+    got, ref, _ = _dense(qtype, N, K, M)
     U.check_close(got, ref, "bf16")
 
 
 @pytest.mark.parametrize("ydt", ["f32", "f16"])
 def test_dense_gemm_out_dtypes(ydt):
-    got, ref = _dense(syn.Q5_K, 256, 512, 48, ydt=ydt)
+    got, ref, _ = _dense(syn.Q5_K, 256, 512, 48, ydt=ydt)
     U.check_close(got, ref, ydt, rel=2e-3)
 
 
-def test_dense_gemm_bf16_weights_reported():
-    # bf16 decoded weights carry 8 significant bits: the error is reported and
-    # gated at twice the f16 bound (the bf16 arm of the decode-once comparison)
-    got, ref = _dense(syn.Q8_0, 512, 2048, 128, wdt="bf16")
-    rel = U.check_close(got, ref, "bf16", rel=4e-3)
-    print(f"bf16 decode-once error: {rel:.2e} of max|ref|")
+@pytest.mark.parametrize("qtype", [syn.Q8_0, syn.Q4_K])
+def test_dense_gemm_bf16_weights(qtype):
+    # the bf16 arm of the decode-once comparison.  Gated: against the product
+    # with the weights rounded to bf16 (what this arm computes), at 2e-3.
+    # Reported: its gap to the exact product, with the verdict against 2e-3
+    # (bf16 keeps 8 significant bits of each weight, f16 keeps 11).
+    got, ref, ref_b = _dense(qtype, 512, 2048, 128, wdt="bf16", ydt="f32")
+    U.check_close(got, ref_b, "f32", rel=2e-3)
+    gap = float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
+    print(f"bf16 decode-once arm, q{qtype}: error vs the exact product {gap:.2e} of max|ref| -> "
+          f"{'within' if gap <= 2e-3 else 'OUTSIDE'} the 2e-3 bound")
 
 
-def test_dense_gemm_config_q8_0_2048x8192_m512():
-    N, K, M = 2048, 8192, 512
-    rs = syn.rng(1003)
-    w = syn.weight_blocks(rs, syn.Q8_0, N, K)
-    x = syn.normal(rs, (M, K), "bf16")
+@pytest.mark.parametrize("M", [128, 512, 4096])
+@pytest.mark.parametrize("wdt", ["f16", "bf16"])
+def test_dense_gemm_config_q8_0_2048x8192(M, wdt):
+    # the decode-once arm at the Q8_0 2048 x 8192 prefill workload's row counts
+    rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 7)), [M - 1]]))
+    got, ref, ref_b = _dense(syn.Q8_0, 2048, 8192, M, wdt=wdt, residual=False, seed=1003, rows=rows)
+    U.check_close(got, ref if wdt == "f16" else ref_b, "bf16")
+    if wdt == "bf16":
+        gap = float(np.max(np.abs(got - ref)) / np.max(np.abs(ref)))
+        print(f"bf16 decode-once arm, 2048x8192 M={M}: error vs the exact product {gap:.2e} -> "
+              f"{'within' if gap <= 2e-3 else 'OUTSIDE'} the 2e-3 bound")
+
+
+def test_dense_gemm_activation_rows_beyond_f16_range():
+    # bf16 activations against an f16 decoded buffer: converted row by row with
+    # a power-of-two scale, as on the fused path; each row checked on its own
+    N, K, M = 256, 1024, 20
+    rs = syn.rng(88)
+    w = syn.weight_blocks(rs, syn.Q5_K, N, K)
+    x32 = rs.standard_normal((M, K)).astype(np.float32)
+    x32[0] *= 3e5
+    x32[1] *= 1e20
+    x32[2] *= 1e-7
+    x = syn.f32_to_bf16_bits(x32)
     ld = K + 64
     wd = torch.empty((N, ld), dtype=torch.float16, device="cuda")
-    g.gguf_dequant_padded(U.dev(w), syn.Q8_0, 0, N, K, wd, g.GGUF_DT_F16, ld)
-    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    g.gguf_dequant_padded(U.dev(w), syn.Q5_K, 0, N, K, wd, g.GGUF_DT_F16, ld)
+    y = U.guarded((M, N), torch.float32)
     ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_DENSE, 0, N, K, M)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-    g.gguf_dense_gemm(wd, g.GGUF_DT_F16, ld, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, None, y, g.GGUF_DT_BF16,
-                      ws, ws_bytes)
+    ws = U.workspace(ws_bytes)
+    g.gguf_dense_gemm(wd, g.GGUF_DT_F16, ld, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, None, y.t, g.GGUF_DT_F32,
+                      ws.t, ws_bytes)
     torch.cuda.synchronize()
-    rows = np.arange(0, M, 61)
-    ref = O.matmul_exact(U.act_f64(x[rows], "bf16"), O.dequant(w, syn.Q8_0, N, K))
-    U.check_close(U.host64(y)[rows], ref, "bf16")
-    assert g.gguf_mm_check_errors() == 0
+    y.check("y")
+    ws.check("workspace")
+    got = U.host64(y.t)
+    ref = O.matmul_exact(U.act_f64(x, "bf16"), O.dequant(w, syn.Q5_K, N, K))
+    for m in range(M):
+        U.check_close(got[m], ref[m], "f32", rel=2e-3, what=f"row {m}")

@@ -1,7 +1,8 @@
-"""Decode-once K-padded buffer: every value is the exact decoded weight rounded
-to f16/bf16 (one of its two neighbours in the output type: the kernel computes
-the K-quant value in f32 first), pad columns are zero, and padding changes only
-the stride."""
+"""Decode-once K-padded buffer: every value is the exact decoded weight
+correctly rounded to f16/bf16 (bit for bit against the oracle's RN(w)), pad
+columns are zero, and padding changes only the stride (ROCm llama.cpp PR #37
+"one-time K-padded f16 dequantization for prefill GEMMs", "How it works" and
+"Correctness")."""
 import numpy as np
 import pytest
 import torch
@@ -19,20 +20,12 @@ def _gpu():
     U.require_gpu()
 
 
-def _bits_to_f64(bits, odt):
-    if odt == "f16":
-        return bits.view(np.float16).astype(np.float64)
-    return O.bf16_bits_to_f64(bits)
-
-
-def _faithful(got_bits, w64, odt):
-    """got is RN(w) exactly, or one of the two output-type neighbours of w."""
-    got = _bits_to_f64(got_bits, odt)
-    rn = _bits_to_f64(O.round_f64_to_f16_bits(w64) if odt == "f16" else O.round_f64_to_bf16_bits(w64), odt)
-    exact_match = np.mean(got == rn)
-    ulp = 2 * U.half_ulp(w64, odt)
-    assert np.all(np.abs(got - w64) <= ulp * (1 + 1e-9) + 2.0 ** -24), "not faithfully rounded"
-    return exact_match
+def _decode(w, qtype, N, K, ld, odt, layout=0):
+    out = U.guarded((N, ld), torch.int16, fill=0x7777)
+    g.gguf_dequant_padded(U.dev(w), qtype, layout, N, K, out.t, U.DT[odt], ld)
+    torch.cuda.synchronize()
+    out.check("decoded buffer")
+    return out.t.cpu().numpy().view(np.uint16)
 
 
 @pytest.mark.parametrize("qtype", [syn.Q8_0, syn.Q4_K, syn.Q5_K, syn.Q6_K])
@@ -42,15 +35,24 @@ def test_dequant_padded(qtype, odt, N, K, pad):
     rs = syn.rng(qtype * 100 + N + K)
     w = syn.weight_blocks(rs, qtype, N, K)
     ld = K + pad
-    out = torch.full((N, ld), 0x7777, dtype=torch.int16, device="cuda")
-    g.gguf_dequant_padded(U.dev(w), qtype, 0, N, K, out, U.DT[odt], ld)
-    torch.cuda.synchronize()
-    bits = out.cpu().numpy().view(np.uint16)
-    assert np.all(bits[:, K:] == 0)
-    match = _faithful(bits[:, :K], O.dequant(w, qtype, N, K), odt)
-    assert match > 0.999
-    if qtype in (syn.Q8_0, syn.Q6_K):   # products exact in f32: correctly rounded
-        assert match == 1.0
+    bits = _decode(w, qtype, N, K, ld, odt)
+    assert np.array_equal(bits, O.dequant_padded_bits(w, qtype, N, K, ld, odt))   # pad columns included
+
+
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q5_K])
+@pytest.mark.parametrize("odt", ["f16", "bf16"])
+def test_dequant_kquant_min_rounded_once(qtype, odt):
+    # d*sc*q and dmin*m close to each other, so that their difference needs
+    # more bits than the output type holds: one rounding of the exact weight,
+    # never the f32 difference rounded again
+    N, K = 64, 512
+    rs = syn.rng(31 + qtype)
+    w = syn.weight_blocks(rs, qtype, N, K).reshape(-1, 144 if qtype == syn.Q4_K else 176)
+    w[:, 0:2] = np.frombuffer(np.float16(0.0123).tobytes(), np.uint8)
+    w[:, 2:4] = np.frombuffer(np.float16(0.0119).tobytes(), np.uint8)
+    w = w.reshape(N, -1)
+    bits = _decode(w, qtype, N, K, K, odt)
+    assert np.array_equal(bits, O.dequant_padded_bits(w, qtype, N, K, K, odt))
 
 
 def test_dequant_planes_equals_blocks():

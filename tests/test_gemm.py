@@ -1,6 +1,8 @@
 """Fused prefill GEMM (gguf_mm_gemm, path FUSED): weights decoded in the kernel
 to f16 and multiplied on tcgen05 tensor cores, against the exact f64 oracle
 (OpenVINO PR #39119, "Implementation", DPAS prefill row)."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -18,6 +20,19 @@ def _gpu():
     U.require_gpu()
 
 
+def _launch(wd, qtype, layout, N, K, x, xdt, M, r, ydt, path=g.GGUF_PATH_FUSED, ws_fill=0x3C):
+    y = U.guarded((M, N), U.TORCH_DT[ydt])
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qtype, N, K, M)
+    ws = U.workspace(ws_bytes, ws_fill)
+    g.gguf_mm_gemm(wd, qtype, layout, N, K, U.dev(x, xdt), U.DT[xdt], M, None if r is None else U.dev(r, ydt),
+                   y.t, U.DT[ydt], ws.t, ws_bytes, path)
+    torch.cuda.synchronize()
+    y.check("y")
+    ws.check("workspace")
+    assert g.gguf_mm_check_errors() == 0
+    return U.host64(y.t)
+
+
 def _gemm(qtype, N, K, M, layout=0, ydt="bf16", xdt="bf16", residual=True, seed=0, path=g.GGUF_PATH_FUSED,
           rows=None):
     rs = syn.rng(seed + 7 * N + K + 3 * M + qtype)
@@ -25,17 +40,11 @@ def _gemm(qtype, N, K, M, layout=0, ydt="bf16", xdt="bf16", residual=True, seed=
     x = syn.normal(rs, (M, K), xdt)
     r = syn.normal(rs, (M, N), ydt) if residual else None
     wd = U.dev(O.q6k_to_planes(w) if layout else w)
-    y = torch.empty((M, N), dtype=U.TORCH_DT[ydt], device="cuda")
-    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qtype, N, K, M)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
-    g.gguf_mm_gemm(wd, qtype, layout, N, K, U.dev(x, xdt), U.DT[xdt], M, None if r is None else U.dev(r, ydt), y,
-                   U.DT[ydt], ws, ws_bytes, path)
-    torch.cuda.synchronize()
-    assert g.gguf_mm_check_errors() == 0
+    got = _launch(wd, qtype, layout, N, K, x, xdt, M, r, ydt, path)
     sel = slice(None) if rows is None else rows
     ref = O.matmul_exact(U.act_f64(x[sel], xdt), O.dequant(w, qtype, N, K),
                          None if r is None else U.act_f64(r[sel], ydt))
-    return U.host64(y)[sel], ref
+    return got[sel], ref
 
 
 @pytest.mark.parametrize("qtype,K", [(syn.Q8_0, 256), (syn.Q8_0, 1024), (syn.Q4_K, 256), (syn.Q4_K, 768),
@@ -53,9 +62,9 @@ def test_fused_q6k_planes(N, M):
 
 
 @pytest.mark.parametrize("ydt", ["f32", "f16"])
-@pytest.mark.parametrize("qtype", [syn.Q5_K, syn.Q8_0])
+@pytest.mark.parametrize("qtype", [syn.Q5_K, syn.Q8_0, syn.Q4_K, syn.Q6_K])
 def test_fused_out_dtypes(qtype, ydt):
-    got, ref = _gemm(qtype, 256, 512, 48, ydt=ydt)
+    got, ref = _gemm(qtype, 256, 512 if qtype != syn.Q6_K else 2048, 48, ydt=ydt)
     U.check_close(got, ref, ydt, rel=2e-3)
 
 
@@ -64,40 +73,72 @@ def test_fused_f16_activations_no_residual():
     U.check_close(got, ref, "bf16")
 
 
-def test_auto_path_picks_gemv_below_8_rows_and_fused_above():
-    # same inputs through AUTO: M = 7 goes to the int8 GEMV (int8-path oracle),
-    # M = 8 to the fused tensor-core GEMM (exact oracle)
+@pytest.mark.parametrize("M", [9, 40, 300])
+def test_fused_f32_activations(M):
+    # f32 activations are converted to f16 row by row (one rounding each)
+    got, ref = _gemm(syn.Q5_K, 256, 1024, M, xdt="f32", ydt="f32")
+    U.check_close(got, ref, "f32", rel=2e-3)
+
+
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+def test_auto_path_by_row_count_and_dtype(xdt):
+    # the pages' path table: fewer than 8 rows (and f32 up to 8 rows, the
+    # GEMV's limit) -> int8 GEMV, checked against the int8-path oracle; more
+    # rows -> fused tensor-core GEMM, checked against the exact oracle
     rs = syn.rng(3)
     N, K = 256, 1024
     w = syn.weight_blocks(rs, syn.Q5_K, N, K)
-    for M in (7, 8):
-        x = syn.normal(rs, (M, K), "bf16")
-        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-        ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, syn.Q5_K, N, K, M)
-        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
-        g.gguf_mm_gemm(U.dev(w), syn.Q5_K, 0, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, None, y, g.GGUF_DT_F32,
-                       ws, ws_bytes, g.GGUF_PATH_AUTO)
-        torch.cuda.synchronize()
-        if M == 7:
-            ref = O.gemv_int8_path(w, syn.Q5_K, N, K, U.act_f32(x, "bf16"))
+    for M in (7, 8, 9):
+        x = syn.normal(rs, (M, K), xdt)
+        got = _launch(U.dev(w), syn.Q5_K, 0, N, K, x, xdt, M, None, "f32", path=g.GGUF_PATH_AUTO)
+        to_gemv = M < 8 or (xdt == "f32" and M <= 8)
+        if to_gemv:
+            ref = O.gemv_int8_path(w, syn.Q5_K, N, K, U.act_f32(x, xdt))
+            U.check_close(got, ref, "f32")
         else:
-            ref = O.matmul_exact(U.act_f64(x, "bf16"), O.dequant(w, syn.Q5_K, N, K))
-        U.check_close(U.host64(y), ref, "f32", rel=2e-3)
+            ref = O.matmul_exact(U.act_f64(x, xdt), O.dequant(w, syn.Q5_K, N, K))
+            U.check_close(got, ref, "f32", rel=2e-3)
 
 
-@pytest.mark.parametrize("qtype,layout", [(syn.Q6_K, 0), (syn.Q6_K, 1), (syn.Q5_K, 0)])
-@pytest.mark.parametrize("M", [8, 512])
+# ---------------------------------------------------------------- the prefill workloads at full size
+
+@functools.lru_cache(maxsize=1)
+def _weights(qtype, N, K, seed):
+    w = syn.weight_blocks(syn.rng(seed + qtype), qtype, N, K)
+    return w, O.dequant(w, qtype, N, K)
+
+
+def _full(qtype, layout, N, K, M, seed, ydt="bf16"):
+    w, w64 = _weights(qtype, N, K, seed)
+    rs = syn.rng(seed + M)
+    x = syn.normal(rs, (M, K), "bf16")
+    wd = U.dev(O.q6k_to_planes(w) if layout else w)
+    got = _launch(wd, qtype, layout, N, K, x, "bf16", M, None, ydt)
+    rows = np.unique(np.concatenate([np.arange(0, M, max(1, M // 5)), [M - 1]]))
+    ref = O.matmul_exact(U.act_f64(x[rows], "bf16"), w64)
+    return got[rows], ref
+
+
+@pytest.mark.parametrize("M", [8, 64, 128, 256, 512, 2048])
+@pytest.mark.parametrize("qtype,layout", [(syn.Q6_K, 0), (syn.Q6_K, 1), (syn.Q5_K, 0), (syn.Q4_K, 0),
+                                          (syn.Q8_0, 0)])
 def test_fused_config_14336x4096(qtype, layout, M):
-    # the prefill workload's shapes; rows sampled for the oracle
-    rows = np.arange(0, M, max(1, M // 5))
-    got, ref = _gemm(qtype, 14336, 4096, M, layout=layout, residual=False, seed=1002, rows=rows)
-    U.check_close(got, ref, "bf16")
+    # the prefill workload (every row count); sampled activation rows, all 14336 outputs
+    got, ref = _full(qtype, layout, 14336, 4096, M, 1002)
+    U.check_close(got, ref, "bf16", what=f"q{qtype}/{layout} M{M}")
 
 
-@pytest.mark.parametrize("M", [128, 512])
+@pytest.mark.parametrize("M", [512, 2048])
+@pytest.mark.parametrize("qtype,layout", [(syn.Q5_K, 0), (syn.Q6_K, 1)])
+def test_fused_config_14336x4096_f32_out(qtype, layout, M):
+    # the same with f32 output: the bound holds with nothing granted for rounding
+    got, ref = _full(qtype, layout, 14336, 4096, M, 1002, ydt="f32")
+    U.check_close(got, ref, "f32", rel=2e-3)
+
+
+@pytest.mark.parametrize("M", [128, 512, 4096])
 def test_fused_config_q8_0_2048x8192(M):
-    rows = np.arange(0, M, max(1, M // 6))
-    got, ref = _gemm(syn.Q8_0, 2048, 8192, M, residual=False, seed=1003, rows=rows)
+    got, ref = _full(syn.Q8_0, 0, 2048, 8192, M, 1003)
     U.check_close(got, ref, "bf16")
 
 
@@ -112,50 +153,48 @@ def test_fused_rejects_q6k_rows_without_16_byte_stride():
     assert e.value.status == g.GGUF_ERR_UNSUPPORTED
 
 
-def test_fused_split_k_residual_exact_and_deterministic():
-    # 2 row tiles and K = 4096 leave most SMs idle, so the plan splits K; the
-    # slices' sums meet in the workspace and the last slice adds them in a
-    # fixed order: two runs agree bit for bit, and both match the oracle
-    qtype, N, K, M = syn.Q4_K, 256, 4096, 40
-    rs = syn.rng(4242)
+@pytest.mark.parametrize("qtype,N,K,M", [(syn.Q4_K, 256, 4096, 40), (syn.Q4_K, 14336, 1024, 512)])
+def test_fused_split_k_residual_exact_and_deterministic(qtype, N, K, M):
+    # 2 row tiles at K = 4096 leave most SMs idle, so the plan splits every
+    # tile's K; 224 tiles on 152 SMs keep one round whole and split the other
+    # 72 into K halves.  Stale workspace bytes (tickets included) must not
+    # matter, two runs agree bit for bit, and both match the oracle.
+    rs = syn.rng(4242 + N)
     w = syn.weight_blocks(rs, qtype, N, K)
     x = syn.normal(rs, (M, K), "bf16")
     r = syn.normal(rs, (M, N), "bf16")
     ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qtype, N, K, M)
-    assert ws_bytes > M * K * 2   # room for the partial tiles
-    outs = []
-    for fill in (0x00, 0xFF):   # stale workspace bytes (tickets included) must not matter
-        ws = torch.full((ws_bytes,), fill, dtype=torch.uint8, device="cuda")
-        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        g.gguf_mm_gemm(U.dev(w), qtype, 0, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, U.dev(r, "bf16"), y,
-                       g.GGUF_DT_BF16, ws, ws_bytes, g.GGUF_PATH_FUSED)
-        torch.cuda.synchronize()
-        assert g.gguf_mm_check_errors() == 0
-        outs.append(U.host64(y))
+    assert ws_bytes > M * K * 2 + M * 4   # room for the partial tiles
+    outs = [_launch(U.dev(w), qtype, 0, N, K, x, "bf16", M, r, "bf16", ws_fill=fill) for fill in (0x00, 0xFF)]
     assert np.array_equal(outs[0], outs[1])
     ref = O.matmul_exact(U.act_f64(x, "bf16"), O.dequant(w, qtype, N, K), U.act_f64(r, "bf16"))
     U.check_close(outs[0], ref, "bf16")
 
 
-def test_fused_tail_split_whole_then_halves():
-    # 224 tiles on a 152-SM GB300: the plan keeps one round of 152 tiles whole
-    # and splits the other 72 into K halves; stale workspace bytes must not
-    # matter and two runs agree bit for bit
-    qtype, N, K, M = syn.Q4_K, 14336, 1024, 512
-    rs = syn.rng(4343)
+def _range_rows(rs, M, K):
+    """Activation rows of every magnitude: f16's range is 6.1e-5 .. 65504."""
+    x32 = rs.standard_normal((M, K)).astype(np.float32)
+    x32[0] *= 3e5
+    x32[1] *= 1e20
+    x32[2] *= 1e-7
+    x32[3, ::7] *= 1e5          # a few large values in an ordinary row
+    x32[4] *= 1e-30
+    return x32
+
+
+@pytest.mark.parametrize("xdt", ["bf16", "f32"])
+@pytest.mark.parametrize("qtype,N,K,M", [(syn.Q4_K, 256, 1024, 24), (syn.Q6_K, 14336, 2048, 512),
+                                         (syn.Q8_0, 2048, 8192, 128)])
+def test_fused_activation_rows_beyond_f16_range(qtype, N, K, M, xdt):
+    # each activation row is converted to f16 scaled by a power of two that
+    # puts its largest magnitude in [2^14, 2^15); the epilogue scales its sums
+    # back.  Checked row by row, each against its own scale (f32 output).
+    rs = syn.rng(61 + qtype + M)
     w = syn.weight_blocks(rs, qtype, N, K)
-    x = syn.normal(rs, (M, K), "bf16")
-    r = syn.normal(rs, (M, N), "bf16")
-    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qtype, N, K, M)
-    outs = []
-    for fill in (0x00, 0xFF):
-        ws = torch.full((ws_bytes,), fill, dtype=torch.uint8, device="cuda")
-        y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        g.gguf_mm_gemm(U.dev(w), qtype, 0, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, M, U.dev(r, "bf16"), y,
-                       g.GGUF_DT_BF16, ws, ws_bytes, g.GGUF_PATH_FUSED)
-        torch.cuda.synchronize()
-        assert g.gguf_mm_check_errors() == 0
-        outs.append(U.host64(y))
-    assert np.array_equal(outs[0], outs[1])
-    ref = O.matmul_exact(U.act_f64(x, "bf16"), O.dequant(w, qtype, N, K), U.act_f64(r, "bf16"))
-    U.check_close(outs[0], ref, "bf16")
+    x32 = _range_rows(rs, M, K)
+    x = syn.f32_to_bf16_bits(x32) if xdt == "bf16" else x32
+    got = _launch(U.dev(w), qtype, 0, N, K, x, xdt, M, None, "f32")
+    rows = np.array([0, 1, 2, 3, 4, 5, M - 1])
+    ref = O.matmul_exact(U.act_f64(x[rows], xdt), O.dequant(w, qtype, N, K))
+    for i, m in enumerate(rows):
+        U.check_close(got[m], ref[i], "f32", rel=2e-3, what=f"row {m}")

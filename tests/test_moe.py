@@ -22,13 +22,15 @@ def _run(qtype, E, N, K, T, top_k, ids, residual=False, ydt="bf16", seed=0, toke
     wE = syn.weight_blocks(rs, qtype, E * N, K)
     x = syn.normal(rs, (T, K), "bf16")
     r = syn.normal(rs, (T, top_k, N), ydt) if residual else None
-    y = torch.full((T, top_k, N), float("nan") if sentinel is None else sentinel, dtype=U.TORCH_DT[ydt],
-                   device="cuda")
+    yb = U.guarded((T, top_k, N), U.TORCH_DT[ydt], fill=float("nan") if sentinel is None else sentinel)
+    y = yb.t
     ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    ws = U.workspace(ws_bytes, 0x6B)
     g.gguf_mm_id(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids.astype(np.int32)),
-                 top_k, None if r is None else U.dev(r, ydt), y, U.DT[ydt], ws, ws_bytes)
+                 top_k, None if r is None else U.dev(r, ydt), y, U.DT[ydt], ws.t, ws_bytes)
     torch.cuda.synchronize()
+    yb.check("y")
+    ws.check("workspace")
     assert g.gguf_mm_check_errors() == 0
     rr = None if r is None else U.act_f64(r, ydt)
     if mv_form(qtype, T * top_k):
@@ -174,3 +176,70 @@ def test_moe_decode_form_128_experts_768x2048(qtype, T, top_k, per_slot):
     assert g.gguf_mm_check_errors() == 0
     ref = O.moe_mv_id_int8(wE, qtype, E, N, K, U.act_f32(x, "bf16"), ids, U.act_f64(r, "bf16"))
     U.check_close(U.host64(y).reshape(-1, N), ref.reshape(-1, N), "bf16")
+
+
+@pytest.mark.parametrize("T,E,top_k", [(256, 128, 8), (5, 16, 3), (600, 4, 2)])
+def test_moe_routing_tables_match_the_oracle(T, E, top_k):
+    # the routing step's integer tables: per-expert offsets bit for bit against
+    # the oracle's counts, the (expert, <= 128-row tile) work list in expert
+    # order, and every expert's group holding exactly its routed entries
+    ids = syn.zipf_ids(syn.rng(500 + T), T, E, top_k, 1.1)
+    ids[0, 0], ids[T - 1, top_k - 1] = -3, E
+    entries = T * top_k
+    max_tiles = min(E, entries) + -(-entries // 128)
+    offsets = U.guarded((E + 1,), torch.int32, fill=-7)
+    ntiles = U.guarded((1,), torch.int32, fill=-7)
+    tiles = U.guarded((max_tiles, 4), torch.int32, fill=-7)
+    rows = U.guarded((entries,), torch.int32, fill=-7)
+    g.gguf_mm_debug_moe_route(U.dev(ids.astype(np.int32)), entries, E, offsets.t, ntiles.t, tiles.t, max_tiles,
+                              rows.t)
+    torch.cuda.synchronize()
+    for b, nm in ((offsets, "offsets"), (ntiles, "ntiles"), (tiles, "tiles"), (rows, "rows")):
+        b.check(nm)
+    counts, offs = O.moe_routing(ids, E)
+    got_off = offsets.t.cpu().numpy().astype(np.int64)
+    assert np.array_equal(got_off[:E], offs)
+    assert got_off[E] == counts.sum()
+    want_tiles = [(e, s0, min(128, int(counts[e]) - s0), 0) for e in range(E) for s0 in range(0, int(counts[e]), 128)]
+    assert int(ntiles.t.item()) == len(want_tiles)
+    assert [tuple(t) for t in tiles.t.cpu().numpy()[:len(want_tiles)].tolist()] == want_tiles
+    got_rows = rows.t.cpu().numpy()
+    flat = ids.ravel()
+    for e in range(E):
+        group = got_rows[offs[e]:offs[e] + counts[e]]
+        assert sorted(group.tolist()) == np.flatnonzero(flat == e).tolist()
+
+
+@pytest.mark.parametrize("T,top_k", [(70, 2), (9, 2)])
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q8_0])
+def test_moe_activation_rows_beyond_f16_range(qtype, T, top_k):
+    # bf16 rows reaching 3e5, 1e20 and down to 1e-7 (f16 holds 6.1e-5 .. 65504):
+    # each gathered row is scaled by a power of two into f16's range and the
+    # epilogue scales its sums back; every row is checked against its own scale
+    E, N, K = 8, 128, 512
+    rs = syn.rng(55 + T + qtype)
+    wE = syn.weight_blocks(rs, qtype, E * N, K)
+    x32 = rs.standard_normal((T, K)).astype(np.float32)
+    x32[0] *= 3e5
+    x32[1] *= 1e20
+    x32[2] *= 1e-7
+    x32[3, ::7] *= 1e5
+    x = syn.f32_to_bf16_bits(x32)
+    ids = _distinct_ids(syn.rng(56), T, E, top_k)
+    y = U.guarded((T, top_k, N), torch.float32)
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
+    ws = U.workspace(ws_bytes)
+    g.gguf_mm_id(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids), top_k, None, y.t,
+                 g.GGUF_DT_F32, ws.t, ws_bytes)
+    torch.cuda.synchronize()
+    y.check("y")
+    assert g.gguf_mm_check_errors() == 0
+    got = U.host64(y.t)
+    if mv_form(qtype, T * top_k):
+        ref = O.moe_mv_id_int8(wE, qtype, E, N, K, U.act_f32(x, "bf16"), ids)
+        rel = 1e-4
+    else:
+        ref = O.moe_mm_id_exact(wE, qtype, E, N, K, U.act_f64(x, "bf16"), ids)
+        rel = 2e-3
+    for t in range(T):
+        U.check_close(got[t], ref[t], "f32", rel=rel, what=f"token {t}")

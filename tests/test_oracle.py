@@ -265,6 +265,40 @@ def test_rounding_helpers_ties_to_even():
     assert O.round_f64_to_bf16_bits(np.array([-2.0, 0.0]))[0] == 0xC000
     assert O.round_f64_to_f16_bits(np.array([one + 2 ** -11]))[0] == 0x3C00
     assert O.round_f64_to_f16_bits(np.array([one + 3 * 2 ** -11]))[0] == 0x3C02
+    # the sign of zero survives rounding
+    assert list(O.round_f64_to_bf16_bits(np.array([-0.0, 0.0]))) == [0x8000, 0x0000]
+    assert list(O.round_f64_to_f16_bits(np.array([-0.0, 0.0]))) == [0x8000, 0x0000]
+
+
+def _nearest_bits_brute_force(v: float, all_vals: np.ndarray, all_bits: np.ndarray) -> int:
+    """Nearest representable value by exhaustive search (exact rationals), ties
+    to the even bit pattern."""
+    from fractions import Fraction
+    fv = Fraction(v)
+    i = int(np.searchsorted(all_vals, v))
+    best = None
+    for j in (i - 1, i, i + 1):
+        if 0 <= j < len(all_vals):
+            d = abs(Fraction(float(all_vals[j])) - fv)
+            key = (d, int(all_bits[j]) & 1)
+            if best is None or key < best[0]:
+                best = (key, int(all_bits[j]))
+    return best[1]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_rounding_helpers_against_exhaustive_search(dtype):
+    # every finite positive value of the type, sorted; random f64 inputs of
+    # both signs within the normal and subnormal ranges
+    bits = np.arange(0x0000, 0x7C00 if dtype == "f16" else 0x7F80, dtype=np.uint16)
+    vals = bits.view(np.float16).astype(np.float64) if dtype == "f16" else O.bf16_bits_to_f64(bits)
+    rs = np.random.default_rng(8)
+    mag = rs.uniform(0.5, 2.0, 3000) * 2.0 ** rs.integers(-30 if dtype == "f16" else -140, 15, 3000)
+    rnd = O.round_f64_to_f16_bits if dtype == "f16" else O.round_f64_to_bf16_bits
+    got = rnd(mag)
+    for v, gb in zip(mag, got):
+        assert int(gb) == _nearest_bits_brute_force(float(v), vals, bits), (v, hex(int(gb)))
+    assert np.array_equal(rnd(-mag), got | 0x8000)
 
 
 @pytest.mark.parametrize("odt", ["f16", "bf16"])
@@ -294,13 +328,28 @@ def test_moe_with_one_expert_equals_dense():
         assert np.max(np.abs(y[:, slot] - dense)) <= 1e-12 * np.max(np.abs(dense))
 
 
-def test_moe_routing_counts():
+def test_moe_routing_counts_by_brute_force():
+    # counts and offsets restated as explicit loops over every (token, slot),
+    # including ids outside [0, n_expert), which select nothing
     g = syn.rng(23)
-    ids = syn.zipf_ids(g, 64, 128, 8)
+    E = 128
+    ids = syn.zipf_ids(g, 64, E, 8)
     assert all(len(set(r)) == 8 for r in ids.tolist())
-    counts, offsets = O.moe_routing(ids, 128)
-    assert counts.sum() == 64 * 8 and offsets[0] == 0
-    assert np.array_equal(offsets[1:], np.cumsum(counts)[:-1])
+    ids[3, 2], ids[9, 0], ids[40, 7] = -1, E, E + 5
+    counts, offsets = O.moe_routing(ids, E)
+    for e in range(E):
+        n = 0
+        for t in range(ids.shape[0]):
+            for k in range(ids.shape[1]):
+                n += int(ids[t, k] == e)
+        assert counts[e] == n
+        before = 0
+        for e2 in range(e):
+            for t in range(ids.shape[0]):
+                for k in range(ids.shape[1]):
+                    before += int(ids[t, k] == e2)
+        assert offsets[e] == before
+    assert counts.sum() == 64 * 8 - 3
     assert counts[0] >= counts[64]                     # Zipf: low ranks hit more often
 
 
