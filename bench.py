@@ -3,19 +3,27 @@
 One step = the three GEMV calls (M = 1, 2, 4; bf16 activations, bf16 residual,
 bf16 output) on three different copies of the weight, so every call streams its
 11,534,336 weight bytes from HBM: the copies rotate over more than twice the L2
-size.  Steps are captured in CUDA graphs and replayed; the timed region is
-exactly K steps, bracketed by a barrier and a device synchronization, timed
-with CUDA events on the launching stream.
+size.  A decode step runs every layer at one M, so each M is a chain of calls
+(`steps` calls at M = 1, then at M = 2, then at M = 4).  The timed region is
+exactly those calls, captured in CUDA graphs, bracketed by a barrier and a
+device synchronization, timed with CUDA events on the launching stream.
 
 Printed JSON line (rank 0): value = weight GB/s over the whole job, plus
-  e2e         the same steps fed from pinned host buffers (x and residual copied
-              in, y copied out inside the timed region);
-  roofline    the GEMV kernel's algorithmic bytes per launch / average launch
-              time, against the measured HBM copy bandwidth;
-  cpu_baseline the CPU oracle (int8-path restatement) on a bounded sample;
+  per_m       us per call and weight GB/s at each M (graphs of 270 calls);
+  e2e         the same calls made eagerly through the C ABI from the host,
+              inputs copied in from pinned host memory and y copied out,
+              every call;
+  roofline    the GEMV kernel's algorithmic bytes per launch / its mean
+              launch time in the timed region, against the measured HBM copy
+              bandwidth;
+  cpu_baseline the CPU oracle (int8-path restatement) on a bounded sample, at
+              all host cores (row shards in spawned processes) and at one;
   clocks      SM clock and throttle reasons sampled during the timed region;
-  prefill     tensor-core GEMM figures for the prefill shapes (context).
-`--impl reference` times the CPU oracle instead (the reference arm).
+  prefill     tensor-core figures for the other workloads, last in the line:
+              [us, TFLOPS, fraction of the measured bf16 peak] (GEMVs:
+              [us, GB/s, fraction of HBM]).
+`--impl reference` times the CPU oracle instead (the reference arm);
+`--crossover` times the decode GEMV against the fused GEMM for M = 1..16.
 Multi-GPU runs (torchrun) are independent replicas: every rank runs the same
 workload on its own GPU and value sums over ranks.
 """
@@ -24,6 +32,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import multiprocessing as mproc
 import os
 import subprocess
 import sys
@@ -43,6 +52,7 @@ ROW_BYTES = K // 256 * 176
 W_BYTES = N * ROW_BYTES                      # 11,534,336
 METRIC = "decode GEMV weight GB/s (% of HBM peak); prefill GEMM TFLOPS (% of TC peak)"
 WORKLOAD = "q5_k_gemv_4096x4096_residual_m1_m2_m4"
+GRAPH_CALLS = 270
 
 
 def peaks():
@@ -50,7 +60,8 @@ def peaks():
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
@@ -63,12 +74,13 @@ def dist_env():
 
 # ------------------------------------------------------------------ CPU arm (the oracle)
 
-def cpu_oracle_run(steps: int, rows: int):
-    """Run the CPU oracle's int8-path GEMV over `rows` weight rows for each M in
-    MS, `steps` times; returns (seconds, weight bytes processed, threads)."""
+def _oracle_shard(job):
+    """Worker: the oracle's int8-path GEMV over `rows` weight rows (a shard of
+    the workload), for each M, `steps` times.  Returns its own seconds."""
+    rows, steps, seed = job
     import gguf_synth as syn
     from oracle import gguf_oracle as O
-    rs = syn.rng(1001)
+    rs = syn.rng(seed)
     w = syn.weight_blocks(rs, QTYPE, rows, K)
     xs = {m: O.bf16_bits_to_f32(syn.normal(rs, (m, K), "bf16")) for m in MS}
     rr = {m: O.bf16_bits_to_f64(syn.normal(rs, (m, rows), "bf16")) for m in MS}
@@ -76,36 +88,77 @@ def cpu_oracle_run(steps: int, rows: int):
     for _ in range(steps):
         for m in MS:
             O.gemv_int8_path(w, QTYPE, rows, K, xs[m], rr[m])
-    dt = time.perf_counter() - t0
-    return dt, steps * len(MS) * rows * ROW_BYTES, 1
+    return time.perf_counter() - t0
 
 
-def cpu_baseline(sample_steps: int = 12):
-    dt, nbytes, threads = cpu_oracle_run(sample_steps, N)
-    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{sample_steps} step(s) of the full workload: Q5_K 4096x4096 at M=1,2,4 "
-                      f"through the numpy int8-path oracle, single thread ({dt:.1f} s)"}
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+class OraclePool:
+    """A pool of spawned processes (started before any GPU work), one thread each."""
+
+    def __init__(self, procs: int):
+        self.procs = procs
+        self.pool = None
+        if procs > 1:
+            os.environ.setdefault("OMP_NUM_THREADS", "1")
+            self.pool = mproc.get_context("spawn").Pool(procs)
+            self.pool.map(_oracle_shard, [(8, 1, 1001)] * procs)   # imports done before timing
+
+    def run(self, rows: int, steps: int):
+        """Wall seconds for `rows` weight rows x `steps` steps of the three M,
+        sharded over the pool's processes; returns (seconds, weight bytes, threads)."""
+        if self.pool is None:
+            dt = _oracle_shard((rows, steps, 1001))
+            return dt, steps * len(MS) * rows * ROW_BYTES, 1
+        shard = -(-rows // self.procs)
+        jobs = [(min(shard, rows - i * shard), steps, 1001 + i) for i in range(self.procs) if i * shard < rows]
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_shard, jobs)
+        dt = time.perf_counter() - t0
+        return dt, steps * len(MS) * rows * ROW_BYTES, len(jobs)
+
+    def close(self):
+        if self.pool is not None:
+            self.pool.close()
+            self.pool.join()
+
+
+def cpu_baseline(pool: OraclePool):
+    dt1, b1, _ = OraclePool(1).run(N // 4, 16)       # one thread: a quarter of the rows, 16 steps (~2 s)
+    dtn, bn, used = pool.run(N, 24)                  # all cores: 24 steps of the whole workload (~12 s of CPU)
+    return {"value": round(bn / dtn / 1e9, 4), "unit": "GB/s", "cores": used, "kind": "oracle",
+            "single_thread_value": round(b1 / dt1 / 1e9, 4),
+            "sample": f"numpy int8-path oracle on the Q5_K 4096x4096 M=1,2,4 calls: all {used} host cores "
+                      f"(row shards in spawned processes) {bn // (3 * ROW_BYTES * N)} step(s) of the full "
+                      f"workload in {dtn:.1f} s; one thread 1024 rows x 16 steps in {dt1:.1f} s"}
 
 
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    steps = max(1, args.steps)
-    for _ in range(max(0, min(args.warmup, 1))):
-        cpu_oracle_run(1, 512)
-    dt, nbytes, threads = cpu_oracle_run(steps, 1024)
+    pool = OraclePool(host_cores())
+    try:
+        steps = max(1, args.steps)
+        if args.warmup > 0:
+            pool.run(256, 1)
+        dt, nbytes, used = pool.run(1024, steps)
+    finally:
+        pool.close()
     value = nbytes / dt / 1e9
-    per_step = dt / steps
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps,
-        "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": dt / steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int8", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "N": N, "K": K, "M": list(MS), "qtype": "Q5_K",
-                   "sample_rows": 1024},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+        "config": {"workload": WORKLOAD, "N": N, "K": K, "M": list(MS), "qtype": "Q5_K", "sample_rows": 1024},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": used, "kind": "oracle",
                          "sample": f"each step: 1024 of the 4096 weight rows at M=1,2,4 through the numpy "
-                                   f"int8-path oracle, single thread"},
+                                   f"int8-path oracle, sharded over {used} host processes"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -197,8 +250,8 @@ def kernel_source_hash():
 
 
 def recorded_traffic():
-    """DRAM bytes per GEMV launch from the committed ncu summary, if it was
-    taken on the current kernel source."""
+    """DRAM bytes per GEMV launch per M from the committed ncu summary, if it
+    was taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "gemv_q5k_4096x4096.traffic.json")
     if not os.path.exists(path):
         return None
@@ -211,7 +264,7 @@ def recorded_traffic():
 
 def time_graph(fn, reps, stream, calls):
     """Mean device time of one call: `calls` calls captured in a CUDA graph,
-    replayed `reps` times (after two untimed replays)."""
+    replayed `reps` times (after two untimed replays); median over replays."""
     import torch
     with torch.cuda.stream(stream):
         for i in range(2):
@@ -224,26 +277,57 @@ def time_graph(fn, reps, stream, calls):
         gr.replay()
         gr.replay()
         stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        ts = []
         for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
             gr.replay()
-        e1.record(stream)
-        e1.synchronize()
-    return e0.elapsed_time(e1) / 1e3 / (reps * calls)
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3 / calls)
+    return float(np.median(ts))
+
+
+_CUDART = None
+
+
+def upload_graph(graph, stream) -> bool:
+    """cudaGraphUpload of a captured graph: its first launch then pays no
+    upload inside a timed region.  False if the runtime or handle is unavailable."""
+    global _CUDART
+    import ctypes
+    try:
+        exec_handle = graph.raw_cuda_graph_exec()
+    except (AttributeError, RuntimeError):
+        return False
+    if _CUDART is None:
+        for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+            try:
+                _CUDART = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if _CUDART is None:
+            return False
+    h = exec_handle if isinstance(exec_handle, int) else int(exec_handle)
+    return _CUDART.cudaGraphUpload(ctypes.c_void_p(h), ctypes.c_void_p(stream.cuda_stream)) == 0
+
+
+def _r(x, nd=1):
+    return round(float(x), nd)
 
 
 def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
     """Figures for the other workloads (context for the second half of the
-    metric): the small Q6_K GEMV, the Q6_K / Q5_K and Q8_0 prefill GEMMs and the
-    MoE expert GEMM; weights rotate over copies larger than L2.  `only`: a
-    regular expression; just the entries whose key it matches are run."""
+    metric).  Returns (compact dict for the JSON line, full detail dict).
+    Weights rotate over copies larger than L2.  `only`: a regular expression
+    over the detail keys."""
     import re
     import torch
     import gguf_quant_weight_gb300 as g
     import gguf_synth as syn
-    out = {}
+    compact, detail = {}, {}
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
 
     def want(key):
@@ -256,101 +340,72 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
     # Q6_K GEMV 256x1024, M = 1, f32 activations and output (no residual)
     key = "q6_k_gemv_256x1024_m1_f32"
     if want(key):
-        N, K = 256, 1024
-        w = syn.weight_blocks(syn.rng(1005), 14, N, K)
+        n, k = 256, 1024
+        w = syn.weight_blocks(syn.rng(1005), 14, n, k)
         W, c = copies_of(w)
-        x = torch.from_numpy(syn.normal(syn.rng(1006), (1, K), "f32")).to(dev)
-        y = torch.empty((1, N), dtype=torch.float32, device=dev)
-        wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 14, N, K, 1)
+        x = torch.from_numpy(syn.normal(syn.rng(1006), (1, k), "f32")).to(dev)
+        y = torch.empty((1, n), dtype=torch.float32, device=dev)
+        wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 14, n, k, 1)
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-        t = time_graph(lambda i: g.gguf_mm_gemv(W[i % c], 14, 0, N, K, x, g.GGUF_DT_F32, 1, None, y, g.GGUF_DT_F32,
+        t = time_graph(lambda i: g.gguf_mm_gemv(W[i % c], 14, 0, n, k, x, g.GGUF_DT_F32, 1, None, y, g.GGUF_DT_F32,
                                                 ws, wsb, stream=stream), 5, stream, c)
-        out[key] = {"us": t * 1e6, "weight_gbs": w.size / t / 1e9, "hbm_frac": w.size / t / 1e9 / hbm_peak}
-
-    # Q6_K (planes and raw blocks) and Q5_K prefill, 14336x4096
-    rs = syn.rng(1002)
-    for qt, name, layout, ms in ((14, "q6_k_planes", 1, (8, 64, 128, 256, 512, 2048)),
-                                 (13, "q5_k", 0, (8, 64, 128, 256, 512, 2048)),
-                                 (14, "q6_k", 0, (512, 2048))):
-        N, K = 14336, 4096
-        # M = 8 sits on the border of the two paths: both are timed
-        runs = [(M, path, tag) for M in ms for path, tag in ((g.GGUF_PATH_FUSED, "fused"), (g.GGUF_PATH_GEMV, "gemv"))
-                if (path == g.GGUF_PATH_FUSED or M <= 8) and want(f"{name}_14336x4096_m{M}_{tag}")]
-        if not runs:
-            continue
-        w = syn.weight_blocks(rs, qt, N, K)
-        W, c = copies_of(w)
-        if layout:   # regroup every copy into the QL | QH | SC | D planes on the GPU
-            P = torch.empty_like(W)
-            for i in range(c):
-                g.gguf_repack_q6k_planes(W[i], P[i], N * K // 256, 0, stream=stream)
-            stream.synchronize()
-            W = P
-        for M, path, tag in runs:
-            x = torch.from_numpy(syn.normal(rs, (M, K), "bf16")).to(dev).view(torch.bfloat16)
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qt, N, K, M)
-            ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-            t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], qt, layout, N, K, x, g.GGUF_DT_BF16, M, None, y,
-                                                    g.GGUF_DT_BF16, ws, wsb, path, stream=stream), 5, stream, c)
-            tf = 2 * M * N * K / t / 1e12
-            out[f"{name}_14336x4096_m{M}_{tag}"] = {"us": t * 1e6, "tflops": tf, "tc_frac": tf / tc_peak,
-                                                    "weight_gbs": W[0].numel() / t / 1e9}
+        detail[key] = {"us": t * 1e6, "weight_gbs": w.size / t / 1e9, "hbm_frac": w.size / t / 1e9 / hbm_peak}
+        compact["q6gemv"] = [_r(t * 1e6, 2), _r(w.size / t / 1e9), _r(w.size / t / 1e9 / hbm_peak, 3)]
 
     # Q8_0 2048x8192: fused vs decode-once (K-padded f16) + dense GEMM
-    N, K = 2048, 8192
-    ms = [M for M in (128, 512, 4096) if want(f"q8_0_2048x8192_m{M}_fused") or
-          want(f"q8_0_2048x8192_m{M}_dense_after_decode_once")]
-    if ms or want("q8_0_2048x8192_decode_once"):
-        w = syn.weight_blocks(syn.rng(1003), 8, N, K)
+    n, k = 2048, 8192
+    ms = [M for M in (128, 512, 4096) if want(f"q8_0_2048x8192_m{M}")]
+    if ms:
+        rs = syn.rng(1003)
+        w = syn.weight_blocks(rs, 8, n, k)
         W, c = copies_of(w)
-        ld = K + 64
-        wd = torch.empty((N, ld), dtype=torch.float16, device=dev)
-        g.gguf_dequant_padded(W[0], 8, 0, N, K, wd, g.GGUF_DT_F16, ld, stream=stream)
+        ld = k + 64
+        wd = torch.empty((n, ld), dtype=torch.float16, device=dev)
+        g.gguf_dequant_padded(W[0], 8, 0, n, k, wd, g.GGUF_DT_F16, ld, stream=stream)
         cd = max(2, int(np.ceil(2.2 * l2 / (wd.numel() * 2))))
         WD = wd.unsqueeze(0).repeat(cd, 1, 1)
-        if want("q8_0_2048x8192_decode_once"):
-            t_dec = time_graph(lambda i: g.gguf_dequant_padded(W[i % c], 8, 0, N, K, wd, g.GGUF_DT_F16, ld,
-                                                               stream=stream), 5, stream, c)
-            out["q8_0_2048x8192_decode_once"] = {"us": t_dec * 1e6, "gbs": (w.size + N * ld * 2) / t_dec / 1e9}
+        t_dec = time_graph(lambda i: g.gguf_dequant_padded(W[i % c], 8, 0, n, k, wd, g.GGUF_DT_F16, ld,
+                                                           stream=stream), 5, stream, c)
+        detail["q8_0_2048x8192_decode_once"] = {"us": t_dec * 1e6, "gbs": (w.size + n * ld * 2) / t_dec / 1e9}
+        compact["q8_decode_once"] = [_r(t_dec * 1e6), _r((w.size + n * ld * 2) / t_dec / 1e9)]
         for M in ms:
-            x = torch.from_numpy(syn.normal(rs, (M, K), "bf16")).to(dev).view(torch.bfloat16)
-            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-            wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 8, N, K, M)
+            x = torch.from_numpy(syn.normal(rs, (M, k), "bf16")).to(dev).view(torch.bfloat16)
+            y = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+            wsb = max(g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 8, n, k, M),
+                      g.gguf_mm_workspace_size(g.GGUF_OP_DENSE, 8, n, k, M))
             ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
-            fl = 2 * M * N * K
-            if want(f"q8_0_2048x8192_m{M}_fused"):
-                t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], 8, 0, N, K, x, g.GGUF_DT_BF16, M, None, y,
-                                                        g.GGUF_DT_BF16, ws, wsb, g.GGUF_PATH_FUSED, stream=stream),
-                               5, stream, c)
-                out[f"q8_0_2048x8192_m{M}_fused"] = {"us": t * 1e6, "tflops": fl / t / 1e12,
-                                                     "tc_frac": fl / t / 1e12 / tc_peak}
-            if want(f"q8_0_2048x8192_m{M}_dense_after_decode_once"):
-                t2 = time_graph(lambda i: g.gguf_dense_gemm(WD[i % cd], g.GGUF_DT_F16, ld, N, K, x, g.GGUF_DT_BF16, M,
-                                                            None, y, g.GGUF_DT_BF16, ws, wsb, stream=stream),
-                                5, stream, cd)
-                out[f"q8_0_2048x8192_m{M}_dense_after_decode_once"] = {"us": t2 * 1e6, "tflops": fl / t2 / 1e12,
-                                                                         "tc_frac": fl / t2 / 1e12 / tc_peak}
+            fl = 2 * M * n * k
+            t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], 8, 0, n, k, x, g.GGUF_DT_BF16, M, None, y,
+                                                    g.GGUF_DT_BF16, ws, wsb, g.GGUF_PATH_FUSED, stream=stream),
+                           5, stream, c)
+            t2 = time_graph(lambda i: g.gguf_dense_gemm(WD[i % cd], g.GGUF_DT_F16, ld, n, k, x, g.GGUF_DT_BF16, M,
+                                                        None, y, g.GGUF_DT_BF16, ws, wsb, stream=stream),
+                            5, stream, cd)
+            detail[f"q8_0_2048x8192_m{M}_fused"] = {"us": t * 1e6, "tflops": fl / t / 1e12}
+            detail[f"q8_0_2048x8192_m{M}_dense_after_decode_once"] = {"us": t2 * 1e6, "tflops": fl / t2 / 1e12}
+            compact[f"q8_m{M}"] = [_r(t * 1e6), _r(fl / t / 1e12), _r(fl / t / 1e12 / tc_peak, 3)]
+            compact[f"q8dense_m{M}"] = [_r(t2 * 1e6), _r(fl / t2 / 1e12), _r(fl / t2 / 1e12 / tc_peak, 3)]
 
     # MoE: 128 experts top-8, Q4_K 768x2048; ids rotate over 8 Zipf(1.1) draws.
     # T = 32..512 is the prefill batch; T = 1, 4, 16 the decode form (one int8
     # GEMV per routed row), timed against the routed path as well
-    E, N, K, top_k = 128, 768, 2048, 8
+    E, n, k, top_k = 128, 768, 2048, 8
     ts = [T for T in (1, 4, 16, 32, 64, 256, 512) if want(f"q4_k_moe_128x768x2048_top8_t{T}")]
     if ts:
-        wE = syn.weight_blocks(syn.rng(1004), 12, E * N, K)
+        wE = syn.weight_blocks(syn.rng(1004), 12, E * n, k)
         WE, c = copies_of(wE)
-    per_expert = N * (K // 256) * 144
+    per_expert = n * (k // 256) * 144
+    rs = syn.rng(1007)
     for T in ts:
         id_sets = [syn.zipf_ids(syn.rng(2000 + T + j), T, E, top_k, 1.1) for j in range(8)]
         IDS = [torch.from_numpy(a).to(dev) for a in id_sets]
         touched = float(np.mean([len(np.unique(a)) for a in id_sets])) * per_expert
-        x = torch.from_numpy(syn.normal(rs, (T, K), "bf16")).to(dev).view(torch.bfloat16)
-        y = torch.empty((T, top_k, N), dtype=torch.bfloat16, device=dev)
-        wsb = g.gguf_mm_workspace_size(g.GGUF_OP_ID, 12, N, K, T, E, top_k)
+        x = torch.from_numpy(syn.normal(rs, (T, k), "bf16")).to(dev).view(torch.bfloat16)
+        y = torch.empty((T, top_k, n), dtype=torch.bfloat16, device=dev)
+        wsb = g.gguf_mm_workspace_size(g.GGUF_OP_ID, 12, n, k, T, E, top_k)
         ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
         calls = 8 * c
-        fl = 2 * top_k * T * N * K
+        fl = 2 * top_k * T * n * k
         rec = {}
         # comparison arms (the switches are read when a call is made, so while
         # the graph is captured): the decode form off (T <= 16), and every
@@ -361,33 +416,125 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
         for arm, env in arms:
             os.environ.update(env)
             try:
-                t = time_graph(lambda i: g.gguf_mm_id(WE[i % c], 12, E, N, K, x, g.GGUF_DT_BF16, T, IDS[i % 8], top_k,
-                                                      None, y, g.GGUF_DT_BF16, ws, wsb, stream=stream), 3, stream, calls)
+                t = time_graph(lambda i: g.gguf_mm_id(WE[i % c], 12, E, n, k, x, g.GGUF_DT_BF16, T, IDS[i % 8],
+                                                      top_k, None, y, g.GGUF_DT_BF16, ws, wsb, stream=stream),
+                               3, stream, calls)
             finally:
-                for k in env:
-                    os.environ.pop(k, None)
+                for kk in env:
+                    os.environ.pop(kk, None)
             if arm == "default":
-                rec.update({"us": t * 1e6, "tflops": fl / t / 1e12, "tc_frac": fl / t / 1e12 / tc_peak,
-                            "touched_gbs": touched / t / 1e9, "hbm_frac": touched / t / 1e9 / hbm_peak,
-                            "experts_touched": touched / per_expert})
+                rec.update({"us": t * 1e6, "tflops": fl / t / 1e12, "touched_gbs": touched / t / 1e9,
+                            "hbm_frac": touched / t / 1e9 / hbm_peak, "experts_touched": touched / per_expert})
             else:
                 rec["us_" + arm] = t * 1e6
-        out[f"q4_k_moe_128x768x2048_top8_t{T}"] = rec
-    return out
+        detail[f"q4_k_moe_128x768x2048_top8_t{T}"] = rec
+        compact[f"moe_t{T}"] = [_r(rec["us"]), _r(rec["touched_gbs"]), _r(rec["hbm_frac"], 3), _r(rec["tflops"])]
+
+    # the 14336 x 4096 prefill shapes; Q5_K and Q6_K planes at M = 512 and 2048 last
+    runs = []
+    for M in (8, 64, 128, 256):
+        runs += [(14, "q6p", 1, M), (13, "q5", 0, M)]
+    for M in (512, 2048):
+        runs += [(12, "q4", 0, M), (8, "q8", 0, M), (14, "q6", 0, M)]
+    for M in (512, 2048):
+        runs += [(13, "q5", 0, M), (14, "q6p", 1, M)]
+    n, k = 14336, 4096
+    cache = {}
+    rs = syn.rng(1002)
+    for qt, name, layout, M in runs:
+        full = f"{name}_14336x4096_m{M}"
+        if not want(full):
+            continue
+        if (qt, layout) not in cache:
+            w = syn.weight_blocks(syn.rng(1002 + qt), qt, n, k)
+            W, c = copies_of(w)
+            if layout:   # regroup every copy into the QL | QH | SC | D planes on the GPU
+                P = torch.empty_like(W)
+                for i in range(c):
+                    g.gguf_repack_q6k_planes(W[i], P[i], n * k // 256, 0, stream=stream)
+                stream.synchronize()
+                W = P
+            cache[(qt, layout)] = (W, c)
+        W, c = cache[(qt, layout)]
+        x = torch.from_numpy(syn.normal(rs, (M, k), "bf16")).to(dev).view(torch.bfloat16)
+        y = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+        wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qt, n, k, M)
+        ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], qt, layout, n, k, x, g.GGUF_DT_BF16, M, None, y,
+                                                g.GGUF_DT_BF16, ws, wsb, g.GGUF_PATH_FUSED, stream=stream),
+                       5, stream, c)
+        tf = 2 * M * n * k / t / 1e12
+        detail[full] = {"us": t * 1e6, "tflops": tf, "tc_frac": tf / tc_peak, "weight_gbs": W[0].numel() / t / 1e9}
+        compact[f"{name}_m{M}"] = [_r(t * 1e6), _r(tf), _r(tf / tc_peak, 3)]
+    cache.clear()
+    return compact, detail
+
+
+def crossover(dev, stream, out_path):
+    """GEMV against the fused GEMM for M = 1..16, every format, at the decode
+    shape (4096 x 4096) and the prefill shape (14336 x 4096): us per call in
+    chains of calls on rotating weight copies (both paths forced)."""
+    import torch
+    import gguf_quant_weight_gb300 as g
+    import gguf_synth as syn
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    table = {}
+    for n, k in ((4096, 4096), (14336, 4096)):
+        for qt, layout, name in ((13, 0, "Q5_K"), (12, 0, "Q4_K"), (14, 1, "Q6_K_planes"), (14, 0, "Q6_K"),
+                                 (8, 0, "Q8_0")):
+            w = syn.weight_blocks(syn.rng(7000 + qt), qt, n, k)
+            c = max(2, int(np.ceil(2.2 * l2 / w.size)))
+            W = torch.from_numpy(w.reshape(-1)).to(dev).repeat(c).view(c, -1)
+            if layout:
+                P = torch.empty_like(W)
+                for i in range(c):
+                    g.gguf_repack_q6k_planes(W[i], P[i], n * k // 256, 0, stream=stream)
+                W = P
+            stream.synchronize()
+            row = {}
+            for M in range(1, 17):
+                x = torch.from_numpy(syn.normal(syn.rng(M), (M, k), "bf16")).to(dev).view(torch.bfloat16)
+                y = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+                wsb = g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, qt, n, k, M)
+                ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+                cell = {}
+                for path, tag in ((g.GGUF_PATH_GEMV, "gemv"), (g.GGUF_PATH_FUSED, "fused")):
+                    if path == g.GGUF_PATH_GEMV and M > 8:
+                        continue
+                    calls = 10 * c
+                    t = time_graph(lambda i: g.gguf_mm_gemm(W[i % c], qt, layout, n, k, x, g.GGUF_DT_BF16, M, None,
+                                                            y, g.GGUF_DT_BF16, ws, wsb, path, stream=stream),
+                                   3, stream, calls)
+                    cell[tag] = round(t * 1e6, 2)
+                row[M] = cell
+            table[f"{name}_{n}x{k}"] = row
+            print(name, n, k, json.dumps(row), flush=True)
+            del W
+            torch.cuda.empty_cache()
+    if out_path:
+        with open(out_path, "w") as f:
+            json.dump(table, f, indent=1)
+    return table
 
 
 def run_gpu(args):
+    ws, rank, local = dist_env()
+    # the CPU pool first: spawned processes, before any GPU work in this one
+    pool = OraclePool(host_cores()) if (rank == 0 and not args.no_cpu_baseline) else None
     import torch
     import gguf_quant_weight_gb300 as g
     import gguf_synth as syn
 
-    ws, rank, local = dist_env()
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     g.load_library()
+    stream = torch.cuda.Stream(device=dev)
+    if args.crossover:
+        crossover(dev, stream, args.crossover)
+        return
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     copies = max(3 * 2, int(np.ceil(2.2 * l2 / W_BYTES)))
     copies = (copies + 2) // 3 * 3
@@ -399,47 +546,39 @@ def run_gpu(args):
     ys = {m: torch.empty((m, N), dtype=torch.bfloat16, device=dev) for m in MS}
     wsz = {m: g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, QTYPE, N, K, m) for m in MS}
     wss = {m: torch.empty(wsz[m], dtype=torch.uint8, device=dev) for m in MS}
-    stream = torch.cuda.Stream(device=dev)
-    # A decode step runs every layer at one M, so each M is timed as its own
-    # chain of calls: `steps` calls at M = 1, then at M = 2, then at M = 4 (the
-    # same calls and bytes as `steps` rounds of one call per M).  A graph walks
-    # the weight copies in order ten times (a decode step's graph holds every
-    # layer's calls; ten walks keep the replay's own start-up off the per-call
-    # time), so a copy is reused only after all the others: never an L2 hit.
-    per_graph = 10 * copies
+    kernels = {m: g.GEMV_KERNELS.get(g.gguf_mm_gemv_kernel(QTYPE, 0, N, K, m), "?") for m in MS}
+    launches_per_call = {m: 1 if kernels[m] in ("rowlane", "tile") else 2 for m in MS}
     state = {"c": 0}
 
-    def call(m, xsrc=None, rsrc=None, ydst=None):
-        if xsrc is not None:
-            xs[m].copy_(xsrc[m], non_blocking=True)
-            rsd[m].copy_(rsrc[m], non_blocking=True)
+    def call(m):
         g.gguf_mm_gemv(W[state["c"] % copies], QTYPE, 0, N, K, xs[m], g.GGUF_DT_BF16, m, rsd[m], ys[m],
                        g.GGUF_DT_BF16, wss[m], wsz[m], stream=stream)
-        if ydst is not None:
-            ydst[m].copy_(ys[m], non_blocking=True)
         state["c"] += 1
 
-    def capture(m, ncalls, **kw):
+    def capture(seq):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(graph, stream=stream):
-                for _ in range(ncalls):
-                    call(m, **kw)
+                for m in seq:
+                    call(m)
         return graph
 
-    def make_plan(ncalls, **kw):
-        # [(graph, replays)] covering ncalls calls of each M, M by M
+    def make_plan(ncalls):
+        """[(graph, replays)] for ncalls calls at each M, M by M (a copy is
+        reused only after all the others: never an L2 hit).  One graph per M
+        (up to 270 calls each): a graph that mixes the M's measured slower per
+        call (7.35 us against 4.35 / 5.5 / 8.06 for M = 1 / 2 / 4 alone)."""
         out = []
-        full, rem = divmod(ncalls, per_graph)
+        full, rem = divmod(ncalls, GRAPH_CALLS)
         for m in MS:
             if full:
-                out.append((capture(m, per_graph, **kw), full))
+                out.append((capture([m] * GRAPH_CALLS), full))
             if rem:
-                out.append((capture(m, rem, **kw), 1))
+                out.append((capture([m] * rem), 1))
         return out
 
-    def replay(graphs_counts):
-        for gr, cnt in graphs_counts:
+    def replay(plan_):
+        for gr, cnt in plan_:
             for _ in range(cnt):
                 gr.replay()
 
@@ -449,7 +588,7 @@ def run_gpu(args):
                 call(m)
         stream.synchronize()
     plan = make_plan(args.steps)
-    # warm-up calls (graph replays of the same launches)
+    uploaded = all(upload_graph(gr, stream) for gr, _ in plan)   # no first-launch upload in the timed region
     with torch.cuda.stream(stream):
         replay(make_plan(max(args.warmup, 3)))
     stream.synchronize()
@@ -460,7 +599,7 @@ def run_gpu(args):
     clocks.start()
     time.sleep(0.3)
 
-    def timed(plan_):
+    def timed(body):
         if ws > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
@@ -469,7 +608,7 @@ def run_gpu(args):
         t_host0 = time.time()
         with torch.cuda.stream(stream):
             e0.record(stream)
-            replay(plan_)
+            body()
             e1.record(stream)
         e1.synchronize()
         torch.cuda.synchronize(dev)
@@ -477,20 +616,35 @@ def run_gpu(args):
             torch.distributed.barrier()
         return e0.elapsed_time(e1) / 1e3, t_host0, time.time()
 
-    sec, th0, th1 = timed(plan)
+    sec, th0, th1 = timed(lambda: replay(plan))
     clk = clocks.summary(th0, th1)
 
-    # end to end: pinned host inputs copied in and outputs copied out every step
+    # end to end, eagerly through the C ABI: every call copies its inputs in
+    # from pinned host memory, is launched from the host, and copies y out
     hx = {m: xs[m].cpu().pin_memory() for m in MS}
     hr = {m: rsd[m].cpu().pin_memory() for m in MS}
     hy = {m: torch.empty((m, N), dtype=torch.bfloat16).pin_memory() for m in MS}
-    eplan = make_plan(args.steps, xsrc=hx, rsrc=hr, ydst=hy)
+
+    def eager_steps():
+        for m in MS:
+            for _ in range(args.steps):
+                xs[m].copy_(hx[m], non_blocking=True)
+                rsd[m].copy_(hr[m], non_blocking=True)
+                call(m)
+                hy[m].copy_(ys[m], non_blocking=True)
+
     with torch.cuda.stream(stream):
-        for gr, _ in eplan:
-            gr.replay()
+        for m in MS:
+            call(m)
     stream.synchronize()
-    esec, _, _ = timed(eplan)
+    esec, _, _ = timed(eager_steps)
     clocks.stop()
+
+    # each M on its own: graphs of 270 calls (reported beside the headline)
+    per_m = {}
+    for m in MS:
+        t = time_graph(lambda i, m=m: call(m), 5, stream, GRAPH_CALLS)
+        per_m[m] = t
 
     h2d = sum(m * K * 2 + m * N * 2 for m in MS)
     d2h = sum(m * N * 2 for m in MS)
@@ -504,12 +658,12 @@ def run_gpu(args):
     value = job_gbs(steps, ws, sec)
     e2e = job_gbs(steps, ws, esec)
     hbm, tc, tc_sus, peak_kind = peaks()
-    algo = sum(W_BYTES + m * K * 2 + 2 * m * N * 2 for m in MS) / len(MS)   # weights + x + residual + y
-    calls = steps * len(MS)
-    achieved = algo * calls / sec / 1e9   # per call: every kernel of gguf_mm_gemv, chained
-    # kernels per call: the tile kernel alone at M = 1; the activation quantizer
-    # plus the pair kernel at M = 2, 4 (the library's plan for this shape)
-    launches = steps * sum(1 if m == 1 else 2 for m in MS)
+    algo = {m: W_BYTES + m * K * 2 + 2 * m * N * 2 for m in MS}   # weights + x + residual + y
+    algo_mean = sum(algo.values()) / len(MS)
+    launches = steps * sum(launches_per_call[m] for m in MS)
+    dominant = "gemv_rowlane_kernel" if all(kernels[m] == "rowlane" for m in MS) else "/".join(kernels.values())
+    achieved = algo_mean * steps * len(MS) / sec / 1e9   # every launch of the timed region is this kernel
+    traffic = recorded_traffic()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": steps, "warmup": args.warmup,
         "ms_per_step": sec / steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -517,25 +671,32 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "N": N, "K": K, "M": list(MS), "qtype": "Q5_K",
                    "residual": True, "activations": "bf16", "output": "bf16",
                    "l2": f"weights rotate over {copies} copies ({copies * W_BYTES / 1e6:.0f} MB > 2x L2)",
-                   "order": "each M as its own chain of calls (a decode step runs every layer at one M)",
-                   "graph_calls": per_graph,
+                   "order": "each M a chain of calls", "graphs_uploaded_before_timing": uploaded,
                    "parallelism": f"replicas x{ws}"},
-        "hbm_frac_of_" + peak_kind: value / ws / hbm,
-        "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": recorded_traffic(), "peak_kind": peak_kind,
-                     "kernel": "gguf_mm_gemv: gemv_tile_kernel (M=1); act_quant_kernel + gemv_pair_kernel (M=2,4)",
-                     "algorithmic_bytes_per_launch": algo},
+        "hbm_frac": round(value / ws / hbm, 4),
+        "per_m": {str(m): [round(per_m[m] * 1e6, 3), round(W_BYTES / per_m[m] / 1e9, 1)] for m in MS},
+        "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "eager host calls through the C ABI, pinned copies each call"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4),
+                     "traffic": None if traffic is None else round(sum(traffic[str(m)] for m in MS) / len(MS)),
+                     "peak_kind": peak_kind, "kernel": dominant,
+                     "algorithmic_bytes_per_launch": algo_mean},
         "gpu_launches": launches,
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"], "reasons": clk["reasons"]},
     }
     if rank == 0:
+        if pool is not None:
+            line["cpu_baseline"] = cpu_baseline(pool)
+            pool.close()
         if not args.no_prefill:
-            line["prefill"] = prefill_figures(dev, stream, tc, hbm, args.prefill_only)
-            line["prefill"]["peak_tflops"] = tc
-        if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline()
+            compact, detail = prefill_figures(dev, stream, tc, hbm, args.prefill_only)
+            print("# prefill detail " + json.dumps({k: {kk: round(vv, 3) for kk, vv in v.items()}
+                                                     for k, v in detail.items()}), flush=True)
+            line["prefill"] = {"peak_tf": tc, **compact}
         print(json.dumps(line), flush=True)
+    elif pool is not None:
+        pool.close()
     if ws > 1:
         torch.distributed.destroy_process_group()
 
@@ -543,13 +704,15 @@ def run_gpu(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--prefill-only", default=None, metavar="REGEX",
-                    help="run only the prefill figures whose key matches (e.g. q6_k_planes_14336x4096_m512)")
+                    help="run only the prefill figures whose key matches (e.g. q6p_14336x4096_m512)")
+    ap.add_argument("--crossover", default=None, metavar="OUT.json",
+                    help="time GEMV against fused GEMM for M = 1..16 instead, and write the table")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

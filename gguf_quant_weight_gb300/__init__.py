@@ -53,6 +53,7 @@ _SIGS = {
                                           _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp, _c_sz, _c_int,
                                           ctypes.POINTER(_c_int), _c_vp]),
     "gguf_mm_gemv_kernel": (_c_int, [_c_int, _c_int, _c_i64, _c_i64, _c_i64, _c_int]),
+    "gguf_mm_auto_path": (_c_int, [_c_int, _c_int, _c_i64, _c_i64, _c_i64, _c_int]),
     "gguf_mm_debug_moe_route": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp]),
     "gguf_mm_debug_timeout": (_c_int, [_c_i64, _c_vp]),
 }
@@ -183,6 +184,11 @@ def gguf_mm_debug_gemv_terms(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt
         _p(w), qtype, layout, N, K, _p(x), xdt, M, _p(residual), _p(y), ydt, _p(qa), _p(d_a), _p(s), _p(D),
         _p(workspace), ws_bytes, kernel, ctypes.byref(out), _s(stream)))
     return out.value
+
+
+def gguf_mm_auto_path(qtype, layout, N, K, M, xdt=GGUF_DT_BF16) -> int:
+    """The path GGUF_PATH_AUTO takes for this shape (GGUF_PATH_GEMV or GGUF_PATH_FUSED)."""
+    return load_library().gguf_mm_auto_path(qtype, layout, N, K, M, xdt)
 
 
 def gguf_mm_gemv_kernel(qtype, layout, N, K, M, xdt=GGUF_DT_BF16) -> int:

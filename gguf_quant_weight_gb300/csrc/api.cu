@@ -90,11 +90,32 @@ int check_common(const void* w, int qtype, int layout, int64_t N, int64_t K, con
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA; }
 
-// GGUF_PATH_AUTO's choice (OpenVINO PR #39119, "Implementation", path table:
-// fewer than 8 rows or f32 activations -> GEMV, otherwise the prefill GEMM).
+// The smallest activation row count at which the fused GEMM beat the GEMV on
+// GB300, per format and shape class (chains of calls on weight copies larger
+// than L2, bf16 activations; the crossover table of bench.py --crossover):
+// at most 8192 weight rows (measured at 4096 x 4096: at most 64 tiles of 128
+// rows for 152 SMs, so the fused path splits K) and more (14336 x 4096).  A
+// value above 8 keeps every row count the GEMV can take on the GEMV.  Formats
+// not measured keep the pages' threshold of 8.
+int crossover_rows(int qtype, int layout, int64_t N, int64_t K) {
+    (void)K;
+    const bool large = N > 8192;
+    switch (qtype) {
+        case GGUF_Q4_K: return large ? 7 : 9;
+        case GGUF_Q5_K: return large ? 6 : 9;
+        case GGUF_Q6_K:
+            return layout == GGUF_LAYOUT_Q6K_PLANES ? (large ? 5 : 8) : (large ? 3 : 4);
+        case GGUF_Q8_0: return large ? 2 : 6;
+        default: return 8;
+    }
+}
+
+// GGUF_PATH_AUTO's choice.  OpenVINO PR #39119, "Implementation", path table:
+// few activation rows or f32 activations -> GEMV, otherwise the prefill GEMM;
+// "few" is the measured crossover above (the pages' Xe threshold is 8), and
+// f32 activations stay on the GEMV up to the 8 rows it takes.
 int auto_path(int qtype, int layout, int64_t N, int64_t K, int64_t M, int xdt) {
-    (void)qtype; (void)layout; (void)N; (void)K;
-    if (M < 8) return GGUF_PATH_GEMV;
+    if (M <= 8 && M < crossover_rows(qtype, layout, N, K)) return GGUF_PATH_GEMV;
     if (xdt == GGUF_DT_F32 && M <= 8) return GGUF_PATH_GEMV;
     return GGUF_PATH_FUSED;
 }
@@ -210,6 +231,11 @@ int gguf_mm_debug_gemv_terms(const void* w, int qtype, int layout, int64_t N, in
                              gguf_stream_t stream) {
     return run_gemv(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace, ws_bytes, (cudaStream_t)stream,
                     qa, d_a, s, D, true, kernel, kernel_out);
+}
+
+int gguf_mm_auto_path(int qtype, int layout, int64_t N, int64_t K, int64_t M, int xdt) {
+    if (!valid_qtype(qtype) || !valid_dtype(xdt) || N <= 0 || K <= 0 || M <= 0) return GGUF_ERR_INVALID_ARG;
+    return auto_path(qtype, layout, N, K, M, xdt);
 }
 
 int gguf_mm_gemv_kernel(int qtype, int layout, int64_t N, int64_t K, int64_t M, int xdt) {

@@ -29,7 +29,7 @@ namespace gg {
 
 namespace {
 
-// One warp per activation row.  For an f16 copy the row is scaled by 2^-s
+// Activation rows to 16 bits.  For an f16 copy the row is scaled by 2^-s
 // first, with s = floor(log2(max |x|)) - 14, so that its largest magnitude
 // lands in [2^14, 2^15): a bf16 or f32 row whose values exceed f16's range
 // (65504) or sit below its normal range (2^-14) keeps its 8 (bf16) or 11
@@ -57,52 +57,104 @@ __device__ __forceinline__ void load8(const void* x, int64_t off, float v[8]) {
     }
 }
 
+// One CTA of 256 threads per activation row (rows strided over the grid).
+// Each thread loads its chunks of 8 values -- up to RCH of them, so a row of up
+// to 256 * 8 * RCH values is read once and held in registers with every load
+// in flight -- the CTA reduces the row's largest finite magnitude, and the
+// threads convert their chunks from registers.  Longer rows take a second
+// pass over global memory.
+constexpr int kConvThreads = 256, kConvChunks = 8;
+
 template <int XDT>
-__global__ void __launch_bounds__(256) convert_rows_kernel(const void* __restrict__ x, int64_t M, int64_t K,
-                                                           uint16_t* __restrict__ out, int odt_bf16,
-                                                           float* __restrict__ scale, uint32_t* __restrict__ zero,
-                                                           int nzero) {
+__global__ void __launch_bounds__(kConvThreads) convert_rows_kernel(const void* __restrict__ x, int64_t M, int64_t K,
+                                                                    uint16_t* __restrict__ out, int odt_bf16,
+                                                                    float* __restrict__ scale,
+                                                                    uint32_t* __restrict__ zero, int nzero) {
+    __shared__ float red_max[kConvThreads / 32];
+    __shared__ int red_fin[kConvThreads / 32];
     // the GEMM that follows on the stream counts on these words being zero
     if (blockIdx.x == 0)
         for (int j = threadIdx.x; j < nzero; j += blockDim.x) zero[j] = 0u;
-    const int lane = threadIdx.x & 31;
-    for (int64_t m = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); m < M; m += (int64_t)gridDim.x * 8) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t nch = K / 8;                                  // chunks of 8 values in a row
+    const bool in_regs = nch <= (int64_t)kConvThreads * kConvChunks;
+    for (int64_t m = blockIdx.x; m < M; m += gridDim.x) {
         const int64_t base = m * K;
-        float mul = 1.f, back = 1.f;
-        if (!odt_bf16) {
-            float amax = 0.f;   // largest finite magnitude; a non-finite value marks the row
-            bool finite = true;
-            for (int64_t k = 8 * lane; k < K; k += 256) {
-                float v[8];
-                load8<XDT>(x, base + k, v);
+        float v[kConvChunks][8];
+        float amax = 0.f;   // largest finite magnitude; a non-finite value marks the row
+        bool finite = true;
+        if (in_regs) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    finite = finite && isfinite(v[j]);
-                    amax = fmaxf(amax, fabsf(v[j]));
-                }
+            for (int c = 0; c < kConvChunks; ++c) {
+                const int64_t ch = tid + (int64_t)c * kConvThreads;
+                if (ch < nch) load8<XDT>(x, base + 8 * ch, v[c]);
             }
 #pragma unroll
+            for (int c = 0; c < kConvChunks; ++c) {
+                if (tid + (int64_t)c * kConvThreads < nch) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        finite = finite && isfinite(v[c][j]);
+                        amax = fmaxf(amax, fabsf(v[c][j]));
+                    }
+                }
+            }
+        } else {
+            for (int64_t ch = tid; ch < nch; ch += kConvThreads) {
+                float t[8];
+                load8<XDT>(x, base + 8 * ch, t);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    finite = finite && isfinite(t[j]);
+                    amax = fmaxf(amax, fabsf(t[j]));
+                }
+            }
+        }
+        float mul = 1.f, back = 1.f;
+        if (!odt_bf16) {
+#pragma unroll
             for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            finite = __all_sync(0xffffffffu, finite);
+            const bool wf = __all_sync(0xffffffffu, finite);
+            if (lane == 0) { red_max[warp] = amax; red_fin[warp] = wf ? 1 : 0; }
+            __syncthreads();
+            amax = 0.f;
+            finite = true;
+#pragma unroll
+            for (int w = 0; w < kConvThreads / 32; ++w) {
+                amax = fmaxf(amax, red_max[w]);
+                finite = finite && red_fin[w];
+            }
+            __syncthreads();   // red_* reused by the next row
             if (finite && amax > 0.f) {
                 const int s = max(-100, min(100, ilogbf(amax) - 14));
                 mul = ldexpf(1.f, -s);
                 back = ldexpf(1.f, s);
             }
         }
-        for (int64_t k = 8 * lane; k < K; k += 256) {
-            float v[8];
-            load8<XDT>(x, base + k, v);
+        auto store8 = [&](int64_t ch, const float (&t)[8]) {
             uint16_t o[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                o[j] = odt_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v[j]))
-                                : __half_as_ushort(__float2half_rn(v[j] * mul));
-            *reinterpret_cast<uint4*>(out + base + k) =
+                o[j] = odt_bf16 ? __bfloat16_as_ushort(__float2bfloat16_rn(t[j]))
+                                : __half_as_ushort(__float2half_rn(t[j] * mul));
+            *reinterpret_cast<uint4*>(out + base + 8 * ch) =
                 make_uint4(o[0] | (uint32_t)o[1] << 16, o[2] | (uint32_t)o[3] << 16, o[4] | (uint32_t)o[5] << 16,
                            o[6] | (uint32_t)o[7] << 16);
+        };
+        if (in_regs) {
+#pragma unroll
+            for (int c = 0; c < kConvChunks; ++c) {
+                const int64_t ch = tid + (int64_t)c * kConvThreads;
+                if (ch < nch) store8(ch, v[c]);
+            }
+        } else {
+            for (int64_t ch = tid; ch < nch; ch += kConvThreads) {
+                float t[8];
+                load8<XDT>(x, base + 8 * ch, t);
+                store8(ch, t);
+            }
         }
-        if (lane == 0 && scale) scale[m] = back;
+        if (tid == 0 && scale) scale[m] = back;
     }
 }
 
@@ -111,15 +163,15 @@ __global__ void __launch_bounds__(256) convert_rows_kernel(const void* __restric
 cudaError_t convert_activations(const void* x, int xdt, int64_t M, int64_t K, void* out, int odt, float* scale,
                                 int num_sms, cudaStream_t s, uint32_t* zero, int nzero) {
     if (K % 8 != 0) return cudaErrorInvalidValue;
-    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(ceil_div(M, 8), (int64_t)num_sms * 16));
+    const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(M, (int64_t)num_sms * 8));
     const int bf = odt == GGUF_DT_BF16 ? 1 : 0;
     uint16_t* o = static_cast<uint16_t*>(out);
     if (xdt == GGUF_DT_F32)
-        convert_rows_kernel<GGUF_DT_F32><<<(unsigned)blocks, 256, 0, s>>>(x, M, K, o, bf, scale, zero, nzero);
+        convert_rows_kernel<GGUF_DT_F32><<<(unsigned)blocks, kConvThreads, 0, s>>>(x, M, K, o, bf, scale, zero, nzero);
     else if (xdt == GGUF_DT_F16)
-        convert_rows_kernel<GGUF_DT_F16><<<(unsigned)blocks, 256, 0, s>>>(x, M, K, o, bf, scale, zero, nzero);
+        convert_rows_kernel<GGUF_DT_F16><<<(unsigned)blocks, kConvThreads, 0, s>>>(x, M, K, o, bf, scale, zero, nzero);
     else
-        convert_rows_kernel<GGUF_DT_BF16><<<(unsigned)blocks, 256, 0, s>>>(x, M, K, o, bf, scale, zero, nzero);
+        convert_rows_kernel<GGUF_DT_BF16><<<(unsigned)blocks, kConvThreads, 0, s>>>(x, M, K, o, bf, scale, zero, nzero);
     return cudaGetLastError();
 }
 
@@ -176,6 +228,9 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(tfull + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * 128, t0 = blockIdx.y * BN;
+    __shared__ float s_xscale[BN];   // the tile's activation-row scales, for the epilogue
+    for (int i = threadIdx.x; i < BN; i += blockDim.x)
+        s_xscale[i] = (ep.xscale && t0 + i < ep.M) ? ep.xscale[t0 + i] : 1.f;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
@@ -216,7 +271,7 @@ __global__ void __launch_bounds__(192, 1)
     } else if (warp >= 2) {
         if (mbar_wait(tfull, 0, status)) {
             tc_fence_after();
-            tc_epilogue<BN>(ep, tmem, warp & 3, lane, n0, t0);
+            tc_epilogue<BN>(ep, tmem, warp & 3, lane, n0, t0, s_xscale);
         }
     }
     tc_fence_before();

@@ -427,6 +427,12 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
     // MMA width: the tile's valid token columns rounded up to 16, so an
     // underfilled tile issues only the MMA columns it needs
     const int n_mma = fp.full_width ? BN : min(BN, (cols + 15) & ~15);
+    // the power-of-two scales of the tile's activation rows, staged once for
+    // the epilogue (read before the first barrier: the conversion kernel that
+    // wrote them precedes this one on the stream)
+    __shared__ float s_xscale[BN];
+    for (int i = threadIdx.x; i < BN; i += blockDim.x)
+        s_xscale[i] = i < cols ? fp.xscale[MOE ? (int64_t)gstart + i : t0 + i] : 1.f;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], DW + 1); mbar_init(&empty[s], NI); }
@@ -603,7 +609,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
                         if (col < cols) {
                             // output row: token m (dense) or the routed entry (grouped)
                             const int64_t orow = MOE ? (int64_t)fp.rows[gstart + col] : t0 + col;
-                            float o = __uint_as_float(v[j]) * fp.xscale[MOE ? gstart + col : t0 + col];
+                            float o = __uint_as_float(v[j]) * s_xscale[col];
                             if (fp.residual) o += load_act(fp.residual, fp.ydt, orow * fp.N + n);
                             store_out(fp.y, fp.ydt, orow * fp.N + n, o);
                         }
@@ -642,7 +648,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
                         const int col = 16 * c + j;
                         if (col < cols) {
                             const int64_t orow = t0 + col;
-                            float o = acc[j] * fp.xscale[orow];
+                            float o = acc[j] * s_xscale[col];
                             if (fp.residual) o += load_act(fp.residual, fp.ydt, orow * fp.N + n);
                             store_out(fp.y, fp.ydt, orow * fp.N + n, o);
                         }

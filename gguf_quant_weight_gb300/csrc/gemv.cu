@@ -250,11 +250,11 @@ struct ActSlice {
     uint4 e[REG ? MT : 1][NE];
     uint32_t qa_base, ds_base, qa_row, ds_row;
 
-    __device__ __forceinline__ void init(const Shared& sh, int k0, int nb) {
+    __device__ __forceinline__ void init(const Shared& sh, int k0, int nb, int m0 = 0) {
         qa_row = sh.qa_row;
         ds_row = 16u * (uint32_t)nb;
-        qa_base = sh.qa + qa_pos((uint32_t)k0);
-        ds_base = sh.ds + 16u * (uint32_t)(k0 / 32);
+        qa_base = sh.qa + qa_pos((uint32_t)k0) + (uint32_t)m0 * qa_row;
+        ds_base = sh.ds + 16u * (uint32_t)(k0 / 32) + (uint32_t)m0 * ds_row;
         if (REG) {
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
@@ -301,9 +301,11 @@ struct FragQ45 {
 // R rows of the same unit at once: every activation-code load is shared by the
 // R rows' dot products.  f[r], acc[r], n[r], on[r]: fragment, accumulators,
 // output row and validity of row r.
+// m0: the first activation row the MT accumulators stand for (the accessor's
+// row m is activation row m0 + m).
 template <int QT, int MT, int R, class A, bool DUMP>
 __device__ __forceinline__ void unit_q45k(const GemvParams& p, const FragQ45<QT>* const* f, const A& a, int kb,
-                                          int h, float (*acc)[MT], const int64_t* n, const bool* on) {
+                                          int h, float (*acc)[MT], const int64_t* n, const bool* on, int m0 = 0) {
     float d[R], dmin[R];
     uint32_t scw[R], mnw[R];
 #pragma unroll
@@ -341,7 +343,7 @@ __device__ __forceinline__ void unit_q45k(const GemvParams& p, const FragQ45<QT>
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            if (m < p.M) {
+            if (m0 + m < p.M) {
                 const uint4 l0 = a.codes(m, 4 * pp), l1 = a.codes(m, 4 * pp + 1);
                 const uint4 h0 = a.codes(m, 4 * pp + 2), h1 = a.codes(m, 4 * pp + 3);
                 const uint4 e0 = a.entry(m, 2 * pp), e1 = a.entry(m, 2 * pp + 1);
@@ -361,8 +363,8 @@ __device__ __forceinline__ void unit_q45k(const GemvParams& p, const FragQ45<QT>
                     accd[r][m] += __uint_as_float(e0.x) * i2f(sc0 * D0) + __uint_as_float(e1.x) * i2f(sc1 * D1);
                     accm[r][m] += mn0 * __uint_as_float(e0.y) + mn1 * __uint_as_float(e1.y);
                     if (DUMP && p.dbg_D && on[r]) {
-                        dump_D(p, m, n[r], kb * 8 + jj, 32, D0);
-                        dump_D(p, m, n[r], kb * 8 + jj + 1, 32, D1);
+                        dump_D(p, m0 + m, n[r], kb * 8 + jj, 32, D0);
+                        dump_D(p, m0 + m, n[r], kb * 8 + jj + 1, 32, D1);
                     }
                 }
             }
@@ -372,6 +374,108 @@ __device__ __forceinline__ void unit_q45k(const GemvParams& p, const FragQ45<QT>
     for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[r][m] += d[r] * accd[r][m] - dmin[r] * accm[r][m];
+}
+
+// ------------------------------------------------------------------ Q4_K / Q5_K unit, row-lane form
+// Half H (values 128H .. 128H + 127) of super-block kb of one weight row, whose
+// block starts at shared address blk, against MT activation rows.  The lanes of
+// a warp hold different weight rows of the same unit, so the activation codes
+// (row m at qa + m * qa_row: the unit's 128 codes) and block entries (row m at
+// ds + m * ds_row: four entries of 16 bytes, of which {d_a, d_a * s} are read)
+// sit at warp-uniform addresses and are served as broadcasts.  Each 64-value
+// piece (sub-blocks j = 4H + 2pp and j + 1, the low and high nibbles of the
+// same 32 qs bytes) is decoded once and dotted with every activation row, and
+// only the qs bytes of the current piece are held, so four rows fit in the 64
+// registers a lane has with two CTAs per SM.  With H a compile-time constant
+// every shift amount is one too, and the shifts are written as multiplies
+// (x << s = x * 2^s, x >> s = high half of x * 2^(32-s)), which the FMA pipe
+// executes beside the ALU pipe that takes the masks.
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+template <int S>
+__device__ __forceinline__ uint32_t shift_fma(uint32_t x) {   // x << S for S >= 0, x >> -S for S < 0
+    if constexpr (S >= 0) return x * (1u << S);
+    else return __umulhi(x, 1u << (32 + S));
+}
+
+template <int QT, int MT, int H, bool DUMP>
+__device__ __forceinline__ void unit_rl(const GemvParams& p, uint32_t blk, uint32_t qa, uint32_t qa_row, uint32_t ds,
+                                        uint32_t ds_row, int kb, float (&acc)[MT], int64_t n) {
+    const uint4 hdr = lds128(blk);
+    const float d = f16_bits_to_float(hdr.x), dmin = f16_bits_to_float(hdr.x >> 16);
+    // 6-bit scales and mins of sub-blocks 4H .. 4H + 3, one per byte (GGUF packing)
+    const uint32_t scw = H ? ((hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u)) : (hdr.y & 0x3F3F3F3Fu);
+    const uint32_t mnw = H ? (((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u)) : (hdr.z & 0x3F3F3F3Fu);
+    uint4 qh0 = make_uint4(0, 0, 0, 0), qh1 = qh0;
+    if constexpr (QT == GGUF_Q5_K) { qh0 = lds128(blk + 16); qh1 = lds128(blk + 32); }
+    float accd[MT], accm[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) accd[m] = accm[m] = 0.f;
+#pragma unroll
+    for (int pp = 0; pp < 2; ++pp) {
+        const uint32_t q = blk + (QT == GGUF_Q5_K ? 48u : 16u) + 64u * H + 32u * pp;
+        const uint4 w0 = lds128(q), w1 = lds128(q + 16);
+        uint32_t lo[8], hi[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t w = comp(i < 4 ? w0 : w1, i);
+            lo[i] = w & 0x0F0F0F0Fu;
+            hi[i] = shift_fma<-4>(w) & 0x0F0F0F0Fu;
+            if constexpr (QT == GGUF_Q5_K) {
+                // bit jj (low nibbles) and jj + 1 (high nibbles) of each qh byte to bit 4
+                const uint32_t hb = comp(i < 4 ? qh0 : qh1, i);
+                if (pp == 0) {
+                    lo[i] |= shift_fma<4 - 4 * H>(hb) & 0x10101010u;
+                    hi[i] |= shift_fma<3 - 4 * H>(hb) & 0x10101010u;
+                } else {
+                    lo[i] |= shift_fma<2 - 4 * H>(hb) & 0x10101010u;
+                    hi[i] |= shift_fma<1 - 4 * H>(hb) & 0x10101010u;
+                }
+            }
+        }
+        const int sc0 = (int)((scw >> (16 * pp)) & 0xFF), sc1 = (int)((scw >> (16 * pp + 8)) & 0xFF);
+        const float mn0 = (float)((mnw >> (16 * pp)) & 0xFF), mn1 = (float)((mnw >> (16 * pp + 8)) & 0xFF);
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            if (m < p.M) {
+                const uint32_t c = qa + (uint32_t)m * qa_row + 64u * pp;
+                int D0, D1;
+                {
+                    const uint4 l0 = lds128(c), l1 = lds128(c + 16);
+                    int a = 0, b = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        a = dp4a(lo[i], comp(l0, i), a);
+                        b = dp4a(lo[4 + i], comp(l1, i), b);
+                    }
+                    D0 = a + b;
+                }
+                {
+                    const uint4 h0 = lds128(c + 32), h1 = lds128(c + 48);
+                    int a = 0, b = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        a = dp4a(hi[i], comp(h0, i), a);
+                        b = dp4a(hi[4 + i], comp(h1, i), b);
+                    }
+                    D1 = a + b;
+                }
+                const uint32_t e = ds + (uint32_t)m * ds_row + 32u * pp;
+                const uint2 e0 = lds64(e), e1 = lds64(e + 16);
+                accd[m] += __uint_as_float(e0.x) * i2f(sc0 * D0) + __uint_as_float(e1.x) * i2f(sc1 * D1);
+                accm[m] += mn0 * __uint_as_float(e0.y) + mn1 * __uint_as_float(e1.y);
+                if (DUMP && p.dbg_D) {
+                    dump_D(p, m, n, kb * 8 + 4 * H + 2 * pp, 32, D0);
+                    dump_D(p, m, n, kb * 8 + 4 * H + 2 * pp + 1, 32, D1);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] += d * accd[m] - dmin * accm[m];
 }
 
 // ------------------------------------------------------------------ Q6_K unit
@@ -1370,7 +1474,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, 2) gemv_pair_kernel(const Gem
 // Each warp leaves one partial sum per (row, activation row) in shared
 // memory; the last phase adds the warps' partials in warp order, then the
 // residual, and stores.
-__host__ __device__ constexpr int rowlane_warps(int mt) { return mt == 1 ? 16 : mt == 2 ? 16 : 8; }
+__host__ __device__ constexpr int rowlane_warps(int mt) { return 16; }
 
 struct RowLaneLayout {
     int64_t pitch, img, part, res, bar, total;
@@ -1462,22 +1566,17 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
         for (int m = 0; m < MT; ++m) acc[i][m] = 0.f;
     const bool ok = __syncthreads_and(mbar_wait(bar, 0, p.status) ? 1 : 0) != 0;
     if (ok) {
-        using Act = ActSlice<MT, false, 8, 4>;
+        const uint32_t ds_row = 16u * (uint32_t)nb;
         for (int u = warp; u < U; u += NW) {
-            Act a;
-            a.init(sh, 128 * u, nb);
             const uint32_t ub = (uint32_t)(u >> 1) * bb;
+            const uint32_t qa_u = sh.qa + qa_pos((uint32_t)(128 * u)), ds_u = sh.ds + 64u * (uint32_t)u;
 #pragma unroll
             for (int i = 0; i < RI; ++i) {
                 const int r = lane + 32 * i;
                 if (r < rows) {
-                    FragQ45<QT> f;
-                    f.load(tile + (uint32_t)r * pitch + ub, u & 1);
-                    const FragQ45<QT>* fr[1] = {&f};
-                    const int64_t nn[1] = {row0 + r};
-                    const bool on[1] = {true};
-                    float(*a1)[MT] = reinterpret_cast<float(*)[MT]>(&acc[i][0]);
-                    unit_q45k<QT, MT, 1, Act, DUMP>(p, fr, a, u >> 1, u & 1, a1, nn, on);
+                    const uint32_t blk = tile + (uint32_t)r * pitch + ub;
+                    if (u & 1) unit_rl<QT, MT, 1, DUMP>(p, blk, qa_u, sh.qa_row, ds_u, ds_row, u >> 1, acc[i], row0 + r);
+                    else unit_rl<QT, MT, 0, DUMP>(p, blk, qa_u, sh.qa_row, ds_u, ds_row, u >> 1, acc[i], row0 + r);
                 }
             }
         }
@@ -1493,11 +1592,15 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
     __syncthreads();
 
     // 4. the warps' partial sums of each (row, activation row), in warp order, + residual
-    const int nwu = U < NW ? U : NW;   // warps that owned units
+    // (all NW loads in flight at once; warps that owned no unit wrote zeros)
     for (int t = tid; t < p.M * rows; t += NT) {
         const int m = t / rows, r = t - m * rows;
+        float pw[NW];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) pw[w] = part[(w * rpc + r) * MT + m];
         float v = 0.f;
-        for (int w = 0; w < nwu; ++w) v += part[(w * rpc + r) * MT + m];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) v += pw[w];
         if (has_res) v += res[m * rpc + r];
         store_out(p.y, p.ydt, (int64_t)m * p.N + row0 + r, v);
     }

@@ -176,6 +176,10 @@ __device__ __forceinline__ void load8_16(const uint16_t* src, int xdt, float v[8
     }
 }
 
+// A row of up to 32 lanes x 8 chunks of 8 values is loaded once into
+// registers, all loads in flight; longer rows take a second pass.
+constexpr int kGatherChunks = 8;
+
 __global__ void __launch_bounds__(256) moe_gather_kernel(const void* __restrict__ x, int xdt, int64_t K, int row_div,
                                                          const int* __restrict__ row_count,
                                                          const int* __restrict__ rows, int64_t cap,
@@ -186,15 +190,34 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const void* __restrict_
     const int64_t t = rows[p] / row_div;
     const uint16_t* src = static_cast<const uint16_t*>(x) + t * K;
     uint16_t* dst = xg + p * K;
+    const int64_t nch = K / 8;
+    const bool in_regs = nch <= 32 * kGatherChunks;
+    float v[kGatherChunks][8];
     float amax = 0.f;
     bool finite = true;
-    for (int64_t k = 8 * lane; k < K; k += 256) {
-        float v[8];
-        load8_16(src + k, xdt, v);
+    if (in_regs) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            finite = finite && isfinite(v[j]);
-            amax = fmaxf(amax, fabsf(v[j]));
+        for (int c = 0; c < kGatherChunks; ++c)
+            if (lane + 32 * c < nch) load8_16(src + 8 * (lane + 32 * c), xdt, v[c]);
+#pragma unroll
+        for (int c = 0; c < kGatherChunks; ++c) {
+            if (lane + 32 * c < nch) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    finite = finite && isfinite(v[c][j]);
+                    amax = fmaxf(amax, fabsf(v[c][j]));
+                }
+            }
+        }
+    } else {
+        for (int64_t ch = lane; ch < nch; ch += 32) {
+            float u[8];
+            load8_16(src + 8 * ch, xdt, u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                finite = finite && isfinite(u[j]);
+                amax = fmaxf(amax, fabsf(u[j]));
+            }
         }
     }
 #pragma unroll
@@ -206,16 +229,25 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const void* __restrict_
         mul = ldexpf(1.f, -s);
         back = ldexpf(1.f, s);
     }
-    for (int64_t k = 8 * lane; k < K; k += 256) {
-        float v[8];
-        load8_16(src + k, xdt, v);
+    auto store8 = [&](int64_t ch, const float (&u)[8]) {
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const __half2 h = __floats2half2_rn(v[2 * j] * mul, v[2 * j + 1] * mul);
+            const __half2 h = __floats2half2_rn(u[2 * j] * mul, u[2 * j + 1] * mul);
             o[j] = *reinterpret_cast<const uint32_t*>(&h);
         }
-        *reinterpret_cast<uint4*>(dst + k) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(dst + 8 * ch) = make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    if (in_regs) {
+#pragma unroll
+        for (int c = 0; c < kGatherChunks; ++c)
+            if (lane + 32 * c < nch) store8(lane + 32 * c, v[c]);
+    } else {
+        for (int64_t ch = lane; ch < nch; ch += 32) {
+            float u[8];
+            load8_16(src + 8 * ch, xdt, u);
+            store8(ch, u);
+        }
     }
     if (lane == 0) xscale[p] = back;
 }

@@ -31,9 +31,10 @@ __device__ __forceinline__ uint8_t* align_up_1024(uint8_t* p) {
 
 // Warp q (0..3) of the epilogue reads TMEM lanes 32q..32q+31 (weight rows
 // n0 + 32q + lane) for all BN token columns, adds the residual and stores.
+// xs: the BN activation-row scales of the tile, staged in shared memory.
 template <int BN>
 __device__ __forceinline__ void tc_epilogue(const TcEpilogue& ep, uint32_t tmem, int q, int lane, int64_t n0,
-                                            int64_t t0) {
+                                            int64_t t0, const float* xs) {
     const int64_t n = n0 + 32 * q + lane;
 #pragma unroll 1
     for (int c = 0; c < BN / 16; ++c) {
@@ -46,7 +47,7 @@ __device__ __forceinline__ void tc_epilogue(const TcEpilogue& ep, uint32_t tmem,
                 const int64_t m = t0 + 16 * c + j;
                 if (m < ep.M) {
                     float o = __uint_as_float(v[j]);
-                    if (ep.xscale) o *= ep.xscale[m];
+                    o *= xs[16 * c + j];
                     if (ep.residual) o += load_act(ep.residual, ep.ydt, m * ep.N + n);
                     store_out(ep.y, ep.ydt, m * ep.N + n, o);
                 }

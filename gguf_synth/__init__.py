@@ -6,6 +6,11 @@ CPU oracle and the CUDA path can be fed from it without sharing any method code.
 
 Block structs (byte offsets inside one block) follow the GGUF on-disk layout:
 
+  Q4_0  18 B / 32 values : d f16 @0, qs[16] @2 (element e < 16: low nibble of qs[e], else high of qs[e-16])
+  Q4_1  20 B / 32 values : d f16 @0, m f16 @2, qs[16] @4
+  Q5_0  22 B / 32 values : d f16 @0, qh[4] @2 (bit e: fifth bit of element e), qs[16] @6
+  Q5_1  24 B / 32 values : d f16 @0, m f16 @2, qh[4] @4, qs[16] @8
+
   Q8_0  34 B / 32 values : d f16 @0, qs[32] i8 @2
   Q4_K 144 B / 256 values: d f16 @0, dmin f16 @2, scales[12] @4, qs[128] @16
   Q5_K 176 B / 256 values: d f16 @0, dmin f16 @2, scales[12] @4, qh[32] @16, qs[128] @48
@@ -19,6 +24,8 @@ Recipes (one per workload family, all N(0,1)/uniform draws from numpy PCG64):
   * Q6_K: ql/qh uniform bytes, scales uniform integers in [-32, 31], d = f16(|N(0,1)|*1e-3)
   * Q5_K / Q4_K: qs/qh/scales uniform bytes, d and dmin = f16(|N(0,1)|*1e-3)
   * Q8_0: q uniform integers in [-127, 127], d = f16(|N(0,1)|*1e-3)
+  * Q4_0 / Q5_0: qs/qh uniform bytes, d = f16(|N(0,1)|*1e-3)
+  * Q4_1 / Q5_1: as Q4_0 / Q5_0, plus m = f16(-8e-3 * |N(0,1)| * (1 + |N(0,1)|))
   * activations and residuals: N(0,1), kept as f32 or rounded to bf16/f16
   * MoE ids: per token top_k distinct experts drawn in turn without replacement,
     P(rank r) proportional to r**-s over ranks 1..n_expert, expert id = rank - 1
@@ -27,10 +34,11 @@ from __future__ import annotations
 
 import numpy as np
 
-Q8_0, Q4_K, Q5_K, Q6_K = 8, 12, 13, 14
-QTYPE_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
-BLOCK_VALUES = {Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210}
+Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 3, 6, 7, 8, 12, 13, 14
+QTYPE_NAMES = {Q4_0: "Q4_0", Q4_1: "Q4_1", Q5_0: "Q5_0", Q5_1: "Q5_1", Q8_0: "Q8_0", Q4_K: "Q4_K",
+               Q5_K: "Q5_K", Q6_K: "Q6_K"}
+BLOCK_VALUES = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210}
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -63,6 +71,13 @@ def weight_blocks(g: np.random.Generator, qtype: int, N: int, K: int) -> np.ndar
     elif qtype == Q6_K:
         blk[:, 192:208] = g.integers(-32, 32, size=(nb, 16), dtype=np.int8).view(np.uint8)
         blk[:, 208:210] = _f16_scale_bytes(g, nb)
+    elif qtype in (Q4_0, Q5_0):
+        blk[:, 0:2] = _f16_scale_bytes(g, nb)
+    elif qtype in (Q4_1, Q5_1):
+        blk[:, 0:2] = _f16_scale_bytes(g, nb)
+        # the min: m = -8 * |N(0,1)| * 1e-3 * (1 + |N(0,1)|), negative like a block's smallest weight
+        mv = (-8e-3 * np.abs(g.standard_normal(nb)) * (1 + np.abs(g.standard_normal(nb)))).astype(np.float16)
+        blk[:, 2:4] = mv.view(np.uint8).reshape(nb, 2)
     else:
         raise ValueError(f"unknown qtype {qtype}")
     return np.ascontiguousarray(blk.reshape(N, -1))

@@ -52,7 +52,9 @@ typedef enum { GGUF_DT_F32 = 0, GGUF_DT_F16 = 1, GGUF_DT_BF16 = 2 } gguf_dtype;
 
 /* Execution path of gguf_mm_gemm (OpenVINO PR #39119, "Implementation": the
  * path follows the activation row count; an internal option forces a path).
- * AUTO: M < 8 or f32 activations -> GEMV, otherwise the fused tensor-core GEMM. */
+ * AUTO: fewer activation rows than the format's measured crossover (see
+ * gguf_mm_auto_path), or f32 activations with at most 8 rows -> GEMV;
+ * otherwise the fused tensor-core GEMM. */
 typedef enum { GGUF_PATH_AUTO = 0, GGUF_PATH_GEMV = 1, GGUF_PATH_FUSED = 2 } gguf_path;
 
 typedef enum {
@@ -105,6 +107,14 @@ size_t gguf_mm_workspace_size(int op, int qtype, int64_t N, int64_t K, int64_t M
 int gguf_mm_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K,
                  const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
                  void* workspace, size_t ws_bytes, gguf_stream_t stream);
+
+/* The path GGUF_PATH_AUTO takes for this call shape (GGUF_PATH_GEMV or
+ * GGUF_PATH_FUSED), or GGUF_ERR_INVALID_ARG.  The GEMV takes M below the
+ * smallest row count at which the fused GEMM measured faster on GB300 for the
+ * format and shape class (at most 8192 weight rows, or more): Q4_K 9 / 7,
+ * Q5_K 9 / 6, Q6_K planes 8 / 5, raw Q6_K 4 / 3, Q8_0 6 / 2; other formats 8
+ * (the pages' threshold).  f32 activations stay on the GEMV up to 8 rows. */
+int gguf_mm_auto_path(int qtype, int layout, int64_t N, int64_t K, int64_t M, int xdt);
 
 /* Prefill GEMM (or GEMV when the path says so), same arguments and semantics as
  * gguf_mm_gemv plus `path` (gguf_path) and any M >= 1.  The fused path stages

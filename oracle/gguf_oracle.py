@@ -41,9 +41,9 @@ from __future__ import annotations
 
 import numpy as np
 
-Q8_0, Q4_K, Q5_K, Q6_K = 8, 12, 13, 14
-BLOCK_VALUES = {Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210}
+Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 3, 6, 7, 8, 12, 13, 14   # GGUF type ids
+BLOCK_VALUES = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210}
 
 
 # ----------------------------------------------------------------------------
@@ -187,7 +187,53 @@ def dequant_q6_k(blk: np.ndarray) -> np.ndarray:
                                f16_field(blk[:, 208:210]))
 
 
-_DECODERS = {Q8_0: dequant_q8_0, Q4_K: dequant_q4_k, Q5_K: dequant_q5_k, Q6_K: dequant_q6_k}
+# ---- the 32-value formats of the type table ([mobius] 1.2; 7.1 Q4_0, 7.2 Q4_1)
+
+def b32_nibble(qs: np.ndarray, e: int) -> np.ndarray:
+    """4-bit code of element e (0..31) of a 32-value block whose 16 code bytes are
+    qs [nb, 16]: elements 0..15 are the low nibbles of qs[0..15], elements 16..31
+    the high nibbles (reading: GGUF on-disk order)."""
+    byte = qs[:, e % 16].astype(np.int64)
+    return (byte & 15) if e < 16 else (byte >> 4)
+
+
+def b32_fifth_bit(qh: np.ndarray, e: int) -> np.ndarray:
+    """Fifth bit of element e of a Q5_0 / Q5_1 block: bit e of the 32-bit
+    little-endian word qh [nb, 4] (reading: GGUF on-disk layout)."""
+    return (qh[:, e // 8].astype(np.int64) >> (e % 8)) & 1
+
+
+def dequant_q4_0(blk: np.ndarray) -> np.ndarray:
+    """[nb, 18] u8 {d f16, qs[16]} -> [nb, 32] f64.  w = (q - 8) * d ([mobius] 7.1:
+    unsigned codes 0..15 recentred by the implicit zero point 8)."""
+    d, qs = f16_field(blk[:, 0:2]), blk[:, 2:18]
+    return np.stack([(b32_nibble(qs, e) - 8) * d for e in range(32)], axis=1)
+
+
+def dequant_q4_1(blk: np.ndarray) -> np.ndarray:
+    """[nb, 20] u8 {d f16, m f16, qs[16]} -> [nb, 32] f64.  w = q * d + m
+    ([mobius] 7.2 writes the min added: x = qs * d + m)."""
+    d, m, qs = f16_field(blk[:, 0:2]), f16_field(blk[:, 2:4]), blk[:, 4:20]
+    return np.stack([b32_nibble(qs, e) * d + m for e in range(32)], axis=1)
+
+
+def dequant_q5_0(blk: np.ndarray) -> np.ndarray:
+    """[nb, 22] u8 {d f16, qh[4], qs[16]} -> [nb, 32] f64.  q5 = nibble + 16 * bit e
+    of qh; w = (q5 - 16) * d ([mobius] 1.2: symmetric 5-bit, block 32; the
+    implicit zero point is 16, half the code range, as 8 is for Q4_0)."""
+    d, qh, qs = f16_field(blk[:, 0:2]), blk[:, 2:6], blk[:, 6:22]
+    return np.stack([(b32_nibble(qs, e) + 16 * b32_fifth_bit(qh, e) - 16) * d for e in range(32)], axis=1)
+
+
+def dequant_q5_1(blk: np.ndarray) -> np.ndarray:
+    """[nb, 24] u8 {d f16, m f16, qh[4], qs[16]} -> [nb, 32] f64.  w = q5 * d + m
+    ([mobius] 1.2: asymmetric 5-bit + min, the Q4_1 rule with a fifth bit)."""
+    d, m, qh, qs = f16_field(blk[:, 0:2]), f16_field(blk[:, 2:4]), blk[:, 4:8], blk[:, 8:24]
+    return np.stack([(b32_nibble(qs, e) + 16 * b32_fifth_bit(qh, e)) * d + m for e in range(32)], axis=1)
+
+
+_DECODERS = {Q4_0: dequant_q4_0, Q4_1: dequant_q4_1, Q5_0: dequant_q5_0, Q5_1: dequant_q5_1,
+             Q8_0: dequant_q8_0, Q4_K: dequant_q4_k, Q5_K: dequant_q5_k, Q6_K: dequant_q6_k}
 
 
 def dequant(w: np.ndarray, qtype: int, N: int, K: int) -> np.ndarray:
@@ -292,6 +338,8 @@ def weight_int_terms(w: np.ndarray, qtype: int, N: int, K: int):
     16 for Q6_K), scale [N, K/sub] f64 multiplies the sub-block's integer dot and
     minv [N, K/sub] f64 (zero for Q8_0/Q6_K) multiplies d_a * s of its
     activation block, so that w = scale * q_w - minv element by element.
+      Q4_0: q_w = q - 8,    scale = d;   Q5_0: q_w = q5 - 16, scale = d
+      Q4_1: q_w = q,        scale = d, minv = -m;   Q5_1: q_w = q5, scale = d, minv = -m
       Q8_0: q_w = q,        scale = d
       Q4_K: q_w = nibble,   scale = d*sc_j, minv = dmin*m_j
       Q5_K: q_w = q5,       scale = d*sc_j, minv = dmin*m_j
@@ -300,6 +348,22 @@ def weight_int_terms(w: np.ndarray, qtype: int, N: int, K: int):
     bv, bb = BLOCK_VALUES[qtype], BLOCK_BYTES[qtype]
     nb = N * (K // bv)
     blk = np.ascontiguousarray(w, dtype=np.uint8).reshape(nb, bb)
+    if qtype in (Q4_0, Q4_1, Q5_0, Q5_1):
+        # Q4_0: q_w = q - 8, Q5_0: q_w = q5 - 16 (scale d); Q4_1 / Q5_1: q_w = q (or q5),
+        # scale d, and the added min as minv = -m (w = scale * q_w - minv)
+        q_off = {Q4_0: 2, Q4_1: 4, Q5_0: 6, Q5_1: 8}[qtype]
+        qs = blk[:, q_off:q_off + 16]
+        q = np.stack([b32_nibble(qs, e) for e in range(32)], axis=1)
+        if qtype in (Q5_0, Q5_1):
+            qh = blk[:, q_off - 4:q_off]
+            q = q + 16 * np.stack([b32_fifth_bit(qh, e) for e in range(32)], axis=1)
+        d = f16_field(blk[:, 0:2])
+        if qtype in (Q4_0, Q5_0):
+            q = q - (8 if qtype == Q4_0 else 16)
+            minv = np.zeros(nb)
+        else:
+            minv = -f16_field(blk[:, 2:4])
+        return q.reshape(N, K), 32, d.reshape(N, -1), minv.reshape(N, -1)
     if qtype == Q8_0:
         q = blk[:, 2:34].view(np.int8).astype(np.int64)
         scale = f16_field(blk[:, 0:2])[:, None]

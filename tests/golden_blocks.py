@@ -73,3 +73,33 @@ def q8_0():
     b1[2:34] = 3
     out.append((b1, {int(k): v for k, v in g["blocks"][1]["expected"].items()}))
     return out
+
+
+def _b32(name, size, q_off, qh_off=None, m=False):
+    g = load(name)
+    f = g["fields"]
+    b = np.zeros(size, np.uint8)
+    b[0:2] = _f16(_hexbits(f["d_f16_bits"]))
+    if m:
+        b[2:4] = _f16(_hexbits(f["m_f16_bits"]))
+    if qh_off is not None:
+        b[qh_off:qh_off + 4] = f["qh"]
+    for i, v in f["qs_nonzero"].items():
+        b[q_off + int(i)] = v
+    return b, {int(k): v for k, v in g["expected"].items()}
+
+
+def q4_0():
+    return _b32("q4_0_block.json", 18, 2)
+
+
+def q4_1():
+    return _b32("q4_1_block.json", 20, 4, m=True)
+
+
+def q5_0():
+    return _b32("q5_0_block.json", 22, 6, qh_off=2)
+
+
+def q5_1():
+    return _b32("q5_1_block.json", 24, 8, qh_off=4, m=True)

@@ -97,3 +97,15 @@ def test_gemm_workspace_follows_the_tile_plan(lib):
         act(512, 4096) + _r256(72 * 2 * 256 * 128 * 4) + _r256(72 * 4)
     # 896 tiles: whole rounds only, no split
     assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 13, 14336, 4096, 2048) == act(2048, 4096)
+
+
+def test_auto_path_table(lib):
+    # the measured crossovers, by format and shape class (up to 8192 weight rows / more)
+    big, small = (14336, 4096), (4096, 4096)
+    want = {(12, 0): (9, 7), (13, 0): (9, 6), (14, 1): (8, 5), (14, 0): (4, 3),
+            (8, 0): (6, 2)}
+    for (qt, lay), (c_small, c_big) in want.items():
+        for (n, k), c in ((small, c_small), (big, c_big)):
+            first_fused = next(M for M in range(1, 12)
+                               if g.gguf_mm_auto_path(qt, lay, n, k, M, g.GGUF_DT_BF16) == g.GGUF_PATH_FUSED)
+            assert first_fused == min(c, 9), (qt, lay, n, k)

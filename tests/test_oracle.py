@@ -22,6 +22,15 @@ def test_hand_worked_kquant_blocks(builder, decoder):
         assert w[e] == v, (e, w[e], v)
 
 
+@pytest.mark.parametrize("builder,decoder", [
+    (gb.q4_0, O.dequant_q4_0), (gb.q4_1, O.dequant_q4_1), (gb.q5_0, O.dequant_q5_0), (gb.q5_1, O.dequant_q5_1)])
+def test_hand_worked_32_value_blocks(builder, decoder):
+    blk, expected = builder()
+    w = decoder(blk[None, :])[0]
+    for e, v in expected.items():
+        assert w[e] == v, (e, w[e], v)
+
+
 def test_hand_worked_q8_0_blocks():
     for blk, expected in gb.q8_0():
         w = O.dequant_q8_0(blk[None, :])[0]
@@ -53,19 +62,25 @@ def _set_f16(blk, off, val):
     blk[:, off:off + 2] = np.array([val], np.float16).view(np.uint8)
 
 
-@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_all_zero_blocks_decode_to_zero(qtype):
     w = O._DECODERS[qtype](_blocks_of(qtype, 0))
     assert np.all(w == 0)
 
 
 @pytest.mark.parametrize("qtype,value", [(O.Q4_K, 882.0), (O.Q5_K, 1890.0), (O.Q6_K, -31.0),
-                                         (O.Q8_0, -1.0)])
+                                         (O.Q8_0, -1.0), (O.Q4_0, 7.0), (O.Q4_1, 16.0), (O.Q5_0, 15.0),
+                                         (O.Q5_1, 32.0)])
 def test_all_max_bit_patterns(qtype, value):
-    # all quant/scale bytes 0xFF, d = dmin = 1: sc = m = 63 and q at its maximum
+    # all quant/scale bytes 0xFF, d = dmin = 1: sc = m = 63 and q at its maximum;
+    # 32-value formats: q = 15 (31 with the fifth bit), d = m = 1:
+    # (15 - 8), 15 + 1, (31 - 16), 31 + 1
     blk = _blocks_of(qtype, 0xFF)
-    if qtype == O.Q8_0:
+    if qtype in (O.Q8_0, O.Q4_0, O.Q5_0):
         _set_f16(blk, 0, 1.0)
+    elif qtype in (O.Q4_1, O.Q5_1):
+        _set_f16(blk, 0, 1.0)
+        _set_f16(blk, 2, 1.0)
     elif qtype == O.Q6_K:
         _set_f16(blk, 208, 1.0)
     else:
@@ -86,13 +101,14 @@ def test_q6k_zero_quants_give_minus_32_d_sc():
         assert np.array_equal(w[:, e], -32 * d * sc[:, e // 16])
 
 
-@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_scaling_d_by_power_of_two_scales_w(qtype):
     g = syn.rng(7)
     w = syn.weight_blocks(g, qtype, 2, 256)
     blk = w.reshape(-1, syn.BLOCK_BYTES[qtype]).copy()
     base = O._DECODERS[qtype](blk)
-    offs = {O.Q8_0: [0], O.Q4_K: [0, 2], O.Q5_K: [0, 2], O.Q6_K: [208]}[qtype]
+    offs = {O.Q8_0: [0], O.Q4_K: [0, 2], O.Q5_K: [0, 2], O.Q6_K: [208], O.Q4_0: [0], O.Q5_0: [0],
+            O.Q4_1: [0, 2], O.Q5_1: [0, 2]}[qtype]
     for off in offs:
         d = blk[:, off:off + 2].copy().view(np.float16)[:, 0]
         blk[:, off:off + 2] = (d * np.float16(4)).astype(np.float16).view(np.uint8).reshape(-1, 2)
@@ -113,7 +129,7 @@ def test_synthetic_blocks_follow_the_recipe():
 
 # ---------------------------------------------------------------- matmul vs exact rationals
 
-@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_matmul_exact_vs_fraction_brute_force(qtype):
     g = syn.rng(100 + qtype)
     N, K, M = 3, 256, 2
@@ -183,7 +199,7 @@ def test_act_quant_rounds_half_away_from_zero():
 
 # ---------------------------------------------------------------- int8 path reduces to the plain matmul
 
-@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_int8_path_equals_exact_when_activations_are_on_the_grid(qtype):
     # x = d_a * integers with amax = 127 * d_a in every block: quantization is
     # lossless, so the int8-path result must equal the exact matmul
@@ -200,7 +216,7 @@ def test_int8_path_equals_exact_when_activations_are_on_the_grid(qtype):
     assert np.max(np.abs(y8 - ref)) <= 1e-12 * np.max(np.abs(ref))
 
 
-@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_int8_path_close_to_exact_on_normal_data(qtype):
     # the activation rounding error is the only gap: RMS ~ amax/(127*sqrt(12)) per value
     g = syn.rng(60 + qtype)
@@ -213,7 +229,7 @@ def test_int8_path_close_to_exact_on_normal_data(qtype):
     assert np.max(np.abs(y8 - ref)) > 0
 
 
-@pytest.mark.parametrize("qtype", [O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_integer_terms_rebuild_the_decoded_weights(qtype):
     g = syn.rng(80 + qtype)
     N, K = 3, 512
@@ -403,3 +419,27 @@ def test_moe_decode_form_reduces_to_the_int8_gemv():
     assert np.array_equal(ys[1, 1], O.gemv_int8_path(w1, O.Q5_K, N, K, xs[1, 1][None, :])[0])
     ids[0, 1] = -1
     assert np.all(np.isnan(O.moe_mv_id_int8(wE, O.Q5_K, E, N, K, x, ids)[0, 1]))
+
+
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1])
+def test_32_value_codes_by_bit_addressing(qtype):
+    # element e's 4-bit code is bits 4*(e // 16) .. +3 of byte (e % 16) of the
+    # code field, its fifth bit is bit e of the little-endian 32-bit qh word:
+    # rebuilt here from unpacked bit arrays, compared with the decoders
+    g = syn.rng(123 + qtype)
+    blk = syn.weight_blocks(g, qtype, 4, 64).reshape(-1, syn.BLOCK_BYTES[qtype])
+    q_off = {O.Q4_0: 2, O.Q4_1: 4, O.Q5_0: 6, O.Q5_1: 8}[qtype]
+    bits = np.unpackbits(blk[:, q_off:q_off + 16], axis=1, bitorder="little").reshape(-1, 16, 8)
+    hbits = np.unpackbits(blk[:, q_off - 4:q_off], axis=1, bitorder="little") if qtype in (O.Q5_0, O.Q5_1) else None
+    d = O.f16_field(blk[:, 0:2])
+    m = O.f16_field(blk[:, 2:4]) if qtype in (O.Q4_1, O.Q5_1) else 0.0
+    w = O._DECODERS[qtype](blk)
+    for e in range(32):
+        lo = 4 * (e // 16)
+        q = np.zeros(blk.shape[0], np.int64)
+        for i in range(4):
+            q = q + (bits[:, e % 16, lo + i].astype(np.int64) << i)
+        if hbits is not None:
+            q = q + 16 * hbits[:, e].astype(np.int64)
+        want = {O.Q4_0: (q - 8) * d, O.Q5_0: (q - 16) * d}.get(qtype, q * d + m)
+        assert np.array_equal(w[:, e], want), e
