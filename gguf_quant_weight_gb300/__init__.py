@@ -15,6 +15,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libgguf_mm.so")
 
 # enums (same values as include/gguf_mm.h)
+GGUF_Q4_0, GGUF_Q4_1, GGUF_Q5_0, GGUF_Q5_1 = 2, 3, 6, 7
 GGUF_Q8_0, GGUF_Q4_K, GGUF_Q5_K, GGUF_Q6_K = 8, 12, 13, 14
 GGUF_LAYOUT_BLOCKS, GGUF_LAYOUT_Q6K_PLANES = 0, 1
 GGUF_DT_F32, GGUF_DT_F16, GGUF_DT_BF16 = 0, 1, 2
@@ -23,9 +24,12 @@ GGUF_OP_GEMV, GGUF_OP_GEMM, GGUF_OP_ID, GGUF_OP_DENSE = 0, 1, 2, 3
 GGUF_OK = 0
 GGUF_ERR_INVALID_ARG, GGUF_ERR_UNSUPPORTED, GGUF_ERR_MISALIGNED = -1, -2, -3
 GGUF_ERR_WORKSPACE, GGUF_ERR_CUDA, GGUF_ERR_TIMEOUT, GGUF_ERR_NO_DEVICE = -4, -5, -6, -7
+GGUF_ERR_IO, GGUF_ERR_FORMAT, GGUF_ERR_NOT_FOUND = -8, -9, -10
 
-BLOCK_VALUES = {GGUF_Q8_0: 32, GGUF_Q4_K: 256, GGUF_Q5_K: 256, GGUF_Q6_K: 256}
-BLOCK_BYTES = {GGUF_Q8_0: 34, GGUF_Q4_K: 144, GGUF_Q5_K: 176, GGUF_Q6_K: 210}
+BLOCK_VALUES = {GGUF_Q4_0: 32, GGUF_Q4_1: 32, GGUF_Q5_0: 32, GGUF_Q5_1: 32, GGUF_Q8_0: 32, GGUF_Q4_K: 256,
+                GGUF_Q5_K: 256, GGUF_Q6_K: 256}
+BLOCK_BYTES = {GGUF_Q4_0: 18, GGUF_Q4_1: 20, GGUF_Q5_0: 22, GGUF_Q5_1: 24, GGUF_Q8_0: 34, GGUF_Q4_K: 144,
+               GGUF_Q5_K: 176, GGUF_Q6_K: 210}
 
 _c_i64, _c_int, _c_sz, _c_vp = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
 
@@ -56,6 +60,25 @@ _SIGS = {
     "gguf_mm_auto_path": (_c_int, [_c_int, _c_int, _c_i64, _c_i64, _c_i64, _c_int]),
     "gguf_mm_debug_moe_route": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp]),
     "gguf_mm_debug_timeout": (_c_int, [_c_i64, _c_vp]),
+    "gguf_file_open": (_c_int, [ctypes.c_char_p, ctypes.POINTER(_c_vp)]),
+    "gguf_file_close": (None, [_c_vp]),
+    "gguf_file_version": (_c_int, [_c_vp]),
+    "gguf_file_alignment": (_c_i64, [_c_vp]),
+    "gguf_file_tensor_count": (_c_i64, [_c_vp]),
+    "gguf_file_tensor_info": (_c_int, [_c_vp, _c_i64, ctypes.c_char_p, _c_sz, ctypes.POINTER(_c_int),
+                                       ctypes.POINTER(_c_int), ctypes.POINTER(_c_i64),
+                                       ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]),
+    "gguf_file_find_tensor": (_c_i64, [_c_vp, ctypes.c_char_p]),
+    "gguf_file_read_tensor": (_c_int, [_c_vp, _c_i64, _c_vp, _c_sz]),
+    "gguf_file_tensor_as_weight": (_c_int, [_c_vp, _c_i64, ctypes.POINTER(_c_int), ctypes.POINTER(_c_i64),
+                                            ctypes.POINTER(_c_i64)]),
+    "gguf_file_kv_count": (_c_i64, [_c_vp]),
+    "gguf_file_kv_key": (_c_int, [_c_vp, _c_i64, ctypes.c_char_p, _c_sz, ctypes.POINTER(_c_int)]),
+    "gguf_file_get_int": (_c_int, [_c_vp, ctypes.c_char_p, ctypes.POINTER(_c_i64)]),
+    "gguf_file_get_float": (_c_int, [_c_vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_double)]),
+    "gguf_file_get_string": (_c_int, [_c_vp, ctypes.c_char_p, ctypes.c_char_p, _c_sz, ctypes.POINTER(_c_sz)]),
+    "gguf_file_get_array": (_c_int, [_c_vp, ctypes.c_char_p, ctypes.POINTER(_c_int), ctypes.POINTER(_c_i64),
+                                     _c_vp, _c_sz]),
 }
 
 _lib = None
@@ -203,6 +226,147 @@ def gguf_mm_debug_moe_route(ids, entries, n_expert, offsets, ntiles, tiles, max_
 
 def gguf_mm_debug_timeout(spin_limit, stream=None):
     return _check("gguf_mm_debug_timeout", load_library().gguf_mm_debug_timeout(spin_limit, _s(stream)))
+
+
+# --- GGUF container reader (host only) ---------------------------------------
+
+def _enc(s):
+    return s.encode("utf-8", "surrogateescape")
+
+
+def _dec(b):
+    return b.decode("utf-8", "surrogateescape")
+
+
+class GGUFFile:
+    """A .gguf file opened through gguf_file_open: metadata values and tensor bytes.
+
+    Thin marshalling over the gguf_file_* entry points; the parsing and every
+    bounds check are in the library.  `tensors()` lists (name, type, dims);
+    `tensor_bytes(name)` returns the tensor's bytes as a numpy u8 array, which
+    for a block-quantized weight W[N, K] is the [N, K/blk*bb] block array the
+    matmul entry points take."""
+
+    def __init__(self, path):
+        self._h = None
+        lib = load_library()
+        h = _c_vp()
+        _check("gguf_file_open", lib.gguf_file_open(os.fsencode(path), ctypes.byref(h)))
+        self._h = h.value
+        self._lib = lib
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.gguf_file_close(self._h)
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        self.close()
+
+    @property
+    def version(self) -> int:
+        return self._lib.gguf_file_version(self._h)
+
+    @property
+    def alignment(self) -> int:
+        return self._lib.gguf_file_alignment(self._h)
+
+    def tensor_info(self, index):
+        """(name, type, dims (contiguous first), absolute data offset, nbytes)."""
+        n = 1024
+        while True:
+            name = ctypes.create_string_buffer(n)
+            t, nd = _c_int(), _c_int()
+            dims = (_c_i64 * 4)()
+            off, nb = ctypes.c_uint64(), ctypes.c_uint64()
+            st = self._lib.gguf_file_tensor_info(self._h, index, name, n, ctypes.byref(t), ctypes.byref(nd), dims,
+                                                 ctypes.byref(off), ctypes.byref(nb))
+            if st == GGUF_ERR_WORKSPACE:
+                n *= 16
+                continue
+            _check("gguf_file_tensor_info", st)
+            return _dec(name.value), t.value, tuple(dims[:nd.value]), off.value, nb.value
+
+    def tensors(self):
+        return [self.tensor_info(i)[:3] for i in range(self._lib.gguf_file_tensor_count(self._h))]
+
+    def find_tensor(self, name) -> int:
+        i = self._lib.gguf_file_find_tensor(self._h, _enc(name))
+        if i < 0:
+            raise GGUFError("gguf_file_find_tensor", int(i))
+        return int(i)
+
+    def tensor_bytes(self, name_or_index):
+        import numpy as np
+        i = self.find_tensor(name_or_index) if isinstance(name_or_index, str) else name_or_index
+        nb = self.tensor_info(i)[4]
+        out = np.empty(nb, np.uint8)
+        _check("gguf_file_read_tensor", self._lib.gguf_file_read_tensor(self._h, i, out.ctypes.data, nb))
+        return out
+
+    def weight(self, name):
+        """(blocks as a [N, row_bytes] u8 array, qtype, N, K) of a 2-D block-quantized tensor."""
+        i = self.find_tensor(name)
+        qt, n, k = _c_int(), _c_i64(), _c_i64()
+        _check("gguf_file_tensor_as_weight", self._lib.gguf_file_tensor_as_weight(
+            self._h, i, ctypes.byref(qt), ctypes.byref(n), ctypes.byref(k)))
+        return self.tensor_bytes(i).reshape(n.value, -1), qt.value, n.value, k.value
+
+    def keys(self):
+        out = []
+        for i in range(self._lib.gguf_file_kv_count(self._h)):
+            n = 256
+            while True:
+                buf, vt = ctypes.create_string_buffer(n), _c_int()
+                st = self._lib.gguf_file_kv_key(self._h, i, buf, n, ctypes.byref(vt))
+                if st == GGUF_ERR_WORKSPACE:
+                    n *= 16
+                    continue
+                _check("gguf_file_kv_key", st)
+                out.append((_dec(buf.value), vt.value))
+                break
+        return out
+
+    def get_int(self, key) -> int:
+        v = _c_i64()
+        _check("gguf_file_get_int", self._lib.gguf_file_get_int(self._h, _enc(key), ctypes.byref(v)))
+        return v.value
+
+    def get_float(self, key) -> float:
+        v = ctypes.c_double()
+        _check("gguf_file_get_float", self._lib.gguf_file_get_float(self._h, _enc(key), ctypes.byref(v)))
+        return v.value
+
+    def get_string(self, key) -> str:
+        n = _c_sz()
+        _check("gguf_file_get_string", self._lib.gguf_file_get_string(self._h, _enc(key), None, 0,
+                                                                      ctypes.byref(n)))
+        buf = ctypes.create_string_buffer(n.value + 1)
+        _check("gguf_file_get_string", self._lib.gguf_file_get_string(self._h, _enc(key), buf, n.value + 1,
+                                                                      None))
+        return _dec(buf.raw[:n.value])
+
+    _ARRAY_NP = {0: "u1", 1: "i1", 2: "<u2", 3: "<i2", 4: "<u4", 5: "<i4", 6: "<f4", 7: "u1", 10: "<u8",
+                 11: "<i8", 12: "<f8"}
+
+    def get_array(self, key):
+        """A scalar array as numpy; a string array as (8, count)."""
+        import numpy as np
+        et, cnt = _c_int(), _c_i64()
+        _check("gguf_file_get_array", self._lib.gguf_file_get_array(self._h, _enc(key), ctypes.byref(et),
+                                                                    ctypes.byref(cnt), None, 0))
+        if et.value not in self._ARRAY_NP:
+            return et.value, cnt.value
+        out = np.empty(cnt.value, self._ARRAY_NP[et.value])
+        _check("gguf_file_get_array", self._lib.gguf_file_get_array(self._h, _enc(key), None, None,
+                                                                    out.ctypes.data, out.nbytes))
+        return out
 
 
 def raw_status(fn_name: str, *args) -> int:

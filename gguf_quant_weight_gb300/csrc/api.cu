@@ -70,7 +70,10 @@ bool pdl_enabled() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-bool valid_qtype(int t) { return t == GGUF_Q8_0 || t == GGUF_Q4_K || t == GGUF_Q5_K || t == GGUF_Q6_K; }
+bool valid_qtype(int t) {
+    return t == GGUF_Q4_0 || t == GGUF_Q4_1 || t == GGUF_Q5_0 || t == GGUF_Q5_1 || t == GGUF_Q8_0 || t == GGUF_Q4_K ||
+           t == GGUF_Q5_K || t == GGUF_Q6_K;
+}
 bool valid_dtype(int d) { return d == GGUF_DT_F32 || d == GGUF_DT_F16 || d == GGUF_DT_BF16; }
 
 // Shared checks of the weight / shape / pointer arguments.
@@ -195,6 +198,9 @@ const char* gguf_mm_status_string(int status) {
         case GGUF_ERR_CUDA: return "CUDA error";
         case GGUF_ERR_TIMEOUT: return "bounded device wait expired";
         case GGUF_ERR_NO_DEVICE: return "no sm_103 device current";
+        case GGUF_ERR_IO: return "file cannot be opened or mapped";
+        case GGUF_ERR_FORMAT: return "not a well-formed GGUF v2/v3 file";
+        case GGUF_ERR_NOT_FOUND: return "no tensor or key of that name";
         default: return "unknown status";
     }
 }

@@ -66,6 +66,10 @@ cudaError_t go(const void* w, int64_t N, int64_t K, int64_t ld, void* out, int o
 cudaError_t dequant_padded_launch(const void* w, int qtype, int layout, int64_t N, int64_t K, void* out, int odt,
                                   int64_t ld, int num_sms, cudaStream_t s) {
     switch (qtype) {
+        case GGUF_Q4_0: return go<GGUF_Q4_0, false>(w, N, K, ld, out, odt, num_sms, s);
+        case GGUF_Q4_1: return go<GGUF_Q4_1, false>(w, N, K, ld, out, odt, num_sms, s);
+        case GGUF_Q5_0: return go<GGUF_Q5_0, false>(w, N, K, ld, out, odt, num_sms, s);
+        case GGUF_Q5_1: return go<GGUF_Q5_1, false>(w, N, K, ld, out, odt, num_sms, s);
         case GGUF_Q8_0: return go<GGUF_Q8_0, false>(w, N, K, ld, out, odt, num_sms, s);
         case GGUF_Q4_K: return go<GGUF_Q4_K, false>(w, N, K, ld, out, odt, num_sms, s);
         case GGUF_Q5_K: return go<GGUF_Q5_K, false>(w, N, K, ld, out, odt, num_sms, s);

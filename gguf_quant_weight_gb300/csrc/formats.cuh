@@ -2,6 +2,13 @@
 // on-disk layout (GGUF Support Proposal for mobius, section 7 "Quantization
 // Format Deep Dive" and the 1.2 type table; OpenVINO PR #39119 "Transformation"
 // for the Q6_K fields):
+//   Q4_0  {d f16, qs[16]}                                    w = (q - 8)*d
+//   Q4_1  {d, m f16, qs[16]}                                 w = q*d + m
+//   Q5_0  {d f16, qh[4], qs[16]}                             w = (q5 - 16)*d
+//   Q5_1  {d, m f16, qh[4], qs[16]}                          w = q5*d + m
+//         (32 values; element e < 16 is the low nibble of qs[e], e >= 16 the
+//         high nibble of qs[e - 16]; bit e of the little-endian qh word is the
+//         fifth bit of element e)
 //   Q8_0  {d f16, qs[32] i8}                                 w = d*q
 //   Q4_K  {d, dmin f16, scales[12], qs[128]}                 w = d*sc_j*q - dmin*m_j
 //   Q5_K  {d, dmin f16, scales[12], qh[32], qs[128]}         w = d*sc_j*q5 - dmin*m_j
@@ -13,10 +20,22 @@
 
 namespace gg {
 
-__host__ __device__ constexpr int block_values(int qt) { return qt == GGUF_Q8_0 ? 32 : 256; }
-__host__ __device__ constexpr int block_bytes(int qt) {
-    return qt == GGUF_Q8_0 ? 34 : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176 : 210;
+__host__ __device__ constexpr bool block32(int qt) {
+    return qt == GGUF_Q4_0 || qt == GGUF_Q4_1 || qt == GGUF_Q5_0 || qt == GGUF_Q5_1 || qt == GGUF_Q8_0;
 }
+__host__ __device__ constexpr int block_values(int qt) { return block32(qt) ? 32 : 256; }
+__host__ __device__ constexpr int block_bytes(int qt) {
+    return qt == GGUF_Q4_0 ? 18 : qt == GGUF_Q4_1 ? 20 : qt == GGUF_Q5_0 ? 22 : qt == GGUF_Q5_1 ? 24
+         : qt == GGUF_Q8_0 ? 34 : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176 : 210;
+}
+// byte offset of the 16 code bytes inside a 32-value Q4/Q5 block (the qh word precedes them)
+__host__ __device__ constexpr int b32_qs_offset(int qt) {
+    return qt == GGUF_Q4_0 ? 2 : qt == GGUF_Q4_1 ? 4 : qt == GGUF_Q5_0 ? 6 : 8;
+}
+__host__ __device__ constexpr bool b32_has_min(int qt) { return qt == GGUF_Q4_1 || qt == GGUF_Q5_1; }
+__host__ __device__ constexpr bool b32_has_qh(int qt) { return qt == GGUF_Q5_0 || qt == GGUF_Q5_1; }
+// the implicit zero point of the symmetric formats
+__host__ __device__ constexpr int b32_zero_point(int qt) { return qt == GGUF_Q4_0 ? 8 : qt == GGUF_Q5_0 ? 16 : 0; }
 
 __device__ __forceinline__ float ld_f16_bytes(const uint8_t* p) {
     return f16_bits_to_float((uint32_t)p[0] | ((uint32_t)p[1] << 8));
@@ -66,7 +85,19 @@ __device__ __forceinline__ float sub_round_odd(float a, float b) {
 // the output type is the correct rounding of the exact weight.
 template <int QT>
 __device__ __forceinline__ float decode_elem(const uint8_t* blk, int e) {
-    if (QT == GGUF_Q8_0) {
+    if constexpr (QT == GGUF_Q4_0 || QT == GGUF_Q4_1 || QT == GGUF_Q5_0 || QT == GGUF_Q5_1) {
+        const uint8_t* qs = blk + b32_qs_offset(QT);
+        int q = (e < 16) ? (qs[e] & 15) : (qs[e - 16] >> 4);
+        if (b32_has_qh(QT)) {
+            const uint8_t* qh = qs - 4;
+            q += 16 * ((qh[e >> 3] >> (e & 7)) & 1);
+        }
+        const float d = ld_f16_bytes(blk);
+        // d*(q - zp) and q*d are exact in f32; q*d + m is rounded to odd, so the
+        // one rounding to the output type is the correct rounding of the weight
+        if (b32_has_min(QT)) return sub_round_odd(d * (float)q, -ld_f16_bytes(blk + 2));
+        return d * (float)(q - b32_zero_point(QT));
+    } else if (QT == GGUF_Q8_0) {
         return ld_f16_bytes(blk) * (float)static_cast<int8_t>(blk[2 + e]);
     } else if (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
         const float d = ld_f16_bytes(blk), dmin = ld_f16_bytes(blk + 2);

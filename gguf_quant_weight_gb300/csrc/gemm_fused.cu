@@ -64,7 +64,7 @@ __host__ __device__ constexpr int fused_threads(int qt, int layout, int bn) {
 
 __host__ __device__ constexpr int raw_pitch(int qt, int layout) {
     // bytes per weight row in one raw slot (= the TMA box's inner extent)
-    return qt == GGUF_Q8_0 ? 272 : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176 : (layout ? 0 : 224);
+    return block32(qt) ? 8 * block_bytes(qt) : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176 : (layout ? 0 : 224);
 }
 // bytes of one raw slot (128 rows); the Q6_K planes slot is QL | QH | SC | D
 __host__ __device__ constexpr int raw_slot_bytes(int qt, int layout) {
@@ -309,11 +309,52 @@ __device__ __forceinline__ void q8_block(uint32_t row, uint32_t& d_bits, uint32_
     for (int i = 0; i < 8; ++i) q4[i] = (T & 2) ? __funnelshift_r(w[T / 4 + i], w[T / 4 + i + 1], 16) : w[T / 4 + i];
 }
 
+// Block J (0..7) of a raw row of eight 32-value Q4_0 / Q4_1 / Q5_0 / Q5_1
+// blocks (8 * BB bytes, a multiple of 16): the f16 bits of d (and m), and the
+// 32 codes as 8 words in element order (low nibbles of the 16 code bytes for
+// elements 0..15, high nibbles for 16..31, the fifth bit from qh at bit 4).
+// The blocks sit at 2-byte alignment: the 16-byte pieces covering the block
+// (never past the row's end) are read and words cut out with funnel shifts.
+template <int QT, int J>
+__device__ __forceinline__ void b32_block(uint32_t row, uint32_t& d_bits, uint32_t& m_bits, uint32_t q4[8]) {
+    constexpr int BB = block_bytes(QT), S0 = BB * J, B = S0 & ~15, NP = (S0 + BB - B + 15) / 16;
+    static_assert(NP <= 3 && B + 16 * NP <= 8 * BB, "pieces stay inside the row");
+    uint32_t w[12];
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+        const uint4 c = lds128u(row + B + 16 * k);
+        w[4 * k] = c.x; w[4 * k + 1] = c.y; w[4 * k + 2] = c.z; w[4 * k + 3] = c.w;
+    }
+    auto half_at = [&](int off) -> uint32_t {   // 16 bits at byte S0 + off
+        const int a = S0 + off - B;
+        return (a & 2) ? (w[a / 4] >> 16) : (w[a / 4] & 0xFFFFu);
+    };
+    auto word_at = [&](int off) -> uint32_t {   // 32 bits at byte S0 + off (2-byte aligned)
+        const int a = S0 + off - B;
+        return (a & 2) ? __funnelshift_r(w[a / 4], w[a / 4 + 1], 16) : w[a / 4];
+    };
+    d_bits = half_at(0);
+    m_bits = b32_has_min(QT) ? half_at(2) : 0u;
+    constexpr int QO = b32_qs_offset(QT);
+    uint32_t qh = 0;
+    if constexpr (b32_has_qh(QT)) qh = word_at(QO - 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t q = word_at(QO + 4 * i);
+        q4[i] = q & 0x0F0F0F0Fu;
+        q4[4 + i] = (q >> 4) & 0x0F0F0F0Fu;
+        if constexpr (b32_has_qh(QT)) {
+            q4[i] |= (((qh >> (4 * i)) & 0xFu) * 0x00204081u & 0x01010101u) << 4;
+            q4[4 + i] |= (((qh >> (16 + 4 * i)) & 0xFu) * 0x00204081u & 0x01010101u) << 4;
+        }
+    }
+}
+
 // Decode values 32*hf .. 32*hf+31 of k step q (values 64q .. 64q+63 of the
 // super-block) of one weight row whose raw bytes start at shared address `row`.
 template <int QT, int LAYOUT>
 __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int q, int hf, int kb, uint4 out[4]) {
-    static_assert(QT == GGUF_Q8_0 || (QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_BLOCKS),
+    static_assert(block32(QT) || (QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_BLOCKS),
                   "the other layouts decode from a per-super-block state");
     (void)slot; (void)r; (void)kb;
     const __half2 zero2 = __float2half2_rn(0.f);
@@ -334,6 +375,23 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
 #pragma unroll
         for (int i = 0; i < 8; ++i) q4[i] ^= 0x80808080u;
         emit32_h(q4, __float2half2_rn(1152.f), d2, zero2, d2, zero2, out);
+    } else if constexpr (block32(QT)) {
+        // codes 0..15 (0..31 with the fifth bit): w = (q - zp) * d, or q * d + m
+        // (one fused multiply-add, one rounding of the exact value)
+        uint32_t db, mb, q4[8];
+        switch (2 * q + hf) {
+            case 0: b32_block<QT, 0>(row, db, mb, q4); break;
+            case 1: b32_block<QT, 1>(row, db, mb, q4); break;
+            case 2: b32_block<QT, 2>(row, db, mb, q4); break;
+            case 3: b32_block<QT, 3>(row, db, mb, q4); break;
+            case 4: b32_block<QT, 4>(row, db, mb, q4); break;
+            case 5: b32_block<QT, 5>(row, db, mb, q4); break;
+            case 6: b32_block<QT, 6>(row, db, mb, q4); break;
+            default: b32_block<QT, 7>(row, db, mb, q4); break;
+        }
+        const __half2 d2 = h2_bits(db * 0x10001u);
+        const __half2 noff = b32_has_min(QT) ? __hneg2(h2_bits(mb * 0x10001u)) : zero2;   // emit subtracts the offset
+        emit32_h(q4, __float2half2_rn(1024.f + (float)b32_zero_point(QT)), d2, noff, d2, noff, out);
     } else {
         // raw Q6_K: values 64q + 32hf + l = 128h + 32g + l with h = q/2, g = 2(q%2) + hf
         const int h = q >> 1, g = 2 * (q & 1) + hf;
@@ -783,7 +841,7 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
                             reinterpret_cast<uint32_t*>(tickets), tickets ? ntiles : 0) != cudaSuccess)
         return GGUF_ERR_CUDA;
 
-    const int bb = block_bytes(qtype) * (qtype == GGUF_Q8_0 ? 8 : 1);   // bytes of one 256-value column
+    const int bb = block_bytes(qtype) * (block32(qtype) ? 8 : 1);   // bytes of one 256-value column
     const int64_t rb = KB * bb;
     CUtensorMap tw[4];
     std::memset(tw, 0, sizeof(tw));
@@ -818,6 +876,10 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
                    (int)pl.n_full, (int)ceil_div(N, 128), xscale};
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {
+        case GGUF_Q4_0: e = launch_bn<GGUF_Q4_0, 0>(bn, tw, tb, fp, stream); break;
+        case GGUF_Q4_1: e = launch_bn<GGUF_Q4_1, 0>(bn, tw, tb, fp, stream); break;
+        case GGUF_Q5_0: e = launch_bn<GGUF_Q5_0, 0>(bn, tw, tb, fp, stream); break;
+        case GGUF_Q5_1: e = launch_bn<GGUF_Q5_1, 0>(bn, tw, tb, fp, stream); break;
         case GGUF_Q8_0: e = launch_bn<GGUF_Q8_0, 0>(bn, tw, tb, fp, stream); break;
         case GGUF_Q4_K: e = launch_bn<GGUF_Q4_K, 0>(bn, tw, tb, fp, stream); break;
         case GGUF_Q5_K: e = launch_bn<GGUF_Q5_K, 0>(bn, tw, tb, fp, stream); break;
@@ -836,7 +898,7 @@ int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t
     const int64_t KB = K / 256;
     if (qtype == GGUF_Q6_K && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;   // 16-byte row strides for TMA
     if (max_tiles > 65535 || KB > (1 << 20)) return GGUF_ERR_UNSUPPORTED;
-    const int bb = block_bytes(qtype) * (qtype == GGUF_Q8_0 ? 8 : 1);
+    const int bb = block_bytes(qtype) * (block32(qtype) ? 8 : 1);
     const int64_t rb = KB * bb;
     CUtensorMap tw[4];
     std::memset(tw, 0, sizeof(tw));
@@ -858,6 +920,10 @@ int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t
     const int gy = (int)max_tiles;
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {
+        case GGUF_Q4_0: e = launch_fused<GGUF_Q4_0, 0, 128, true>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q4_1: e = launch_fused<GGUF_Q4_1, 0, 128, true>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q5_0: e = launch_fused<GGUF_Q5_0, 0, 128, true>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q5_1: e = launch_fused<GGUF_Q5_1, 0, 128, true>(tw, tb, fp, stream, gy); break;
         case GGUF_Q8_0: e = launch_fused<GGUF_Q8_0, 0, 128, true>(tw, tb, fp, stream, gy); break;
         case GGUF_Q4_K: e = launch_fused<GGUF_Q4_K, 0, 128, true>(tw, tb, fp, stream, gy); break;
         case GGUF_Q5_K: e = launch_fused<GGUF_Q5_K, 0, 128, true>(tw, tb, fp, stream, gy); break;

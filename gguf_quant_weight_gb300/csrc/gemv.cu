@@ -22,6 +22,7 @@
 //    activation block, a (segmented) warp-shuffle reduction, and the residual
 //    Add fused into the store.
 #include "common.cuh"
+#include "formats.cuh"
 #include "gemv.cuh"
 #include <type_traits>
 
@@ -592,6 +593,59 @@ __device__ __forceinline__ void unit_q8_0(const GemvParams& p, uint32_t blk, con
     }
 }
 
+// ------------------------------------------------------------------ Q4_0 / Q4_1 / Q5_0 / Q5_1 unit (from shared memory)
+// One 32-value block at the 2-byte-aligned shared address blk.  The codes are
+// dotted unsigned (0..15, or 0..31 with the fifth bit); the formats' zero
+// point and min are applied through the activation block's code sum s:
+//   Q4_0: D = sum (q - 8) qa = sum q qa - 8 s      y += d * d_a * D
+//   Q5_0: D = sum (q5 - 16) qa = sum q5 qa - 16 s  y += d * d_a * D
+//   Q4_1 / Q5_1: D = sum q qa                      y += d * d_a * D + m * d_a * s
+// Four bits of the qh word are spread to bit 4 of four bytes with one multiply
+// (b * 0x00204081 puts bit i of b at bit 8i + i ... then a mask).
+__device__ __forceinline__ uint32_t spread4_to_bit4(uint32_t b) {
+    return ((b & 0xFu) * 0x00204081u & 0x01010101u) << 4;
+}
+template <int QT, int MT, class A, bool DUMP>
+__device__ __forceinline__ void unit_b32(const GemvParams& p, uint32_t blk, const A& a, int b, float acc[MT],
+                                         int64_t n) {
+    const float d = f16_bits_to_float(lds16(blk));
+    const float mval = b32_has_min(QT) ? f16_bits_to_float(lds16(blk + 2)) : 0.f;
+    const uint32_t qs = blk + b32_qs_offset(QT);
+    uint32_t lo[4], hi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t w = lds16(qs + 4 * i) | (lds16(qs + 4 * i + 2) << 16);
+        lo[i] = w & 0x0F0F0F0Fu;
+        hi[i] = (w >> 4) & 0x0F0F0F0Fu;
+    }
+    if constexpr (b32_has_qh(QT)) {
+        const uint32_t qh = lds16(qs - 4) | (lds16(qs - 2) << 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            lo[i] |= spread4_to_bit4(qh >> (4 * i));
+            hi[i] |= spread4_to_bit4(qh >> (16 + 4 * i));
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (m < p.M) {
+            const uint4 c0 = a.codes(m, 0), c1 = a.codes(m, 1);
+            int Da = 0, Db = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                Da = dp4a(lo[i], comp(c0, i), Da);
+                Db = dp4a(hi[i], comp(c1, i), Db);
+            }
+            const uint4 e = a.entry(m, 0);
+            int D = Da + Db;
+            if (b32_zero_point(QT)) D -= b32_zero_point(QT) * (int)(e.z + e.w);
+            acc[m] += d * (__uint_as_float(e.x) * i2f(D));
+            if (b32_has_min(QT)) acc[m] += mval * __uint_as_float(e.y);
+            if (DUMP && p.dbg_D) dump_D(p, m, n, b, 32, D);
+        }
+    }
+}
+
 // Q6_K fragment of half h from a 2-byte-aligned raw block in shared memory.
 __device__ __forceinline__ void frag_q6_from_smem(FragQ6& f, uint32_t blk, int h) {
     auto w32 = [&](uint32_t a) { return lds16(a) | (lds16(a + 2) << 16); };
@@ -650,9 +704,10 @@ template <int QT, int MT, int LAYOUT, bool REG, bool DUMP>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
     constexpr int NT = kThreads, NW = NT / 32;
     constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
-    constexpr int NQ = QT == GGUF_Q8_0 ? 2 : 8, NE = QT == GGUF_Q8_0 ? 1 : 4;
-    constexpr int UV = QT == GGUF_Q8_0 ? 32 : 128;   // values per unit
-    constexpr int bb = QT == GGUF_Q8_0 ? 34 : QT == GGUF_Q4_K ? 144 : QT == GGUF_Q5_K ? 176 : 210;
+    constexpr bool B32 = block32(QT);                 // 32-value blocks: a unit is one block
+    constexpr int NQ = B32 ? 2 : 8, NE = B32 ? 1 : 4;
+    constexpr int UV = B32 ? 32 : 128;                // values per unit
+    constexpr int bb = block_bytes(QT);
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nb = (int)(p.K / 32);
@@ -760,6 +815,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
                 if constexpr (QT == GGUF_Q8_0) {
                     if (single_unit) unit_q8_0<MT, decltype(act), DUMP>(p, rowp + 34u * u, act, u, acc, n);
                     else unit_q8_0<MT, decltype(as), DUMP>(p, rowp + 34u * u, as, u, acc, n);
+                } else if constexpr (B32) {
+                    if (single_unit) unit_b32<QT, MT, decltype(act), DUMP>(p, rowp + (uint32_t)bb * u, act, u, acc, n);
+                    else unit_b32<QT, MT, decltype(as), DUMP>(p, rowp + (uint32_t)bb * u, as, u, acc, n);
                 } else if constexpr (QT == GGUF_Q6_K) {
                     FragQ6 f;
                     if constexpr (PLANES) {
@@ -1608,7 +1666,7 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
 
 template <int QT, int MT, int LAYOUT, bool DUMP>
 cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t stream) {
-    const int U = (int)(p.K / (QT == GGUF_Q8_0 ? 32 : 128));
+    const int U = (int)(p.K / (block32(QT) ? 32 : 128));
     auto k = gemv_kernel<QT, MT, LAYOUT, false, DUMP>;
     if constexpr (MT == 1) {
         if (U <= 32) k = gemv_kernel<QT, MT, LAYOUT, true, DUMP>;
@@ -1663,6 +1721,10 @@ cudaError_t launch_mt(const GemvParams& p, int grid, size_t smem, cudaStream_t s
 template <bool DUMP>
 cudaError_t launch_dispatch(const GemvParams& p, int grid, size_t smem, cudaStream_t s) {
     switch (p.qtype) {
+        case GGUF_Q4_0: return launch_mt<GGUF_Q4_0, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
+        case GGUF_Q4_1: return launch_mt<GGUF_Q4_1, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
+        case GGUF_Q5_0: return launch_mt<GGUF_Q5_0, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
+        case GGUF_Q5_1: return launch_mt<GGUF_Q5_1, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
         case GGUF_Q8_0: return launch_mt<GGUF_Q8_0, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
         case GGUF_Q4_K: return launch_mt<GGUF_Q4_K, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
         case GGUF_Q5_K: return launch_mt<GGUF_Q5_K, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
@@ -1809,11 +1871,11 @@ __global__ void __launch_bounds__(kMvThreads) moe_mv_kernel(const MoeMvParams mp
 }  // namespace
 
 int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem) {
-    const int bv = p.qtype == GGUF_Q8_0 ? 32 : 256;
-    const int bb = p.qtype == GGUF_Q8_0 ? 34 : p.qtype == GGUF_Q4_K ? 144 : p.qtype == GGUF_Q5_K ? 176 : 210;
+    const int bv = block_values(p.qtype);
+    const int bb = block_bytes(p.qtype);
     p.rb = p.K / bv * bb;
     const int64_t act = act_image_bytes(p.M, p.K);
-    const int U = (int)(p.K / (p.qtype == GGUF_Q8_0 ? 32 : 128));
+    const int U = (int)(p.K / (block32(p.qtype) ? 32 : 128));
     const int64_t P = U < 32 ? 32 / U : 1;
     const int NW = kThreads / 32;
     // a slot holds one row group plus 16-byte alignment slack (the D plane

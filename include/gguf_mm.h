@@ -17,7 +17,12 @@
  *    blocks covering W[n, 0..K) back to back, i.e. a [N, K/blk*block_bytes] u8
  *    array (OpenVINO PR #39119 "FullyConnectedGGUF", "Why a new primitive").
  *  - Block structs (GGUF on-disk layout; GGUF Support Proposal for mobius,
- *    sections 1.2 and 7): Q8_0 34 B / 32 values {d f16, qs[32] i8}, w = d*q;
+ *    sections 1.2 and 7): Q4_0 18 B / 32 values {d f16, qs[16]}, w = (q-8)*d;
+ *    Q4_1 20 B {d, m f16, qs[16]}, w = q*d + m; Q5_0 22 B {d, qh[4], qs[16]},
+ *    w = (q5-16)*d; Q5_1 24 B {d, m, qh[4], qs[16]}, w = q5*d + m (element
+ *    e < 16 in the low nibble of qs[e], e >= 16 in the high nibble of
+ *    qs[e-16], its fifth bit bit e of the little-endian qh word);
+ *    Q8_0 34 B / 32 values {d f16, qs[32] i8}, w = d*q;
  *    Q4_K 144 B / 256 {d, dmin f16, scales[12], qs[128]}; Q5_K 176 B / 256
  *    {d, dmin, scales[12], qh[32], qs[128]}; for both w = d*sc_j*q - dmin*m_j
  *    (OpenVINO PR #38696 "Details"); Q6_K 210 B / 256 {ql[128], qh[64],
@@ -41,7 +46,13 @@ extern "C" {
 
 typedef struct CUstream_st* gguf_stream_t; /* same type as cudaStream_t */
 
-typedef enum { GGUF_Q8_0 = 8, GGUF_Q4_K = 12, GGUF_Q5_K = 13, GGUF_Q6_K = 14 } gguf_qtype;
+/* GGUF type ids.  Q4_0 / Q4_1 / Q5_0 / Q5_1 / Q8_0 hold 32 values per block,
+ * the K-quants 256 (GGUF Support Proposal for mobius, 1.2 "Quantization
+ * Types"). */
+typedef enum {
+    GGUF_Q4_0 = 2, GGUF_Q4_1 = 3, GGUF_Q5_0 = 6, GGUF_Q5_1 = 7,
+    GGUF_Q8_0 = 8, GGUF_Q4_K = 12, GGUF_Q5_K = 13, GGUF_Q6_K = 14
+} gguf_qtype;
 
 /* GGUF_LAYOUT_Q6K_PLANES: the Q6_K tensor regrouped once into
  * QL[nblk][128] | QH[nblk][64] | SC[nblk][16] | D[nblk] (2 bytes each), same
@@ -65,7 +76,10 @@ typedef enum {
     GGUF_ERR_WORKSPACE = -4,    /* workspace missing or smaller than gguf_mm_workspace_size() */
     GGUF_ERR_CUDA = -5,         /* a CUDA runtime call or kernel launch failed */
     GGUF_ERR_TIMEOUT = -6,      /* a bounded device-side wait expired (reported by check_errors) */
-    GGUF_ERR_NO_DEVICE = -7     /* no sm_103 device current */
+    GGUF_ERR_NO_DEVICE = -7,    /* no sm_103 device current */
+    GGUF_ERR_IO = -8,           /* gguf_file_*: the file cannot be opened, read or mapped */
+    GGUF_ERR_FORMAT = -9,       /* gguf_file_*: not a GGUF v2/v3 file, or a field runs past its end */
+    GGUF_ERR_NOT_FOUND = -10    /* gguf_file_*: no tensor or key of that name */
 } gguf_status;
 
 typedef enum { GGUF_OP_GEMV = 0, GGUF_OP_GEMM = 1, GGUF_OP_ID = 2, GGUF_OP_DENSE = 3 } gguf_op;
@@ -265,6 +279,72 @@ int gguf_mm_debug_moe_route(const int32_t* ids, int64_t entries, int64_t n_exper
  * records GGUF_ERR_TIMEOUT in the device status word (read it with
  * gguf_mm_check_errors).  No GPU fault is involved. */
 int gguf_mm_debug_timeout(int64_t spin_limit, gguf_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * GGUF container reader (host only: no device memory, no CUDA call)
+ *
+ * A .gguf file holds the model's metadata as key-value pairs and its tensors,
+ * each with its own type (GGUF Support Proposal for mobius, 1.1 "Overview";
+ * the tensor names of 1.3).  The reader memory-maps the file, parses the
+ * header, the key-value pairs and the tensor table, and checks every field
+ * against the file's size: a truncated or malformed file gives
+ * GGUF_ERR_FORMAT, never a read past the mapping.  Versions 2 and 3 of the
+ * published container layout are read (little-endian):
+ *   "GGUF" u32 version, u64 n_tensors, u64 n_kv, n_kv x {string key, u32
+ *   value type, value}, n_tensors x {string name, u32 n_dims, u64 dims[],
+ *   u32 type, u64 offset}, padding to general.alignment (default 32), data.
+ * Value types: 0 u8, 1 i8, 2 u16, 3 i16, 4 u32, 5 i32, 6 f32, 7 bool,
+ * 8 string, 9 array, 10 u64, 11 i64, 12 f64.  Tensor dims[0] is the
+ * contiguous dimension: a weight W[N, K] has dims {K, N}, and its bytes are
+ * exactly the [N, K/blk*bb] block array the matmul entry points take.
+ * A handle is used by one thread at a time; distinct handles are independent.
+ * ------------------------------------------------------------------------- */
+typedef struct gguf_file* gguf_file_t;
+
+/* Opens and parses `path`; *out receives the handle (NULL on error).
+ * GGUF_ERR_IO (open/stat/mmap failed), GGUF_ERR_FORMAT. */
+int gguf_file_open(const char* path, gguf_file_t* out);
+void gguf_file_close(gguf_file_t f);              /* NULL is a no-op */
+int gguf_file_version(gguf_file_t f);             /* 2 or 3 */
+int64_t gguf_file_alignment(gguf_file_t f);       /* data alignment in bytes */
+int64_t gguf_file_tensor_count(gguf_file_t f);
+
+/* Tensor `index`: its name (NUL-terminated into name[name_cap], WORKSPACE when
+ * it does not fit), GGUF type id, number of dims, dims (unused ones 1), the
+ * absolute file offset of its data and its size in bytes (0 when the type's
+ * size is not known to the reader: known are F32 0, F16 1, BF16 30, Q4_0,
+ * Q4_1, Q5_0, Q5_1, Q8_0, Q2_K 10, Q3_K 11, Q4_K, Q5_K, Q6_K).  Any output
+ * pointer may be NULL. */
+int gguf_file_tensor_info(gguf_file_t f, int64_t index, char* name, size_t name_cap, int* type, int* n_dims,
+                          int64_t dims[4], uint64_t* file_offset, uint64_t* nbytes);
+
+/* Index of the tensor called `name`, or GGUF_ERR_NOT_FOUND. */
+int64_t gguf_file_find_tensor(gguf_file_t f, const char* name);
+
+/* Copies tensor `index`'s bytes into HOST memory host_dst[dst_bytes]
+ * (WORKSPACE when smaller than the tensor, UNSUPPORTED when its size is
+ * unknown).  Copy them to the device with one cudaMemcpy to run a matmul. */
+int gguf_file_read_tensor(gguf_file_t f, int64_t index, void* host_dst, size_t dst_bytes);
+
+/* For a 2-D tensor of a type the matmul entry points take (gguf_qtype):
+ * its qtype, N = dims[1] and K = dims[0].  UNSUPPORTED otherwise. */
+int gguf_file_tensor_as_weight(gguf_file_t f, int64_t index, int* qtype, int64_t* N, int64_t* K);
+
+int64_t gguf_file_kv_count(gguf_file_t f);
+/* Key of pair `index` into key[cap] and its value type (either may be NULL). */
+int gguf_file_kv_key(gguf_file_t f, int64_t index, char* key, size_t cap, int* value_type);
+/* Value of `key` as an integer (any integer or bool type; a u64 above
+ * INT64_MAX is UNSUPPORTED) or a float (f32, f64 or any integer type).
+ * NOT_FOUND, UNSUPPORTED for another value type. */
+int gguf_file_get_int(gguf_file_t f, const char* key, int64_t* out);
+int gguf_file_get_float(gguf_file_t f, const char* key, double* out);
+/* A string value: *len receives its byte length; buf (may be NULL) receives
+ * the bytes plus a NUL when cap > len (else WORKSPACE). */
+int gguf_file_get_string(gguf_file_t f, const char* key, char* buf, size_t cap, size_t* len);
+/* An array value: its element type and count; dst (may be NULL) receives the
+ * elements of a scalar array (cap bytes; WORKSPACE when smaller).  String
+ * arrays report type and count only. */
+int gguf_file_get_array(gguf_file_t f, const char* key, int* elem_type, int64_t* count, void* dst, size_t cap);
 
 #ifdef __cplusplus
 }

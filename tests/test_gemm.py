@@ -55,6 +55,20 @@ def test_fused_small(qtype, K, N, M):
     U.check_close(got, ref, "bf16", what=f"q{qtype} N{N} K{K} M{M}")
 
 
+@pytest.mark.parametrize("qtype", [syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1])
+@pytest.mark.parametrize("N,K,M", [(128, 256, 16), (200, 768, 40), (384, 1024, 130), (130, 2048, 300)])
+def test_fused_32_value_formats(qtype, N, K, M):
+    got, ref = _gemm(qtype, N, K, M)
+    U.check_close(got, ref, "bf16", what=f"q{qtype} N{N} K{K} M{M}")
+
+
+@pytest.mark.parametrize("qtype", [syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1])
+def test_fused_32_value_formats_f32_out_split_k(qtype):
+    # few row tiles: the plan splits K; f32 output holds the bound raw
+    got, ref = _gemm(qtype, 256, 4096, 48, ydt="f32")
+    U.check_close(got, ref, "f32", rel=2e-3)
+
+
 @pytest.mark.parametrize("N,M", [(128, 8), (256, 64), (200, 257)])
 def test_fused_q6k_planes(N, M):
     got, ref = _gemm(syn.Q6_K, N, 2048, M, layout=1)

@@ -15,6 +15,7 @@ from tests import gpu_util as U
 pytestmark = pytest.mark.gpu
 
 QTYPES = [syn.Q8_0, syn.Q4_K, syn.Q5_K, syn.Q6_K]
+QTYPES_32 = [syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1]
 STAGED, DIRECT, TILE, PAIR, ROWLANE = 0, 1, 2, 3, 4
 
 
@@ -123,6 +124,22 @@ def test_direct_kernel_integer_terms_bit_exact(qtype, layout, M):
 @pytest.mark.parametrize("M", [1, 3, 8])
 def test_staged_kernel_integer_terms_bit_exact(qtype, layout, M):
     _assert_terms_exact(qtype, layout, 37, 768, M, STAGED)
+
+
+@pytest.mark.parametrize("qtype", QTYPES_32)
+@pytest.mark.parametrize("N,K,M", [(37, 768, 1), (37, 96, 3), (300, 2048, 8), (129, 4352, 2)])
+def test_32_value_formats_integer_terms_bit_exact(qtype, N, K, M):
+    # Q4_0 / Q4_1 / Q5_0 / Q5_1 on the staged kernel: dots of (q - 8), (q5 - 16)
+    # or the unsigned codes, bit for bit; K need only be a multiple of 32
+    assert _assert_terms_exact(qtype, 0, N, K, M, -1, residual=(M == 2)) == STAGED
+
+
+@pytest.mark.parametrize("qtype", QTYPES_32)
+@pytest.mark.parametrize("N,K", [(1, 32), (3, 512), (128, 1024), (129, 800)])
+@pytest.mark.parametrize("M", [1, 4])
+def test_32_value_formats_outputs(qtype, N, K, M):
+    got, ref, _, _ = _case(qtype, N, K, M)
+    U.check_close(got, ref, "bf16", what=f"q{qtype} N{N} K{K} M{M}")
 
 
 @pytest.mark.parametrize("M", [1, 2, 4])
