@@ -322,7 +322,10 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
     """Figures for the other workloads (context for the second half of the
     metric).  Returns (compact dict for the JSON line, full detail dict).
     Weights rotate over copies larger than L2.  `only`: a regular expression
-    over the detail keys."""
+    over the detail keys.  Compact keys: q8s_mM / q8sdense_mM = Q8_0 2048 x 8192
+    fused / dense after decode-once, [us, TFLOP/s, fraction of the tensor peak];
+    q4_, q5_, q6_ (raw Q6_K), q6p_ (Q6_K planes), q8_mM = 14336 x 4096, same
+    triple; moe_tT = [us, touched-expert GB/s, fraction of HBM, TFLOP/s]."""
     import re
     import torch
     import gguf_quant_weight_gb300 as g
@@ -383,8 +386,8 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
                             5, stream, cd)
             detail[f"q8_0_2048x8192_m{M}_fused"] = {"us": t * 1e6, "tflops": fl / t / 1e12}
             detail[f"q8_0_2048x8192_m{M}_dense_after_decode_once"] = {"us": t2 * 1e6, "tflops": fl / t2 / 1e12}
-            compact[f"q8_m{M}"] = [_r(t * 1e6), _r(fl / t / 1e12), _r(fl / t / 1e12 / tc_peak, 3)]
-            compact[f"q8dense_m{M}"] = [_r(t2 * 1e6), _r(fl / t2 / 1e12), _r(fl / t2 / 1e12 / tc_peak, 3)]
+            compact[f"q8s_m{M}"] = [_r(t * 1e6), _r(fl / t / 1e12), _r(fl / t / 1e12 / tc_peak, 3)]
+            compact[f"q8sdense_m{M}"] = [_r(t2 * 1e6), _r(fl / t2 / 1e12), _r(fl / t2 / 1e12 / tc_peak, 3)]
 
     # MoE: 128 experts top-8, Q4_K 768x2048; ids rotate over 8 Zipf(1.1) draws.
     # T = 32..512 is the prefill batch; T = 1, 4, 16 the decode form (one int8

@@ -274,7 +274,7 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K, con
     if (need && (!workspace || ws_bytes < need)) return GGUF_ERR_WORKSPACE;
     if (workspace && !aligned16(workspace)) return GGUF_ERR_MISALIGNED;
     return gemm_fused_run(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace, f->num_sms, f->status,
-                          (cudaStream_t)stream);
+                          (cudaStream_t)stream, pdl_enabled() ? 1 : 0);
 }
 
 static int run_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,

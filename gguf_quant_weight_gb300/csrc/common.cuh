@@ -17,6 +17,13 @@ namespace gg {
 // GGUF_ERR_TIMEOUT in the status word and lets the kernel return.
 constexpr long long kSpinLimit = 1ll << 26;
 
+// Programmatic dependent launch: let the next kernel on the stream start (its
+// launch carries the programmatic-serialization attribute), and wait until the
+// kernel before this one has completed and its writes are visible.  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void report(int* status, int code) {
     if (status) atomicCAS(status, 0, code);
 }

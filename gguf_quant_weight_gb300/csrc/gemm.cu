@@ -72,6 +72,9 @@ __global__ void __launch_bounds__(kConvThreads) convert_rows_kernel(const void* 
                                                                     uint32_t* __restrict__ zero, int nzero) {
     __shared__ float red_max[kConvThreads / 32];
     __shared__ int red_fin[kConvThreads / 32];
+    // the fused GEMM after this kernel may start now (its weight stream and
+    // decoding need nothing from here; what reads these outputs waits first)
+    pdl_launch_dependents();
     // the GEMM that follows on the stream counts on these words being zero
     if (blockIdx.x == 0)
         for (int j = threadIdx.x; j < nzero; j += blockDim.x) zero[j] = 0u;

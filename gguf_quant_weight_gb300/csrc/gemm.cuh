@@ -13,9 +13,11 @@ namespace gg {
 size_t gemm_workspace_bytes(int qtype, int64_t N, int64_t K, int64_t M, int num_sms);
 size_t dense_workspace_bytes(int64_t N, int64_t K, int64_t M);
 
+// pdl: launch the GEMM as a programmatic dependent of its activation
+// conversion kernel (overlaps its start with the conversion)
 int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
                    const void* residual, void* y, int ydt, void* workspace, int num_sms, int* status,
-                   cudaStream_t stream);
+                   cudaStream_t stream, int pdl);
 
 int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
                    const void* residual, void* y, int ydt, void* workspace, int num_sms, int* status,

@@ -98,7 +98,7 @@ struct FusedCfg {
     static constexpr int RS_FIT = (232448 - 2048 - S * B_BYTES) / RAW;
     static constexpr int RS = RS_FIT > 6 ? 6 : RS_FIT;
     static constexpr int SMEM = S * B_BYTES + RS * RAW + 1024 + 512;   // + alignment + barriers
-    static_assert(8 * (2 * S + 2 * RS + 1) + 8 <= 512, "barrier area");
+    static_assert(8 * (2 * S + 2 * RS + 2) + 8 <= 512, "barrier area");
     static_assert(RS >= 2, "raw ring needs two slots");
     static_assert(A_COL0 + S * A_COLS <= TMEM_COLS && NI * BN <= A_COL0 && 4 % NI == 0, "TMEM columns");
 };
@@ -127,6 +127,10 @@ struct FusedParams {
     // power-of-two scale of each activation row's f16 copy (dense: row t0 +
     // col; grouped: gathered row gstart + col); the epilogue multiplies by it
     const float* xscale;
+    // launched as a programmatic dependent of the activation conversion: the
+    // weight stream and decoding start at once, what reads the conversion's
+    // outputs waits for it (host-side launch choice)
+    int pdl;
 };
 
 // barrier `id` over the first `threads` threads that reach it (whole warps)
@@ -440,7 +444,8 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
     uint64_t* rfull = empty + C::S;
     uint64_t* rempty = rfull + C::RS;
     uint64_t* tfull = rempty + C::RS;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(tfull + 1);
+    uint64_t* xs_ready = tfull + 1;                                     // s_xscale filled
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(xs_ready + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     static_assert(!(MOE && SPLIT), "the grouped form does not split K");
     // tile (row tile bx, token tile by) and K slice z of ks; the split form
@@ -485,17 +490,15 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
     // MMA width: the tile's valid token columns rounded up to 16, so an
     // underfilled tile issues only the MMA columns it needs
     const int n_mma = fp.full_width ? BN : min(BN, (cols + 15) & ~15);
-    // the power-of-two scales of the tile's activation rows, staged once for
-    // the epilogue (read before the first barrier: the conversion kernel that
-    // wrote them precedes this one on the stream)
+    // the power-of-two scales of the tile's activation rows, staged for the
+    // epilogue by the activation producer's warp (off the start-up path)
     __shared__ float s_xscale[BN];
-    for (int i = threadIdx.x; i < BN; i += blockDim.x)
-        s_xscale[i] = i < cols ? fp.xscale[MOE ? (int64_t)gstart + i : t0 + i] : 1.f;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::S; ++s) { mbar_init(&full[s], DW + 1); mbar_init(&empty[s], NI); }
         for (int s = 0; s < C::RS; ++s) { mbar_init(&rfull[s], 1); mbar_init(&rempty[s], DW); }
         mbar_init(tfull, NI);
+        mbar_init(xs_ready, 32);
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(tslot, C::TMEM_COLS);
@@ -526,9 +529,14 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
             }
         }
     } else if (warp == 2) {
-        // the activation tile of every 64-value k step, as far ahead as the ring allows
+        // the activation tile of every 64-value k step, as far ahead as the ring
+        // allows; first the tile's row scales into shared memory (all lanes)
+        if (lane == 0) prefetch_tmap(&tmB);
+        pdl_wait();   // the f16 activations and their scales come from the kernel before this one
+        for (int i = lane; i < BN; i += 32)
+            s_xscale[i] = i < cols ? fp.xscale[MOE ? (int64_t)gstart + i : t0 + i] : 1.f;
+        mbar_arrive(xs_ready);
         if (lane == 0) {
-            prefetch_tmap(&tmB);
             for (int i = 0; i < nk; ++i) {
                 const int s = i % C::S;
                 if (!mbar_wait(&empty[s], ((i / C::S) & 1) ^ 1, fp.status)) break;
@@ -634,7 +642,8 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
         constexpr int G = DW / 4, CH = BN / 16;
         const int qd = warp & 3, grp = (warp - 3) >> 2;
         const int64_t n = n0 + 32 * qd + lane;
-        const bool ep_ok = __all_sync(0xffffffffu, mbar_wait(tfull, 0, fp.status));
+        const bool ep_ok = __all_sync(0xffffffffu, mbar_wait(tfull, 0, fp.status) && mbar_wait(xs_ready, 0, fp.status));
+        pdl_wait();   // the split tickets are zeroed by the kernel before this one
         // split K: this slice's sums go to its slot [BN][128] of the tile
         float* const slots = SPLIT ? fp.partial + split_tile * ks * (BN * 128) : nullptr;
         if (ep_ok) {
@@ -798,8 +807,17 @@ cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const Fused
         const int64_t tiles = ceil_div(fp.N, 128) * ceil_div(fp.M, BN);
         grid = dim3((unsigned)(fp.n_full + (tiles - fp.n_full) * fp.ks));
     }
-    k<<<grid, fused_threads(QT, LAYOUT, BN), smem, s>>>(w[0], w[1], w[2], w[3], b, fp);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(fused_threads(QT, LAYOUT, BN));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = (!MOE && fp.pdl) ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, w[0], w[1], w[2], w[3], b, fp);
 }
 
 template <int QT, int LAYOUT>
@@ -826,7 +844,7 @@ size_t gemm_workspace_bytes(int, int64_t N, int64_t K, int64_t M, int num_sms) {
 
 int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt, int64_t M,
                    const void* residual, void* y, int ydt, void* workspace, int num_sms, int* status,
-                   cudaStream_t stream) {
+                   cudaStream_t stream, int pdl) {
     if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
     const int64_t KB = K / 256;
     if (qtype == GGUF_Q6_K && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;   // 16-byte row strides for TMA
@@ -873,7 +891,12 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
         return st;
     FusedParams fp{N, M, (int)KB, residual, y, ydt, status, nullptr, nullptr, nullptr, nullptr, 0,
                    pl.ks, pl.ks > 1 ? reinterpret_cast<float*>(wsb + wl.partial) : nullptr, tickets,
-                   (int)pl.n_full, (int)ceil_div(N, 128), xscale};
+                   (int)pl.n_full, (int)ceil_div(N, 128), xscale,
+                   // as a dependent launch where whole tiles remain (measured on GB300: Q5_K /
+                   // Q6_K planes 14336 x 4096 M = 512 67.2 -> 64.2 / 64.7 -> 61.9 us, Q8_0
+                   // 2048 x 8192 M = 4096 138.3 -> 134.1 us), not when every tile is split
+                   // along K (M = 128 / 512 there: 25.7 -> 28.6 / 37.8 -> 40.3 us)
+                   (pdl && !(pl.ks > 1 && pl.n_full == 0)) ? 1 : 0};
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {
         case GGUF_Q4_0: e = launch_bn<GGUF_Q4_0, 0>(bn, tw, tb, fp, stream); break;

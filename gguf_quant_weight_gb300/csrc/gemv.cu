@@ -65,8 +65,6 @@ __device__ __forceinline__ uint32_t lds16(uint32_t a) {
 }
 __device__ __forceinline__ float i2f(int v) { return (float)v; }
 
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ float max_nan(float a, float b) {
     float r;
