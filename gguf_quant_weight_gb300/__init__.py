@@ -60,6 +60,9 @@ _SIGS = {
     "gguf_mm_auto_path": (_c_int, [_c_int, _c_int, _c_i64, _c_i64, _c_i64, _c_int]),
     "gguf_mm_debug_moe_route": (_c_int, [_c_vp, _c_i64, _c_i64, _c_vp, _c_vp, _c_vp, _c_i64, _c_vp, _c_vp]),
     "gguf_mm_debug_timeout": (_c_int, [_c_i64, _c_vp]),
+    "gguf_mm_debug_moe_mv_terms": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp,
+                                            _c_i64, _c_int, _c_vp, _c_vp, _c_int, _c_vp, _c_vp, _c_vp, _c_vp, _c_vp,
+                                            _c_sz, _c_vp]),
     "gguf_file_open": (_c_int, [ctypes.c_char_p, ctypes.POINTER(_c_vp)]),
     "gguf_file_close": (None, [_c_vp]),
     "gguf_file_version": (_c_int, [_c_vp]),
@@ -222,6 +225,13 @@ def gguf_mm_gemv_kernel(qtype, layout, N, K, M, xdt=GGUF_DT_BF16) -> int:
 def gguf_mm_debug_moe_route(ids, entries, n_expert, offsets, ntiles, tiles, max_tiles, rows, stream=None):
     return _check("gguf_mm_debug_moe_route", load_library().gguf_mm_debug_moe_route(
         _p(ids), entries, n_expert, _p(offsets), _p(ntiles), _p(tiles), max_tiles, _p(rows), _s(stream)))
+
+
+def gguf_mm_debug_moe_mv_terms(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, per_slot, residual, y, ydt,
+                               qa=None, d_a=None, s=None, D=None, workspace=None, ws_bytes=0, stream=None):
+    return _check("gguf_mm_debug_moe_mv_terms", load_library().gguf_mm_debug_moe_mv_terms(
+        _p(w_experts), qtype, n_expert, N, K, _p(x), xdt, T, _p(ids), top_k, per_slot, _p(residual), _p(y), ydt,
+        _p(qa), _p(d_a), _p(s), _p(D), _p(workspace), ws_bytes, _s(stream)))
 
 
 def gguf_mm_debug_timeout(spin_limit, stream=None):

@@ -279,7 +279,8 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K, con
 
 static int run_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
                   int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt,
-                  void* workspace, size_t ws_bytes, gguf_stream_t stream, bool per_slot) {
+                  void* workspace, size_t ws_bytes, gguf_stream_t stream, bool per_slot,
+                  const MoeMvDump* dump = nullptr) {
     if (!ids || n_expert <= 0 || top_k <= 0) return GGUF_ERR_INVALID_ARG;
     int st = check_common(w_experts, qtype, GGUF_LAYOUT_BLOCKS, N, K, x, xdt, T, residual, y, ydt);
     if (st != GGUF_OK) return st;
@@ -291,7 +292,16 @@ static int run_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N,
     DeviceFacts* f = nullptr;
     if ((st = facts(&f)) != GGUF_OK) return st;
     return moe_run(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace,
-                   f->num_sms, f->status, (cudaStream_t)stream, per_slot);
+                   f->num_sms, f->status, (cudaStream_t)stream, per_slot, dump);
+}
+
+int gguf_mm_debug_moe_mv_terms(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K,
+                               const void* x, int xdt, int64_t T, const int32_t* ids, int64_t top_k, int per_slot,
+                               const void* residual, void* y, int ydt, int8_t* qa, float* d_a, int32_t* s,
+                               int32_t* D, void* workspace, size_t ws_bytes, gguf_stream_t stream) {
+    const MoeMvDump dump{qa, d_a, s, D};
+    return run_id(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace, ws_bytes,
+                  stream, per_slot != 0, &dump);
 }
 
 int gguf_mm_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,

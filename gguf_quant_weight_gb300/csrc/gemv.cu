@@ -1747,7 +1747,7 @@ cudaError_t launch_dispatch(const GemvParams& p, int grid, size_t smem, cudaStre
 // us at 128 rows; 5.5 vs 6.5 us at 8).
 constexpr int kMvThreads = 256, kMvRows = 32, kMvFuseRows = 8;
 
-template <int QT, bool QUANT>
+template <int QT, bool QUANT, bool DUMP>
 __global__ void __launch_bounds__(kMvThreads) moe_mv_kernel(const MoeMvParams mp) {
     constexpr int bb = QT == GGUF_Q4_K ? 144 : 176;
     constexpr int NW = kMvThreads / 32;
@@ -1812,6 +1812,20 @@ __global__ void __launch_bounds__(kMvThreads) moe_mv_kernel(const MoeMvParams mp
     gp.M = 1;
     gp.K = mp.K;
     gp.N = mp.N;
+    if constexpr (DUMP) {
+        if (blockIdx.x == 0) {
+            for (int64_t k = threadIdx.x; k < mp.K; k += kMvThreads) {
+                const uint32_t a = sh.qa + qa_pos((uint32_t)k);
+                if (mp.dbg_qa) mp.dbg_qa[(int64_t)p * mp.K + k] = (int8_t)(lds32(a & ~3u) >> (8 * (a & 3)));
+            }
+            for (int b = threadIdx.x; b < nb; b += kMvThreads) {
+                const uint4 en = lds128(sh.ds + 16u * b);
+                if (mp.dbg_da) mp.dbg_da[(int64_t)p * nb + b] = __uint_as_float(en.x);
+                if (mp.dbg_s) mp.dbg_s[(int64_t)p * nb + b] = (int32_t)(en.z + en.w);
+            }
+        }
+        gp.dbg_D = mp.dbg_D ? mp.dbg_D + (int64_t)p * mp.N * nb : nullptr;   // [N][K/32] of row p
+    }
     const int seg_end = (lane / seg) * seg + seg;
     const bool head = lane_on && (lane % seg) == 0;
     using Act = ActSlice<1, false, 8, 4>;
@@ -1822,7 +1836,7 @@ __global__ void __launch_bounds__(kMvThreads) moe_mv_kernel(const MoeMvParams mp
         const FragQ45<QT>* fr[1] = {&f};
         const int64_t nn[1] = {row_of(g)};
         const bool on[1] = {true};
-        unit_q45k<QT, 1, 1, Act, false>(gp, fr, a, u >> 1, u & 1, acc, nn, on);
+        unit_q45k<QT, 1, 1, Act, DUMP>(gp, fr, a, u >> 1, u & 1, acc, nn, on);
     };
     auto finish = [&](float (&acc)[1][1], int g) {
         if (seg == 32) {
@@ -1981,7 +1995,7 @@ size_t gemv_workspace_bytes(int64_t M, int64_t K) { return (size_t)(ceil_div(act
 // ------------------------------------------------------------------ MoE decode form entry
 size_t moe_mv_image_bytes(int64_t rows, int64_t K) { return (size_t)(ceil_div(act_image_bytes(rows, K), 256) * 256); }
 
-cudaError_t moe_mv_launch(const MoeMvParams& mp, cudaStream_t stream) {
+cudaError_t moe_mv_launch(const MoeMvParams& mp, cudaStream_t stream, bool dump) {
     cudaError_t e = cudaSuccess;
     const bool quant = mp.entries <= kMvFuseRows;
     if (!quant) {
@@ -1999,8 +2013,11 @@ cudaError_t moe_mv_launch(const MoeMvParams& mp, cudaStream_t stream) {
     }
     // one CTA per (kMvRows weight rows, routed row); the activation row's image in shared memory
     const size_t smem = (size_t)(qa_row_stride(mp.K) + (mp.K / 32) * 16);
-    auto k = mp.qtype == GGUF_Q4_K ? (quant ? moe_mv_kernel<GGUF_Q4_K, true> : moe_mv_kernel<GGUF_Q4_K, false>)
-                                   : (quant ? moe_mv_kernel<GGUF_Q5_K, true> : moe_mv_kernel<GGUF_Q5_K, false>);
+    auto k = mp.qtype == GGUF_Q4_K ? (quant ? moe_mv_kernel<GGUF_Q4_K, true, false> : moe_mv_kernel<GGUF_Q4_K, false, false>)
+                                   : (quant ? moe_mv_kernel<GGUF_Q5_K, true, false> : moe_mv_kernel<GGUF_Q5_K, false, false>);
+    if (dump)
+        k = mp.qtype == GGUF_Q4_K ? (quant ? moe_mv_kernel<GGUF_Q4_K, true, true> : moe_mv_kernel<GGUF_Q4_K, false, true>)
+                                  : (quant ? moe_mv_kernel<GGUF_Q5_K, true, true> : moe_mv_kernel<GGUF_Q5_K, false, true>);
     if (smem > 48 * 1024 &&
         (e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;

@@ -63,8 +63,14 @@ struct MoeMvParams {
     void* y;
     int ydt;
     int* status;
+    // test hook (a separate instantiation): routed row p's activation codes
+    // [p][K], scales and sums [p][K/32], sub-block dots [p][N][K/32]
+    int8_t* dbg_qa;
+    float* dbg_da;
+    int32_t* dbg_s;
+    int32_t* dbg_D;
 };
 size_t moe_mv_image_bytes(int64_t rows, int64_t K);
-cudaError_t moe_mv_launch(const MoeMvParams& mp, cudaStream_t stream);
+cudaError_t moe_mv_launch(const MoeMvParams& mp, cudaStream_t stream, bool dump = false);
 
 }  // namespace gg

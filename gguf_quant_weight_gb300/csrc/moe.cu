@@ -279,11 +279,12 @@ size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, in
 
 int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
             int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
-            int num_sms, int* status, cudaStream_t stream, bool per_slot) {
+            int num_sms, int* status, cudaStream_t stream, bool per_slot, const MoeMvDump* dump) {
     (void)num_sms;
     if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
     const int64_t entries = T * top_k;
     if (entries > INT32_MAX / 2 || n_expert * N > INT32_MAX) return GGUF_ERR_UNSUPPORTED;
+    if (dump && !mv_form(qtype, entries)) return GGUF_ERR_UNSUPPORTED;
     if (mv_form(qtype, entries)) {
         MoeMvParams mp{};
         mp.w = static_cast<const uint8_t*>(w_experts);
@@ -304,7 +305,13 @@ int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64
         mp.y = y;
         mp.ydt = ydt;
         mp.status = status;
-        return moe_mv_launch(mp, stream) == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
+        if (dump) {
+            mp.dbg_qa = dump->qa;
+            mp.dbg_da = dump->da;
+            mp.dbg_s = dump->s;
+            mp.dbg_D = dump->D;
+        }
+        return moe_mv_launch(mp, stream, dump != nullptr) == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
     }
     const MoeLayout L = moe_layout(workspace, n_expert, K, T, top_k);
     const size_t route_smem = (size_t)(2 * n_expert + 128) * sizeof(int);

@@ -12,9 +12,20 @@ constexpr int kMoeMvRows = 128;
 
 size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k);
 
+// Integer intermediates of the decode form (test hook): routed row p's
+// activation codes [p][K], scales and sums [p][K/32], dots [p][N][K/32].
+struct MoeMvDump {
+    int8_t* qa;
+    float* da;
+    int32_t* s;
+    int32_t* D;
+};
+
+// dump: run the decode form with its integer terms written out
+// (GGUF_ERR_UNSUPPORTED when this batch does not take the decode form)
 int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
             int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
-            int num_sms, int* status, cudaStream_t stream, bool per_slot = false);
+            int num_sms, int* status, cudaStream_t stream, bool per_slot = false, const MoeMvDump* dump = nullptr);
 
 // The routing step alone (test hook): per-expert group offsets [E + 1], the
 // number of (expert, token tile) work items, the items {expert, first row,

@@ -274,6 +274,20 @@ int gguf_mm_debug_moe_route(const int32_t* ids, int64_t entries, int64_t n_exper
                             int32_t* ntiles, int32_t* tiles, int64_t max_tiles, int32_t* rows,
                             gguf_stream_t stream);
 
+/* Test hook: gguf_mm_id (per_slot = 0) or gguf_mm_id_slots (per_slot = 1) in
+ * its decode form -- one int8 GEMV per routed row, taken by Q4_K / Q5_K experts
+ * for at most 128 routed rows; GGUF_ERR_UNSUPPORTED for any other batch --
+ * with the integer intermediates of every routed row p = token * top_k + slot
+ * whose expert id is valid written out (device memory; any may be NULL):
+ *   qa [entries, K] int8, d_a [entries, K/32] f32, s [entries, K/32] int32
+ *   (the row's activation codes, scales and code sums, as gguf_mm_debug_gemv_terms)
+ *   D  [entries, N, K/32] int32 (the sub-block dots of row p against its expert)
+ * Rows with an invalid id are left untouched.  Allocates nothing. */
+int gguf_mm_debug_moe_mv_terms(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K,
+                               const void* x, int xdt, int64_t T, const int32_t* ids, int64_t top_k, int per_slot,
+                               const void* residual, void* y, int ydt, int8_t* qa, float* d_a, int32_t* s,
+                               int32_t* D, void* workspace, size_t ws_bytes, gguf_stream_t stream);
+
 /* Test hook for the bounded device waits: launches a kernel whose wait on an
  * mbarrier that nothing completes gives up after about `spin_limit` polls and
  * records GGUF_ERR_TIMEOUT in the device status word (read it with

@@ -252,3 +252,62 @@ def test_moe_activation_rows_beyond_f16_range(qtype, T, top_k):
         rel = 2e-3
     for t in range(T):
         U.check_close(got[t], ref[t], "f32", rel=rel, what=f"token {t}")
+
+
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q5_K])
+@pytest.mark.parametrize("T,top_k,per_slot", [(1, 8, 0), (3, 2, 0), (16, 8, 0), (4, 4, 1), (60, 2, 1)])
+def test_moe_decode_form_integer_terms_bit_exact(qtype, T, top_k, per_slot):
+    """The decode form's integer intermediates, row by routed row: the
+    activation codes, scales and sums (in-kernel quantizer at <= 8 routed rows,
+    the shared image above) and every sub-block dot against the row's expert
+    equal the int8-path oracle's bit for bit (OpenVINO PR #39119
+    "Implementation", GEMV row, applied per routed row as mul_mv_id does)."""
+    E, N, K = 12, 96, 1024
+    rs = syn.rng(900 + qtype + T + per_slot)
+    wE = syn.weight_blocks(rs, qtype, E * N, K)
+    ids = _distinct_ids(rs, T, E, top_k)
+    ids[0, -1] = -1                                          # an invalid id: its row is left alone
+    entries = T * top_k
+    xrows = entries if per_slot else T
+    x = syn.normal(rs, (xrows, K), "bf16")
+    qa = torch.zeros((entries, K), dtype=torch.int8, device="cuda")
+    da = torch.zeros((entries, K // 32), dtype=torch.float32, device="cuda")
+    s = torch.zeros((entries, K // 32), dtype=torch.int32, device="cuda")
+    D = U.guarded((entries, N, K // 32), torch.int32, fill=-999999)
+    y = U.guarded((T, top_k, N), torch.float32)
+    nws = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
+    ws = U.workspace(nws)
+    g.gguf_mm_debug_moe_mv_terms(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids), top_k,
+                                 per_slot, None, y.t, g.GGUF_DT_F32, qa, da, s, D.t, ws.t, nws)
+    torch.cuda.synchronize()
+    for b, nm in ((D, "D"), (y, "y"), (ws, "workspace")):
+        b.check(nm)
+    assert g.gguf_mm_check_errors() == 0
+    qa, da, s, Dh = qa.cpu().numpy(), da.cpu().numpy(), s.cpu().numpy(), D.t.cpu().numpy()
+    x32 = U.act_f32(x, "bf16")
+    rb = K // 256 * syn.BLOCK_BYTES[qtype]
+    wv = wE.reshape(E, N, rb)
+    for p, e in enumerate(ids.reshape(-1)):
+        if e < 0:
+            assert np.all(Dh[p] == -999999), "a row without an expert was written"
+            continue
+        arow = p if per_slot else p // top_k
+        _, t = O.gemv_int8_path(wv[e], qtype, N, K, x32[arow:arow + 1], return_terms=True)
+        assert np.array_equal(qa[p], t["qa"][0]), p
+        assert np.array_equal(da[p], t["d_a"][0]), p
+        assert np.array_equal(s[p], t["s"][0]), p
+        assert np.array_equal(Dh[p].astype(np.int64), t["D"][0]), f"row {p}: D differs at {np.argwhere(Dh[p] != t['D'][0])[:5]}"
+
+
+def test_moe_decode_form_terms_hook_refuses_the_routed_path():
+    E, N, K, T, top_k = 4, 64, 256, 40, 4          # 160 routed rows: above the decode form
+    ids = np.zeros((T, top_k), np.int32)
+    nws = g.gguf_mm_workspace_size(g.GGUF_OP_ID, syn.Q4_K, N, K, T, E, top_k)
+    ws = U.workspace(nws)
+    w = U.dev(np.zeros(E * N * K // 256 * 144, np.uint8))
+    x = torch.zeros((T, K), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros((T, top_k, N), dtype=torch.float32, device="cuda")
+    with pytest.raises(g.GGUFError) as e:
+        g.gguf_mm_debug_moe_mv_terms(w, syn.Q4_K, E, N, K, x, g.GGUF_DT_BF16, T, U.dev(ids), top_k, 0, None, y,
+                                     g.GGUF_DT_F32, workspace=ws.t, ws_bytes=nws)
+    assert e.value.status == g.GGUF_ERR_UNSUPPORTED
