@@ -54,12 +54,13 @@ __host__ __device__ constexpr int decode_warps(int qt, int layout) { return stat
 // of each k step, each accumulating into its own BN TMEM columns (K split
 // NI ways); the epilogue adds the NI partial sums.  (Two, not four: the TMEM
 // columns are worth more as operand stages.)
-__host__ __device__ constexpr int mma_issuers(int bn) { return bn <= 128 ? 2 : 1; }
+// Two CTAs per SM (CTAS = 2, each with half of tensor memory) take one issuer.
+__host__ __device__ constexpr int mma_issuers(int bn, int ctas = 1) { return (bn <= 128 && ctas == 1) ? 2 : 1; }
 // warp 0: raw-weight TMA producer; warp 1: TMEM + MMA issuer 0; warp 2:
 // activation TMA producer; warps 3 .. 3+DW-1: decoders (and the epilogue);
 // the last NI - 1 warps: MMA issuers 1 .. NI-1
-__host__ __device__ constexpr int fused_threads(int qt, int layout, int bn) {
-    return 96 + 32 * decode_warps(qt, layout) + 32 * (mma_issuers(bn) - 1);
+__host__ __device__ constexpr int fused_threads(int qt, int layout, int bn, int ctas = 1) {
+    return 96 + 32 * decode_warps(qt, layout) + 32 * (mma_issuers(bn, ctas) - 1);
 }
 
 __host__ __device__ constexpr int raw_pitch(int qt, int layout) {
@@ -71,7 +72,11 @@ __host__ __device__ constexpr int raw_slot_bytes(int qt, int layout) {
     return (qt == GGUF_Q6_K && layout) ? 128 * (128 + 64 + 16 + 16) : 128 * raw_pitch(qt, layout);
 }
 
-template <int BN, int RAW>
+// CTAS: CTAs resident per SM.  With two, each holds half of tensor memory
+// (256 columns) and half of shared memory, so that one CTA's start-up,
+// epilogue and decoder chain overlap the other's (the decoder-bound tiles:
+// MoE work items with few token columns).
+template <int BN, int RAW, int CTAS = 1>
 struct FusedCfg {
     // The decoded weight tile (the MMA's A operand, 128 rows x 64 f16 per k
     // step) lives in tensor memory: decoders write it with tcgen05.st and the
@@ -80,26 +85,31 @@ struct FusedCfg {
     // of a k step (one "full" barrier: the decoder warps plus the activation
     // TMA; one "empty" barrier: one commit per issuer), which keeps the
     // MMA-issuing threads' work per step small.
-    static constexpr int NI = mma_issuers(BN);       // issuers; accumulator j at columns [j*BN, (j+1)*BN)
+    static constexpr int NI = mma_issuers(BN, CTAS); // issuers; accumulator j at columns [j*BN, (j+1)*BN)
     static constexpr int A_COLS = 32;                 // TMEM columns per decoded stage
     static constexpr int A_COL0 = NI * BN < 32 ? 32 : NI * BN;   // first decoded-stage column
     static constexpr int B_BYTES = BN * 64 * 2;
-    static constexpr int TMEM_COLS = 512;             // accumulators [0, NI*BN) + decoded stages
+    static constexpr int TMEM_COLS = 512 / CTAS;      // accumulators [0, NI*BN) + decoded stages
+    // dynamic shared memory one CTA may use: all of it, or half of the SM's
+    // 228 KB less the per-CTA reserve and the static scale array
+    static constexpr int SMEM_CAP = CTAS == 1 ? 232448 : (233472 - 2 * 1024) / 2 - 4 * BN;
     // Stages: as many as tensor memory holds (up to 12) while shared memory
     // keeps three raw slots -- the activation tile of a step is requested
     // when its stage frees, and under the weight stream it lands ~3000 cycles
     // later, so the ring must reach that far ahead of the MMAs.  BN = 256
     // keeps four (its tiles are wide enough that the MMAs cover the wait).
     static constexpr int S_TMEM = (TMEM_COLS - A_COL0) / A_COLS;
-    static constexpr int S_SMEM = (232448 - 2048 - 3 * RAW) / B_BYTES;
+    static constexpr int S_SMEM = (SMEM_CAP - 2048 - (CTAS == 1 ? 3 : 2) * RAW) / B_BYTES;
     static constexpr int S_MIN = S_TMEM < S_SMEM ? S_TMEM : S_SMEM;
     static constexpr int S = BN >= 256 ? 4 : (S_MIN > 12 ? 12 : S_MIN);
     // raw slots: what the activation stages leave (each covers four k steps)
-    static constexpr int RS_FIT = (232448 - 2048 - S * B_BYTES) / RAW;
+    static constexpr int RS_FIT = (SMEM_CAP - 2048 - S * B_BYTES) / RAW;
     static constexpr int RS = RS_FIT > 6 ? 6 : RS_FIT;
     static constexpr int SMEM = S * B_BYTES + RS * RAW + 1024 + 512;   // + alignment + barriers
     static_assert(8 * (2 * S + 2 * RS + 2) + 8 <= 512, "barrier area");
-    static_assert(RS >= 2, "raw ring needs two slots");
+    // usable: two raw slots at least (a configuration without them is only
+    // ever inspected, never launched: the kernel asserts OK)
+    static constexpr bool OK = RS >= 2 && S >= 2;
     static_assert(A_COL0 + S * A_COLS <= TMEM_COLS && NI * BN <= A_COL0 && 4 % NI == 0, "TMEM columns");
 };
 
@@ -419,13 +429,14 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
 
 // SPLIT: the K-split form (a separate instantiation: its epilogue code in the
 // kernel slowed the unsplit form by ~3 %, measured)
-template <int QT, int LAYOUT, int BN, bool MOE, bool SPLIT>
-__global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN), 1)
+template <int QT, int LAYOUT, int BN, bool MOE, bool SPLIT, int CTAS = 1>
+__global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN, CTAS), CTAS)
     fused_tc_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
                     const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmW3,
                     const __grid_constant__ CUtensorMap tmB, const FusedParams fp) {
     constexpr int RAW = raw_slot_bytes(QT, LAYOUT);
-    using C = FusedCfg<BN, RAW>;
+    using C = FusedCfg<BN, RAW, CTAS>;
+    static_assert(C::OK, "raw ring needs two slots");
     constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
     constexpr int PITCH = raw_pitch(QT, LAYOUT);
     constexpr int DW = decode_warps(QT, LAYOUT);   // decoder warps
@@ -775,6 +786,20 @@ FusedPlan plan_fused(int64_t N, int64_t M, int64_t KB, int num_sms) {
     return best;
 }
 
+// Whether format QT (layout LAYOUT) can run two CTAs per SM at BN = 128: half
+// of shared memory still holds four activation stages and two raw slots.
+// Used by the grouped (MoE) form only: dense tiles measured slower two per SM
+// (Q5_K 14336 x 4096, M = 8 / 128 / 512: 26.4 -> 31.7, 28.2 -> 38.8, 63.7 ->
+// 87.4 us) -- half of shared memory leaves two or three raw slots, too few to
+// cover the weight stream's latency over a 64-step tile, while MoE work items
+// (K = 2048, a few token columns) gain more from overlapping one CTA's
+// start-up and epilogue with the other's decoding.
+template <int QT, int LAYOUT>
+constexpr bool two_ctas_fit() {
+    using C2 = FusedCfg<128, raw_slot_bytes(QT, LAYOUT), 2>;
+    return C2::OK && C2::S >= 4;
+}
+
 // Workspace layout of the fused GEMM: F16 activations | split-K slots | tickets.
 struct FusedWorkspace {
     size_t act, scale, partial, tickets, total;   // act: bytes of the f16 copy; the others are offsets
@@ -794,14 +819,18 @@ FusedWorkspace fused_workspace(int64_t N, int64_t K, int64_t M, const FusedPlan&
     return w;
 }
 
-template <int QT, int LAYOUT, int BN, bool MOE = false, bool SPLIT = false>
+template <int QT, int LAYOUT, int BN, bool MOE = false, bool SPLIT = false, int CTAS = 1>
 cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const FusedParams& fp, cudaStream_t s,
                          int grid_y = 0) {
-    using C = FusedCfg<BN, raw_slot_bytes(QT, LAYOUT)>;
+    using C = FusedCfg<BN, raw_slot_bytes(QT, LAYOUT), CTAS>;
     const int smem = C::SMEM;
-    auto k = fused_tc_kernel<QT, LAYOUT, BN, MOE, SPLIT>;
+    auto k = fused_tc_kernel<QT, LAYOUT, BN, MOE, SPLIT, CTAS>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (CTAS > 1 &&   // the whole carveout to shared memory, so that two CTAs fit
+        (e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  (int)cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+        return e;
     dim3 grid((unsigned)ceil_div(fp.N, 128), MOE ? (unsigned)grid_y : (unsigned)ceil_div(fp.M, BN));
     if (SPLIT) {
         const int64_t tiles = ceil_div(fp.N, 128) * ceil_div(fp.M, BN);
@@ -809,7 +838,7 @@ cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const Fused
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(fused_threads(QT, LAYOUT, BN));
+    cfg.blockDim = dim3(fused_threads(QT, LAYOUT, BN, CTAS));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -833,6 +862,19 @@ cudaError_t launch_bn(int bn, const CUtensorMap* w, const CUtensorMap& b, const 
         default: return split ? launch_fused<QT, LAYOUT, 32, false, true>(w, b, fp, s)
                               : launch_fused<QT, LAYOUT, 32>(w, b, fp, s);
     }
+}
+
+// The grouped (MoE) form: two CTAs per SM where half of shared memory still
+// holds four activation stages and two raw slots (GGUF_MM_MOE_CTAS=1 in the
+// environment, read at each call, keeps one: a comparison arm).
+template <int QT>
+cudaError_t launch_grouped(const CUtensorMap* w, const CUtensorMap& b, const FusedParams& fp, cudaStream_t s,
+                           int grid_y) {
+    if constexpr (two_ctas_fit<QT, 0>()) {
+        const char* env = std::getenv("GGUF_MM_MOE_CTAS");
+        if (!(env && env[0] == '1')) return launch_fused<QT, 0, 128, true, false, 2>(w, b, fp, s, grid_y);
+    }
+    return launch_fused<QT, 0, 128, true>(w, b, fp, s, grid_y);
 }
 
 }  // namespace
@@ -943,14 +985,14 @@ int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t
     const int gy = (int)max_tiles;
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {
-        case GGUF_Q4_0: e = launch_fused<GGUF_Q4_0, 0, 128, true>(tw, tb, fp, stream, gy); break;
-        case GGUF_Q4_1: e = launch_fused<GGUF_Q4_1, 0, 128, true>(tw, tb, fp, stream, gy); break;
-        case GGUF_Q5_0: e = launch_fused<GGUF_Q5_0, 0, 128, true>(tw, tb, fp, stream, gy); break;
-        case GGUF_Q5_1: e = launch_fused<GGUF_Q5_1, 0, 128, true>(tw, tb, fp, stream, gy); break;
-        case GGUF_Q8_0: e = launch_fused<GGUF_Q8_0, 0, 128, true>(tw, tb, fp, stream, gy); break;
-        case GGUF_Q4_K: e = launch_fused<GGUF_Q4_K, 0, 128, true>(tw, tb, fp, stream, gy); break;
-        case GGUF_Q5_K: e = launch_fused<GGUF_Q5_K, 0, 128, true>(tw, tb, fp, stream, gy); break;
-        case GGUF_Q6_K: e = launch_fused<GGUF_Q6_K, 0, 128, true>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q4_0: e = launch_grouped<GGUF_Q4_0>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q4_1: e = launch_grouped<GGUF_Q4_1>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q5_0: e = launch_grouped<GGUF_Q5_0>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q5_1: e = launch_grouped<GGUF_Q5_1>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q8_0: e = launch_grouped<GGUF_Q8_0>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q4_K: e = launch_grouped<GGUF_Q4_K>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q5_K: e = launch_grouped<GGUF_Q5_K>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q6_K: e = launch_grouped<GGUF_Q6_K>(tw, tb, fp, stream, gy); break;
     }
     return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
 }

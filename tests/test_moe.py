@@ -121,6 +121,20 @@ def test_moe_full_width_tiles_give_the_same_output(monkeypatch):
     assert np.array_equal(got_full, got)
 
 
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q5_K, syn.Q4_0, syn.Q4_1, syn.Q5_0])
+def test_moe_one_cta_per_sm_arm(qtype, monkeypatch):
+    # the grouped GEMM of these formats runs two CTAs per SM (each with one MMA
+    # issuer); the comparison arm keeps one per SM (two issuers) -- both against
+    # the oracle, on tiles with a residual and ragged token columns
+    E, N, K, T, top_k = 12, 384, 1024, 70, 4
+    ids = syn.zipf_ids(syn.rng(78), T, E, top_k, 1.1)
+    got, ref = _run(qtype, E, N, K, T, top_k, ids, residual=True)
+    U.check_close(got.reshape(-1, N), ref.reshape(-1, N), "bf16")
+    monkeypatch.setenv("GGUF_MM_MOE_CTAS", "1")
+    got1, ref1 = _run(qtype, E, N, K, T, top_k, ids, residual=True)
+    U.check_close(got1.reshape(-1, N), ref1.reshape(-1, N), "bf16")
+
+
 @pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q8_0])
 def test_moe_per_slot_activations(qtype):
     # down-projection form: every (token, slot) row has its own activations
