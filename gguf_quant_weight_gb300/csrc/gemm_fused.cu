@@ -41,11 +41,18 @@ namespace gg {
 namespace {
 
 // decoder warps: 16 (each thread a quarter of a 64-value k step) for the
-// layouts decoded from a per-super-block state, else 8 (each thread a half)
+// layouts decoded from a per-super-block state, else 8 (each thread a half).
+// Q4_K / Q5_K take 8 half-step warps below BN = 256: a warp's per-step work
+// of waits, addresses and the TMEM store is then spread over twice the values
+// (measured, Q5_K 14336 x 4096: M = 8 / 64 / 128 26.5 -> 24.2, 27.7 -> 25.8,
+// 28.3 -> 27.1 us; MoE T = 32 / 512 43.3 -> 39.3, 73.8 -> 68.6 us), while the
+// BN = 256 tiles of M >= 256 keep 16 (8 cost them 3-5 %).
 __host__ __device__ constexpr bool state_decoder(int qt, int layout) {
     return qt == GGUF_Q4_K || qt == GGUF_Q5_K || (qt == GGUF_Q6_K && layout == GGUF_LAYOUT_Q6K_PLANES);
 }
-__host__ __device__ constexpr int decode_warps(int qt, int layout) { return state_decoder(qt, layout) ? 16 : 8; }
+__host__ __device__ constexpr int decode_warps(int qt, int layout, int bn) {
+    return state_decoder(qt, layout) && !((qt == GGUF_Q4_K || qt == GGUF_Q5_K) && bn <= 128) ? 16 : 8;
+}
 // MMA-issuing threads.  One tcgen05.mma costs the thread that issues it ~60
 // cycles (more beside busy decoder warps) -- at BN <= 128 far longer than the
 // tensor core takes to run it -- while threads in different warps issue in
@@ -60,7 +67,7 @@ __host__ __device__ constexpr int mma_issuers(int bn, int ctas = 1) { return (bn
 // activation TMA producer; warps 3 .. 3+DW-1: decoders (and the epilogue);
 // the last NI - 1 warps: MMA issuers 1 .. NI-1
 __host__ __device__ constexpr int fused_threads(int qt, int layout, int bn, int ctas = 1) {
-    return 96 + 32 * decode_warps(qt, layout) + 32 * (mma_issuers(bn, ctas) - 1);
+    return 96 + 32 * decode_warps(qt, layout, bn) + 32 * (mma_issuers(bn, ctas) - 1);
 }
 
 __host__ __device__ constexpr int raw_pitch(int qt, int layout) {
@@ -260,10 +267,13 @@ struct KbState {
 
 // A quarter of k step q of a super-block from a prepared state (Q4_K, Q5_K,
 // Q6_K planes): values 32hf + 16hh .. +15 of the step (one 16-byte piece of the
-// code bytes; Q6_K: exactly one 16-value sub-block).
-template <int QT, int LAYOUT>
+// code bytes; Q6_K: exactly one 16-value sub-block).  HALF: the state was
+// prepared for a half-step decoder (all of its 32 Q5_K high-bit bytes kept;
+// Q4_K / Q5_K only).
+template <int QT, int LAYOUT, bool HALF = false>
 __device__ __forceinline__ void decode_quarter(const KbState<QT, LAYOUT>& st, uint32_t row, uint32_t slot, int r,
                                                int q, int hf, int hh, uint4 out[2]) {
+    static_assert(!HALF || QT == GGUF_Q4_K || QT == GGUF_Q5_K, "half-step states: Q4_K / Q5_K");
     uint32_t q4[4];
     __half2 scv, noffv, bias;
     if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K) {
@@ -273,7 +283,10 @@ __device__ __forceinline__ void decode_quarter(const KbState<QT, LAYOUT>& st, ui
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             uint32_t v = (word_of(a, i) >> sh) & 0x0F0F0F0Fu;
-            if constexpr (QT == GGUF_Q5_K) v |= __funnelshift_l(st.qh[i], st.qh[i], rot) & 0x10101010u;
+            if constexpr (QT == GGUF_Q5_K) {
+                const uint32_t h = st.qh[(HALF ? 4 * hh : 0) + i];
+                v |= __funnelshift_l(h, h, rot) & 0x10101010u;
+            }
             q4[i] = v;
         }
         scv = st.sc[q];
@@ -439,7 +452,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN, CTAS), CTAS)
     static_assert(C::OK, "raw ring needs two slots");
     constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
     constexpr int PITCH = raw_pitch(QT, LAYOUT);
-    constexpr int DW = decode_warps(QT, LAYOUT);   // decoder warps
+    constexpr int DW = decode_warps(QT, LAYOUT, BN);   // decoder warps
     constexpr int NI = C::NI;                      // MMA issuers
     // k steps a decoder warp takes per round: two for Q6_K (measured: raw
     // blocks 170 -> 101 us, planes 187 -> 182 us at M = 512 / 2048), one for
@@ -624,6 +637,18 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN, CTAS), CTAS)
                     for (int d = 0; d < DB; ++d) {   // values 32hf + 16hh .. +15 of step i + d
                         const uint32_t ta = tmem + t_lane + (uint32_t)(C::A_COL0 + ((i + d) % C::S) * C::A_COLS);
                         tmem_st8(ta + (uint32_t)(16 * hf + 8 * hh), v[d]);
+                    }
+                } else if constexpr (STATE) {
+#pragma unroll
+                    for (int d = 0; d < DB; ++d) {   // values 32hf .. +31 of step i + d: two quarters
+                        uint4 out[4];
+                        decode_quarter<QT, LAYOUT, true>(st, row, slot, r, q + d, hf, 0, out);
+                        decode_quarter<QT, LAYOUT, true>(st, row, slot, r, q + d, hf, 1, out + 2);
+                        const uint32_t v[16] = {out[0].x, out[0].y, out[0].z, out[0].w, out[1].x, out[1].y,
+                                                out[1].z, out[1].w, out[2].x, out[2].y, out[2].z, out[2].w,
+                                                out[3].x, out[3].y, out[3].z, out[3].w};
+                        const uint32_t ta = tmem + t_lane + (uint32_t)(C::A_COL0 + ((i + d) % C::S) * C::A_COLS);
+                        tmem_st16(ta + (uint32_t)(16 * hf), v);
                     }
                 } else {
 #pragma unroll
