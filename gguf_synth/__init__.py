@@ -11,6 +11,9 @@ Block structs (byte offsets inside one block) follow the GGUF on-disk layout:
   Q5_0  22 B / 32 values : d f16 @0, qh[4] @2 (bit e: fifth bit of element e), qs[16] @6
   Q5_1  24 B / 32 values : d f16 @0, m f16 @2, qh[4] @4, qs[16] @8
 
+  Q2_K  84 B / 256 values: scales[16] @0 (scale | min << 4), qs[64] @16, d f16 @80, dmin f16 @82
+  Q3_K 110 B / 256 values: hmask[32] @0, qs[64] @32, scales[12] @96, d f16 @108
+
   Q8_0  34 B / 32 values : d f16 @0, qs[32] i8 @2
   Q4_K 144 B / 256 values: d f16 @0, dmin f16 @2, scales[12] @4, qs[128] @16
   Q5_K 176 B / 256 values: d f16 @0, dmin f16 @2, scales[12] @4, qh[32] @16, qs[128] @48
@@ -26,6 +29,8 @@ Recipes (one per workload family, all N(0,1)/uniform draws from numpy PCG64):
   * Q8_0: q uniform integers in [-127, 127], d = f16(|N(0,1)|*1e-3)
   * Q4_0 / Q5_0: qs/qh uniform bytes, d = f16(|N(0,1)|*1e-3)
   * Q4_1 / Q5_1: as Q4_0 / Q5_0, plus m = f16(-8e-3 * |N(0,1)| * (1 + |N(0,1)|))
+  * Q2_K: scales/qs uniform bytes, d and dmin = f16(|N(0,1)|*1e-3)
+  * Q3_K: hmask/qs/scales uniform bytes, d = f16(|N(0,1)|*1e-3)
   * activations and residuals: N(0,1), kept as f32 or rounded to bf16/f16
   * MoE ids: per token top_k distinct experts drawn in turn without replacement,
     P(rank r) proportional to r**-s over ranks 1..n_expert, expert id = rank - 1
@@ -35,10 +40,13 @@ from __future__ import annotations
 import numpy as np
 
 Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 3, 6, 7, 8, 12, 13, 14
-QTYPE_NAMES = {Q4_0: "Q4_0", Q4_1: "Q4_1", Q5_0: "Q5_0", Q5_1: "Q5_1", Q8_0: "Q8_0", Q4_K: "Q4_K",
-               Q5_K: "Q5_K", Q6_K: "Q6_K"}
-BLOCK_VALUES = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210}
+Q2_K, Q3_K = 10, 11
+QTYPE_NAMES = {Q4_0: "Q4_0", Q4_1: "Q4_1", Q5_0: "Q5_0", Q5_1: "Q5_1", Q8_0: "Q8_0", Q2_K: "Q2_K", Q3_K: "Q3_K",
+               Q4_K: "Q4_K", Q5_K: "Q5_K", Q6_K: "Q6_K"}
+BLOCK_VALUES = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q2_K: 256, Q3_K: 256, Q4_K: 256, Q5_K: 256,
+                Q6_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q2_K: 84, Q3_K: 110, Q4_K: 144, Q5_K: 176,
+               Q6_K: 210}
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -73,6 +81,11 @@ def weight_blocks(g: np.random.Generator, qtype: int, N: int, K: int) -> np.ndar
         blk[:, 208:210] = _f16_scale_bytes(g, nb)
     elif qtype in (Q4_0, Q5_0):
         blk[:, 0:2] = _f16_scale_bytes(g, nb)
+    elif qtype == Q2_K:
+        blk[:, 80:82] = _f16_scale_bytes(g, nb)
+        blk[:, 82:84] = _f16_scale_bytes(g, nb)
+    elif qtype == Q3_K:
+        blk[:, 108:110] = _f16_scale_bytes(g, nb)
     elif qtype in (Q4_1, Q5_1):
         blk[:, 0:2] = _f16_scale_bytes(g, nb)
         # the min: m = -8 * |N(0,1)| * 1e-3 * (1 + |N(0,1)|), negative like a block's smallest weight

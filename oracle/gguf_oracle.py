@@ -42,8 +42,11 @@ from __future__ import annotations
 import numpy as np
 
 Q4_0, Q4_1, Q5_0, Q5_1, Q8_0, Q4_K, Q5_K, Q6_K = 2, 3, 6, 7, 8, 12, 13, 14   # GGUF type ids
-BLOCK_VALUES = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q4_K: 256, Q5_K: 256, Q6_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q4_K: 144, Q5_K: 176, Q6_K: 210}
+Q2_K, Q3_K = 10, 11
+BLOCK_VALUES = {Q4_0: 32, Q4_1: 32, Q5_0: 32, Q5_1: 32, Q8_0: 32, Q2_K: 256, Q3_K: 256, Q4_K: 256, Q5_K: 256,
+                Q6_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q4_1: 20, Q5_0: 22, Q5_1: 24, Q8_0: 34, Q2_K: 84, Q3_K: 110, Q4_K: 144, Q5_K: 176,
+               Q6_K: 210}
 
 
 # ----------------------------------------------------------------------------
@@ -232,7 +235,75 @@ def dequant_q5_1(blk: np.ndarray) -> np.ndarray:
     return np.stack([(b32_nibble(qs, e) + 16 * b32_fifth_bit(qh, e)) * d + m for e in range(32)], axis=1)
 
 
+# ---- the 2- and 3-bit K-quants of the type table ([mobius] 1.2: Q2_K "K-quant
+# super-blocks, mixed", Q3_K "3-bit dominant"; 256 values, 16 sub-blocks of 16).
+# The pages give neither struct; the readings (GGUF on-disk layout) are:
+#   Q2_K 84 B  {scales[16] @0, qs[64] @16, d f16 @80, dmin f16 @82}
+#              scales byte j: low nibble = sub-block scale, high nibble = min;
+#              w = d * (scales[j] & 15) * q2 - dmin * (scales[j] >> 4)
+#   Q3_K 110 B {hmask[32] @0, qs[64] @32, scales[12] @96, d f16 @108}
+#              q3 = q2 - 4 when the element's hmask bit is clear, else q2;
+#              w = d * (scale6_j - 32) * q3
+# with the 2-bit codes laid out alike in both (k2_position).
+
+def k2_position(e: int):
+    """(byte of qs, bit shift) of the 2-bit code of element e (0..255) of a
+    Q2_K / Q3_K super-block: two halves of 128; in half h, element
+    r = 32j + 16p + l (j = 0..3, p = 0..1, l = 0..15) is bits 2j..2j+1 of
+    qs[32h + 16p + l].  Its sub-block (scale) is e // 16."""
+    h, r = divmod(e, 128)
+    j, r2 = divmod(r, 32)
+    p, l = divmod(r2, 16)
+    return 32 * h + 16 * p + l, 2 * j
+
+
+def q2_code(qs: np.ndarray, e: int) -> np.ndarray:
+    byte, shift = k2_position(e)
+    return (qs[:, byte].astype(np.int64) >> shift) & 3
+
+
+def dequant_q2_k(blk: np.ndarray) -> np.ndarray:
+    """[nb, 84] u8 -> [nb, 256] f64 (reading above)."""
+    sc = blk[:, 0:16].astype(np.int64)
+    qs = blk[:, 16:80]
+    d, dmin = f16_field(blk[:, 80:82]), f16_field(blk[:, 82:84])
+    out = np.empty((blk.shape[0], 256), dtype=np.float64)
+    for e in range(256):
+        j = e // 16
+        out[:, e] = d * (sc[:, j] & 15) * q2_code(qs, e) - dmin * (sc[:, j] >> 4)
+    return out
+
+
+def q3k_scale6(s: np.ndarray, i: int) -> np.ndarray:
+    """Sub-block scale i (0..15, unsigned 6 bits) of a Q3_K block from its 12
+    scale bytes s [nb, 12] (reading: GGUF packing): the low 4 bits are the low
+    (i < 8) or high (i >= 8) nibble of byte i % 8, the top 2 bits are bits
+    2 * (i // 4) .. +1 of byte 8 + i % 4."""
+    s = s.astype(np.int64)
+    low = (s[:, i % 8] & 15) if i < 8 else (s[:, i % 8] >> 4)
+    top = (s[:, 8 + i % 4] >> (2 * (i // 4))) & 3
+    return low | (top << 4)
+
+
+def q3_code(hmask: np.ndarray, qs: np.ndarray, e: int) -> np.ndarray:
+    """Signed 3-bit code (-4..3) of element e: its 2-bit code, less 4 when bit
+    e // 32 of hmask[e % 32] is clear."""
+    hbit = (hmask[:, e % 32].astype(np.int64) >> (e // 32)) & 1
+    return q2_code(qs, e) - 4 * (1 - hbit)
+
+
+def dequant_q3_k(blk: np.ndarray) -> np.ndarray:
+    """[nb, 110] u8 -> [nb, 256] f64 (reading above)."""
+    hmask, qs, s = blk[:, 0:32], blk[:, 32:96], blk[:, 96:108]
+    d = f16_field(blk[:, 108:110])
+    out = np.empty((blk.shape[0], 256), dtype=np.float64)
+    for e in range(256):
+        out[:, e] = d * (q3k_scale6(s, e // 16) - 32) * q3_code(hmask, qs, e)
+    return out
+
+
 _DECODERS = {Q4_0: dequant_q4_0, Q4_1: dequant_q4_1, Q5_0: dequant_q5_0, Q5_1: dequant_q5_1,
+             Q2_K: dequant_q2_k, Q3_K: dequant_q3_k,
              Q8_0: dequant_q8_0, Q4_K: dequant_q4_k, Q5_K: dequant_q5_k, Q6_K: dequant_q6_k}
 
 
@@ -344,6 +415,8 @@ def weight_int_terms(w: np.ndarray, qtype: int, N: int, K: int):
       Q4_K: q_w = nibble,   scale = d*sc_j, minv = dmin*m_j
       Q5_K: q_w = q5,       scale = d*sc_j, minv = dmin*m_j
       Q6_K: q_w = q6 - 32,  scale = d*scales[j] (16-wide sub-blocks)
+      Q2_K: q_w = q2,       scale = d*(sc_j & 15), minv = dmin*(sc_j >> 4) (16-wide)
+      Q3_K: q_w = q3,       scale = d*(scale6_j - 32) (16-wide)
     """
     bv, bb = BLOCK_VALUES[qtype], BLOCK_BYTES[qtype]
     nb = N * (K // bv)
@@ -381,6 +454,16 @@ def weight_int_terms(w: np.ndarray, qtype: int, N: int, K: int):
         scale = np.stack([d * decode_6bit(s, j) for j in range(8)], axis=1)
         minv = np.stack([dmin * decode_6bit(s, j + 8) for j in range(8)], axis=1)
         return q.reshape(N, K), 32, scale.reshape(N, -1), minv.reshape(N, -1)
+    if qtype == Q2_K:
+        sc = blk[:, 0:16].astype(np.int64)
+        d, dmin = f16_field(blk[:, 80:82]), f16_field(blk[:, 82:84])
+        q = np.stack([q2_code(blk[:, 16:80], e) for e in range(256)], axis=1)
+        return q.reshape(N, K), 16, (d[:, None] * (sc & 15)).reshape(N, -1), (dmin[:, None] * (sc >> 4)).reshape(N, -1)
+    if qtype == Q3_K:
+        d = f16_field(blk[:, 108:110])
+        q = np.stack([q3_code(blk[:, 0:32], blk[:, 32:96], e) for e in range(256)], axis=1)
+        scale = np.stack([d * (q3k_scale6(blk[:, 96:108], j) - 32) for j in range(16)], axis=1)
+        return q.reshape(N, K), 16, scale.reshape(N, -1), np.zeros((N, K // 16))
     if qtype == Q6_K:
         ql, qh = blk[:, 0:128], blk[:, 128:192]
         sc = blk[:, 192:208].view(np.int8).astype(np.float64)
@@ -402,15 +485,18 @@ def int8_dots(q_w: np.ndarray, sub: int, qa: np.ndarray) -> np.ndarray:
 def gemv_int8_path(w: np.ndarray, qtype: int, N: int, K: int, x32: np.ndarray,
                    residual: np.ndarray | None = None, return_terms: bool = False):
     """y[m, n] = sum_j scale[n,j] * d_a[m,b(j)] * D[m,n,j]
-                - sum_j minv[n,j]  * d_a[m,b(j)] * s[m,b(j)]   (+ residual)
+                - sum_j minv[n,j]  * d_a[m,b(j)] * s_j[m,j]   (+ residual)
     with b(j) the 32-wide activation block holding sub-block j (b = j for 32-wide
-    sub-blocks, b = j // 2 for Q6_K's 16-wide ones).  Terms in float64."""
+    sub-blocks, b = j // 2 for the 16-wide ones of Q2_K/Q3_K/Q6_K) and s_j the
+    sum of the activation codes over sub-block j itself (the block's s for
+    32-wide sub-blocks, one half of it for 16-wide ones).  Terms in float64."""
     qa, d_a, s = quantize_act_q8(x32)
     q_w, sub, scale, minv = weight_int_terms(w, qtype, N, K)
     D = int8_dots(q_w, sub, qa)                                # [M, N, K/sub] int64
     per = 32 // sub                                            # sub-blocks per activation block
     da_j = np.repeat(d_a.astype(np.float64), per, axis=1)      # [M, K/sub]
-    s_j = np.repeat(s.astype(np.float64), per, axis=1)         # minv is 0 whenever per > 1
+    M = qa.shape[0]
+    s_j = qa.astype(np.int64).reshape(M, K // sub, sub).sum(axis=2).astype(np.float64)
     y = np.einsum("nj,mj,mnj->mn", scale, da_j, D.astype(np.float64))
     y = y - np.einsum("nj,mj,mj->mn", minv, da_j, s_j)
     if residual is not None:

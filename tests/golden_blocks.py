@@ -103,3 +103,28 @@ def q5_0():
 
 def q5_1():
     return _b32("q5_1_block.json", 24, 8, qh_off=4, m=True)
+
+
+def q2_k():
+    g = load("q2_k_block.json")
+    f = g["fields"]
+    b = np.zeros(84, np.uint8)
+    b[0:16] = f["scales"]
+    for i, v in f["qs_nonzero"].items():
+        b[16 + int(i)] = v
+    b[80:82] = _f16(_hexbits(f["d_f16_bits"]))
+    b[82:84] = _f16(_hexbits(f["dmin_f16_bits"]))
+    return b, {int(k): v for k, v in g["expected"].items()}
+
+
+def q3_k():
+    g = load("q3_k_block.json")
+    f = g["fields"]
+    b = np.zeros(110, np.uint8)
+    for i, v in f["hmask_nonzero"].items():
+        b[int(i)] = v
+    for i, v in f["qs_nonzero"].items():
+        b[32 + int(i)] = v
+    b[96:108] = f["scales"]
+    b[108:110] = _f16(_hexbits(f["d_f16_bits"]))
+    return b, {int(k): v for k, v in g["expected"].items()}

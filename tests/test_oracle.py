@@ -14,7 +14,8 @@ from tests import golden_blocks as gb
 # ---------------------------------------------------------------- hand-worked blocks
 
 @pytest.mark.parametrize("builder,decoder", [
-    (gb.q4_k, O.dequant_q4_k), (gb.q5_k, O.dequant_q5_k), (gb.q6_k, O.dequant_q6_k)])
+    (gb.q4_k, O.dequant_q4_k), (gb.q5_k, O.dequant_q5_k), (gb.q6_k, O.dequant_q6_k), (gb.q2_k, O.dequant_q2_k),
+    (gb.q3_k, O.dequant_q3_k)])
 def test_hand_worked_kquant_blocks(builder, decoder):
     blk, expected = builder()
     w = decoder(blk[None, :])[0]
@@ -62,7 +63,7 @@ def _set_f16(blk, off, val):
     blk[:, off:off + 2] = np.array([val], np.float16).view(np.uint8)
 
 
-@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q2_K, O.Q3_K, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_all_zero_blocks_decode_to_zero(qtype):
     w = O._DECODERS[qtype](_blocks_of(qtype, 0))
     assert np.all(w == 0)
@@ -70,13 +71,19 @@ def test_all_zero_blocks_decode_to_zero(qtype):
 
 @pytest.mark.parametrize("qtype,value", [(O.Q4_K, 882.0), (O.Q5_K, 1890.0), (O.Q6_K, -31.0),
                                          (O.Q8_0, -1.0), (O.Q4_0, 7.0), (O.Q4_1, 16.0), (O.Q5_0, 15.0),
-                                         (O.Q5_1, 32.0)])
+                                         (O.Q5_1, 32.0), (O.Q2_K, 30.0), (O.Q3_K, 93.0)])
 def test_all_max_bit_patterns(qtype, value):
     # all quant/scale bytes 0xFF, d = dmin = 1: sc = m = 63 and q at its maximum;
     # 32-value formats: q = 15 (31 with the fifth bit), d = m = 1:
-    # (15 - 8), 15 + 1, (31 - 16), 31 + 1
+    # (15 - 8), 15 + 1, (31 - 16), 31 + 1; Q2_K: sc = m = 15, q = 3: 15*3 - 15;
+    # Q3_K: scale6 = 63, every hmask bit set, q = 3: (63 - 32) * 3
     blk = _blocks_of(qtype, 0xFF)
-    if qtype in (O.Q8_0, O.Q4_0, O.Q5_0):
+    if qtype == O.Q2_K:
+        _set_f16(blk, 80, 1.0)
+        _set_f16(blk, 82, 1.0)
+    elif qtype == O.Q3_K:
+        _set_f16(blk, 108, 1.0)
+    elif qtype in (O.Q8_0, O.Q4_0, O.Q5_0):
         _set_f16(blk, 0, 1.0)
     elif qtype in (O.Q4_1, O.Q5_1):
         _set_f16(blk, 0, 1.0)
@@ -101,14 +108,14 @@ def test_q6k_zero_quants_give_minus_32_d_sc():
         assert np.array_equal(w[:, e], -32 * d * sc[:, e // 16])
 
 
-@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q2_K, O.Q3_K, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_scaling_d_by_power_of_two_scales_w(qtype):
     g = syn.rng(7)
     w = syn.weight_blocks(g, qtype, 2, 256)
     blk = w.reshape(-1, syn.BLOCK_BYTES[qtype]).copy()
     base = O._DECODERS[qtype](blk)
     offs = {O.Q8_0: [0], O.Q4_K: [0, 2], O.Q5_K: [0, 2], O.Q6_K: [208], O.Q4_0: [0], O.Q5_0: [0],
-            O.Q4_1: [0, 2], O.Q5_1: [0, 2]}[qtype]
+            O.Q4_1: [0, 2], O.Q5_1: [0, 2], O.Q2_K: [80, 82], O.Q3_K: [108]}[qtype]
     for off in offs:
         d = blk[:, off:off + 2].copy().view(np.float16)[:, 0]
         blk[:, off:off + 2] = (d * np.float16(4)).astype(np.float16).view(np.uint8).reshape(-1, 2)
@@ -129,7 +136,7 @@ def test_synthetic_blocks_follow_the_recipe():
 
 # ---------------------------------------------------------------- matmul vs exact rationals
 
-@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q2_K, O.Q3_K, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_matmul_exact_vs_fraction_brute_force(qtype):
     g = syn.rng(100 + qtype)
     N, K, M = 3, 256, 2
@@ -199,7 +206,7 @@ def test_act_quant_rounds_half_away_from_zero():
 
 # ---------------------------------------------------------------- int8 path reduces to the plain matmul
 
-@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q2_K, O.Q3_K, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_int8_path_equals_exact_when_activations_are_on_the_grid(qtype):
     # x = d_a * integers with amax = 127 * d_a in every block: quantization is
     # lossless, so the int8-path result must equal the exact matmul
@@ -216,7 +223,7 @@ def test_int8_path_equals_exact_when_activations_are_on_the_grid(qtype):
     assert np.max(np.abs(y8 - ref)) <= 1e-12 * np.max(np.abs(ref))
 
 
-@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q2_K, O.Q3_K, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_int8_path_close_to_exact_on_normal_data(qtype):
     # the activation rounding error is the only gap: RMS ~ amax/(127*sqrt(12)) per value
     g = syn.rng(60 + qtype)
@@ -229,7 +236,7 @@ def test_int8_path_close_to_exact_on_normal_data(qtype):
     assert np.max(np.abs(y8 - ref)) > 0
 
 
-@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q4_K, O.Q5_K, O.Q6_K])
+@pytest.mark.parametrize("qtype", [O.Q4_0, O.Q4_1, O.Q5_0, O.Q5_1, O.Q8_0, O.Q2_K, O.Q3_K, O.Q4_K, O.Q5_K, O.Q6_K])
 def test_integer_terms_rebuild_the_decoded_weights(qtype):
     g = syn.rng(80 + qtype)
     N, K = 3, 512
@@ -442,4 +449,52 @@ def test_32_value_codes_by_bit_addressing(qtype):
         if hbits is not None:
             q = q + 16 * hbits[:, e].astype(np.int64)
         want = {O.Q4_0: (q - 8) * d, O.Q5_0: (q - 16) * d}.get(qtype, q * d + m)
+        assert np.array_equal(w[:, e], want), e
+
+
+def test_q3k_zero_codes_give_minus_4_d_scale():
+    # every 2-bit code and hmask bit 0: q3 = -4 everywhere, w = -4 * d * (scale6 - 32)
+    g = syn.rng(9)
+    blk = syn.weight_blocks(g, O.Q3_K, 4, 256).reshape(4, 110)
+    blk[:, 0:96] = 0
+    w = O.dequant_q3_k(blk)
+    d = O.f16_field(blk[:, 108:110])
+    for e in range(256):
+        assert np.array_equal(w[:, e], -4 * d * (O.q3k_scale6(blk[:, 96:108], e // 16) - 32))
+
+
+@pytest.mark.parametrize("qtype", [O.Q2_K, O.Q3_K])
+def test_2_bit_codes_and_q3k_scales_by_bit_addressing(qtype):
+    # element e = 128h + 32j + 16p + l: its code is bits 2j..2j+1 of qs byte
+    # 32h + 16p + l, its Q3_K high bit is bit e // 32 of hmask byte e % 32, and
+    # Q3_K scale i is assembled from unpacked bits of the 12 scale bytes: rebuilt
+    # here from bit arrays and compared with the decoders
+    g = syn.rng(321 + qtype)
+    bb = syn.BLOCK_BYTES[qtype]
+    blk = syn.weight_blocks(g, qtype, 4, 256).reshape(-1, bb)
+    q_off = 16 if qtype == O.Q2_K else 32
+    qbits = np.unpackbits(blk[:, q_off:q_off + 64], axis=1, bitorder="little").reshape(-1, 64, 8)
+    w = O._DECODERS[qtype](blk)
+    if qtype == O.Q2_K:
+        d, dmin = O.f16_field(blk[:, 80:82]), O.f16_field(blk[:, 82:84])
+        sc = blk[:, 0:16].astype(np.int64)
+    else:
+        d = O.f16_field(blk[:, 108:110])
+        hbits = np.unpackbits(blk[:, 0:32], axis=1, bitorder="little").reshape(-1, 32, 8)
+        sbits = np.unpackbits(blk[:, 96:108], axis=1, bitorder="little").reshape(-1, 12, 8)
+    for e in range(256):
+        h, r = divmod(e, 128)
+        j, r2 = divmod(r, 32)
+        byte = 32 * h + r2
+        q = qbits[:, byte, 2 * j].astype(np.int64) + 2 * qbits[:, byte, 2 * j + 1].astype(np.int64)
+        i = e // 16
+        if qtype == O.Q2_K:
+            want = d * (sc[:, i] & 15) * q - dmin * (sc[:, i] >> 4)
+        else:
+            q = q - 4 * (1 - hbits[:, e % 32, e // 32].astype(np.int64))
+            lo_bits = range(0, 4) if i < 8 else range(4, 8)
+            s6 = sum(sbits[:, i % 8, b].astype(np.int64) << k for k, b in enumerate(lo_bits))
+            s6 = s6 + (sbits[:, 8 + i % 4, 2 * (i // 4)].astype(np.int64) << 4)
+            s6 = s6 + (sbits[:, 8 + i % 4, 2 * (i // 4) + 1].astype(np.int64) << 5)
+            want = d * (s6 - 32) * q
         assert np.array_equal(w[:, e], want), e
