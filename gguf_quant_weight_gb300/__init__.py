@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(PKG, "libgguf_mm.so")
 # enums (same values as include/gguf_mm.h)
 GGUF_Q4_0, GGUF_Q4_1, GGUF_Q5_0, GGUF_Q5_1 = 2, 3, 6, 7
 GGUF_Q8_0, GGUF_Q4_K, GGUF_Q5_K, GGUF_Q6_K = 8, 12, 13, 14
+GGUF_Q2_K, GGUF_Q3_K = 10, 11
 GGUF_LAYOUT_BLOCKS, GGUF_LAYOUT_Q6K_PLANES = 0, 1
 GGUF_DT_F32, GGUF_DT_F16, GGUF_DT_BF16 = 0, 1, 2
 GGUF_PATH_AUTO, GGUF_PATH_GEMV, GGUF_PATH_FUSED = 0, 1, 2
@@ -26,10 +27,10 @@ GGUF_ERR_INVALID_ARG, GGUF_ERR_UNSUPPORTED, GGUF_ERR_MISALIGNED = -1, -2, -3
 GGUF_ERR_WORKSPACE, GGUF_ERR_CUDA, GGUF_ERR_TIMEOUT, GGUF_ERR_NO_DEVICE = -4, -5, -6, -7
 GGUF_ERR_IO, GGUF_ERR_FORMAT, GGUF_ERR_NOT_FOUND = -8, -9, -10
 
-BLOCK_VALUES = {GGUF_Q4_0: 32, GGUF_Q4_1: 32, GGUF_Q5_0: 32, GGUF_Q5_1: 32, GGUF_Q8_0: 32, GGUF_Q4_K: 256,
-                GGUF_Q5_K: 256, GGUF_Q6_K: 256}
-BLOCK_BYTES = {GGUF_Q4_0: 18, GGUF_Q4_1: 20, GGUF_Q5_0: 22, GGUF_Q5_1: 24, GGUF_Q8_0: 34, GGUF_Q4_K: 144,
-               GGUF_Q5_K: 176, GGUF_Q6_K: 210}
+BLOCK_VALUES = {GGUF_Q4_0: 32, GGUF_Q4_1: 32, GGUF_Q5_0: 32, GGUF_Q5_1: 32, GGUF_Q8_0: 32, GGUF_Q2_K: 256,
+                GGUF_Q3_K: 256, GGUF_Q4_K: 256, GGUF_Q5_K: 256, GGUF_Q6_K: 256}
+BLOCK_BYTES = {GGUF_Q4_0: 18, GGUF_Q4_1: 20, GGUF_Q5_0: 22, GGUF_Q5_1: 24, GGUF_Q8_0: 34, GGUF_Q2_K: 84,
+               GGUF_Q3_K: 110, GGUF_Q4_K: 144, GGUF_Q5_K: 176, GGUF_Q6_K: 210}
 
 _c_i64, _c_int, _c_sz, _c_vp = ctypes.c_int64, ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
 

@@ -71,8 +71,8 @@ bool pdl_enabled() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool valid_qtype(int t) {
-    return t == GGUF_Q4_0 || t == GGUF_Q4_1 || t == GGUF_Q5_0 || t == GGUF_Q5_1 || t == GGUF_Q8_0 || t == GGUF_Q4_K ||
-           t == GGUF_Q5_K || t == GGUF_Q6_K;
+    return t == GGUF_Q4_0 || t == GGUF_Q4_1 || t == GGUF_Q5_0 || t == GGUF_Q5_1 || t == GGUF_Q8_0 || t == GGUF_Q2_K ||
+           t == GGUF_Q3_K || t == GGUF_Q4_K || t == GGUF_Q5_K || t == GGUF_Q6_K;
 }
 bool valid_dtype(int d) { return d == GGUF_DT_F32 || d == GGUF_DT_F16 || d == GGUF_DT_BF16; }
 

@@ -71,6 +71,8 @@ cudaError_t dequant_padded_launch(const void* w, int qtype, int layout, int64_t 
         case GGUF_Q5_0: return go<GGUF_Q5_0, false>(w, N, K, ld, out, odt, num_sms, s);
         case GGUF_Q5_1: return go<GGUF_Q5_1, false>(w, N, K, ld, out, odt, num_sms, s);
         case GGUF_Q8_0: return go<GGUF_Q8_0, false>(w, N, K, ld, out, odt, num_sms, s);
+        case GGUF_Q2_K: return go<GGUF_Q2_K, false>(w, N, K, ld, out, odt, num_sms, s);
+        case GGUF_Q3_K: return go<GGUF_Q3_K, false>(w, N, K, ld, out, odt, num_sms, s);
         case GGUF_Q4_K: return go<GGUF_Q4_K, false>(w, N, K, ld, out, odt, num_sms, s);
         case GGUF_Q5_K: return go<GGUF_Q5_K, false>(w, N, K, ld, out, odt, num_sms, s);
         case GGUF_Q6_K:

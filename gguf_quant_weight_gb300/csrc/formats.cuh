@@ -13,6 +13,12 @@
 //   Q4_K  {d, dmin f16, scales[12], qs[128]}                 w = d*sc_j*q - dmin*m_j
 //   Q5_K  {d, dmin f16, scales[12], qh[32], qs[128]}         w = d*sc_j*q5 - dmin*m_j
 //   Q6_K  {ql[128], qh[64], scales[16] i8, d f16}            w = d*scales[e/16]*(q6 - 32)
+//   Q2_K  {scales[16], qs[64], d, dmin f16}                  w = d*(sc&15)*q2 - dmin*(sc>>4)
+//   Q3_K  {hmask[32], qs[64], scales[12], d f16}             w = d*(scale6 - 32)*q3
+//         (256 values, sub-block e/16; element 128h + 32j + 16p + l takes bits
+//         2j..2j+1 of qs[32h + 16p + l]; Q3_K: q3 = q2 - 4 when bit e/32 of
+//         hmask[e%32] is clear, scale6 i = low / high nibble of byte i%8 (i < 8 /
+//         i >= 8) | bits 2(i/4)..+1 of byte 8 + i%4 << 4)
 // The min is subtracted exactly, never folded into a rounded integer zero
 // point (OpenVINO PR #38696, "Details").
 #pragma once
@@ -26,8 +32,11 @@ __host__ __device__ constexpr bool block32(int qt) {
 __host__ __device__ constexpr int block_values(int qt) { return block32(qt) ? 32 : 256; }
 __host__ __device__ constexpr int block_bytes(int qt) {
     return qt == GGUF_Q4_0 ? 18 : qt == GGUF_Q4_1 ? 20 : qt == GGUF_Q5_0 ? 22 : qt == GGUF_Q5_1 ? 24
-         : qt == GGUF_Q8_0 ? 34 : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176 : 210;
+         : qt == GGUF_Q8_0 ? 34 : qt == GGUF_Q2_K ? 84 : qt == GGUF_Q3_K ? 110 : qt == GGUF_Q4_K ? 144
+         : qt == GGUF_Q5_K ? 176 : 210;
 }
+// the 2- and 3-bit K-quants (16 sub-blocks of 16 values, 2-byte aligned blocks)
+__host__ __device__ constexpr bool k23(int qt) { return qt == GGUF_Q2_K || qt == GGUF_Q3_K; }
 // byte offset of the 16 code bytes inside a 32-value Q4/Q5 block (the qh word precedes them)
 __host__ __device__ constexpr int b32_qs_offset(int qt) {
     return qt == GGUF_Q4_0 ? 2 : qt == GGUF_Q4_1 ? 4 : qt == GGUF_Q5_0 ? 6 : 8;
@@ -79,6 +88,18 @@ __device__ __forceinline__ float sub_round_odd(float a, float b) {
     return (err != 0.f && isfinite(t)) ? __uint_as_float(__float_as_uint(t) | 1u) : t;   // inf, NaN pass as they are
 }
 
+// 2-bit code of element e of a Q2_K / Q3_K super-block (qs = its 64 code bytes).
+__device__ __forceinline__ int k2_code(const uint8_t* qs, int e) {
+    const int h = e >> 7, j = (e >> 5) & 3;
+    return (qs[32 * h + (e & 31)] >> (2 * j)) & 3;
+}
+
+// Unsigned 6-bit scale i (0..15) of a Q3_K block from its 12 scale bytes.
+__device__ __forceinline__ int q3k_scale6(const uint8_t* s, int i) {
+    const int low = i < 8 ? (s[i & 7] & 15) : (s[i & 7] >> 4);
+    return low | (((s[8 + (i & 3)] >> (2 * (i >> 2))) & 3) << 4);
+}
+
 // Weight value of element e of one block as f32.  Every product is exact in
 // f32 (d, dmin: 11 significant bits; sc, m: 6; q: at most 6); a K-quant's
 // "- dmin*m" is rounded to odd (sub_round_odd), so that the one rounding to
@@ -110,6 +131,15 @@ __device__ __forceinline__ float decode_elem(const uint8_t* blk, int e) {
             q = kquant_nibble(blk + 48, e) + 16 * ((blk[16 + (e & 31)] >> j) & 1);
         }
         return sub_round_odd((d * (float)kquant_6bit(s, j)) * (float)q, dmin * (float)kquant_6bit(s, j + 8));
+    } else if (QT == GGUF_Q2_K) {
+        // d*sc*q2 (11 + 4 + 2 bits) and dmin*m are exact; the difference is rounded to odd
+        const int sc = blk[e >> 4];
+        const float d = ld_f16_bytes(blk + 80), dmin = ld_f16_bytes(blk + 82);
+        return sub_round_odd((d * (float)(sc & 15)) * (float)k2_code(blk + 16, e), dmin * (float)(sc >> 4));
+    } else if (QT == GGUF_Q3_K) {
+        // d*(scale6 - 32)*q3: 11 + 6 + 3 significant bits, exact in f32
+        const int q3 = k2_code(blk + 32, e) - 4 * (1 - ((blk[e & 31] >> (e >> 5)) & 1));
+        return (ld_f16_bytes(blk + 108) * (float)(q3k_scale6(blk + 96, e >> 4) - 32)) * (float)q3;
     } else {
         const float d = ld_f16_bytes(blk + 208);
         const int8_t sc = static_cast<int8_t>(blk[192 + (e >> 4)]);

@@ -71,8 +71,11 @@ __host__ __device__ constexpr int fused_threads(int qt, int layout, int bn, int 
 }
 
 __host__ __device__ constexpr int raw_pitch(int qt, int layout) {
-    // bytes per weight row in one raw slot (= the TMA box's inner extent)
-    return block32(qt) ? 8 * block_bytes(qt) : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176 : (layout ? 0 : 224);
+    // bytes per weight row in one raw slot (= the TMA box's inner extent); the
+    // 2-byte aligned super-blocks (raw Q6_K, Q2_K, Q3_K) are boxed from their
+    // 16-byte boundary, so the box also covers up to 14 leading bytes
+    return block32(qt) ? 8 * block_bytes(qt) : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176
+         : qt == GGUF_Q2_K ? 96 : qt == GGUF_Q3_K ? 128 : (layout ? 0 : 224);
 }
 // bytes of one raw slot (128 rows); the Q6_K planes slot is QL | QH | SC | D
 __host__ __device__ constexpr int raw_slot_bytes(int qt, int layout) {
@@ -381,7 +384,7 @@ __device__ __forceinline__ void b32_block(uint32_t row, uint32_t& d_bits, uint32
 // super-block) of one weight row whose raw bytes start at shared address `row`.
 template <int QT, int LAYOUT>
 __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int q, int hf, int kb, uint4 out[4]) {
-    static_assert(block32(QT) || (QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_BLOCKS),
+    static_assert(block32(QT) || k23(QT) || (QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_BLOCKS),
                   "the other layouts decode from a per-super-block state");
     (void)slot; (void)r; (void)kb;
     const __half2 zero2 = __float2half2_rn(0.f);
@@ -419,6 +422,38 @@ __device__ __forceinline__ void decode32(uint32_t row, uint32_t slot, int r, int
         const __half2 d2 = h2_bits(db * 0x10001u);
         const __half2 noff = b32_has_min(QT) ? __hneg2(h2_bits(mb * 0x10001u)) : zero2;   // emit subtracts the offset
         emit32_h(q4, __float2half2_rn(1024.f + (float)b32_zero_point(QT)), d2, noff, d2, noff, out);
+    } else if constexpr (k23(QT)) {
+        // Q2_K / Q3_K: values 64q + 32hf + t = 128h + 32j + t with h = q/2,
+        // j = 2(q%2) + hf; value t is bits 2j..2j+1 of qs[32h + t], in
+        // sub-block 8h + 2j + t/16 (two 16-value halves, two scales)
+        const int h = q >> 1, j = 2 * (q & 1) + hf, s0 = 8 * h + 2 * j;
+        constexpr uint32_t QS = QT == GGUF_Q2_K ? 16 : 32;
+        uint32_t c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = (lds_w2(row + QS + 32u * h + 4u * i) >> (2 * j)) & 0x03030303u;
+        if constexpr (QT == GGUF_Q2_K) {
+            // w = fl16(d*sc) * q2 - fl16(dmin*m) per half
+            const float d = f16_bits_to_float(lds16u(row + 80)), dmin = f16_bits_to_float(lds16u(row + 82));
+            const uint32_t sw = lds16u(row + (uint32_t)s0);   // scale bytes s0, s0 + 1
+            const float sa = (float)(sw & 15), ma = (float)((sw >> 4) & 15);
+            const float sb = (float)((sw >> 8) & 15), mb = (float)((sw >> 12) & 15);
+            emit32_h(c, __float2half2_rn(1024.f), __float2half2_rn(d * sa), __float2half2_rn(dmin * ma),
+                     __float2half2_rn(d * sb), __float2half2_rn(dmin * mb), out);
+        } else {
+            // the high bit (bit 4h + j of hmask[t]) makes the code q3 + 4 (0..7)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) c[i] |= ((lds_w2(row + 4u * i) >> (4 * h + j)) & 0x01010101u) << 2;
+            const float d = f16_bits_to_float(lds16u(row + 108));
+            const uint32_t lo = (s0 & 7) < 4 ? lds_w2(row + 96) : lds_w2(row + 100);   // bytes s0 % 8, s0 % 8 + 1
+            const uint32_t w8 = lds_w2(row + 104);
+            auto scale6 = [&](int i) {   // i = 8h + t with t = s0 % 8 or s0 % 8 + 1
+                const uint32_t byte = (lo >> (8 * ((i & 7) & 3))) & 0xFF;
+                const uint32_t low = i < 8 ? (byte & 15) : (byte >> 4);
+                return (int)(low | ((((w8 >> (8 * (i & 3))) >> (2 * (i >> 2))) & 3) << 4)) - 32;
+            };
+            emit32_h(c, __float2half2_rn(1028.f), __float2half2_rn(d * (float)scale6(s0)), zero2,
+                     __float2half2_rn(d * (float)scale6(s0 + 1)), zero2, out);
+        }
     } else {
         // raw Q6_K: values 64q + 32hf + l = 128h + 32g + l with h = q/2, g = 2(q%2) + hf
         const int h = q >> 1, g = 2 * (q & 1) + hf;
@@ -545,8 +580,9 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN, CTAS), CTAS)
                     tma_load_2d(dst + 128 * 128, &tmW1, kb * 32, (int)wrow0, &rfull[rs]);         // QH: 64 B
                     tma_load_2d(dst + 128 * 192, &tmW2, kb * 8, (int)wrow0, &rfull[rs]);          // SC: 16 B
                     tma_load_2d(dst + 128 * 208, &tmW3, ((2 * kb) & ~15) / 2, (int)wrow0, &rfull[rs]);  // D: 16 B
-                } else if constexpr (QT == GGUF_Q6_K) {
-                    tma_load_2d(dst, &tmW0, ((210 * kb) & ~15) / 2, (int)wrow0, &rfull[rs]);
+                } else if constexpr (QT == GGUF_Q6_K || k23(QT)) {
+                    constexpr int BB = block_bytes(QT);
+                    tma_load_2d(dst, &tmW0, ((BB * kb) & ~15) / 2, (int)wrow0, &rfull[rs]);
                 } else {
                     tma_load_2d(dst, &tmW0, kb * (PITCH / 2), (int)wrow0, &rfull[rs]);
                 }
@@ -607,7 +643,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN, CTAS), CTAS)
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             const uint32_t slot = smem_u32(sR + rs * RAW);
             uint32_t row = slot + (uint32_t)(r * PITCH);
-            if constexpr (QT == GGUF_Q6_K && !PLANES) row += (uint32_t)((210 * kb) & 15);
+            if constexpr ((QT == GGUF_Q6_K && !PLANES) || k23(QT)) row += (uint32_t)((block_bytes(QT) * kb) & 15);
             constexpr bool STATE = QT == GGUF_Q4_K || QT == GGUF_Q5_K || PLANES;
             KbState<QT, LAYOUT> st;
             if constexpr (STATE) st.prepare(row, slot, r, hf, kb, DW == 16 ? hh : -1);
@@ -914,7 +950,9 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
                    cudaStream_t stream, int pdl) {
     if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
     const int64_t KB = K / 256;
-    if (qtype == GGUF_Q6_K && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;   // 16-byte row strides for TMA
+    // 16-byte row strides for TMA: raw Q6_K and Q3_K rows need K % 2048, Q2_K K % 1024
+    if ((qtype == GGUF_Q6_K || qtype == GGUF_Q3_K) && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;
+    if (qtype == GGUF_Q2_K && KB % 4 != 0) return GGUF_ERR_UNSUPPORTED;
     if (N > INT32_MAX || M > INT32_MAX || KB > (1 << 20)) return GGUF_ERR_UNSUPPORTED;
     const FusedPlan pl = plan_fused(N, M, KB, num_sms);
     const FusedWorkspace wl = fused_workspace(N, K, M, pl);
@@ -971,6 +1009,8 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
         case GGUF_Q5_0: e = launch_bn<GGUF_Q5_0, 0>(bn, tw, tb, fp, stream); break;
         case GGUF_Q5_1: e = launch_bn<GGUF_Q5_1, 0>(bn, tw, tb, fp, stream); break;
         case GGUF_Q8_0: e = launch_bn<GGUF_Q8_0, 0>(bn, tw, tb, fp, stream); break;
+        case GGUF_Q2_K: e = launch_bn<GGUF_Q2_K, 0>(bn, tw, tb, fp, stream); break;
+        case GGUF_Q3_K: e = launch_bn<GGUF_Q3_K, 0>(bn, tw, tb, fp, stream); break;
         case GGUF_Q4_K: e = launch_bn<GGUF_Q4_K, 0>(bn, tw, tb, fp, stream); break;
         case GGUF_Q5_K: e = launch_bn<GGUF_Q5_K, 0>(bn, tw, tb, fp, stream); break;
         case GGUF_Q6_K:
@@ -986,7 +1026,9 @@ int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t
                      const int* rows, int64_t max_tiles, const void* residual, void* y, int ydt, int* status,
                      cudaStream_t stream) {
     const int64_t KB = K / 256;
-    if (qtype == GGUF_Q6_K && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;   // 16-byte row strides for TMA
+    // 16-byte row strides for TMA: raw Q6_K and Q3_K rows need K % 2048, Q2_K K % 1024
+    if ((qtype == GGUF_Q6_K || qtype == GGUF_Q3_K) && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;
+    if (qtype == GGUF_Q2_K && KB % 4 != 0) return GGUF_ERR_UNSUPPORTED;
     if (max_tiles > 65535 || KB > (1 << 20)) return GGUF_ERR_UNSUPPORTED;
     const int bb = block_bytes(qtype) * (block32(qtype) ? 8 : 1);
     const int64_t rb = KB * bb;
@@ -1015,6 +1057,8 @@ int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t
         case GGUF_Q5_0: e = launch_grouped<GGUF_Q5_0>(tw, tb, fp, stream, gy); break;
         case GGUF_Q5_1: e = launch_grouped<GGUF_Q5_1>(tw, tb, fp, stream, gy); break;
         case GGUF_Q8_0: e = launch_grouped<GGUF_Q8_0>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q2_K: e = launch_grouped<GGUF_Q2_K>(tw, tb, fp, stream, gy); break;
+        case GGUF_Q3_K: e = launch_grouped<GGUF_Q3_K>(tw, tb, fp, stream, gy); break;
         case GGUF_Q4_K: e = launch_grouped<GGUF_Q4_K>(tw, tb, fp, stream, gy); break;
         case GGUF_Q5_K: e = launch_grouped<GGUF_Q5_K>(tw, tb, fp, stream, gy); break;
         case GGUF_Q6_K: e = launch_grouped<GGUF_Q6_K>(tw, tb, fp, stream, gy); break;

@@ -477,6 +477,82 @@ __device__ __forceinline__ void unit_rl(const GemvParams& p, uint32_t blk, uint3
     for (int m = 0; m < MT; ++m) acc[m] += d * accd[m] - dmin * accm[m];
 }
 
+// ------------------------------------------------------------------ Q2_K / Q3_K unit
+// Half h of a super-block (128 values; sub-blocks 8h .. 8h+7 of 16 values),
+// its raw block staged in shared memory at `blk` (2-byte aligned).  Element
+// r = 32j + 16p + l of the half is bits 2j..2j+1 of qs[32h + 16p + l]; its
+// sub-block is 8h + 2j + p and its activation block is j (codes 16(2j+p) ..
+// of the unit).  Q3_K's high bit (bit 4h + j of hmask[16p + l]) makes the code
+// q2 + 4 hbit = q3 + 4 in 0..7, so a sub-block's dot of q3 is the unsigned
+// dot less 4 times the sum of its 16 activation codes (the entry's s_lo or s_hi).
+template <int QT, int MT, class A, bool DUMP>
+__device__ __forceinline__ void unit_k23(const GemvParams& p, uint32_t blk, const A& a, int kb, int h,
+                                         float (&acc)[MT], int64_t n) {
+    constexpr bool Q2 = QT == GGUF_Q2_K;
+    auto w32 = [&](uint32_t ad) { return lds16(ad) | (lds16(ad + 2) << 16); };   // word at a 2-byte aligned address
+    uint32_t q[8];                                          // the half's 32 code bytes
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = w32(blk + (Q2 ? 16u : 32u) + 32u * (uint32_t)h + 4u * i);
+    uint32_t hm[8];
+    float d, dmin = 0.f;
+    int sc[8], mn[8];                                       // sub-blocks 8h + t
+    if constexpr (Q2) {
+        d = f16_bits_to_float(lds16(blk + 80));
+        dmin = f16_bits_to_float(lds16(blk + 82));
+        const uint32_t s0 = w32(blk + 8u * (uint32_t)h), s1 = w32(blk + 8u * (uint32_t)h + 4u);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const int b = (int)(((t < 4 ? s0 : s1) >> (8 * (t & 3))) & 0xFF);
+            sc[t] = b & 15;
+            mn[t] = b >> 4;
+        }
+    } else {
+        d = f16_bits_to_float(lds16(blk + 108));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) hm[i] = w32(blk + 4u * i);
+        const uint32_t s0 = w32(blk + 96), s1 = w32(blk + 100), s2 = w32(blk + 104);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            // scale 8h + t: low 4 bits from byte t (low nibble in half 0, high in half 1),
+            // top 2 bits from byte 8 + t%4, bits 2((8h + t)/4) = 4h + 2(t/4)
+            const uint32_t byte = ((t < 4 ? s0 : s1) >> (8 * (t & 3))) & 0xFF;
+            const uint32_t low = h ? (byte >> 4) : (byte & 15);
+            const uint32_t top = ((s2 >> (8 * (t & 3))) >> (4 * h + 2 * (t >> 2))) & 3;
+            sc[t] = (int)(low | (top << 4)) - 32;
+            mn[t] = 0;
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        if (m < p.M) {
+            float u = 0.f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint4 en = a.entry(m, j);
+                int S = 0, Mn = 0;
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    const uint4 codes = a.codes(m, 2 * j + pp);
+                    const int s16 = (int)(pp ? en.w : en.z);
+                    int D = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t v = (q[4 * pp + i] >> (2 * j)) & 0x03030303u;
+                        if constexpr (!Q2) v |= ((hm[4 * pp + i] >> (4 * h + j)) & 0x01010101u) << 2;
+                        D = dp4a(v, comp(codes, i), D);
+                    }
+                    if constexpr (!Q2) D -= 4 * s16;
+                    S += sc[2 * j + pp] * D;
+                    Mn += mn[2 * j + pp] * s16;
+                    if (DUMP && p.dbg_D) dump_D(p, m, n, kb * 16 + 8 * h + 2 * j + pp, 16, D);
+                }
+                u += __uint_as_float(en.x) * (d * i2f(S) - dmin * i2f(Mn));
+            }
+            acc[m] += u;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ Q6_K unit
 struct FragQ6 {
     uint4 ql[4];   // 64 bytes of ql for half h
@@ -816,6 +892,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
                 } else if constexpr (B32) {
                     if (single_unit) unit_b32<QT, MT, decltype(act), DUMP>(p, rowp + (uint32_t)bb * u, act, u, acc, n);
                     else unit_b32<QT, MT, decltype(as), DUMP>(p, rowp + (uint32_t)bb * u, as, u, acc, n);
+                } else if constexpr (k23(QT)) {
+                    if (single_unit) unit_k23<QT, MT, decltype(act), DUMP>(p, rowp + (uint32_t)bb * kb, act, kb, h, acc, n);
+                    else unit_k23<QT, MT, decltype(as), DUMP>(p, rowp + (uint32_t)bb * kb, as, kb, h, acc, n);
                 } else if constexpr (QT == GGUF_Q6_K) {
                     FragQ6 f;
                     if constexpr (PLANES) {
@@ -1724,6 +1803,8 @@ cudaError_t launch_dispatch(const GemvParams& p, int grid, size_t smem, cudaStre
         case GGUF_Q5_0: return launch_mt<GGUF_Q5_0, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
         case GGUF_Q5_1: return launch_mt<GGUF_Q5_1, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
         case GGUF_Q8_0: return launch_mt<GGUF_Q8_0, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
+        case GGUF_Q2_K: return launch_mt<GGUF_Q2_K, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
+        case GGUF_Q3_K: return launch_mt<GGUF_Q3_K, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
         case GGUF_Q4_K: return launch_mt<GGUF_Q4_K, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
         case GGUF_Q5_K: return launch_mt<GGUF_Q5_K, GGUF_LAYOUT_BLOCKS, DUMP>(p, grid, smem, s);
         case GGUF_Q6_K:

@@ -326,7 +326,7 @@ int gguf_file_tensor_as_weight(gguf_file_t f, int64_t index, int* qtype, int64_t
     const Tensor& t = f->tensors[(size_t)index];
     switch (t.type) {
         case GGUF_Q4_0: case GGUF_Q4_1: case GGUF_Q5_0: case GGUF_Q5_1: case GGUF_Q8_0:
-        case GGUF_Q4_K: case GGUF_Q5_K: case GGUF_Q6_K: break;
+        case GGUF_Q2_K: case GGUF_Q3_K: case GGUF_Q4_K: case GGUF_Q5_K: case GGUF_Q6_K: break;
         default: return GGUF_ERR_UNSUPPORTED;
     }
     if (t.dims[2] != 1 || t.dims[3] != 1) return GGUF_ERR_UNSUPPORTED;

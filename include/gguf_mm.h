@@ -23,6 +23,11 @@
  *    e < 16 in the low nibble of qs[e], e >= 16 in the high nibble of
  *    qs[e-16], its fifth bit bit e of the little-endian qh word);
  *    Q8_0 34 B / 32 values {d f16, qs[32] i8}, w = d*q;
+ *    Q2_K 84 B / 256 {scales[16], qs[64], d, dmin f16}, w = d*(sc&15)*q2 -
+ *    dmin*(sc>>4) per 16-value sub-block; Q3_K 110 B / 256 {hmask[32], qs[64],
+ *    scales[12], d f16}, w = d*(scale6 - 32)*q3 with q3 = q2 - 4 where the
+ *    element's hmask bit is clear (element 128h + 32j + 16p + l: bits 2j..2j+1
+ *    of qs[32h + 16p + l]; hmask bit e/32 of byte e%32);
  *    Q4_K 144 B / 256 {d, dmin f16, scales[12], qs[128]}; Q5_K 176 B / 256
  *    {d, dmin, scales[12], qh[32], qs[128]}; for both w = d*sc_j*q - dmin*m_j
  *    (OpenVINO PR #38696 "Details"); Q6_K 210 B / 256 {ql[128], qh[64],
@@ -51,7 +56,7 @@ typedef struct CUstream_st* gguf_stream_t; /* same type as cudaStream_t */
  * Types"). */
 typedef enum {
     GGUF_Q4_0 = 2, GGUF_Q4_1 = 3, GGUF_Q5_0 = 6, GGUF_Q5_1 = 7,
-    GGUF_Q8_0 = 8, GGUF_Q4_K = 12, GGUF_Q5_K = 13, GGUF_Q6_K = 14
+    GGUF_Q8_0 = 8, GGUF_Q2_K = 10, GGUF_Q3_K = 11, GGUF_Q4_K = 12, GGUF_Q5_K = 13, GGUF_Q6_K = 14
 } gguf_qtype;
 
 /* GGUF_LAYOUT_Q6K_PLANES: the Q6_K tensor regrouped once into

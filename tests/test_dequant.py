@@ -28,7 +28,8 @@ def _decode(w, qtype, N, K, ld, odt, layout=0):
     return out.t.cpu().numpy().view(np.uint16)
 
 
-@pytest.mark.parametrize("qtype", [syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1, syn.Q8_0, syn.Q4_K, syn.Q5_K, syn.Q6_K])
+@pytest.mark.parametrize("qtype", [syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1, syn.Q8_0, syn.Q2_K, syn.Q3_K, syn.Q4_K,
+                                   syn.Q5_K, syn.Q6_K])
 @pytest.mark.parametrize("odt", ["f16", "bf16"])
 @pytest.mark.parametrize("N,K,pad", [(3, 256, 64), (65, 512, 0), (17, 1024, 64)])
 def test_dequant_padded(qtype, odt, N, K, pad):

@@ -3,12 +3,13 @@ blocks hit the ends of each field (GGUF Support Proposal for mobius, 7.3 / 7.4
 block structs; OpenVINO PR #39119 "Transformation" for the Q6_K fields):
 
   allff      every quant and scale byte 0xFF, d = dmin = 1 (Q4_K 882, Q5_K 1890,
-             Q6_K -31, Q8_0 -1, Q4_0 7, Q4_1 16, Q5_0 15, Q5_1 32 per the
-             oracle's invariants)
+             Q6_K -31, Q8_0 -1, Q4_0 7, Q4_1 16, Q5_0 15, Q5_1 32, Q2_K 30,
+             Q3_K 93 per the oracle's invariants)
   zero       every byte 0 (d = 0: all weights zero)
   extreme    Q8_0 q = -128 everywhere; K-quants: every 6-bit scale and min 63;
              Q6_K: every scale -128 or 127; Q4_0/Q4_1/Q5_0/Q5_1: codes 0 and
-             15 (31 with every fifth bit set)
+             15 (31 with every fifth bit set); Q2_K: every scale and min 15;
+             Q3_K: 6-bit scales 0 or 63 with every 2-bit code 0
   half_d0    random blocks, d (and dmin) = 0 in every other block
   tiny_d     random blocks with d, dmin = |N(0,1)| * 1e-7 (f16 subnormals)
   q6_scales  random blocks, Q6_K scales uniform over the whole i8 range
@@ -30,7 +31,7 @@ from tests import gpu_util as U
 
 pytestmark = pytest.mark.gpu
 
-QTYPES = [syn.Q8_0, syn.Q4_K, syn.Q5_K, syn.Q6_K, syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1]
+QTYPES = [syn.Q8_0, syn.Q4_K, syn.Q5_K, syn.Q6_K, syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1, syn.Q2_K, syn.Q3_K]
 PATTERNS = ["allff", "zero", "extreme", "half_d0", "tiny_d", "q6_scales", "nan_d"]
 N, K = 128, 2048
 F16_ONE = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
@@ -40,7 +41,7 @@ F16_NAN = np.array([0x00, 0x7E], np.uint8)
 def _d_fields(qtype):
     """Byte offsets of the f16 scale fields d (and dmin) inside a block."""
     return {syn.Q8_0: [0], syn.Q4_K: [0, 2], syn.Q5_K: [0, 2], syn.Q6_K: [208], syn.Q4_0: [0], syn.Q5_0: [0],
-            syn.Q4_1: [0, 2], syn.Q5_1: [0, 2]}[qtype]
+            syn.Q4_1: [0, 2], syn.Q5_1: [0, 2], syn.Q2_K: [80, 82], syn.Q3_K: [108]}[qtype]
 
 
 def edge_weights(qtype, pattern, seed=0):
@@ -61,6 +62,11 @@ def edge_weights(qtype, pattern, seed=0):
             w[:, 4:16] = 0xFF                       # every 6-bit scale and min = 63
         elif qtype == syn.Q6_K:
             w[:, 192:208] = np.where(rs.integers(0, 2, (nb, 16)) > 0, 0x7F, 0x80).astype(np.uint8)
+        elif qtype == syn.Q2_K:                     # every scale and min 15
+            w[:, 0:16] = 0xFF
+        elif qtype == syn.Q3_K:                     # every 6-bit scale 63 or 0 (w scale 31 or -32), codes 0
+            w[:, 96:108] = np.where(rs.integers(0, 2, (nb, 12)) > 0, 0xFF, 0x00).astype(np.uint8)
+            w[:, 32:96] = 0
         else:                                       # 32-value blocks: codes 0 and 15 (31), every fifth bit set
             qo = {syn.Q4_0: 2, syn.Q4_1: 4, syn.Q5_0: 6, syn.Q5_1: 8}[qtype]
             w[:, qo:qo + 16] = np.where(rs.integers(0, 2, (nb, 16)) > 0, 0x0F, 0xF0).astype(np.uint8)

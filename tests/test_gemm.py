@@ -62,6 +62,20 @@ def test_fused_32_value_formats(qtype, N, K, M):
     U.check_close(got, ref, "bf16", what=f"q{qtype} N{N} K{K} M{M}")
 
 
+@pytest.mark.parametrize("qtype,K", [(syn.Q2_K, 1024), (syn.Q2_K, 4096), (syn.Q3_K, 2048), (syn.Q3_K, 4096)])
+@pytest.mark.parametrize("N,M", [(128, 16), (200, 40), (384, 130), (130, 300)])
+def test_fused_2_and_3_bit_kquants(qtype, K, N, M):
+    # raw rows staged by TMA from their 16-byte boundary (84- and 110-byte blocks)
+    got, ref = _gemm(qtype, N, K, M)
+    U.check_close(got, ref, "bf16", what=f"q{qtype} N{N} K{K} M{M}")
+
+
+@pytest.mark.parametrize("qtype", [syn.Q2_K, syn.Q3_K])
+def test_fused_2_and_3_bit_kquants_f32_out_split_k(qtype):
+    got, ref = _gemm(qtype, 256, 4096, 48, ydt="f32")
+    U.check_close(got, ref, "f32", rel=2e-3)
+
+
 @pytest.mark.parametrize("qtype", [syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1])
 def test_fused_32_value_formats_f32_out_split_k(qtype):
     # few row tiles: the plan splits K; f32 output holds the bound raw

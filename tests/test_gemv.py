@@ -49,7 +49,7 @@ def _case(qtype, N, K, M, xdt="bf16", ydt="bf16", residual=True, layout=0, seed=
 def _terms(w, qtype, layout, N, K, x, xdt, M, kernel, residual=None):
     """Runs the debug build of the GEMV (forced kernel, f32 output); returns
     (kernel id that ran, qa, d_a, s, D, y) as numpy."""
-    sub = 16 if qtype == syn.Q6_K else 32
+    sub = 16 if qtype in (syn.Q6_K, syn.Q2_K, syn.Q3_K) else 32   # sub-block width of the dots
     qa = torch.zeros((M, K), dtype=torch.int8, device="cuda")
     da = torch.zeros((M, K // 32), dtype=torch.float32, device="cuda")
     s = torch.zeros((M, K // 32), dtype=torch.int32, device="cuda")
@@ -132,6 +132,22 @@ def test_32_value_formats_integer_terms_bit_exact(qtype, N, K, M):
     # Q4_0 / Q4_1 / Q5_0 / Q5_1 on the staged kernel: dots of (q - 8), (q5 - 16)
     # or the unsigned codes, bit for bit; K need only be a multiple of 32
     assert _assert_terms_exact(qtype, 0, N, K, M, -1, residual=(M == 2)) == STAGED
+
+
+@pytest.mark.parametrize("qtype", [syn.Q2_K, syn.Q3_K])
+@pytest.mark.parametrize("N,K,M", [(37, 768, 1), (37, 256, 3), (300, 2048, 8), (129, 4352, 2)])
+def test_2_and_3_bit_kquants_integer_terms_bit_exact(qtype, N, K, M):
+    # Q2_K / Q3_K on the staged kernel: 16-value sub-block dots of q2 and of q3
+    # (the unsigned q3 + 4 dot less 4 times the sub-block's code sum), bit for bit
+    assert _assert_terms_exact(qtype, 0, N, K, M, -1, residual=(M == 2)) == STAGED
+
+
+@pytest.mark.parametrize("qtype", [syn.Q2_K, syn.Q3_K])
+@pytest.mark.parametrize("N,K", [(1, 256), (3, 512), (128, 1024), (200, 4352)])
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_2_and_3_bit_kquants_outputs(qtype, N, K, M):
+    got, ref, _, _ = _case(qtype, N, K, M)
+    U.check_close(got, ref, "bf16", what=f"q{qtype} N{N} K{K} M{M}")
 
 
 @pytest.mark.parametrize("qtype", QTYPES_32)

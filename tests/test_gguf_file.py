@@ -19,7 +19,7 @@ from oracle import gguf_oracle as O
 from tests import gguf_writer as W
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-QTYPES = [syn.Q8_0, syn.Q4_K, syn.Q5_K, syn.Q6_K, syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1]
+QTYPES = [syn.Q8_0, syn.Q4_K, syn.Q5_K, syn.Q6_K, syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1, syn.Q2_K, syn.Q3_K]
 
 
 @pytest.fixture(scope="module", autouse=True)

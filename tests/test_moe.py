@@ -59,10 +59,10 @@ def test_moe_small_all_rows(qtype, T, top_k):
     U.check_close(got.reshape(T * top_k, N), ref.reshape(T * top_k, N), "bf16")
 
 
-@pytest.mark.parametrize("qtype", [syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1])
+@pytest.mark.parametrize("qtype", [syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1, syn.Q2_K, syn.Q3_K])
 def test_moe_32_value_formats(qtype):
-    # the routed tensor-core path (T * top_k > 128 rows)
-    E, N, K, T, top_k = 6, 128, 512, 70, 2
+    # the routed tensor-core path (T * top_k > 128 rows); also Q2_K / Q3_K (K % 2048)
+    E, N, K, T, top_k = 6, 128, 512 if syn.BLOCK_VALUES[qtype] == 32 else 2048, 70, 2
     ids = _distinct_ids(syn.rng(qtype), T, E, top_k)
     got, ref = _run(qtype, E, N, K, T, top_k, ids)
     U.check_close(got.reshape(-1, N), ref.reshape(-1, N), "bf16")
