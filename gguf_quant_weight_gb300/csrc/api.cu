@@ -292,7 +292,7 @@ static int run_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N,
     DeviceFacts* f = nullptr;
     if ((st = facts(&f)) != GGUF_OK) return st;
     return moe_run(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace,
-                   f->num_sms, f->status, (cudaStream_t)stream, per_slot, dump);
+                   f->num_sms, f->status, (cudaStream_t)stream, per_slot, dump, pdl_enabled() ? 1 : 0);
 }
 
 int gguf_mm_debug_moe_mv_terms(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K,

@@ -28,7 +28,7 @@ int dense_gemm_run(const void* wdense, int wdt, int64_t ld, int64_t N, int64_t K
 int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* xg,
                      const float* xscale, int64_t rows_cap, const int4* tiles, const int* ntiles, const int* offsets,
                      const int* rows, int64_t max_tiles, const void* residual, void* y, int ydt, int* status,
-                     cudaStream_t stream);
+                     cudaStream_t stream, int pdl = 0);
 
 // Launch facts of the current device (SM count, device address of the status
 // word), as the C entry points use them.

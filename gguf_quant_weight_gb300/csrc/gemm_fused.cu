@@ -533,6 +533,7 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN, CTAS), CTAS)
     int64_t wrow0, brow0, t0 = 0;
     int cols, expert = 0, gstart = 0;
     if constexpr (MOE) {
+        pdl_wait();   // the work items and gathered rows come from the kernels before
         if ((int)blockIdx.y >= *fp.ntiles) return;   // uniform exit before any shared state exists
         const int4 tl = fp.tiles[blockIdx.y];
         expert = tl.x;
@@ -904,7 +905,7 @@ cudaError_t launch_fused(const CUtensorMap* w, const CUtensorMap& b, const Fused
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = (!MOE && fp.pdl) ? 1 : 0;
+    attr[0].val.programmaticStreamSerializationAllowed = fp.pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k, w[0], w[1], w[2], w[3], b, fp);
@@ -1024,7 +1025,7 @@ int gemm_fused_run(const void* w, int qtype, int layout, int64_t N, int64_t K, c
 int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* xg,
                      const float* xscale, int64_t rows_cap, const int4* tiles, const int* ntiles, const int* offsets,
                      const int* rows, int64_t max_tiles, const void* residual, void* y, int ydt, int* status,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, int pdl) {
     const int64_t KB = K / 256;
     // 16-byte row strides for TMA: raw Q6_K and Q3_K rows need K % 2048, Q2_K K % 1024
     if ((qtype == GGUF_Q6_K || qtype == GGUF_Q3_K) && KB % 8 != 0) return GGUF_ERR_UNSUPPORTED;
@@ -1048,7 +1049,7 @@ int grouped_gemm_run(const void* w_experts, int qtype, int64_t n_expert, int64_t
     // without the tile-skip (a comparison arm for measurement; same output)
     const char* full = std::getenv("GGUF_MM_MOE_FULL_TILES");
     FusedParams fp{N, rows_cap, (int)KB, residual, y, ydt, status, tiles, ntiles, offsets, rows,
-                   (full && full[0] == '1') ? 1 : 0, 1, nullptr, nullptr, 0, 0, xscale};
+                   (full && full[0] == '1') ? 1 : 0, 1, nullptr, nullptr, 0, 0, xscale, pdl};
     const int gy = (int)max_tiles;
     cudaError_t e = cudaErrorInvalidValue;
     switch (qtype) {

@@ -111,6 +111,7 @@ __device__ __forceinline__ void block_scan2(int a, int b, int& ea, int& eb, int&
 __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const int32_t* __restrict__ ids, int total, int E,
                                                                   int max_tiles, int* offsets, int* ntiles,
                                                                   int4* tiles, int* rows) {
+    pdl_launch_dependents();   // the gather kernel may launch; it waits for these tables
     extern __shared__ int sm[];
     int* cnt = sm;             // [E] rows per expert
     int* cur = sm + E;         // [E] next free position of each group
@@ -185,6 +186,8 @@ __global__ void __launch_bounds__(256) moe_gather_kernel(const void* __restrict_
                                                          const int* __restrict__ rows, int64_t cap,
                                                          uint16_t* __restrict__ xg, float* __restrict__ xscale) {
     const int lane = threadIdx.x & 31;
+    pdl_launch_dependents();   // the grouped GEMM may launch; it waits for the gathered rows
+    pdl_wait();                // the routing tables come from the kernel before
     const int64_t p = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     if (p >= cap || p >= *row_count) return;
     const int64_t t = rows[p] / row_div;
@@ -279,7 +282,7 @@ size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, in
 
 int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
             int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
-            int num_sms, int* status, cudaStream_t stream, bool per_slot, const MoeMvDump* dump) {
+            int num_sms, int* status, cudaStream_t stream, bool per_slot, const MoeMvDump* dump, int pdl) {
     (void)num_sms;
     if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
     const int64_t entries = T * top_k;
@@ -322,12 +325,23 @@ int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64
     moe_route_kernel<<<1, kRouteThreads, route_smem, stream>>>(ids, (int)entries, (int)n_expert, (int)L.max_tiles,
                                                               L.offsets, L.ntiles, L.tiles, L.rows);
     if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;
-    moe_gather_kernel<<<(unsigned)ceil_div(entries, 8), 256, 0, stream>>>(x, xdt, K, per_slot ? 1 : (int)top_k,
-                                                                           L.offsets + n_expert, L.rows, entries,
-                                                                           L.xg, L.xscale);
-    if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;
+    {   // a programmatic dependent of the routing kernel
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ceil_div(entries, 8));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, moe_gather_kernel, x, xdt, (int64_t)K, per_slot ? 1 : (int)top_k,
+                               (const int*)(L.offsets + n_expert), (const int*)L.rows, (int64_t)entries, L.xg,
+                               L.xscale) != cudaSuccess)
+            return GGUF_ERR_CUDA;
+    }
     return grouped_gemm_run(w_experts, qtype, n_expert, N, K, L.xg, L.xscale, entries, L.tiles, L.ntiles, L.offsets,
-                            L.rows, L.max_tiles, residual, y, ydt, status, stream);
+                            L.rows, L.max_tiles, residual, y, ydt, status, stream, pdl);
 }
 
 }  // namespace gg
