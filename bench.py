@@ -473,10 +473,11 @@ def prefill_figures(dev, stream, tc_peak, hbm_peak, only=None):
     return compact, detail
 
 
-def crossover(dev, stream, out_path):
+def crossover(dev, stream, out_path, formats=None):
     """GEMV against the fused GEMM for M = 1..16, every format, at the decode
     shape (4096 x 4096) and the prefill shape (14336 x 4096): us per call in
-    chains of calls on rotating weight copies (both paths forced)."""
+    chains of calls on rotating weight copies (both paths forced).  `formats`:
+    a regular expression over the format names (default: all)."""
     import torch
     import gguf_quant_weight_gb300 as g
     import gguf_synth as syn
@@ -484,7 +485,10 @@ def crossover(dev, stream, out_path):
     table = {}
     for n, k in ((4096, 4096), (14336, 4096)):
         for qt, layout, name in ((13, 0, "Q5_K"), (12, 0, "Q4_K"), (14, 1, "Q6_K_planes"), (14, 0, "Q6_K"),
-                                 (8, 0, "Q8_0")):
+                                 (8, 0, "Q8_0"), (2, 0, "Q4_0"), (3, 0, "Q4_1"), (6, 0, "Q5_0"), (7, 0, "Q5_1"),
+                                 (10, 0, "Q2_K"), (11, 0, "Q3_K")):
+            if formats and not __import__("re").search(formats, name):
+                continue
             w = syn.weight_blocks(syn.rng(7000 + qt), qt, n, k)
             c = max(2, int(np.ceil(2.2 * l2 / w.size)))
             W = torch.from_numpy(w.reshape(-1)).to(dev).repeat(c).view(c, -1)
@@ -536,7 +540,7 @@ def run_gpu(args):
     g.load_library()
     stream = torch.cuda.Stream(device=dev)
     if args.crossover:
-        crossover(dev, stream, args.crossover)
+        crossover(dev, stream, args.crossover, args.crossover_formats)
         return
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     copies = max(3 * 2, int(np.ceil(2.2 * l2 / W_BYTES)))
@@ -716,6 +720,8 @@ def main():
                     help="run only the prefill figures whose key matches (e.g. q6p_14336x4096_m512)")
     ap.add_argument("--crossover", default=None, metavar="OUT.json",
                     help="time GEMV against fused GEMM for M = 1..16 instead, and write the table")
+    ap.add_argument("--crossover-formats", default=None, metavar="REGEX",
+                    help="with --crossover: only the formats whose name matches")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

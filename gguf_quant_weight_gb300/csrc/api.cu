@@ -98,8 +98,7 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CU
 // than L2, bf16 activations; the crossover table of bench.py --crossover):
 // at most 8192 weight rows (measured at 4096 x 4096: at most 64 tiles of 128
 // rows for 152 SMs, so the fused path splits K) and more (14336 x 4096).  A
-// value above 8 keeps every row count the GEMV can take on the GEMV.  Formats
-// not measured keep the pages' threshold of 8.
+// value above 8 keeps every row count the GEMV can take on the GEMV.
 int crossover_rows(int qtype, int layout, int64_t N, int64_t K) {
     (void)K;
     const bool large = N > 8192;
@@ -107,8 +106,14 @@ int crossover_rows(int qtype, int layout, int64_t N, int64_t K) {
         case GGUF_Q4_K: return large ? 7 : 9;
         case GGUF_Q5_K: return large ? 6 : 9;
         case GGUF_Q6_K:
-            return layout == GGUF_LAYOUT_Q6K_PLANES ? (large ? 5 : 8) : (large ? 3 : 4);
+            return layout == GGUF_LAYOUT_Q6K_PLANES ? (large ? 4 : 7) : (large ? 2 : 3);
         case GGUF_Q8_0: return large ? 2 : 6;
+        case GGUF_Q4_0: return large ? 2 : 6;
+        case GGUF_Q4_1: return large ? 3 : 6;
+        case GGUF_Q5_0: return large ? 3 : 6;
+        case GGUF_Q5_1: return large ? 2 : 5;
+        case GGUF_Q2_K: return large ? 2 : 4;
+        case GGUF_Q3_K: return large ? 4 : 5;
         default: return 8;
     }
 }

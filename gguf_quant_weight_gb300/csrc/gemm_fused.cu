@@ -70,13 +70,25 @@ __host__ __device__ constexpr int fused_threads(int qt, int layout, int bn, int 
     return 96 + 32 * decode_warps(qt, layout, bn) + 32 * (mma_issuers(bn, ctas) - 1);
 }
 
+// bytes of one 256-value column of a weight row: eight 32-value blocks or one super-block
+__host__ __device__ constexpr int col_bytes(int qt) { return block32(qt) ? 8 * block_bytes(qt) : block_bytes(qt); }
 __host__ __device__ constexpr int raw_pitch(int qt, int layout) {
-    // bytes per weight row in one raw slot (= the TMA box's inner extent); the
-    // 2-byte aligned super-blocks (raw Q6_K, Q2_K, Q3_K) are boxed from their
-    // 16-byte boundary, so the box also covers up to 14 leading bytes
-    return block32(qt) ? 8 * block_bytes(qt) : qt == GGUF_Q4_K ? 144 : qt == GGUF_Q5_K ? 176
-         : qt == GGUF_Q2_K ? 96 : qt == GGUF_Q3_K ? 128 : (layout ? 0 : 224);
+    // bytes per weight row in one raw slot (= the TMA box's inner extent): the
+    // column, plus up to 14 leading bytes where it is boxed from a 16-byte
+    // boundary (the 2-byte aligned super-blocks of raw Q6_K, Q2_K, Q3_K),
+    // rounded up to an ODD multiple of 16 bytes: the decoder warps read 32
+    // consecutive rows at once, and an even multiple puts them in a few banks
+    // (a 128-byte pitch: every row in the same bank -- Q3_K ran 326 us at
+    // 14336 x 4096, M <= 16, against 45 us for Q2_K)
+    return (qt == GGUF_Q6_K && layout) ? 0
+         : ((((col_bytes(qt) + (col_bytes(qt) % 16 ? 14 : 0) + 15) / 16) % 2 == 0)
+                ? (col_bytes(qt) + (col_bytes(qt) % 16 ? 14 : 0) + 15) / 16 * 16 + 16
+                : (col_bytes(qt) + (col_bytes(qt) % 16 ? 14 : 0) + 15) / 16 * 16);
 }
+static_assert(raw_pitch(GGUF_Q2_K, 0) == 112 && raw_pitch(GGUF_Q3_K, 0) == 144 && raw_pitch(GGUF_Q6_K, 0) == 240 &&
+                  raw_pitch(GGUF_Q4_K, 0) == 144 && raw_pitch(GGUF_Q5_K, 0) == 176 && raw_pitch(GGUF_Q5_1, 0) == 208 &&
+                  raw_pitch(GGUF_Q8_0, 0) == 272 && raw_pitch(GGUF_Q4_1, 0) == 176,
+              "odd multiples of 16 bytes");
 // bytes of one raw slot (128 rows); the Q6_K planes slot is QL | QH | SC | D
 __host__ __device__ constexpr int raw_slot_bytes(int qt, int layout) {
     return (qt == GGUF_Q6_K && layout) ? 128 * (128 + 64 + 16 + 16) : 128 * raw_pitch(qt, layout);
@@ -584,8 +596,8 @@ __global__ void __launch_bounds__(fused_threads(QT, LAYOUT, BN, CTAS), CTAS)
                 } else if constexpr (QT == GGUF_Q6_K || k23(QT)) {
                     constexpr int BB = block_bytes(QT);
                     tma_load_2d(dst, &tmW0, ((BB * kb) & ~15) / 2, (int)wrow0, &rfull[rs]);
-                } else {
-                    tma_load_2d(dst, &tmW0, kb * (PITCH / 2), (int)wrow0, &rfull[rs]);
+                } else {   // columns of a multiple of 16 bytes: boxed from their own start
+                    tma_load_2d(dst, &tmW0, kb * (col_bytes(QT) / 2), (int)wrow0, &rfull[rs]);
                 }
             }
         }

@@ -102,8 +102,8 @@ def test_gemm_workspace_follows_the_tile_plan(lib):
 def test_auto_path_table(lib):
     # the measured crossovers, by format and shape class (up to 8192 weight rows / more)
     big, small = (14336, 4096), (4096, 4096)
-    want = {(12, 0): (9, 7), (13, 0): (9, 6), (14, 1): (8, 5), (14, 0): (4, 3),
-            (8, 0): (6, 2)}
+    want = {(12, 0): (9, 7), (13, 0): (9, 6), (14, 1): (7, 4), (14, 0): (3, 2), (8, 0): (6, 2),
+            (2, 0): (6, 2), (3, 0): (6, 3), (6, 0): (6, 3), (7, 0): (5, 2), (10, 0): (4, 2), (11, 0): (5, 4)}
     for (qt, lay), (c_small, c_big) in want.items():
         for (n, k), c in ((small, c_small), (big, c_big)):
             first_fused = next(M for M in range(1, 12)
