@@ -774,7 +774,7 @@ __device__ __forceinline__ BulkPiece stage_range(uint32_t dst, const uint8_t* w,
 // Row groups: a warp pass covers P rows (P = 32 / U when a row has U < 32
 // units, else 1); groups are dealt to warps round-robin.  Each warp stages its
 // groups through a ring of R slots of p.stage_bytes in shared memory.
-template <int QT, int MT, int LAYOUT, bool REG, bool DUMP>
+template <int QT, int MT, int LAYOUT, bool REG, bool DUMP, bool ROUTED = false>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
     constexpr int NT = kThreads, NW = NT / 32;
     constexpr bool PLANES = QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES;
@@ -785,6 +785,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nb = (int)(p.K / 32);
+    static_assert(!ROUTED || (MT == 1 && !DUMP), "routed rows: one activation row, no dumps");
+    // routed mode: this grid row's expert (a row without one is left untouched),
+    // its weights, and the output row it writes
+    const uint8_t* wsrc = p.w;
+    int64_t out_off = 0, arow = 0;
+    if constexpr (ROUTED) {
+        const int r = (int)blockIdx.y;
+        const int e = p.ids[r];
+        if (e < 0 || e >= p.n_expert) return;   // uniform exit before any shared state exists
+        wsrc = p.w + (int64_t)e * p.N * p.rb;
+        out_off = (int64_t)r * p.N;
+        arow = r / p.route_div;
+    }
     Shared sh;
     sh.qa_row = (uint32_t)qa_row_stride(p.K);
     sh.qa = smem_u32(smem_raw);
@@ -828,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
             pc[np++] = stage_range(dst + (uint32_t)(192 * pb), p.w, 192 * nblk + 16 * b0, 192 * nblk + 16 * (b0 + cb), total);
             pc[np++] = stage_range(dst + (uint32_t)(208 * pb), p.w, 208 * nblk + 2 * b0, 208 * nblk + 2 * (b0 + cb), total);
         } else {
-            pc[np++] = stage_range(dst, p.w, r_begin * p.rb, (r_begin + rows) * p.rb, total);
+            pc[np++] = stage_range(dst, wsrc, r_begin * p.rb, (r_begin + rows) * p.rb, total);
         }
         uint32_t tx = 0;
         for (int i = 0; i < np; ++i) tx += pc[i].bytes;
@@ -846,7 +859,25 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
 
     // 2. activation prologue, once the producer of X has finished
     pdl_wait();
-    load_act_image(p, sh, bars + (NW - warp) * R);   // the barrier after the ring's
+    if constexpr (ROUTED) {
+        // this row's codes and block entries out of the image of img_rows rows
+        uint64_t* bar = bars + (NW - warp) * R;
+        if (threadIdx.x == 0) {
+            mbar_init(bar, 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const uint8_t* img = static_cast<const uint8_t*>(p.act_image);
+            const uint32_t cb = sh.qa_row, eb = 16u * (uint32_t)nb;
+            mbar_arrive_expect_tx(bar, cb + eb);
+            bulk_g2s_u32(sh.qa, img + arow * cb, cb, bar);
+            bulk_g2s_u32(sh.ds, img + p.img_rows * cb + arow * eb, eb, bar);
+        }
+        mbar_wait(bar, 0, p.status);
+    } else {
+        load_act_image(p, sh, bars + (NW - warp) * R);   // the barrier after the ring's
+    }
     __syncthreads();
     if (DUMP && blockIdx.x == 0) {
         for (int64_t i = tid; i < (int64_t)p.M * p.K; i += NT) {
@@ -944,8 +975,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvParams p) {
         if (head && valid) {
             for (int m = 0; m < p.M && m < MT; ++m) {
                 float v = acc[m];
-                if (p.residual) v += load_act(p.residual, p.ydt, (int64_t)m * p.N + n);
-                store_out(p.y, p.ydt, (int64_t)m * p.N + n, v);
+                if (p.residual) v += load_act(p.residual, p.ydt, out_off + (int64_t)m * p.N + n);
+                store_out(p.y, p.ydt, out_off + (int64_t)m * p.N + n, v);
             }
         }
     }
@@ -2105,6 +2136,84 @@ cudaError_t moe_mv_launch(const MoeMvParams& mp, cudaStream_t stream, bool dump)
     dim3 grid((unsigned)ceil_div(mp.N, kMvRows), (unsigned)mp.entries);
     k<<<grid, kMvThreads, smem, stream>>>(mp);
     return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ MoE decode form, other formats
+// The routed rows' activations quantized once into the workspace image, then
+// the staged GEMV kernel in routed mode: grid (row CTAs, routed rows), each
+// CTA streaming its rows of the routed row's expert.
+template <int QT>
+cudaError_t launch_routed(const GemvParams& p, int grid, int rows, size_t smem, cudaStream_t stream) {
+    const int U = (int)(p.K / (block32(QT) ? 32 : 128));
+    auto k = U <= 32 ? gemv_kernel<QT, 1, GGUF_LAYOUT_BLOCKS, true, false, true>
+                     : gemv_kernel<QT, 1, GGUF_LAYOUT_BLOCKS, false, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid, (unsigned)rows);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+int moe_mv_staged_run(const MoeMvParams& mp, int num_sms, int max_smem, cudaStream_t stream) {
+    GemvParams q{};
+    q.x = mp.x;
+    q.xdt = mp.xdt;
+    q.M = (int)mp.rows;
+    q.K = mp.K;
+    q.act_image = const_cast<uint8_t*>(mp.image);
+    q.status = mp.status;
+    GemvParams p{};
+    p.w = mp.w;
+    p.qtype = mp.qtype;
+    p.layout = GGUF_LAYOUT_BLOCKS;
+    p.N = mp.N;
+    p.K = mp.K;
+    p.x = mp.x;
+    p.xdt = mp.xdt;
+    p.M = 1;
+    p.residual = mp.residual;
+    p.y = mp.y;
+    p.ydt = mp.ydt;
+    p.status = mp.status;
+    p.pdl = mp.pdl;
+    p.act_image = q.act_image;
+    p.force = GEMV_STAGED;
+    int grid = 0;
+    size_t smem = 0;
+    // CTAs sized over the whole batch: two per SM up to 16 routed rows, four
+    // above (measured best on 128 experts of 768 x 2048); the plain plan would
+    // give every routed row all the SMs, thousands of few-row CTAs
+    const int fac = mp.entries <= 16 ? 2 : 4;
+    const int per_row = (int)std::max<int64_t>(1, std::min<int64_t>(num_sms, ceil_div((int64_t)fac * num_sms, mp.entries)));
+    if (gemv_plan(p, per_row, max_smem, &grid, &smem) != GGUF_OK) return GGUF_ERR_UNSUPPORTED;
+    p.ids = mp.ids;
+    p.n_expert = mp.n_expert;
+    p.route_div = mp.per_slot ? 1 : mp.top_k;
+    p.img_rows = mp.rows;
+    const int quarters = 4 * q.M * (int)(mp.K / 32);
+    act_quant_kernel<<<(unsigned)ceil_div(quarters, 256), 256, 0, stream>>>(q);
+    if (cudaGetLastError() != cudaSuccess) return GGUF_ERR_CUDA;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (mp.qtype) {
+        case GGUF_Q4_0: e = launch_routed<GGUF_Q4_0>(p, grid, mp.entries, smem, stream); break;
+        case GGUF_Q4_1: e = launch_routed<GGUF_Q4_1>(p, grid, mp.entries, smem, stream); break;
+        case GGUF_Q5_0: e = launch_routed<GGUF_Q5_0>(p, grid, mp.entries, smem, stream); break;
+        case GGUF_Q5_1: e = launch_routed<GGUF_Q5_1>(p, grid, mp.entries, smem, stream); break;
+        case GGUF_Q8_0: e = launch_routed<GGUF_Q8_0>(p, grid, mp.entries, smem, stream); break;
+        case GGUF_Q2_K: e = launch_routed<GGUF_Q2_K>(p, grid, mp.entries, smem, stream); break;
+        case GGUF_Q3_K: e = launch_routed<GGUF_Q3_K>(p, grid, mp.entries, smem, stream); break;
+        case GGUF_Q6_K: e = launch_routed<GGUF_Q6_K>(p, grid, mp.entries, smem, stream); break;
+        default: return GGUF_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? GGUF_OK : GGUF_ERR_CUDA;
 }
 
 }  // namespace gg

@@ -27,6 +27,14 @@ struct GemvParams {
     int chunk_rows;        // rows per staged chunk
     int stages;            // chunk buffers in shared memory
     int64_t stage_bytes;
+    // routed mode (the MoE decode form of the staged kernel): grid.y runs over
+    // the routed rows; row r multiplies activation row r / route_div of the
+    // image (img_rows rows) against the expert ids[r] of n_expert (w holds the
+    // experts' [N, rb] blocks back to back) and writes output row r
+    const int32_t* ids;
+    int64_t n_expert;
+    int route_div;
+    int64_t img_rows;
     // test-only dumps (nullptr in production)
     int8_t* dbg_qa;
     float* dbg_da;
@@ -63,6 +71,7 @@ struct MoeMvParams {
     void* y;
     int ydt;
     int* status;
+    int pdl;                // the GEMV as a dependent launch of the quantizer (other formats)
     // test hook (a separate instantiation): routed row p's activation codes
     // [p][K], scales and sums [p][K/32], sub-block dots [p][N][K/32]
     int8_t* dbg_qa;
@@ -72,5 +81,8 @@ struct MoeMvParams {
 };
 size_t moe_mv_image_bytes(int64_t rows, int64_t K);
 cudaError_t moe_mv_launch(const MoeMvParams& mp, cudaStream_t stream, bool dump = false);
+// The decode form for the other formats: the activation rows quantized once,
+// then the staged GEMV kernel in routed mode (one grid row per routed row).
+int moe_mv_staged_run(const MoeMvParams& mp, int num_sms, int max_smem, cudaStream_t stream);
 
 }  // namespace gg

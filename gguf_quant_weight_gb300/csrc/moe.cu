@@ -19,13 +19,15 @@
 // Nothing waits on the host: the counts never leave the device, so the GEMM
 // grid is the upper bound on work items and surplus CTAs exit at once.
 //
-// Decode form (mul_mv_id): with at most kMoeMvRows routed rows (Q4_K / Q5_K;
-// 128: measured against the routed path, 23 vs 33 us at 64 rows, 38 vs 44 at
-// 128, 66 vs 54 at 256, Q4_K 128 x 768 x 2048)
-// every row is a GEMV of its own, on the int8 path of the decode GEMV
-// (ov39119's path table sends small batches to the GEMV): no routing, no
-// grouping, and one CTA per (32 weight rows, routed row) instead of a tile per
-// expert that decodes 128 rows to f16 for one token column.
+// Decode form (mul_mv_id): with at most moe_mv_max_rows(qtype) routed rows
+// (Q4_K 128: measured against the routed path, 23 vs 33 us at 64 rows, 38 vs
+// 44 at 128, 66 vs 54 at 256, Q4_K 128 x 768 x 2048; the other formats' limits
+// from the same comparison) every row is a GEMV of its own, on the int8 path of
+// the decode GEMV (ov39119's path table sends small batches to the GEMV): no
+// routing, no grouping, and CTAs over (weight rows, routed row) instead of a
+// tile per expert that decodes 128 rows to f16 for one token column. Q4_K and
+// Q5_K use a kernel of their own (one CTA per 32 weight rows of a routed row);
+// the other formats the staged GEMV kernel in routed mode.
 #include <algorithm>
 #include <cstdlib>
 
@@ -47,7 +49,7 @@ constexpr int kMoeTile = 128;   // token rows per work item (the GEMM's BN)
 bool mv_form(int qtype, int64_t entries) {
     const char* env = std::getenv("GGUF_MM_MOE_MV");
     if (env && env[0] == '0') return false;
-    return (qtype == GGUF_Q4_K || qtype == GGUF_Q5_K) && entries <= kMoeMvRows;
+    return entries <= moe_mv_max_rows(qtype);
 }
 
 struct MoeLayout {
@@ -271,23 +273,30 @@ int moe_route_debug(const int32_t* ids, int64_t entries, int64_t n_expert, int* 
 
 int64_t moe_max_tiles(int64_t n_expert, int64_t entries) { return std::min(n_expert, entries) + ceil_div(entries, kMoeTile); }
 
+int moe_mv_max_rows(int qtype) {
+    switch (qtype) {
+        case GGUF_Q4_K: case GGUF_Q5_K: case GGUF_Q2_K: case GGUF_Q3_K: case GGUF_Q6_K: return kMoeMvRows;
+        case GGUF_Q8_0: return 16;
+        default: return 32;
+    }
+}
+
 size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k) {
     (void)N;
     // enough for either form, so a comparison run may switch between them
     const size_t routed = moe_layout(nullptr, n_expert, K, T, top_k).bytes;
-    if ((qtype == GGUF_Q4_K || qtype == GGUF_Q5_K) && T * top_k <= kMoeMvRows)
-        return std::max(routed, moe_mv_image_bytes(T * top_k, K));
+    if (T * top_k <= kMoeMvRows) return std::max(routed, moe_mv_image_bytes(T * top_k, K));
     return routed;
 }
 
 int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
             int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
             int num_sms, int* status, cudaStream_t stream, bool per_slot, const MoeMvDump* dump, int pdl) {
-    (void)num_sms;
     if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
     const int64_t entries = T * top_k;
     if (entries > INT32_MAX / 2 || n_expert * N > INT32_MAX) return GGUF_ERR_UNSUPPORTED;
-    if (dump && !mv_form(qtype, entries)) return GGUF_ERR_UNSUPPORTED;
+    const bool q45 = qtype == GGUF_Q4_K || qtype == GGUF_Q5_K;
+    if (dump && !(mv_form(qtype, entries) && q45)) return GGUF_ERR_UNSUPPORTED;
     if (mv_form(qtype, entries)) {
         MoeMvParams mp{};
         mp.w = static_cast<const uint8_t*>(w_experts);
@@ -308,6 +317,10 @@ int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64
         mp.y = y;
         mp.ydt = ydt;
         mp.status = status;
+        mp.pdl = pdl;
+        // Q4_K / Q5_K: the decode-form kernel with its row-group fragments;
+        // the other formats: the staged GEMV kernel in routed mode
+        if (!q45) return moe_mv_staged_run(mp, num_sms, 232448, stream);   // the sm_103 opt-in maximum
         if (dump) {
             mp.dbg_qa = dump->qa;
             mp.dbg_da = dump->da;

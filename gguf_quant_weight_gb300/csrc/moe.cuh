@@ -6,9 +6,12 @@
 
 namespace gg {
 
-// At most this many routed rows (T * top_k) of Q4_K / Q5_K experts take the
-// decode form: one int8 GEMV per row, no routing.
+// At most this many routed rows (T * top_k) take the decode form (one int8
+// GEMV per routed row, no routing): 128 for Q4_K, Q5_K, Q2_K, Q3_K and Q6_K,
+// 32 for Q4_0, Q4_1, Q5_0 and Q5_1, 16 for Q8_0 (where the routed tensor-core
+// path measured faster above that on 128 experts of 768 x 2048, top-8).
 constexpr int kMoeMvRows = 128;
+int moe_mv_max_rows(int qtype);
 
 size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k);
 

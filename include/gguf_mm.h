@@ -163,10 +163,11 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K,
  * runs, the environment variable GGUF_MM_MOE_FULL_TILES=1, read at each call,
  * issues every tile's MMAs at the full width instead; the output is the same.)
  * Ids outside [0, n_expert) are skipped (their Y rows are left untouched).
- * Decode form (mul_mv_id): when T * top_k <= 128 and the experts are Q4_K or
- * Q5_K, every routed row is instead one GEMV of the decode path (int8
- * activation codes, integer sub-block dots; the results are those of
- * gguf_mm_gemv on that expert and row), with no routing step.
+ * Decode form (mul_mv_id): when T * top_k is at most 128 (Q4_K, Q5_K, Q2_K,
+ * Q3_K, Q6_K experts), 32 (Q4_0, Q4_1, Q5_0, Q5_1) or 16 (Q8_0), every routed
+ * row is instead one GEMV of the decode path (int8 activation codes, integer
+ * sub-block dots; the results are those of gguf_mm_gemv on that expert and
+ * row), with no routing step.
  * GGUF_MM_MOE_MV=0 in the environment keeps every batch on the routed path.
  * Workspace: gguf_mm_workspace_size(GGUF_OP_ID, ...) bytes. */
 int gguf_mm_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K,
@@ -280,8 +281,8 @@ int gguf_mm_debug_moe_route(const int32_t* ids, int64_t entries, int64_t n_exper
                             gguf_stream_t stream);
 
 /* Test hook: gguf_mm_id (per_slot = 0) or gguf_mm_id_slots (per_slot = 1) in
- * its decode form -- one int8 GEMV per routed row, taken by Q4_K / Q5_K experts
- * for at most 128 routed rows; GGUF_ERR_UNSUPPORTED for any other batch --
+ * its decode form for Q4_K / Q5_K experts (at most 128 routed rows; other
+ * formats and larger batches give GGUF_ERR_UNSUPPORTED) --
  * with the integer intermediates of every routed row p = token * top_k + slot
  * whose expert id is valid written out (device memory; any may be NULL):
  *   qa [entries, K] int8, d_a [entries, K/32] f32, s [entries, K/32] int32

@@ -146,3 +146,15 @@ def gemv_workspace(M: int, K: int):
     """A device workspace for gguf_mm_gemv of M rows of K values: (tensor, bytes)."""
     n = g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, 0, 1, K, M)
     return torch.empty(max(n, 256), dtype=torch.uint8, device="cuda"), n
+
+
+def moe_mv_max_rows(qtype: int) -> int:
+    """Routed rows (T * top_k) up to which gguf_mm_id takes its decode form (one
+    int8 GEMV per routed row), as the library's header states it."""
+    if qtype in (g.GGUF_Q4_K, g.GGUF_Q5_K, g.GGUF_Q2_K, g.GGUF_Q3_K, g.GGUF_Q6_K):
+        return 128
+    return 16 if qtype == g.GGUF_Q8_0 else 32
+
+
+def moe_decode_form(qtype: int, entries: int) -> bool:
+    return entries <= moe_mv_max_rows(qtype)

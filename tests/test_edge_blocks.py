@@ -177,7 +177,7 @@ def test_edge_blocks_decode_once_and_dense(qtype, pattern, odt):
 @pytest.mark.parametrize("qtype", QTYPES)
 def test_edge_blocks_moe(qtype, T, top_k):
     # every pattern is one expert; T * top_k = 12 rows take the decode form
-    # (Q4_K / Q5_K), 160 rows the routed tensor-core path
+    # (every format), 160 rows the routed tensor-core path
     E = len(PATTERNS)
     wE = np.concatenate([edge_weights(qtype, p) for p in PATTERNS])
     x = syn.normal(syn.rng(T), (T, K), "bf16")
@@ -192,7 +192,7 @@ def test_edge_blocks_moe(qtype, T, top_k):
     y.check("y")
     ws.check("workspace")
     assert g.gguf_mm_check_errors() == 0
-    decode_form = qtype in (syn.Q4_K, syn.Q5_K) and T * top_k <= 128
+    decode_form = U.moe_decode_form(qtype, T * top_k)
     with np.errstate(invalid="ignore"):
         if decode_form:
             ref = O.moe_mv_id_int8(wE, qtype, E, N, K, U.act_f32(x, "bf16"), ids)

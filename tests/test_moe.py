@@ -41,9 +41,9 @@ def _run(qtype, E, N, K, T, top_k, ids, residual=False, ydt="bf16", seed=0, toke
 
 
 def mv_form(qtype, entries):
-    # the library's decode form: at most 128 routed rows of Q4_K / Q5_K experts
-    # are computed one int8 GEMV per row (the GEMV's arithmetic)
-    return qtype in (syn.Q4_K, syn.Q5_K) and entries <= 128
+    # the library's decode form: up to a per-format number of routed rows are
+    # computed one int8 GEMV per row (the GEMV's arithmetic)
+    return U.moe_decode_form(qtype, entries)
 
 
 def _distinct_ids(rs, T, E, top_k):
@@ -176,6 +176,36 @@ def test_moe_per_slot_with_repeated_rows_equals_shared_rows():
         ys.append(U.host64(y))
     assert g.gguf_mm_check_errors() == 0
     assert np.array_equal(ys[0], ys[1])
+
+
+@pytest.mark.parametrize("qtype", [syn.Q8_0, syn.Q6_K, syn.Q4_0, syn.Q4_1, syn.Q5_0, syn.Q5_1, syn.Q2_K, syn.Q3_K])
+@pytest.mark.parametrize("T,top_k,per_slot", [(1, 8, False), (3, 4, True), ("limit", 8, False)])
+def test_moe_decode_form_other_formats(qtype, T, top_k, per_slot):
+    # the staged GEMV kernel in routed mode: every routed row an int8 GEMV of its
+    # activation row against its expert; an invalid id leaves its row untouched.
+    # "limit": the largest batch of this format that takes the decode form
+    if T == "limit":
+        T = U.moe_mv_max_rows(qtype) // top_k
+    assert mv_form(qtype, T * top_k)
+    E, N, K = 24, 320, 1024
+    rs = syn.rng(310 + T * top_k + qtype)
+    wE = syn.weight_blocks(rs, qtype, E * N, K)
+    x = syn.normal(rs, (T, top_k, K) if per_slot else (T, K), "bf16")
+    r = syn.normal(rs, (T, top_k, N), "f32")                 # the residual has y's type (f32)
+    ids = syn.zipf_ids(syn.rng(311 + T), T, E, top_k, 1.1)
+    ids[0, -1] = E + 3
+    y = U.guarded((T, top_k, N), torch.float32, fill=float("nan"))
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
+    ws = U.workspace(ws_bytes)
+    fn = g.gguf_mm_id_slots if per_slot else g.gguf_mm_id
+    fn(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids), top_k, U.dev(r), y.t,
+       g.GGUF_DT_F32, ws.t, ws_bytes)
+    torch.cuda.synchronize()
+    y.check("y")
+    ws.check("workspace")
+    assert g.gguf_mm_check_errors() == 0
+    ref = O.moe_mv_id_int8(wE, qtype, E, N, K, U.act_f32(x, "bf16"), ids, r.astype(np.float64))
+    U.check_close(U.host64(y.t).reshape(-1, N), ref.reshape(-1, N), "f32", allow_nan=True)
 
 
 @pytest.mark.parametrize("T,top_k,per_slot", [(1, 8, False), (2, 8, True), (16, 8, False), (3, 5, True)])
