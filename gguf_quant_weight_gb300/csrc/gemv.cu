@@ -24,6 +24,7 @@
 #include "common.cuh"
 #include "formats.cuh"
 #include "gemv.cuh"
+#include <cstdlib>
 #include <type_traits>
 
 namespace gg {
@@ -120,9 +121,10 @@ __device__ __forceinline__ void load_quarter(const GemvParams& p, bool on, int64
     }
 }
 
-// Quantizes one quarter; writes its 8 codes at `codes` and (quarter 0) the
-// block's entry at `entry` (generic pointers: global workspace or shared).
-__device__ __forceinline__ void quant_values(const float (&v)[8], bool on, int qtr, uint8_t* codes, uint8_t* entry) {
+// Quantizes one quarter: its 8 codes in word[0..1] and the block's entry
+// {d_a, d_a * s, s of quarters 0-1, s of quarters 2-3} (complete in the
+// lanes of quarter 0 and 2; quarter 0's is the one stored).
+__device__ __forceinline__ void quant_core(const float (&v)[8], uint32_t (&word)[2], uint4& entry) {
     // amax propagates NaN (a NaN anywhere in the block makes d_a NaN)
     float amax = 0.f;
 #pragma unroll
@@ -136,7 +138,6 @@ __device__ __forceinline__ void quant_values(const float (&v)[8], bool on, int q
     int q[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) q[i] = round_half_away(fminf(fmaxf(v[i] * id, -127.f), 127.f));
-    uint32_t word[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         // cvt.pack.sat.s8.s32.b32 d, a, b, c: d = (c << 16) | (a << 8) | b
@@ -148,13 +149,19 @@ __device__ __forceinline__ void quant_values(const float (&v)[8], bool on, int q
     const int s8 = dp4a(word[0], 0x01010101u, dp4a(word[1], 0x01010101u, 0));
     const int s_pair = s8 + __shfl_xor_sync(0xffffffffu, s8, 1);   // s_lo (quarters 0,1) or s_hi (2,3)
     const int s_other = __shfl_xor_sync(0xffffffffu, s_pair, 2);
+    const int s = s_pair + s_other;
+    entry = make_uint4(__float_as_uint(d), __float_as_uint(d * (float)s), (uint32_t)s_pair, (uint32_t)s_other);
+}
+
+// Quantizes one quarter; writes its 8 codes at `codes` and (quarter 0) the
+// block's entry at `entry` (generic pointers: global workspace or shared).
+__device__ __forceinline__ void quant_values(const float (&v)[8], bool on, int qtr, uint8_t* codes, uint8_t* entry) {
+    uint32_t word[2];
+    uint4 e;
+    quant_core(v, word, e);
     if (on) {
         *reinterpret_cast<uint2*>(codes) = make_uint2(word[0], word[1]);
-        if (qtr == 0) {
-            const int s = s_pair + s_other;
-            *reinterpret_cast<uint4*>(entry) =
-                make_uint4(__float_as_uint(d), __float_as_uint(d * (float)s), (uint32_t)s_pair, (uint32_t)s_other);
-        }
+        if (qtr == 0) *reinterpret_cast<uint4*>(entry) = e;
     }
 }
 
@@ -201,6 +208,55 @@ __device__ __forceinline__ void quantize_slice(const GemvParams& p, int64_t k0, 
         for (int u = 0; u < UNR; ++u)
             quant_values(v[u], on[u], qtr, img + m[u] * qa_row + qa_pos(32 * b[u]) + 8 * qtr,
                          img + (uint32_t)p.M * qa_row + 16u * (uint32_t)(m[u] * nb + b[u]));
+    }
+}
+
+// Threads [0, nthreads) of CTA `rank` of a cluster of CL CTAs quantize blocks
+// [rank * nb / CL, (rank + 1) * nb / CL) of all M rows (nb = K / 32) and store
+// the codes and entries into the image over all of K at shared address `img`
+// of every CTA of the cluster (same layout as quantize_slice over all of K),
+// so that the CL CTAs share one quantization of X.  The caller has made sure
+// that every CTA of the cluster is running, and ends with a cluster barrier.
+template <int CL, int UNR>
+__device__ __forceinline__ void quantize_cluster(const GemvParams& p, uint32_t img, int t0, int nthreads) {
+    const int nb = (int)(p.K / 32), nbs = nb / CL;
+    const int b0 = (int)cluster_rank() * nbs;
+    const int per_row = 4 * nbs;
+    const int quarters = p.M * per_row;
+    const uint32_t qa_row = (uint32_t)qa_row_stride(p.K);
+    uint32_t dst[CL];
+#pragma unroll
+    for (int c = 0; c < CL; ++c) dst[c] = cluster_map(img, (uint32_t)c);
+    const int qtr = t0 & 3;
+    for (int base = 0; base < quarters; base += UNR * nthreads) {
+        if (base + (t0 & ~31) >= quarters) break;
+        float v[UNR][8];
+        int m[UNR], b[UNR];
+        bool on[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int idx = base + u * nthreads + t0;
+            on[u] = idx < quarters;
+            const int i = on[u] ? idx : 0;
+            m[u] = i / per_row;
+            b[u] = b0 + ((i - m[u] * per_row) >> 2);
+            load_quarter(p, on[u], (int64_t)m[u] * p.K + 32 * b[u] + 8 * qtr, v[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            uint32_t w[2];
+            uint4 e;
+            quant_core(v[u], w, e);
+            if (on[u]) {
+                const uint32_t co = (uint32_t)m[u] * qa_row + qa_pos(32u * (uint32_t)b[u]) + 8u * (uint32_t)qtr;
+                const uint32_t eo = (uint32_t)p.M * qa_row + 16u * (uint32_t)(m[u] * nb + b[u]);
+#pragma unroll
+                for (int c = 0; c < CL; ++c) {
+                    st_cluster_v2(dst[c] + co, w[0], w[1]);
+                    if (qtr == 0) st_cluster_v4(dst[c] + eo, e);
+                }
+            }
+        }
     }
 }
 
@@ -1640,7 +1696,24 @@ __global__ void __launch_bounds__(kPairWarps * 32, 2) gemv_pair_kernel(const Gem
 // Each warp leaves one partial sum per (row, activation row) in shared
 // memory; the last phase adds the warps' partials in warp order, then the
 // residual, and stores.
+// With CL > 1 the grid runs in clusters of CL CTAs that share the activation
+// quantization: each CTA quantizes K / CL of X and stores the codes into all
+// CL images (distributed shared memory), which divides the X reads and the
+// quantizer's arithmetic of every CTA by CL.  A residual value is loaded right
+// after the dependency wait and held in a register until the store, so its
+// latency is hidden under the rows phase.
 __host__ __device__ constexpr int rowlane_warps(int mt) { return 16; }
+
+// CTAs per cluster of the row-lane kernel: two from M = 2 on, none at M = 1
+// (measured on Q5_K / Q4_K 4096 x 4096, chained calls, us at M = 1 / 2 / 4:
+// one CTA 4.20 / 5.48 / 8.17, pairs 4.63 / 5.14 / 6.81, fours 5.64 / 6.83 /
+// 9.86 for Q5_K).  GGUF_MM_GEMV_CLUSTER (1, 2 or 4) in the environment, read
+// at each call, overrides it for comparison runs.
+inline int rowlane_cluster(int64_t M) {
+    const char* env = std::getenv("GGUF_MM_GEMV_CLUSTER");
+    if (env && (env[0] == '1' || env[0] == '2' || env[0] == '4') && env[1] == 0) return env[0] - '0';
+    return M >= 2 ? 2 : 1;
+}
 
 struct RowLaneLayout {
     int64_t pitch, img, part, res, bar, total;
@@ -1658,14 +1731,16 @@ __host__ __device__ inline RowLaneLayout rowlane_layout(int64_t M, int64_t K, in
     return L;
 }
 
-template <int QT, int MT, int RI, bool DUMP>
+template <int QT, int MT, int RI, bool DUMP, int CL>
 __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel(const GemvParams p) {
     constexpr int NW = rowlane_warps(MT), NT = NW * 32;
     constexpr int bb = QT == GGUF_Q4_K ? 144 : 176;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t row0 = (int64_t)blockIdx.x * p.rows_per_cta;
-    const int rows = (int)min(p.rows_per_cta, p.N - row0);   // 1 .. 32 * RI
+    // 1 .. 32 * RI (0 for a CTA that only rounds the grid up to whole clusters)
+    const int rows = (int)max((int64_t)0, min(p.rows_per_cta, p.N - row0));
+    if constexpr (CL > 1) cluster_arrive_relaxed();   // this CTA is running (waited on before the first remote store)
     const int rpc = (int)p.rows_per_cta;
     const int nb = (int)(p.K / 32), U = (int)(p.K / 128);
     const RowLaneLayout L = rowlane_layout(p.M, p.K, p.rows_per_cta, p.rb, NW);
@@ -1695,18 +1770,31 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
     const bool has_res = p.residual != nullptr;
     float res0 = 0.f;
     if (has_res && tid < p.M * rows) res0 = load_act(p.residual, p.ydt, (int64_t)(tid / rows) * p.N + row0 + tid % rows);
-    {
+    if constexpr (CL > 1) {
+        cluster_wait_acquire();   // every CTA of the cluster is running: its image may be written
+        const int rounds = (4 * p.M * nb / CL + NT - 1) / NT;
+        if (rounds >= 2) quantize_cluster<CL, 2>(p, smem_u32(img), tid, NT);
+        else quantize_cluster<CL, 1>(p, smem_u32(img), tid, NT);
+    } else {
         const int rounds = (4 * p.M * nb + NT - 1) / NT;   // quarters per thread
         if (rounds >= 4) quantize_slice<4>(p, 0, (int)p.K, img, tid, NT);
         else if (rounds >= 2) quantize_slice<2>(p, 0, (int)p.K, img, tid, NT);
         else quantize_slice<1>(p, 0, (int)p.K, img, tid, NT);
     }
+    // residual values past the first NT through shared memory (the first NT
+    // stay in the registers of the threads that store them)
     if (has_res) {
-        if (tid < p.M * rows) res[(tid / rows) * rpc + tid % rows] = res0;
         for (int i = tid + NT; i < p.M * rows; i += NT)
             res[(i / rows) * rpc + i % rows] = load_act(p.residual, p.ydt, (int64_t)(i / rows) * p.N + row0 + i % rows);
     }
-    __syncthreads();   // the image, the residual values and the barrier's initialisation are visible
+    if constexpr (CL > 1) {
+        // the cluster's images, the residual values and the barrier's
+        // initialisation are visible; no CTA touches another's memory after this
+        cluster_arrive_release();
+        cluster_wait_acquire();
+    } else {
+        __syncthreads();   // the image, the residual values and the barrier's initialisation are visible
+    }
     Shared sh;
     sh.qa_row = (uint32_t)qa_row_stride(p.K);
     sh.qa = smem_u32(img);
@@ -1767,7 +1855,7 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
         float v = 0.f;
 #pragma unroll
         for (int w = 0; w < NW; ++w) v += pw[w];
-        if (has_res) v += res[m * rpc + r];
+        if (has_res) v += t == tid ? res0 : res[m * rpc + r];
         store_out(p.y, p.ydt, (int64_t)m * p.N + row0 + r, v);
     }
 }
@@ -1780,6 +1868,7 @@ cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t 
         if (U <= 32) k = gemv_kernel<QT, MT, LAYOUT, true, DUMP>;
     }
     int threads = p.direct ? direct_threads(MT) : kThreads;
+    int cl = 1;   // CTAs per cluster
     if constexpr (QT == GGUF_Q4_K || QT == GGUF_Q5_K || (QT == GGUF_Q6_K && LAYOUT == GGUF_LAYOUT_Q6K_PLANES)) {
         if (p.direct) k = gemv_direct_kernel<QT, MT, DUMP>;
     }
@@ -1798,8 +1887,12 @@ cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t 
         }
         if constexpr (MT <= 4) {
             if (p.tile == 3) {
-                k = p.rows_per_cta <= 32 ? gemv_rowlane_kernel<QT, MT, 1, DUMP> : gemv_rowlane_kernel<QT, MT, 2, DUMP>;
+                k = p.rows_per_cta > 32   ? gemv_rowlane_kernel<QT, MT, 2, DUMP, 1>
+                    : p.cluster == 4      ? gemv_rowlane_kernel<QT, MT, 1, DUMP, 4>
+                    : p.cluster == 2      ? gemv_rowlane_kernel<QT, MT, 1, DUMP, 2>
+                                          : gemv_rowlane_kernel<QT, MT, 1, DUMP, 1>;
                 threads = rowlane_warps(MT) * 32;
+                cl = p.rows_per_cta > 32 ? 1 : p.cluster;
             }
         }
     }
@@ -1810,11 +1903,16 @@ cudaError_t launch_one(const GemvParams& p, int grid, size_t smem, cudaStream_t 
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = p.pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cl;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cl > 1 ? 2 : 1;
+    if (grid % cl != 0) return cudaErrorInvalidConfiguration;
     return cudaLaunchKernelEx(&cfg, k, p);
 }
 
@@ -2026,6 +2124,10 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
             p.rows_per_cta = rpc_t;
             *grid = (int)ceil_div(p.N, rpc_t);
             *smem = (size_t)L.total;
+            // clusters sharing the quantization: whole clusters (a CTA past N
+            // only quantizes), at most 32 rows per CTA
+            p.cluster = rpc_t <= 32 ? rowlane_cluster(p.M) : 1;
+            *grid = (int)ceil_div(*grid, p.cluster) * p.cluster;
             return GGUF_OK;
         }
     }

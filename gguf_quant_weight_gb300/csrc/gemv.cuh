@@ -21,6 +21,7 @@ struct GemvParams {
     int direct;            // unit fields 16-byte aligned: load straight into registers
     int tile;              // rows staged whole in shared memory, two CTAs per SM: 1 tile, 2 pair, 3 row-lane kernel
     int force;             // -1: the plan's choice; else one of the GEMV_* kernels (test hook)
+    int cluster;           // row-lane kernel: CTAs per cluster sharing the activation quantization (1, 2, 4)
     // plan (filled by gemv_plan)
     int64_t rb;            // bytes per weight row (raw layout)
     int64_t rows_per_cta;  // rows owned by one CTA

@@ -104,15 +104,22 @@ size_t gguf_mm_workspace_size(int op, int qtype, int64_t N, int64_t K, int64_t M
  * 32 values to int8 with one f32 scale per block -- d_a = amax/127, q =
  * round(x/d_a) -- and every weight sub-block is dotted in integers against them.)
  *   w        [N, K/blk*bb] u8 blocks, or Q6_K planes when layout = PLANES
- *   qtype    GGUF_Q8_0 / Q4_K / Q5_K / Q6_K;  K % 256 == 0 (K % 32 for Q8_0)
+ *   qtype    any of the ten GGUF_Q* formats;  K a multiple of the format's
+ *            block (256 values for the K-quants, 32 for the others)
  *   x        [M, K] of xdt (F32, F16 or BF16), 1 <= M <= 8
  *   residual [M, N] of ydt or NULL;  y [M, N] of ydt
  *   workspace  device buffer of at least gguf_mm_workspace_size(GGUF_OP_GEMV,
- *              qtype, N, K, M, 0, 0) bytes, caller-owned, 16-byte aligned.  A
- *              first kernel writes the quantized activations there (codes, then
- *              per-32 {d_a, d_a*s, s_lo, s_hi}); the GEMV kernel copies that
- *              image into every CTA's shared memory.  Its contents are
- *              meaningless between calls.
+ *              qtype, N, K, M, 0, 0) bytes, caller-owned, 16-byte aligned.  On
+ *              the paths with a separate quantizer kernel, that kernel writes
+ *              the quantized activations there (codes, then per-32 {d_a,
+ *              d_a*s, s_lo, s_hi}) and the GEMV kernel copies that image into
+ *              every CTA's shared memory.  Its contents are meaningless between
+ *              calls.
+ * Q4_K / Q5_K at M <= 4 run one kernel that quantizes X itself; from M = 2
+ * on its CTAs run in clusters of two that share that quantization through
+ * distributed shared memory (GGUF_MM_GEMV_CLUSTER = 1, 2 or 4 in the
+ * environment, read at each call, sets the cluster size for comparison runs;
+ * the results are the same).
  * Errors: INVALID_ARG, UNSUPPORTED (M > 8, M*K too large for on-chip staging),
  * WORKSPACE (missing or too small), MISALIGNED, CUDA.
  * Weights are static inputs: the kernel is launched with programmatic

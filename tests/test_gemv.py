@@ -102,6 +102,17 @@ def test_rowlane_kernel_integer_terms_bit_exact(qtype, M, N, K):
     _assert_terms_exact(qtype, 0, N, K, M, ROWLANE, residual=(M == 2))
 
 
+@pytest.mark.parametrize("cluster", ["1", "2", "4"])
+@pytest.mark.parametrize("M", [1, 2, 4])
+@pytest.mark.parametrize("N,K", [(37, 1024), (129, 2048), (4096, 4096)])
+def test_rowlane_cluster_sizes_integer_terms_bit_exact(cluster, M, N, K, monkeypatch):
+    # CTAs in clusters of 1, 2 or 4 share the activation quantization (each
+    # quantizes K / cluster of X into every image of the cluster); the grid is
+    # rounded up to whole clusters at N = 37 and 129 (CTAs past N only quantize)
+    monkeypatch.setenv("GGUF_MM_GEMV_CLUSTER", cluster)
+    _assert_terms_exact(syn.Q5_K, 0, N, K, M, ROWLANE, seed=int(cluster), residual=(M != 2))
+
+
 @pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q5_K])
 @pytest.mark.parametrize("N,K", [(37, 1024), (4096, 4096), (129, 768)])
 def test_tile_kernel_integer_terms_bit_exact(qtype, N, K):
