@@ -64,6 +64,12 @@ __device__ __forceinline__ uint32_t lds16(uint32_t a) {
     asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
     return v;
 }
+__device__ __forceinline__ void sts64(uint32_t a, uint32_t x, uint32_t y) {
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
 __device__ __forceinline__ float i2f(int v) { return (float)v; }
 
 
@@ -215,18 +221,27 @@ __device__ __forceinline__ void quantize_slice(const GemvParams& p, int64_t k0, 
 // [rank * nb / CL, (rank + 1) * nb / CL) of all M rows (nb = K / 32) and store
 // the codes and entries into the image over all of K at shared address `img`
 // of every CTA of the cluster (same layout as quantize_slice over all of K),
-// so that the CL CTAs share one quantization of X.  The caller has made sure
-// that every CTA of the cluster is running, and ends with a cluster barrier.
+// so that the CL CTAs share one quantization of X: plain stores into this
+// CTA's image, asynchronous stores into the others', each completing its
+// bytes on the mbarrier at shared address `bar` of the receiving CTA
+// (cluster_xbytes(CL, M, K) bytes per receiver, which its expect_tx counts).
+// The caller has made sure that every CTA of the cluster is running and has
+// initialised that barrier.
 template <int CL, int UNR>
-__device__ __forceinline__ void quantize_cluster(const GemvParams& p, uint32_t img, int t0, int nthreads) {
+__device__ __forceinline__ void quantize_cluster(const GemvParams& p, uint32_t img, uint32_t bar, int t0,
+                                                 int nthreads) {
     const int nb = (int)(p.K / 32), nbs = nb / CL;
-    const int b0 = (int)cluster_rank() * nbs;
+    const uint32_t rank = cluster_rank();
+    const int b0 = (int)rank * nbs;
     const int per_row = 4 * nbs;
     const int quarters = p.M * per_row;
     const uint32_t qa_row = (uint32_t)qa_row_stride(p.K);
-    uint32_t dst[CL];
+    uint32_t dst[CL], dbar[CL];
 #pragma unroll
-    for (int c = 0; c < CL; ++c) dst[c] = cluster_map(img, (uint32_t)c);
+    for (int c = 0; c < CL; ++c) {
+        dst[c] = cluster_map(img, (uint32_t)c);
+        dbar[c] = cluster_map(bar, (uint32_t)c);
+    }
     const int qtr = t0 & 3;
     for (int base = 0; base < quarters; base += UNR * nthreads) {
         if (base + (t0 & ~31) >= quarters) break;
@@ -250,14 +265,23 @@ __device__ __forceinline__ void quantize_cluster(const GemvParams& p, uint32_t i
             if (on[u]) {
                 const uint32_t co = (uint32_t)m[u] * qa_row + qa_pos(32u * (uint32_t)b[u]) + 8u * (uint32_t)qtr;
                 const uint32_t eo = (uint32_t)p.M * qa_row + 16u * (uint32_t)(m[u] * nb + b[u]);
+                sts64(img + co, w[0], w[1]);
+                if (qtr == 0) sts128(img + eo, e);
 #pragma unroll
                 for (int c = 0; c < CL; ++c) {
-                    st_cluster_v2(dst[c] + co, w[0], w[1]);
-                    if (qtr == 0) st_cluster_v4(dst[c] + eo, e);
+                    if ((uint32_t)c == rank) continue;
+                    st_async_v2(dst[c] + co, w[0], w[1], dbar[c]);
+                    if (qtr == 0) st_async_v4(dst[c] + eo, e, dbar[c]);
                 }
             }
         }
     }
+}
+
+// Bytes of the activation image a CTA of a cluster of CL receives from the
+// other CTAs (their blocks: 32 code bytes and a 16-byte entry each).
+__host__ __device__ constexpr int64_t cluster_xbytes(int CL, int64_t M, int64_t K) {
+    return (CL - 1) * M * (K / 32 / CL) * 48;
 }
 
 // The stand-alone quantizer for the kernels that take the image from the
@@ -1705,9 +1729,8 @@ __global__ void __launch_bounds__(kPairWarps * 32, 2) gemv_pair_kernel(const Gem
 __host__ __device__ constexpr int rowlane_warps(int mt) { return 16; }
 
 // CTAs per cluster of the row-lane kernel: two from M = 2 on, none at M = 1
-// (measured on Q5_K / Q4_K 4096 x 4096, chained calls, us at M = 1 / 2 / 4:
-// one CTA 4.20 / 5.48 / 8.17, pairs 4.63 / 5.14 / 6.81, fours 5.64 / 6.83 /
-// 9.86 for Q5_K).  GGUF_MM_GEMV_CLUSTER (1, 2 or 4) in the environment, read
+// (measured on Q5_K 4096 x 4096, chained calls, us at M = 1 / 2 / 4: one CTA
+// 4.21 / 5.47 / 8.14, pairs 4.23 / 4.65 / 7.02, fours 5.06 / 6.60 / 9.86).  GGUF_MM_GEMV_CLUSTER (1, 2 or 4) in the environment, read
 // at each call, overrides it for comparison runs.
 inline int rowlane_cluster(int64_t M) {
     const char* env = std::getenv("GGUF_MM_GEMV_CLUSTER");
@@ -1740,7 +1763,6 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
     const int64_t row0 = (int64_t)blockIdx.x * p.rows_per_cta;
     // 1 .. 32 * RI (0 for a CTA that only rounds the grid up to whole clusters)
     const int rows = (int)max((int64_t)0, min(p.rows_per_cta, p.N - row0));
-    if constexpr (CL > 1) cluster_arrive_relaxed();   // this CTA is running (waited on before the first remote store)
     const int rpc = (int)p.rows_per_cta;
     const int nb = (int)(p.K / 32), U = (int)(p.K / 128);
     const RowLaneLayout L = rowlane_layout(p.M, p.K, p.rows_per_cta, p.rb, NW);
@@ -1751,17 +1773,21 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
     float* res = reinterpret_cast<float*>(smem_raw + L.res);     // [M][rows_per_cta]
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw + L.bar);
 
-    // 1. every row of the CTA requested at once, before the dependency wait
+    // 1. every row of the CTA requested at once, before the dependency wait;
+    // the same barrier counts the other cluster CTAs' parts of the image
     if (warp == 0) {
         if (lane == 0) {
             mbar_init(bar, 1);
             fence_mbar_init();
-            mbar_arrive_expect_tx(bar, (uint32_t)rows * rb);
+            mbar_arrive_expect_tx(bar, (uint32_t)rows * rb + (uint32_t)cluster_xbytes(CL, p.M, p.K));
         }
         __syncwarp();
         for (int r = lane; r < rows; r += 32)
             bulk_g2s_u32(tile + (uint32_t)r * pitch, p.w + (row0 + r) * p.rb, rb, bar);
     }
+    // this CTA is running and its barrier initialised (waited on before the
+    // first store into another CTA)
+    if constexpr (CL > 1) cluster_arrive_relaxed();
     pdl_launch_dependents();
 
     // 2. after the producer of X: the tile's residual values (one load per
@@ -1773,8 +1799,8 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
     if constexpr (CL > 1) {
         cluster_wait_acquire();   // every CTA of the cluster is running: its image may be written
         const int rounds = (4 * p.M * nb / CL + NT - 1) / NT;
-        if (rounds >= 2) quantize_cluster<CL, 2>(p, smem_u32(img), tid, NT);
-        else quantize_cluster<CL, 1>(p, smem_u32(img), tid, NT);
+        if (rounds >= 2) quantize_cluster<CL, 2>(p, smem_u32(img), smem_u32(bar), tid, NT);
+        else quantize_cluster<CL, 1>(p, smem_u32(img), smem_u32(bar), tid, NT);
     } else {
         const int rounds = (4 * p.M * nb + NT - 1) / NT;   // quarters per thread
         if (rounds >= 4) quantize_slice<4>(p, 0, (int)p.K, img, tid, NT);
@@ -1787,20 +1813,23 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
         for (int i = tid + NT; i < p.M * rows; i += NT)
             res[(i / rows) * rpc + i % rows] = load_act(p.residual, p.ydt, (int64_t)(i / rows) * p.N + row0 + i % rows);
     }
-    if constexpr (CL > 1) {
-        // the cluster's images, the residual values and the barrier's
-        // initialisation are visible; no CTA touches another's memory after this
-        cluster_arrive_release();
-        cluster_wait_acquire();
-    } else {
-        __syncthreads();   // the image, the residual values and the barrier's initialisation are visible
-    }
+    // this CTA's part of the image, the residual values and the barrier's
+    // initialisation are visible (the other CTAs' parts arrive on the barrier)
+    __syncthreads();
     Shared sh;
     sh.qa_row = (uint32_t)qa_row_stride(p.K);
     sh.qa = smem_u32(img);
     sh.ds = sh.qa + (uint32_t)p.M * sh.qa_row;
     sh.stage = tile;
-    if (DUMP && blockIdx.x == 0) {
+
+    // 3. lane = row (lane, lane + 32, ...), warp = units warp, warp + NW, ...
+    float acc[RI][MT];
+#pragma unroll
+    for (int i = 0; i < RI; ++i)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[i][m] = 0.f;
+    const bool ok = __syncthreads_and(mbar_wait(bar, 0, p.status) ? 1 : 0) != 0;   // W and the whole image
+    if (DUMP && ok && blockIdx.x == 0) {
         for (int64_t i = tid; i < (int64_t)p.M * p.K; i += NT) {
             const uint32_t a = sh.qa + (uint32_t)(i / p.K) * sh.qa_row + qa_pos((uint32_t)(i % p.K));
             if (p.dbg_qa) p.dbg_qa[i] = (int8_t)(lds32(a & ~3u) >> (8 * (a & 3)));
@@ -1811,14 +1840,6 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
             if (p.dbg_s) p.dbg_s[i] = (int32_t)(e.z + e.w);
         }
     }
-
-    // 3. lane = row (lane, lane + 32, ...), warp = units warp, warp + NW, ...
-    float acc[RI][MT];
-#pragma unroll
-    for (int i = 0; i < RI; ++i)
-#pragma unroll
-        for (int m = 0; m < MT; ++m) acc[i][m] = 0.f;
-    const bool ok = __syncthreads_and(mbar_wait(bar, 0, p.status) ? 1 : 0) != 0;
     if (ok) {
         const uint32_t ds_row = 16u * (uint32_t)nb;
         for (int u = warp; u < U; u += NW) {
@@ -2117,17 +2138,19 @@ int gemv_plan(GemvParams& p, int num_sms, int max_smem, int* grid, size_t* smem)
         const int64_t rpc_t = ceil_div(p.N, (int64_t)num_sms);
         const int mt = p.M <= 1 ? 1 : p.M <= 2 ? 2 : 4;
         const RowLaneLayout L = rowlane_layout(p.M, p.K, rpc_t, p.rb, rowlane_warps(mt));
+        // clusters sharing the quantization (at most 32 rows per CTA): whole
+        // clusters, a CTA past N only quantizes
+        const int cl = rpc_t <= 32 ? rowlane_cluster(p.M) : 1;
+        // one barrier phase counts the CTA's rows and the image parts of the
+        // other CTAs (transaction counts stay below 2^20 bytes)
         if (rpc_t <= 64 && (rpc_t >= 16 || p.force == GEMV_ROWLANE) && L.total <= half &&
-            rpc_t * p.rb < (int64_t(1) << 20)) {
+            rpc_t * p.rb + cluster_xbytes(cl, p.M, p.K) < (int64_t(1) << 20)) {
             p.tile = 3;
             p.direct = 0;
             p.rows_per_cta = rpc_t;
-            *grid = (int)ceil_div(p.N, rpc_t);
+            p.cluster = cl;
+            *grid = (int)(ceil_div(ceil_div(p.N, rpc_t), (int64_t)cl) * cl);
             *smem = (size_t)L.total;
-            // clusters sharing the quantization: whole clusters (a CTA past N
-            // only quantizes), at most 32 rows per CTA
-            p.cluster = rpc_t <= 32 ? rowlane_cluster(p.M) : 1;
-            *grid = (int)ceil_div(*grid, p.cluster) * p.cluster;
             return GGUF_OK;
         }
     }
