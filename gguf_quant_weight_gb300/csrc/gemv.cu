@@ -1730,7 +1730,7 @@ __host__ __device__ constexpr int rowlane_warps(int mt) { return 16; }
 
 // CTAs per cluster of the row-lane kernel: two from M = 2 on, none at M = 1
 // (measured on Q5_K 4096 x 4096, chained calls, us at M = 1 / 2 / 4: one CTA
-// 4.21 / 5.47 / 8.14, pairs 4.23 / 4.65 / 7.02, fours 5.06 / 6.60 / 9.86).  GGUF_MM_GEMV_CLUSTER (1, 2 or 4) in the environment, read
+// 4.20 / 5.48 / 8.17, pairs 4.22 / 4.66 / 6.37, fours 5.06 / 6.60 / 9.86).  GGUF_MM_GEMV_CLUSTER (1, 2 or 4) in the environment, read
 // at each call, overrides it for comparison runs.
 inline int rowlane_cluster(int64_t M) {
     const char* env = std::getenv("GGUF_MM_GEMV_CLUSTER");
@@ -1799,7 +1799,9 @@ __global__ void __launch_bounds__(rowlane_warps(MT) * 32, 2) gemv_rowlane_kernel
     if constexpr (CL > 1) {
         cluster_wait_acquire();   // every CTA of the cluster is running: its image may be written
         const int rounds = (4 * p.M * nb / CL + NT - 1) / NT;
-        if (rounds >= 2) quantize_cluster<CL, 2>(p, smem_u32(img), smem_u32(bar), tid, NT);
+        // (one quarter per round for Q5_K at 3-4 rows keeps its rows phase free
+        // of register spills: M = 4 in pairs 7.02 -> 6.37 us)
+        if (!(QT == GGUF_Q5_K && MT == 4) && rounds >= 2) quantize_cluster<CL, 2>(p, smem_u32(img), smem_u32(bar), tid, NT);
         else quantize_cluster<CL, 1>(p, smem_u32(img), smem_u32(bar), tid, NT);
     } else {
         const int rounds = (4 * p.M * nb + NT - 1) / NT;   // quarters per thread
