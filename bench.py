@@ -10,9 +10,9 @@ device synchronization, timed with CUDA events on the launching stream.
 
 Printed JSON line (rank 0): value = weight GB/s over the whole job, plus
   per_m       us per call and weight GB/s at each M (graphs of 270 calls);
-  e2e         the same calls made eagerly through the C ABI from the host,
-              inputs copied in from pinned host memory and y copied out,
-              every call;
+  e2e         the same calls made eagerly from the host through the C ABI's
+              host-buffer entry (gguf_mm_gemv_host): x and the residual
+              copied in from pinned host memory and y copied out, every call;
   roofline    the GEMV kernel's algorithmic bytes per launch / its mean
               launch time in the timed region, against the measured HBM copy
               bandwidth;
@@ -632,17 +632,27 @@ def run_gpu(args):
     hr = {m: rsd[m].cpu().pin_memory() for m in MS}
     hy = {m: torch.empty((m, N), dtype=torch.bfloat16).pin_memory() for m in MS}
 
+    # the host leg holds raw pointers, as a C caller would (no tensor indexing per call)
+    w_ptrs = [W[i].data_ptr() for i in range(copies)]
+    host_args = {m: (hx[m].data_ptr(), xs[m].data_ptr(), hr[m].data_ptr(), rsd[m].data_ptr(), hy[m].data_ptr(),
+                     ys[m].data_ptr(), wss[m].data_ptr(), wsz[m]) for m in MS}
+    stream_ptr = stream.cuda_stream
+
+    def call_host(m):
+        # one C-ABI call: x and the residual copied in, the GEMV, y copied out
+        xh, xd, rh, rd, yh, yd, wsp, wsn = host_args[m]
+        g.gguf_mm_gemv_host(w_ptrs[state["c"] % copies], QTYPE, 0, N, K, xh, xd, g.GGUF_DT_BF16, m, rh, rd, yh, yd,
+                            g.GGUF_DT_BF16, wsp, wsn, stream=stream_ptr)
+        state["c"] += 1
+
     def eager_steps():
         for m in MS:
             for _ in range(args.steps):
-                xs[m].copy_(hx[m], non_blocking=True)
-                rsd[m].copy_(hr[m], non_blocking=True)
-                call(m)
-                hy[m].copy_(ys[m], non_blocking=True)
+                call_host(m)
 
     with torch.cuda.stream(stream):
         for m in MS:
-            call(m)
+            call_host(m)
     stream.synchronize()
     esec, _, _ = timed(eager_steps)
     clocks.stop()
@@ -683,7 +693,8 @@ def run_gpu(args):
         "hbm_frac": round(value / ws / hbm, 4),
         "per_m": {str(m): [round(per_m[m] * 1e6, 3), round(W_BYTES / per_m[m] / 1e9, 1)] for m in MS},
         "e2e": {"value": e2e, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "path": "eager host calls through the C ABI, pinned copies each call"},
+                "path": "eager host calls of gguf_mm_gemv_host (x and residual copied in from pinned memory, "
+                        "the GEMV, y copied out: one C-ABI call per step)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4),
                      "traffic": None if traffic is None else round(sum(traffic[str(m)] for m in MS) / len(MS)),

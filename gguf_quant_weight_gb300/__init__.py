@@ -39,6 +39,8 @@ _SIGS = {
     "gguf_mm_workspace_size": (_c_sz, [_c_int, _c_int, _c_i64, _c_i64, _c_i64, _c_i64, _c_i64]),
     "gguf_mm_gemv": (_c_int, [_c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_vp,
                               _c_int, _c_vp, _c_sz, _c_vp]),
+    "gguf_mm_gemv_host": (_c_int, [_c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_vp, _c_vp, _c_int, _c_i64, _c_vp,
+                                   _c_vp, _c_vp, _c_vp, _c_int, _c_vp, _c_sz, _c_vp]),
     "gguf_mm_gemm": (_c_int, [_c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_vp,
                               _c_int, _c_vp, _c_sz, _c_int, _c_vp]),
     "gguf_mm_id": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_i64,
@@ -152,6 +154,13 @@ def gguf_mm_workspace_size(op, qtype, N, K, M, n_expert=0, top_k=0) -> int:
 def gguf_mm_gemv(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace=None, ws_bytes=0, stream=None):
     return _check("gguf_mm_gemv", load_library().gguf_mm_gemv(
         _p(w), qtype, layout, N, K, _p(x), xdt, M, _p(residual), _p(y), ydt, _p(workspace), ws_bytes, _s(stream)))
+
+
+def gguf_mm_gemv_host(w, qtype, layout, N, K, x_host, x_dev, xdt, M, residual_host, residual_dev, y_host, y_dev,
+                      ydt, workspace=None, ws_bytes=0, stream=None):
+    return _check("gguf_mm_gemv_host", load_library().gguf_mm_gemv_host(
+        _p(w), qtype, layout, N, K, _p(x_host), _p(x_dev), xdt, M, _p(residual_host), _p(residual_dev),
+        _p(y_host), _p(y_dev), ydt, _p(workspace), ws_bytes, _s(stream)))
 
 
 def gguf_mm_gemm(w, qtype, layout, N, K, x, xdt, M, residual, y, ydt, workspace=None, ws_bytes=0,

@@ -236,6 +236,25 @@ int gguf_mm_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K, con
                     nullptr, nullptr, nullptr, nullptr, false);
 }
 
+int gguf_mm_gemv_host(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x_host, void* x_dev,
+                      int xdt, int64_t M, const void* residual_host, void* residual_dev, void* y_host, void* y_dev,
+                      int ydt, void* workspace, size_t ws_bytes, gguf_stream_t stream) {
+    if (!x_host || !y_host || (residual_host == nullptr) != (residual_dev == nullptr)) return GGUF_ERR_INVALID_ARG;
+    const cudaStream_t s = (cudaStream_t)stream;
+    // every argument of the GEMV checked (its plan, nothing launched) before anything is enqueued
+    int st = run_gemv(w, qtype, layout, N, K, x_dev, xdt, M, residual_dev, y_dev, ydt, workspace, ws_bytes, s, nullptr,
+                      nullptr, nullptr, nullptr, false, -1, nullptr, false);
+    if (st != GGUF_OK) return st;
+    const size_t xb = (size_t)(M * K) * (xdt == GGUF_DT_F32 ? 4 : 2), yb = (size_t)(M * N) * (ydt == GGUF_DT_F32 ? 4 : 2);
+    if (cudaMemcpyAsync(x_dev, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) return GGUF_ERR_CUDA;
+    if (residual_host && cudaMemcpyAsync(residual_dev, residual_host, yb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return GGUF_ERR_CUDA;
+    st = run_gemv(w, qtype, layout, N, K, x_dev, xdt, M, residual_dev, y_dev, ydt, workspace, ws_bytes, s, nullptr,
+                  nullptr, nullptr, nullptr, false);
+    if (st != GGUF_OK) return st;
+    return cuda_status(cudaMemcpyAsync(y_host, y_dev, yb, cudaMemcpyDeviceToHost, s));
+}
+
 int gguf_mm_debug_gemv_terms(const void* w, int qtype, int layout, int64_t N, int64_t K, const void* x, int xdt,
                              int64_t M, const void* residual, void* y, int ydt, int8_t* qa, float* d_a, int32_t* s,
                              int32_t* D, void* workspace, size_t ws_bytes, int kernel, int* kernel_out,

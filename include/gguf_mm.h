@@ -134,6 +134,27 @@ int gguf_mm_gemv(const void* w, int qtype, int layout, int64_t N, int64_t K,
                  const void* x, int xdt, int64_t M, const void* residual, void* y, int ydt,
                  void* workspace, size_t ws_bytes, gguf_stream_t stream);
 
+/* gguf_mm_gemv from host memory, end to end, in one call: enqueues on `stream`
+ * the copy of x_host (and residual_host) into the caller's device buffers
+ * x_dev (residual_dev), the GEMV of gguf_mm_gemv on them into y_dev, and the
+ * copy of y_dev back into y_host.  Asynchronous: the host buffers must stay
+ * valid, and y_host unread, until the stream has passed the call (pinned host
+ * memory lets the copies run asynchronously; pageable memory makes the
+ * runtime stage them).
+ *   x_host, x_dev              [M, K] of xdt (host / device)
+ *   residual_host, residual_dev  [M, N] of ydt, both NULL or both set (the
+ *                              device one may alias y_dev)
+ *   y_host, y_dev              [M, N] of ydt (host / device)
+ *   the other arguments as gguf_mm_gemv (w and workspace in device memory).
+ * Errors: INVALID_ARG (a missing host buffer, or only one of the residual
+ * pair), then those of gguf_mm_gemv, all returned before anything is
+ * enqueued; CUDA for a copy the runtime refused. */
+int gguf_mm_gemv_host(const void* w, int qtype, int layout, int64_t N, int64_t K,
+                      const void* x_host, void* x_dev, int xdt, int64_t M,
+                      const void* residual_host, void* residual_dev,
+                      void* y_host, void* y_dev, int ydt,
+                      void* workspace, size_t ws_bytes, gguf_stream_t stream);
+
 /* The path GGUF_PATH_AUTO takes for this call shape (GGUF_PATH_GEMV or
  * GGUF_PATH_FUSED), or GGUF_ERR_INVALID_ARG.  The GEMV takes M below the
  * smallest row count at which the fused GEMM measured faster on GB300 for the

@@ -226,6 +226,38 @@ def test_gemv_residual_may_alias_output(N, M):
     U.check_close(U.host64(y), ref, "bf16")
 
 
+@pytest.mark.parametrize("qtype,N,K,M,ydt,residual", [
+    (syn.Q5_K, 4096, 4096, 1, "bf16", True), (syn.Q5_K, 4096, 4096, 4, "bf16", True),
+    (syn.Q5_K, 300, 1024, 2, "f32", False), (syn.Q8_0, 200, 768, 3, "bf16", True), (syn.Q4_0, 37, 512, 8, "f32", True)])
+def test_gemv_from_host_buffers(qtype, N, K, M, ydt, residual):
+    # gguf_mm_gemv_host: copy in, the GEMV, copy out, in one call on pinned host
+    # buffers; y_host equals the device-buffer call's output bit for bit
+    rs = syn.rng(17 + qtype + M + N)
+    w = syn.weight_blocks(rs, qtype, N, K)
+    x = syn.normal(rs, (M, K), "bf16")
+    r = syn.normal(rs, (M, N), ydt) if residual else None
+    wd = U.dev(w)
+    tdt = U.TORCH_DT[ydt]
+    xh = torch.from_numpy(x.copy()).view(torch.bfloat16).pin_memory()
+    rh = None if r is None else torch.from_numpy(r.copy()).view(tdt).pin_memory()
+    yh = torch.full((M, N), float("nan"), dtype=tdt).pin_memory()
+    xd = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    rd = None if r is None else torch.empty((M, N), dtype=tdt, device="cuda")
+    yd = U.guarded((M, N), tdt)
+    nws = g.gguf_mm_workspace_size(g.GGUF_OP_GEMV, qtype, N, K, M)
+    ws = U.workspace(nws, 0xCD)
+    g.gguf_mm_gemv_host(wd, qtype, 0, N, K, xh, xd, g.GGUF_DT_BF16, M, rh, rd, yh, yd.t, U.DT[ydt], ws.t, nws)
+    torch.cuda.synchronize()
+    yd.check("y")
+    ws.check("workspace")
+    assert g.gguf_mm_check_errors() == 0
+    y_dev_call = _run_gemv(wd, qtype, 0, N, K, x, "bf16", M, r, ydt)
+    assert torch.equal(yh.view(torch.int16 if ydt == "bf16" else torch.int32),
+                       y_dev_call.cpu().view(torch.int16 if ydt == "bf16" else torch.int32))
+    ref = O.gemv_int8_path(w, qtype, N, K, U.act_f32(x, "bf16"), None if r is None else U.act_f64(r, ydt))
+    U.check_close(yh.double().numpy(), ref, ydt)
+
+
 def test_gemv_config_q6k_256x1024_f32():
     # the small decode workload: Q6_K N=256 K=1024 M=1, f32 in / f32 out
     cfg = syn.CONFIGS["q6k_gemv_256x1024"]
