@@ -47,6 +47,8 @@ _SIGS = {
                             _c_vp, _c_vp, _c_int, _c_vp, _c_sz, _c_vp]),
     "gguf_mm_id_slots": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_i64,
                                   _c_vp, _c_vp, _c_int, _c_vp, _c_sz, _c_vp]),
+    "gguf_mm_id_path": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_i64,
+                                 _c_int, _c_vp, _c_vp, _c_int, _c_vp, _c_sz, _c_int, _c_vp]),
     "gguf_repack_q6k_planes": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_vp]),
     "gguf_dequant_padded": (_c_int, [_c_vp, _c_int, _c_int, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp]),
     "gguf_dense_gemm": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_vp,
@@ -182,6 +184,13 @@ def gguf_mm_id_slots(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, re
     return _check("gguf_mm_id_slots", load_library().gguf_mm_id_slots(
         _p(w_experts), qtype, n_expert, N, K, _p(x), xdt, T, _p(ids), top_k, _p(residual), _p(y), ydt,
         _p(workspace), ws_bytes, _s(stream)))
+
+
+def gguf_mm_id_path(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, per_slot, residual, y, ydt,
+                    workspace=None, ws_bytes=0, path=GGUF_PATH_AUTO, stream=None):
+    return _check("gguf_mm_id_path", load_library().gguf_mm_id_path(
+        _p(w_experts), qtype, n_expert, N, K, _p(x), xdt, T, _p(ids), top_k, per_slot, _p(residual), _p(y), ydt,
+        _p(workspace), ws_bytes, path, _s(stream)))
 
 
 def gguf_repack_q6k_planes(src, dst, nblk, inverse=0, stream=None):

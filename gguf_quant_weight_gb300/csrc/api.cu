@@ -304,7 +304,7 @@ int gguf_mm_gemm(const void* w, int qtype, int layout, int64_t N, int64_t K, con
 static int run_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
                   int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt,
                   void* workspace, size_t ws_bytes, gguf_stream_t stream, bool per_slot,
-                  const MoeMvDump* dump = nullptr) {
+                  const MoeMvDump* dump = nullptr, int form = -1) {
     if (!ids || n_expert <= 0 || top_k <= 0) return GGUF_ERR_INVALID_ARG;
     int st = check_common(w_experts, qtype, GGUF_LAYOUT_BLOCKS, N, K, x, xdt, T, residual, y, ydt);
     if (st != GGUF_OK) return st;
@@ -316,7 +316,7 @@ static int run_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N,
     DeviceFacts* f = nullptr;
     if ((st = facts(&f)) != GGUF_OK) return st;
     return moe_run(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace,
-                   f->num_sms, f->status, (cudaStream_t)stream, per_slot, dump, pdl_enabled() ? 1 : 0);
+                   f->num_sms, f->status, (cudaStream_t)stream, per_slot, dump, pdl_enabled() ? 1 : 0, form);
 }
 
 int gguf_mm_debug_moe_mv_terms(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K,
@@ -333,6 +333,20 @@ int gguf_mm_id(const void* w_experts, int qtype, int64_t n_expert, int64_t N, in
                void* workspace, size_t ws_bytes, gguf_stream_t stream) {
     return run_id(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace, ws_bytes,
                   stream, false);
+}
+
+int gguf_mm_id_path(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
+                    int64_t T, const int32_t* ids, int64_t top_k, int per_slot, const void* residual, void* y, int ydt,
+                    void* workspace, size_t ws_bytes, int path, gguf_stream_t stream) {
+    int form;
+    switch (path) {
+        case GGUF_PATH_AUTO: form = -1; break;
+        case GGUF_PATH_GEMV: form = 1; break;    // the decode form
+        case GGUF_PATH_FUSED: form = 0; break;   // the routed tensor-core path
+        default: return GGUF_ERR_INVALID_ARG;
+    }
+    return run_id(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, residual, y, ydt, workspace, ws_bytes,
+                  stream, per_slot != 0, nullptr, form);
 }
 
 int gguf_mm_id_slots(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x,

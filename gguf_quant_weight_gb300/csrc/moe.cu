@@ -291,13 +291,15 @@ size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, in
 
 int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
             int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
-            int num_sms, int* status, cudaStream_t stream, bool per_slot, const MoeMvDump* dump, int pdl) {
+            int num_sms, int* status, cudaStream_t stream, bool per_slot, const MoeMvDump* dump, int pdl, int form) {
     if (K % 256 != 0) return GGUF_ERR_UNSUPPORTED;
     const int64_t entries = T * top_k;
     if (entries > INT32_MAX / 2 || n_expert * N > INT32_MAX) return GGUF_ERR_UNSUPPORTED;
+    if (form == 1 && entries > kMoeMvRows) return GGUF_ERR_UNSUPPORTED;
+    const bool decode = form < 0 ? mv_form(qtype, entries) : form == 1;
     const bool q45 = qtype == GGUF_Q4_K || qtype == GGUF_Q5_K;
-    if (dump && !(mv_form(qtype, entries) && q45)) return GGUF_ERR_UNSUPPORTED;
-    if (mv_form(qtype, entries)) {
+    if (dump && !(decode && q45)) return GGUF_ERR_UNSUPPORTED;
+    if (decode) {
         MoeMvParams mp{};
         mp.w = static_cast<const uint8_t*>(w_experts);
         mp.qtype = qtype;

@@ -28,10 +28,12 @@ struct MoeMvDump {
 // (GGUF_ERR_UNSUPPORTED when this batch does not take the decode form).
 // pdl: chain the routed path's gather and grouped GEMM as programmatic
 // dependent launches (each waits before reading the kernel before it).
+// form: -1 the batch-size rule (moe_mv_max_rows), 0 the routed tensor-core
+// path, 1 the decode form (GGUF_ERR_UNSUPPORTED above kMoeMvRows routed rows).
 int moe_run(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K, const void* x, int xdt,
             int64_t T, const int32_t* ids, int64_t top_k, const void* residual, void* y, int ydt, void* workspace,
             int num_sms, int* status, cudaStream_t stream, bool per_slot = false, const MoeMvDump* dump = nullptr,
-            int pdl = 0);
+            int pdl = 0, int form = -1);
 
 // The routing step alone (test hook): per-expert group offsets [E + 1], the
 // number of (expert, token tile) work items, the items {expert, first row,

@@ -215,6 +215,22 @@ int gguf_mm_id_slots(const void* w_experts, int qtype, int64_t n_expert, int64_t
                      const void* residual, void* y, int ydt,
                      void* workspace, size_t ws_bytes, gguf_stream_t stream);
 
+/* gguf_mm_id (per_slot = 0) or gguf_mm_id_slots (per_slot = 1) with the form
+ * chosen by the caller instead of by the batch size:
+ *   path = GGUF_PATH_AUTO   the batch-size rule of gguf_mm_id;
+ *          GGUF_PATH_GEMV   the decode form (int8 activation codes, the
+ *                           GEMV's arithmetic) for any format, at most 128
+ *                           routed rows (T * top_k), else UNSUPPORTED;
+ *          GGUF_PATH_FUSED  the routed tensor-core path (f16 operands, f32
+ *                           accumulation) at every batch size.
+ * So a caller that needs one arithmetic for every batch size can fix it.
+ * All other arguments, the workspace size and the errors as gguf_mm_id;
+ * INVALID_ARG for another path value. */
+int gguf_mm_id_path(const void* w_experts, int qtype, int64_t n_expert, int64_t N, int64_t K,
+                    const void* x, int xdt, int64_t T, const int32_t* ids, int64_t top_k, int per_slot,
+                    const void* residual, void* y, int ydt,
+                    void* workspace, size_t ws_bytes, int path, gguf_stream_t stream);
+
 /* Q6_K plane regrouping (OpenVINO PR #39119, "Transformation"): blocks ->
  * QL[nblk][128] | QH[nblk][64] | SC[nblk][16] | D[nblk][2] (inverse = 0), or
  * back (inverse = 1).  src and dst are 210*nblk bytes each and must not

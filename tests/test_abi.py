@@ -61,6 +61,9 @@ def test_argument_errors_need_no_gpu(lib):
     assert f("gguf_dequant_padded", 16, 8, 0, 4, 64, 16, 2, 60, None) == g.GGUF_ERR_INVALID_ARG
     assert f("gguf_dense_gemm", 16, 1, 256, 4, 200, 16, 1, 8, None, 16, 2, None, 0, None) == g.GGUF_ERR_INVALID_ARG
     assert f("gguf_mm_id", 16, 12, 0, 4, 256, 16, 2, 8, None, 8, None, 16, 2, None, 0, None) == g.GGUF_ERR_INVALID_ARG
+    # the MoE call with a chosen form: an unknown path value
+    assert f("gguf_mm_id_path", 16, 12, 8, 256, 256, 16, 2, 1, 16, 2, 0, None, 16, 2, 16, 1 << 20, 7, None) == \
+        g.GGUF_ERR_INVALID_ARG
     # the host-buffer GEMV: its own pointer rules, then the GEMV's, before any copy
     h = "gguf_mm_gemv_host"
     assert f(h, 16, 12, 0, 4, 256, None, 16, 2, 1, None, None, 32, 16, 2, 16, 4096, None) == g.GGUF_ERR_INVALID_ARG

@@ -355,3 +355,55 @@ def test_moe_decode_form_terms_hook_refuses_the_routed_path():
         g.gguf_mm_debug_moe_mv_terms(w, syn.Q4_K, E, N, K, x, g.GGUF_DT_BF16, T, U.dev(ids), top_k, 0, None, y,
                                      g.GGUF_DT_F32, workspace=ws.t, ws_bytes=nws)
     assert e.value.status == g.GGUF_ERR_UNSUPPORTED
+
+
+def _run_path(qtype, E, N, K, T, top_k, wE, x, ids, path):
+    y = U.guarded((T, top_k, N), torch.float32, fill=float("nan"))
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
+    ws = U.workspace(ws_bytes, 0x6B)
+    g.gguf_mm_id_path(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids), top_k, 0, None,
+                      y.t, g.GGUF_DT_F32, ws.t, ws_bytes, path)
+    torch.cuda.synchronize()
+    y.check("y")
+    ws.check("workspace")
+    assert g.gguf_mm_check_errors() == 0
+    return U.host64(y.t)
+
+
+@pytest.mark.parametrize("qtype", [syn.Q4_K, syn.Q8_0])
+def test_moe_form_chosen_by_the_caller(qtype):
+    # gguf_mm_id_path: AUTO is gguf_mm_id bit for bit; GEMV forces the decode form
+    # (int8 path) and FUSED the routed tensor-core path, each where the batch-size
+    # rule would take the other; GEMV above 128 routed rows is refused
+    E, N, K, top_k = 8, 256, 512, 4
+    rs = syn.rng(520 + qtype)
+    wE = syn.weight_blocks(rs, qtype, E * N, K)
+    for T in (2, 10):                                        # 8 and 40 routed rows
+        x = syn.normal(rs, (T, K), "bf16")
+        ids = _distinct_ids(rs, T, E, top_k)
+        auto = _run_path(qtype, E, N, K, T, top_k, wE, x, ids, g.GGUF_PATH_AUTO)
+        y = U.guarded((T, top_k, N), torch.float32, fill=float("nan"))
+        ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
+        ws = U.workspace(ws_bytes, 0x6B)
+        g.gguf_mm_id(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids), top_k, None, y.t,
+                     g.GGUF_DT_F32, ws.t, ws_bytes)
+        torch.cuda.synchronize()
+        assert np.array_equal(auto, U.host64(y.t))
+        dec = _run_path(qtype, E, N, K, T, top_k, wE, x, ids, g.GGUF_PATH_GEMV)
+        U.check_close(dec.reshape(-1, N), O.moe_mv_id_int8(wE, qtype, E, N, K, U.act_f32(x, "bf16"), ids).reshape(-1, N),
+                      "f32", what=f"decode form T={T}")
+        rt = _run_path(qtype, E, N, K, T, top_k, wE, x, ids, g.GGUF_PATH_FUSED)
+        U.check_close(rt.reshape(-1, N), O.moe_mm_id_exact(wE, qtype, E, N, K, U.act_f64(x, "bf16"), ids).reshape(-1, N),
+                      "f32", rel=2e-3, what=f"routed T={T}")
+        assert np.array_equal(auto, dec if mv_form(qtype, T * top_k) else rt)
+    T = 40                                                   # 160 routed rows
+    x = syn.normal(rs, (T, K), "bf16")
+    ids = _distinct_ids(rs, T, E, top_k)
+    ws_bytes = g.gguf_mm_workspace_size(g.GGUF_OP_ID, qtype, N, K, T, E, top_k)
+    ws = U.workspace(ws_bytes)
+    y = torch.empty((T, top_k, N), dtype=torch.float32, device="cuda")
+    with pytest.raises(g.GGUFError) as err:
+        g.gguf_mm_id_path(U.dev(wE), qtype, E, N, K, U.dev(x, "bf16"), g.GGUF_DT_BF16, T, U.dev(ids), top_k, 0,
+                          None, y, g.GGUF_DT_F32, ws.t, ws_bytes, g.GGUF_PATH_GEMV)
+    assert err.value.status == g.GGUF_ERR_UNSUPPORTED
+    assert g.gguf_mm_check_errors() == 0
