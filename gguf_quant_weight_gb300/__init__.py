@@ -47,6 +47,7 @@ _SIGS = {
                             _c_vp, _c_vp, _c_int, _c_vp, _c_sz, _c_vp]),
     "gguf_mm_id_slots": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_i64,
                                   _c_vp, _c_vp, _c_int, _c_vp, _c_sz, _c_vp]),
+    "gguf_mm_id_form": (_c_int, [_c_int, _c_i64, _c_i64]),
     "gguf_mm_id_path": (_c_int, [_c_vp, _c_int, _c_i64, _c_i64, _c_i64, _c_vp, _c_int, _c_i64, _c_vp, _c_i64,
                                  _c_int, _c_vp, _c_vp, _c_int, _c_vp, _c_sz, _c_int, _c_vp]),
     "gguf_repack_q6k_planes": (_c_int, [_c_vp, _c_vp, _c_i64, _c_int, _c_vp]),
@@ -184,6 +185,10 @@ def gguf_mm_id_slots(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, re
     return _check("gguf_mm_id_slots", load_library().gguf_mm_id_slots(
         _p(w_experts), qtype, n_expert, N, K, _p(x), xdt, T, _p(ids), top_k, _p(residual), _p(y), ydt,
         _p(workspace), ws_bytes, _s(stream)))
+
+
+def gguf_mm_id_form(qtype, T, top_k) -> int:
+    return load_library().gguf_mm_id_form(qtype, T, top_k)
 
 
 def gguf_mm_id_path(w_experts, qtype, n_expert, N, K, x, xdt, T, ids, top_k, per_slot, residual, y, ydt,

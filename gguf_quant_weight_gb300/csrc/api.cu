@@ -268,6 +268,12 @@ int gguf_mm_auto_path(int qtype, int layout, int64_t N, int64_t K, int64_t M, in
     return auto_path(qtype, layout, N, K, M, xdt);
 }
 
+int gguf_mm_id_form(int qtype, int64_t T, int64_t top_k) {
+    if (!valid_qtype(qtype) || T <= 0 || top_k <= 0 || top_k > 64 || T > (int64_t(1) << 24))
+        return GGUF_ERR_INVALID_ARG;
+    return moe_decode_form(qtype, T * top_k) ? GGUF_PATH_GEMV : GGUF_PATH_FUSED;
+}
+
 int gguf_mm_gemv_kernel(int qtype, int layout, int64_t N, int64_t K, int64_t M, int xdt) {
     // the plan for dummy (aligned, non-null) pointers: nothing is launched
     static const uint8_t dummy[16] __attribute__((aligned(16))) = {};

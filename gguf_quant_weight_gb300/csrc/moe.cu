@@ -273,6 +273,8 @@ int moe_route_debug(const int32_t* ids, int64_t entries, int64_t n_expert, int* 
 
 int64_t moe_max_tiles(int64_t n_expert, int64_t entries) { return std::min(n_expert, entries) + ceil_div(entries, kMoeTile); }
 
+bool moe_decode_form(int qtype, int64_t entries) { return mv_form(qtype, entries); }
+
 int moe_mv_max_rows(int qtype) {
     switch (qtype) {
         case GGUF_Q4_K: case GGUF_Q5_K: case GGUF_Q2_K: case GGUF_Q3_K: case GGUF_Q6_K: return kMoeMvRows;

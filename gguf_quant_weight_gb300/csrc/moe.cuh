@@ -12,6 +12,9 @@ namespace gg {
 // path measured faster above that on 128 experts of 768 x 2048, top-8).
 constexpr int kMoeMvRows = 128;
 int moe_mv_max_rows(int qtype);
+// The batch-size rule (and its GGUF_MM_MOE_MV=0 override): does this many
+// routed rows of qtype experts take the decode form?  Host only, no CUDA call.
+bool moe_decode_form(int qtype, int64_t entries);
 
 size_t moe_workspace_bytes(int qtype, int64_t n_expert, int64_t N, int64_t K, int64_t T, int64_t top_k);
 

@@ -215,6 +215,12 @@ int gguf_mm_id_slots(const void* w_experts, int qtype, int64_t n_expert, int64_t
                      const void* residual, void* y, int ydt,
                      void* workspace, size_t ws_bytes, gguf_stream_t stream);
 
+/* The form gguf_mm_id / gguf_mm_id_slots take for T tokens of top_k routed
+ * rows of qtype experts: GGUF_PATH_GEMV (the decode form) or GGUF_PATH_FUSED
+ * (the routed tensor-core path); GGUF_ERR_INVALID_ARG for a bad argument.
+ * Host only: nothing is launched and no GPU is needed. */
+int gguf_mm_id_form(int qtype, int64_t T, int64_t top_k);
+
 /* gguf_mm_id (per_slot = 0) or gguf_mm_id_slots (per_slot = 1) with the form
  * chosen by the caller instead of by the batch size:
  *   path = GGUF_PATH_AUTO   the batch-size rule of gguf_mm_id;

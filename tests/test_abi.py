@@ -109,6 +109,25 @@ def test_gemm_workspace_follows_the_tile_plan(lib):
     assert g.gguf_mm_workspace_size(g.GGUF_OP_GEMM, 13, 14336, 4096, 2048) == act(2048, 4096)
 
 
+def test_moe_form_rule(lib, monkeypatch):
+    # the decode form up to a per-format number of routed rows (T * top_k), as
+    # the header states, and the routed tensor-core path above it; the tests'
+    # mirror of the rule agrees; GGUF_MM_MOE_MV=0 keeps every batch routed
+    from tests import gpu_util as U
+    limits = {12: 128, 13: 128, 10: 128, 11: 128, 14: 128, 8: 16, 2: 32, 3: 32, 6: 32, 7: 32}
+    for qt, lim in limits.items():
+        assert U.moe_mv_max_rows(qt) == lim
+        for top_k in (1, 2, 8):
+            for T in sorted({1, max(1, lim // top_k), lim // top_k + 1, 4 * lim}):
+                want = g.GGUF_PATH_GEMV if T * top_k <= lim else g.GGUF_PATH_FUSED
+                assert g.gguf_mm_id_form(qt, T, top_k) == want, (qt, T, top_k)
+    assert g.gguf_mm_id_form(99, 1, 1) == g.GGUF_ERR_INVALID_ARG
+    assert g.gguf_mm_id_form(12, 0, 8) == g.GGUF_ERR_INVALID_ARG
+    assert g.gguf_mm_id_form(12, 1, 0) == g.GGUF_ERR_INVALID_ARG
+    monkeypatch.setenv("GGUF_MM_MOE_MV", "0")
+    assert g.gguf_mm_id_form(12, 1, 8) == g.GGUF_PATH_FUSED
+
+
 def test_auto_path_table(lib):
     # the measured crossovers, by format and shape class (up to 8192 weight rows / more)
     big, small = (14336, 4096), (4096, 4096)
