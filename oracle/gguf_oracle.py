@@ -12,8 +12,9 @@ shortcut.
 
 Sources (web pages; cited by title and section):
   [mobius]  "GGUF Support Proposal for mobius": section 1.2 "Quantization Types"
-            (type table), section 7 "Quantization Format Deep Dive" (7.3 Q4_K,
-            7.4 Q8_0 block structs and the Q4_K dequantization formula).
+            (type table: Q4_0 .. Q8_0, Q2_K .. Q6_K), section 7 "Quantization
+            Format Deep Dive" (7.1 Q4_0, 7.2 Q4_1, 7.3 Q4_K, 7.4 Q8_0 block
+            structs and their dequantization formulas).
   [ov39119] OpenVINO PR #39119 "FullyConnectedGGUF": "Transformation" (Q6_K plane
             regrouping QL|QH|SC|D), "Implementation" (GEMV: activations quantized
             per 32 values, int8 dot products against the blocks).
@@ -32,7 +33,14 @@ Readings taken where the pages are silent (all listed in the design notes):
     order as in decode_6bit below;
   * activation quantizer rounding: f32 d_a = amax/127, multiply by f32 1/d_a,
     clamp to [-127, 127], round half away from zero; zero block -> d_a = 0;
-  * a Q6_K 16-wide sub-block uses the activation block floor(j/2);
+  * a Q6_K 16-wide sub-block uses the activation block floor(j/2), and so do the
+    16-value sub-blocks of Q2_K and Q3_K;
+  * the 32-value formats: element e < 16 in the low nibble of qs[e], e >= 16 in
+    the high nibble of qs[e-16], Q5_0/Q5_1's fifth bit bit e of the qh word;
+    zero points 8 (Q4_0) and 16 (Q5_0); Q4_1/Q5_1 add the min (w = q*d + m, as
+    mobius 7.2 writes it) where the K-quants subtract it;
+  * Q2_K / Q3_K (named in the type table only): the GGUF on-disk structs, with
+    Q3_K's q3 = q2 - 4 where the element's hmask bit is clear;
   * K-padding: one 128-byte line, i.e. 64 two-byte elements, pad written as 0.
 Parity against real GGUF files is unpinned: no GGUF file or reference
 implementation is available to this build.
